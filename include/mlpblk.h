@@ -1,0 +1,153 @@
+/*
+ * mlpblk.h -- C ABI of the GB300 (sm_103a) forward and backward of the
+ * pre-normalised residual ReLU² MLP block
+ *
+ *     n = RMSNorm(x) = x * r * gamma,     r[t] = 1 / sqrt(mean_k x[t,k]^2 + eps)
+ *     h = n . W1^T                        (saved)
+ *     a = relu(h)^2                       (saved: it is also the W2 operand)
+ *     y = x + a . W2^T
+ *
+ * Sources (page title -- section):
+ *   "Nemotron Kernels From Inference To Backpropagation" -- "Setup: The Shared
+ *     Transformer Shell" (pre-norm residual shell; backward starts at the residual
+ *     split; RMSNorm backward needs x, gamma and the inverse RMS) and "Kernel 3:
+ *     Dense ReLU2 Inference And Backpropagation" (project, relu squared, project;
+ *     the pre-activation is kept for backward).
+ *   "Reverse-mode automatic differentiation" -- section 5 (MatMul: g.B^T and
+ *     A^T.g; Relu; LayerNorm rule, here without the mean terms).
+ *   "grow_a_language_model_backprop" -- forward/backward kernel pairing, saved
+ *     tensors, += accumulation across microbatches, scale_grads(1/n), zero_grads(),
+ *     preallocated buffers.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense and row-major.  x, y, dy, dx: [tokens, d_model];
+ *     h, a: [tokens, ffn]; W1, dW1: [ffn, d_model]; W2, dW2: [d_model, ffn];
+ *     gamma, dgamma: [d_model]; rstd: [tokens].
+ *   - Element types.  MLPBLK_BF16: x, gamma, W1, W2, y, h, a, dy, dx are bfloat16
+ *     (passed as 16-bit storage); rstd and the gradient buffers dgamma, dW1, dW2
+ *     are float32.  MLPBLK_FP32: every tensor is float32.
+ *   - Every pointer except `stream` is a DEVICE pointer, 16-byte aligned, owned by
+ *     the caller.  The library allocates no device memory and keeps no per-call
+ *     state; the scratch it needs lives in the caller's workspace.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and does not synchronise the host.  Argument errors are
+ *     reported by the return value before anything is enqueued.  A device-side
+ *     failure (a bounded wait that gave up) is reported later by
+ *     mlpblk_last_error().
+ *   - Limits: d_model and ffn positive multiples of 8 (16-byte rows); tokens >= 0
+ *     and tokens * max(d_model, ffn) < 2^31; eps finite and >= 0.  tokens == 0 is a
+ *     valid empty microbatch: the call checks the descriptor and returns MLPBLK_OK
+ *     without touching any buffer.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef MLPBLK_H
+#define MLPBLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MLPBLK_OK          0  /* success (work enqueued)                                 */
+#define MLPBLK_EINVAL      1  /* null or misaligned pointer, bad size, bad eps          */
+#define MLPBLK_ENOTSUP     2  /* unknown dtype, or d_model/ffn not a multiple of 8      */
+#define MLPBLK_EWORKSPACE  3  /* workspace smaller than mlpblk_workspace_size()         */
+#define MLPBLK_ECUDA       4  /* a CUDA runtime call or a kernel launch failed          */
+#define MLPBLK_ETIMEOUT    5  /* a device-side bounded wait gave up (mlpblk_last_error) */
+#define MLPBLK_ENODEV      6  /* the current device is not sm_103 (GB300)               */
+
+/* Element-type selector for mlpblk_desc.dtype. */
+#define MLPBLK_BF16 1
+#define MLPBLK_FP32 2
+
+/* Shape of one microbatch through one block. */
+typedef struct {
+    int64_t tokens;   /* T: rows of x in this microbatch                     */
+    int64_t d_model;  /* d: model width                                      */
+    int64_t ffn;      /* F: hidden width of the MLP                          */
+    float   eps;      /* RMSNorm epsilon, added to mean(x^2) inside the root */
+    int32_t dtype;    /* MLPBLK_BF16 or MLPBLK_FP32                          */
+} mlpblk_desc;
+
+/*
+ * Bytes of device workspace that mlpblk_forward and mlpblk_backward need for
+ * `desc` (one size serves both).  Returns 0 for an invalid descriptor.  The
+ * workspace holds scratch only (gamma-folded W1, the rstd-scaled dh, dn, and
+ * the per-block dgamma partials); its contents need not be preserved between
+ * calls, but two calls in flight at once must not share one workspace.
+ */
+size_t mlpblk_workspace_size(const mlpblk_desc *desc);
+
+/*
+ * Forward of one microbatch ("Setup: The Shared Transformer Shell";
+ * "Kernel 3: Dense ReLU2 ...").
+ *   in : x[T,d], gamma[d], w1[F,d], w2[d,F]
+ *   out: y[T,d]          = x + relu(h)^2 . W2^T                      (written)
+ *        h_saved[T,F]    = RMSNorm(x) . W1^T, rounded to the dtype    (written)
+ *        a_saved[T,F]    = relu(h)^2, rounded to the dtype            (written)
+ *        rstd_saved[T]   = 1/sqrt(mean_k x^2 + eps), float32          (written)
+ * y must not alias x.  Returns an MLPBLK_* code.
+ */
+int mlpblk_forward(const mlpblk_desc *desc,
+                   const void *x, const void *gamma, const void *w1, const void *w2,
+                   void *y, void *h_saved, void *a_saved, float *rstd_saved,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of one microbatch (the residual branch copies forward and adds
+ * backward; d relu(h)^2/dh = 2 relu(h), 0 at h = 0; RMSNorm backward from the
+ * saved rstd).  Consumes the forward's saved h, a and rstd for the same x.
+ *   in : dy[T,d], x[T,d], gamma[d], w1[F,d], w2[d,F], h_saved, a_saved, rstd_saved
+ *   out: dx[T,d]        = dy + RMSNorm backward of dn                 (written)
+ *        dgamma[d]     += sum_t dn[t,k] * x[t,k] * r[t]      float32 (accumulated)
+ *        dw1[F,d]      += dh^T . n                           float32 (accumulated)
+ *        dw2[d,F]      += dy^T . a                           float32 (accumulated)
+ *   where dh = (dy . W2) * 2 relu(h) and dn = dh . W1.  The gradient buffers keep
+ *   a running sum across calls until mlpblk_zero_grads.  dx must not alias dy or
+ *   x.  Returns an MLPBLK_* code.
+ */
+int mlpblk_backward(const mlpblk_desc *desc,
+                    const void *dy, const void *x, const void *gamma,
+                    const void *w1, const void *w2,
+                    const void *h_saved, const void *a_saved, const float *rstd_saved,
+                    void *dx, float *dgamma, float *dw1, float *dw2,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --
+ * accumulation across microbatches): dgamma[d], dw1[F,d], dw2[d,F] = 0 (float32).
+ * desc->tokens is ignored.  Returns an MLPBLK_* code.
+ */
+int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2,
+                      void *stream);
+
+/*
+ * scale_grads(s) of the same loop, e.g. s = 1/n_microbatches:
+ * dgamma, dw1, dw2 *= s (float32, one rounding per element).  s must be finite.
+ * desc->tokens is ignored.  Returns an MLPBLK_* code.
+ */
+int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2,
+                       float s, void *stream);
+
+/*
+ * First device-side error recorded since the previous call (MLPBLK_OK if none),
+ * then clears it.  Synchronises the current device.  MLPBLK_ETIMEOUT means a
+ * kernel's bounded wait on a pipeline barrier gave up and the kernel returned
+ * early: its outputs are not valid.
+ */
+int mlpblk_last_error(void);
+
+/* Static, NUL-terminated description of an MLPBLK_* code. */
+const char *mlpblk_strerror(int code);
+
+/* ABI version (major * 100 + minor). */
+int mlpblk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLPBLK_H */

@@ -1,0 +1,188 @@
+"""Python binding of libmlpblk.so, the GB300 forward/backward of the pre-norm
+residual ReLU² MLP block (C ABI in include/mlpblk.h).
+
+Argument marshalling only: every step of the block runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (device memory and streams are the
+only things torch provides); the functions keep the C names and raise
+``MlpBlkError`` on a non-zero status.  Importing this package fails loudly when
+the library has not been built: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmlpblk.so")
+
+MLPBLK_OK = 0
+MLPBLK_EINVAL = 1
+MLPBLK_ENOTSUP = 2
+MLPBLK_EWORKSPACE = 3
+MLPBLK_ECUDA = 4
+MLPBLK_ETIMEOUT = 5
+MLPBLK_ENODEV = 6
+MLPBLK_BF16 = 1
+MLPBLK_FP32 = 2
+
+EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads",
+            "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version")
+
+
+class MlpBlkError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: status {code} ({strerror(code)})")
+
+
+class Desc(ctypes.Structure):
+    """mlpblk_desc: shape of one microbatch through one block."""
+    _fields_ = [("tokens", ctypes.c_int64), ("d_model", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: run mlp_block_backprop_gb300.build.build_library() "
+                          "(or __graft_entry__.build()) first; there is no non-CUDA fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    pd = ctypes.POINTER(Desc)
+    lib.mlpblk_workspace_size.argtypes = [pd]
+    lib.mlpblk_workspace_size.restype = sz
+    lib.mlpblk_forward.argtypes = [pd] + [vp] * 9 + [sz, vp]
+    lib.mlpblk_forward.restype = i32
+    lib.mlpblk_backward.argtypes = [pd] + [vp] * 13 + [sz, vp]
+    lib.mlpblk_backward.restype = i32
+    lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
+    lib.mlpblk_zero_grads.restype = i32
+    lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
+    lib.mlpblk_scale_grads.restype = i32
+    lib.mlpblk_last_error.argtypes = []
+    lib.mlpblk_last_error.restype = i32
+    lib.mlpblk_strerror.argtypes = [i32]
+    lib.mlpblk_strerror.restype = ctypes.c_char_p
+    lib.mlpblk_version.argtypes = []
+    lib.mlpblk_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def strerror(code: int) -> str:
+    return lib.mlpblk_strerror(int(code)).decode()
+
+
+def make_desc(tokens: int, d_model: int, ffn: int, eps: float = 1e-6, dtype: int = MLPBLK_BF16) -> Desc:
+    return Desc(int(tokens), int(d_model), int(ffn), float(eps), int(dtype))
+
+
+def _ptr(t):
+    """Device address of a tensor, an int address, or None (NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc, where):
+    if rc != MLPBLK_OK:
+        raise MlpBlkError(rc, where)
+
+
+def mlpblk_workspace_size(desc: Desc) -> int:
+    return int(lib.mlpblk_workspace_size(ctypes.byref(desc)))
+
+
+def mlpblk_forward(desc, x, gamma, w1, w2, y, h_saved, a_saved, rstd_saved, workspace,
+                   workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_forward(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2), _ptr(y),
+                            _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(workspace),
+                            nbytes, _stream(stream))
+    _check(rc, "mlpblk_forward")
+
+
+def mlpblk_backward(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
+                    workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_backward(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
+                             _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(dx), _ptr(dgamma),
+                             _ptr(dw1), _ptr(dw2), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_backward")
+
+
+def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):
+    _check(lib.mlpblk_zero_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
+                                 _stream(stream)), "mlpblk_zero_grads")
+
+
+def mlpblk_scale_grads(desc, dgamma, dw1, dw2, s, stream=None):
+    _check(lib.mlpblk_scale_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2), float(s),
+                                  _stream(stream)), "mlpblk_scale_grads")
+
+
+def mlpblk_last_error() -> int:
+    return int(lib.mlpblk_last_error())
+
+
+def mlpblk_version() -> int:
+    return int(lib.mlpblk_version())
+
+
+class BlockBuffers:
+    """Device buffers of one block for microbatches of up to `tokens` rows:
+    parameters, saved tensors, outputs, fp32 gradient buffers and workspace."""
+
+    def __init__(self, tokens, d_model, ffn, dtype="bf16", eps=1e-6, device="cuda"):
+        import torch
+        self.torch = torch
+        self.dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.code = MLPBLK_BF16 if dtype == "bf16" else MLPBLK_FP32
+        self.T, self.d, self.F, self.eps = tokens, d_model, ffn, eps
+        self.desc = make_desc(tokens, d_model, ffn, eps, self.code)
+        e = dict(device=device)
+        T, d, F = tokens, d_model, ffn
+        self.gamma = torch.empty(d, dtype=self.dt, **e)
+        self.w1 = torch.empty(F, d, dtype=self.dt, **e)
+        self.w2 = torch.empty(d, F, dtype=self.dt, **e)
+        self.x = torch.empty(T, d, dtype=self.dt, **e)
+        self.dy = torch.empty(T, d, dtype=self.dt, **e)
+        self.y = torch.empty(T, d, dtype=self.dt, **e)
+        self.h = torch.empty(T, F, dtype=self.dt, **e)
+        self.a = torch.empty(T, F, dtype=self.dt, **e)
+        self.rstd = torch.empty(T, dtype=torch.float32, **e)
+        self.dx = torch.empty(T, d, dtype=self.dt, **e)
+        self.dgamma = torch.zeros(d, dtype=torch.float32, **e)
+        self.dw1 = torch.zeros(F, d, dtype=torch.float32, **e)
+        self.dw2 = torch.zeros(d, F, dtype=torch.float32, **e)
+        ws = mlpblk_workspace_size(self.desc)
+        if ws == 0:
+            raise MlpBlkError(MLPBLK_EINVAL, "mlpblk_workspace_size")
+        self.ws = torch.empty(ws, dtype=torch.uint8, **e)
+
+    def forward(self, stream=None):
+        mlpblk_forward(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.h, self.a,
+                       self.rstd, self.ws, stream=stream)
+
+    def backward(self, stream=None):
+        mlpblk_backward(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a,
+                        self.rstd, self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)
+
+    def zero_grads(self, stream=None):
+        mlpblk_zero_grads(self.desc, self.dgamma, self.dw1, self.dw2, stream=stream)
+
+    def scale_grads(self, s, stream=None):
+        mlpblk_scale_grads(self.desc, self.dgamma, self.dw1, self.dw2, s, stream=stream)

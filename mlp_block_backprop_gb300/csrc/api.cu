@@ -1,0 +1,255 @@
+// api.cu -- the C ABI (include/mlpblk.h): argument checks, workspace layout and
+// the order of kernels for one microbatch forward and backward.
+//
+// Forward  (bf16): fold gamma into W1 -> W1 GEMM (rstd prologue, h/a epilogue)
+//                  -> W2 GEMM (residual epilogue)
+// Backward (bf16): dgrad-h GEMM (gate, dh_s = rstd*dh) -> wgrad W2 GEMM (+=)
+//                  -> dgrad-n GEMM (dn_s = rstd*dn) -> wgrad W1 GEMM (+= , gamma)
+//                  -> RMSNorm backward rows (dx, dgamma partials) -> dgamma (+=)
+// The fp32 element type runs the same sequence on CUDA cores.
+#include <math.h>
+
+#include <new>
+
+#include "mlpblk_internal.h"
+
+namespace mlpblk {
+int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
+                       void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s);
+int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
+                       void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s);
+int take_device_error_gemm_fwd();
+int take_device_error_gemm_bwd();
+}  // namespace mlpblk
+
+using namespace mlpblk;
+
+namespace {
+
+constexpr int kMaxParts = 512;  // dgamma partial rows the workspace holds
+
+int64_t align256(int64_t b) { return (b + 255) & ~static_cast<int64_t>(255); }
+
+int check_desc(const mlpblk_desc *d) {
+    if (!d) return MLPBLK_EINVAL;
+    if (d->dtype != MLPBLK_BF16 && d->dtype != MLPBLK_FP32) return MLPBLK_ENOTSUP;
+    if (d->tokens < 0 || d->d_model <= 0 || d->ffn <= 0) return MLPBLK_EINVAL;
+    if (d->d_model % 8 != 0 || d->ffn % 8 != 0) return MLPBLK_ENOTSUP;
+    if (!(d->eps >= 0.0f) || !isfinite(d->eps)) return MLPBLK_EINVAL;
+    const int64_t lim = static_cast<int64_t>(1) << 31;
+    const int64_t wide = d->d_model > d->ffn ? d->d_model : d->ffn;
+    if (d->ffn >= lim / d->d_model) return MLPBLK_EINVAL;
+    if (d->tokens >= lim / wide) return MLPBLK_EINVAL;
+    if (d->d_model > kMaxNormD) return MLPBLK_ENOTSUP;
+    return MLPBLK_OK;
+}
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct WsLayout {
+    int64_t w1g, dh, dn, part, total;
+};
+
+WsLayout ws_layout(const mlpblk_desc *d) {
+    const int64_t elt = d->dtype == MLPBLK_BF16 ? 2 : 4;
+    WsLayout l;
+    l.w1g = 0;
+    const int64_t fwd = align256(d->ffn * d->d_model * elt);
+    l.dh = 0;
+    l.dn = align256(d->tokens * d->ffn * elt);
+    l.part = l.dn + align256(d->tokens * d->d_model * 4);
+    const int64_t bwd = l.part + align256(static_cast<int64_t>(kMaxParts) * d->d_model * 4);
+    l.total = fwd > bwd ? fwd : bwd;
+    return l;
+}
+
+// Device properties, checked once per device: sm_103 and its SM count.
+int device_sms(int *sms) {
+    static int cached[64] = {0};  // 0 unknown, -1 unsupported, else SM count
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MLPBLK_ECUDA;
+        cached[dev] = (major == 10 && minor == 3 && n > 0) ? n : -1;
+    }
+    if (cached[dev] < 0) return MLPBLK_ENODEV;
+    *sms = cached[dev];
+    return MLPBLK_OK;
+}
+
+#define MLPBLK_TRY(expr)              \
+    do {                              \
+        const int rc_ = (expr);       \
+        if (rc_ != MLPBLK_OK) return rc_; \
+    } while (0)
+
+int norm_parts(int64_t T, int sms) {
+    int p = norm_bwd_parts(T);
+    if (p > 2 * sms) p = 2 * sms;
+    if (p > kMaxParts) p = kMaxParts;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlpblk_version(void) { return 100; }
+
+const char *mlpblk_strerror(int code) {
+    switch (code) {
+        case MLPBLK_OK: return "success";
+        case MLPBLK_EINVAL: return "invalid argument (null or misaligned pointer, bad size or eps)";
+        case MLPBLK_ENOTSUP: return "unsupported dtype or shape (d_model, ffn multiples of 8; d_model <= 4096)";
+        case MLPBLK_EWORKSPACE: return "workspace smaller than mlpblk_workspace_size()";
+        case MLPBLK_ECUDA: return "CUDA runtime error or kernel launch failure";
+        case MLPBLK_ETIMEOUT: return "a device-side bounded wait gave up; outputs are invalid";
+        case MLPBLK_ENODEV: return "current device is not sm_103 (GB300)";
+        default: return "unknown mlpblk status code";
+    }
+}
+
+size_t mlpblk_workspace_size(const mlpblk_desc *desc) {
+    if (check_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(ws_layout(desc).total);
+}
+
+int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1,
+                   const void *w2, void *y, void *h_saved, void *a_saved, float *rstd_saved,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) ||
+        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *w1g = ws + l.w1g;
+
+    MLPBLK_TRY(launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
+    if (desc->dtype == MLPBLK_BF16) {
+        GemmArgs g1 = {};
+        g1.rstd_out = rstd_saved;
+        g1.inv_k = 1.0f / static_cast<float>(d);
+        g1.eps = desc->eps;
+        MLPBLK_TRY(launch_gemm_tc_fwd(kEpiFwdW1, (int)T, (int)F, (int)d, x, w1g, h_saved, a_saved, g1, sms, s));
+        GemmArgs g2 = {};
+        g2.aux = static_cast<const uint16_t *>(x);
+        g2.ld_aux = (int)d;
+        MLPBLK_TRY(launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
+    } else {
+        const float *xf = static_cast<const float *>(x);
+        MLPBLK_TRY(launch_rstd_f32(xf, rstd_saved, T, d, desc->eps, s));
+        SimtEpi e1 = {nullptr, rstd_saved, nullptr};
+        MLPBLK_TRY(launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, xf, d, 1,
+                                    static_cast<const float *>(w1g), d, 1,
+                                    static_cast<float *>(h_saved), static_cast<float *>(a_saved), e1, s));
+        SimtEpi e2 = {xf, nullptr, nullptr};
+        MLPBLK_TRY(launch_gemm_simt(kEpiFwdW2, (int)T, (int)d, (int)F,
+                                    static_cast<const float *>(a_saved), F, 1,
+                                    static_cast<const float *>(w2), F, 1, static_cast<float *>(y),
+                                    nullptr, e2, s));
+    }
+    return MLPBLK_OK;
+}
+
+int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                    const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                    const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
+        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(dx) ||
+        !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *dh_s = ws + l.dh;
+    float *dn_s = reinterpret_cast<float *>(ws + l.dn);
+    float *part = reinterpret_cast<float *>(ws + l.part);
+    const int parts = norm_parts(T, sms);
+
+    if (desc->dtype == MLPBLK_BF16) {
+        GemmArgs gd = {};
+        gd.aux = static_cast<const uint16_t *>(h_saved);
+        gd.ld_aux = (int)F;
+        gd.rstd_in = rstd_saved;
+        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
+        GemmArgs gw2 = {};
+        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
+        GemmArgs gn = {};
+        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
+        GemmArgs gw1 = {};
+        gw1.colscale = static_cast<const uint16_t *>(gamma);
+        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
+    } else {
+        const float *dyf = static_cast<const float *>(dy);
+        const float *xf = static_cast<const float *>(x);
+        const float *dhf = static_cast<const float *>(dh_s);
+        SimtEpi ed = {static_cast<const float *>(h_saved), rstd_saved, nullptr};
+        MLPBLK_TRY(launch_gemm_simt(kEpiDgradH, (int)T, (int)F, (int)d, dyf, d, 1,
+                                    static_cast<const float *>(w2), 1, F, static_cast<float *>(dh_s),
+                                    nullptr, ed, s));
+        SimtEpi e0 = {nullptr, nullptr, nullptr};
+        MLPBLK_TRY(launch_gemm_simt(kEpiAccF32, (int)d, (int)F, (int)T, dyf, 1, d,
+                                    static_cast<const float *>(a_saved), 1, F, dw2, nullptr, e0, s));
+        MLPBLK_TRY(launch_gemm_simt(kEpiStoreF32, (int)T, (int)d, (int)F, dhf, F, 1,
+                                    static_cast<const float *>(w1), 1, d, dn_s, nullptr, e0, s));
+        SimtEpi ec = {nullptr, nullptr, static_cast<const float *>(gamma)};
+        MLPBLK_TRY(launch_gemm_simt(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dhf, 1, F, xf, 1, d,
+                                    dw1, nullptr, ec, s));
+    }
+    MLPBLK_TRY(launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, parts, s));
+    MLPBLK_TRY(launch_dgamma_finalize(part, parts, dgamma, d, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t d = desc->d_model, F = desc->ffn;
+    MLPBLK_TRY(launch_fill_zero(dgamma, d, s));
+    MLPBLK_TRY(launch_fill_zero(dw1, F * d, s));
+    MLPBLK_TRY(launch_fill_zero(dw2, F * d, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, float sc,
+                       void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
+    if (!isfinite(sc)) return MLPBLK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t d = desc->d_model, F = desc->ffn;
+    MLPBLK_TRY(launch_scale(dgamma, d, sc, s));
+    MLPBLK_TRY(launch_scale(dw1, F * d, sc, s));
+    MLPBLK_TRY(launch_scale(dw2, F * d, sc, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_last_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MLPBLK_ECUDA;
+    const int a = take_device_error_gemm_fwd();
+    const int b = take_device_error_gemm_bwd();
+    return a != MLPBLK_OK ? a : b;
+}
+
+}  // extern "C"

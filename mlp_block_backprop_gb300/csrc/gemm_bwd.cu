@@ -1,0 +1,38 @@
+// gemm_bwd.cu -- tensor-core GEMMs of the block backward (MatMul rule g.B^T and
+// A^T.g of "Reverse-mode automatic differentiation", section 5):
+//   dgrad h : dh_s = rstd * (dy . W2) * 2 relu(h)       (ReLU^2 gate in the epilogue;
+//                                                         W2 read MN-major)
+//   wgrad W2: dW2 += dy^T . a                             (both operands MN-major)
+//   dgrad n : dn_s = dh_s . W1                            (fp32 out; W1 MN-major)
+//   wgrad W1: dW1 += (dh_s^T . x) * gamma[col]            (both operands MN-major)
+// dh_s = rstd*dh and dn_s = rstd*dn carry the per-row RMSNorm scale, so the
+// normalised input n never has to be stored or rebuilt: dh^T.n = (dh_s^T.x)*gamma.
+#include "gemm_tc.cuh"
+
+namespace mlpblk {
+
+int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
+                       void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
+    const int bn = choose_bn(M, N, num_sms);
+#define MLPBLK_RUN(E, AMN, BMN)                                                                    \
+    return bn == 256                                                                               \
+               ? run_gemm_tc<GemmCfg<256, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s)  \
+               : run_gemm_tc<GemmCfg<128, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+    switch (epi) {
+        case kEpiDgradH: MLPBLK_RUN(kEpiDgradH, false, true);
+        case kEpiStoreF32: MLPBLK_RUN(kEpiStoreF32, false, true);
+        case kEpiAccF32: MLPBLK_RUN(kEpiAccF32, true, true);
+        case kEpiAccF32ColScale: MLPBLK_RUN(kEpiAccF32ColScale, true, true);
+        default: return MLPBLK_EINVAL;
+    }
+#undef MLPBLK_RUN
+}
+
+int take_device_error_gemm_bwd() {
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MLPBLK_ECUDA;
+    if (v != 0) cudaMemcpyToSymbol(g_device_error, &z, sizeof(int));
+    return v;
+}
+
+}  // namespace mlpblk

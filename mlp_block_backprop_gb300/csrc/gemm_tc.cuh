@@ -1,0 +1,497 @@
+// gemm_tc.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with the
+// block's fused prologue/epilogues.
+//
+//   D[M,N] = sum_k A[m,k] * B[n,k]      bf16 operands, fp32 accumulator in TMEM
+//
+// A and B are each either K-major (stored [rows][K]) or MN-major (stored [K][rows]);
+// the tensor core reads both layouts straight from shared memory, so the
+// transposed products of the backward pass (g.B and A^T.g of the MatMul rule of
+// "Reverse-mode automatic differentiation", section 5) need no transpose copies.
+//
+// CTA layout (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A/B tiles -> shared-memory ring of kStages stages
+//   warp 1      owns TMEM; one lane issues tcgen05.mma (128 x BN x 16 per step)
+//   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
+//   warps 6..9  (forward W1 only) RMSNorm prologue: sum of x^2 per row, read from
+//               the A stages already in shared memory, gives rstd for the epilogue
+// The accumulator is double buffered in TMEM (2 x BN columns) so the epilogue of
+// one tile overlaps the main loop of the next.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace mlpblk {
+
+constexpr int kBM = 128;      // tile rows (UMMA M)
+constexpr int kBK = 64;       // K per stage: one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;    // K per tcgen05.mma for 16-bit inputs
+constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
+
+template <int BN_, int EPI_, bool A_MN_, bool B_MN_>
+struct GemmCfg {
+    static constexpr int BN = BN_;
+    static constexpr int EPI = EPI_;
+    static constexpr bool A_MN = A_MN_;
+    static constexpr bool B_MN = B_MN_;
+    static constexpr bool kNorm = (EPI == kEpiFwdW1);
+    static constexpr bool kOutBf16 = (EPI == kEpiFwdW1 || EPI == kEpiFwdW2 || EPI == kEpiDgradH);
+    static constexpr bool kReduce = (EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
+    static constexpr int kNumOut = (EPI == kEpiFwdW1) ? 2 : 1;
+    static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
+    static constexpr int kNumChunks = BN / kChunkCols;
+    static constexpr int kStagingBufs = 2;
+    static constexpr int kThreads = kNorm ? 320 : 192;
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStagingBytes = 4 * kNumOut * kStagingBufs * 4096;
+    static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
+    static constexpr int kAlignSlack = 1024;
+    static constexpr int kStagesRaw =
+        (kSmemLimit - kAlignSlack - kCtrlBytes - kStagingBytes) / kStageBytes;
+    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+    static constexpr int kSmemBytes = kAlignSlack + kCtrlBytes + kStagingBytes + kStages * kStageBytes;
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+    static_assert(kStages >= 2, "not enough shared memory for a pipeline");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory over budget");
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+};
+
+struct WorkUnit {
+    int m0, n0, n_blk, kb0, kb1;
+};
+
+// Unit u -> (split, tile); tiles are rastered in groups of group_m M-tiles that
+// sweep all N-tiles together, so CTAs running at the same time share operand
+// tiles in L2.  The split index is outermost for the same reason.
+template <int BN>
+__device__ __forceinline__ WorkUnit decode_unit(const GemmArgs &a, int u) {
+    const int tiles = a.m_tiles * a.n_tiles;
+    const int split = u / tiles;
+    const int t = u - split * tiles;
+    const int group = a.group_m * a.n_tiles;
+    const int g = t / group;
+    const int first_m = g * a.group_m;
+    const int gm = min(a.m_tiles - first_m, a.group_m);
+    const int r = t - g * group;
+    WorkUnit w;
+    const int m_blk = first_m + r % gm;
+    w.n_blk = r / gm;
+    w.m0 = m_blk * kBM;
+    w.n0 = w.n_blk * BN;
+    w.kb0 = split * a.kb_per_split;
+    w.kb1 = min(a.k_blocks, w.kb0 + a.kb_per_split);
+    return w;
+}
+
+__device__ __forceinline__ float sq(float v) { return v * v; }
+
+// Sum of squares of the 8 bf16 values in a 16-byte vector.
+__device__ __forceinline__ float sumsq_bf16x8(uint4 v) {
+    return sq(bf16_lo(v.x)) + sq(bf16_hi(v.x)) + sq(bf16_lo(v.y)) + sq(bf16_hi(v.y)) +
+           sq(bf16_lo(v.z)) + sq(bf16_hi(v.z)) + sq(bf16_lo(v.w)) + sq(bf16_hi(v.w));
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+               const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *stages = smem;
+    uint8_t *staging = smem + C::kStages * C::kStageBytes;
+    uint8_t *ctrl = staging + C::kStagingBytes;
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(ctrl);
+    uint64_t *empty_bar = full_bar + C::kStages;
+    uint64_t *accf_bar = empty_bar + C::kStages;
+    uint64_t *acce_bar = accf_bar + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
+    float *rs = reinterpret_cast<float *>(ctrl + 1024);  // [2][128], forward W1 only
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kNormArrivals = C::kNorm ? 4u : 0u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1 + kNormArrivals);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf_bar[b], 1 + kNormArrivals);
+            mbar_init(&acce_bar[b], 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC0);
+        if (C::kNumOut == 2) prefetch_tensormap(&tmC1);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
+                const WorkUnit w = decode_unit<C::BN>(args, u);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) goto producer_done;
+                    uint8_t *sa = stages + stage * C::kStageBytes;
+                    uint8_t *sb = sa + C::kABytes;
+                    mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+                    const int k0 = kb * kBK;
+                    if (C::A_MN) {
+                        tma_load_2d(&tmA, &full_bar[stage], sa, w.m0, k0);
+                        tma_load_2d(&tmA, &full_bar[stage], sa + 8192, w.m0 + 64, k0);
+                    } else {
+                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, w.m0);
+                    }
+                    if (C::B_MN) {
+#pragma unroll
+                        for (int j = 0; j < C::BN / 64; ++j)
+                            tma_load_2d(&tmB, &full_bar[stage], sb + j * 8192, w.n0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d(&tmB, &full_bar[stage], sb, k0, w.n0);
+                    }
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        producer_done:;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+                const WorkUnit w = decode_unit<C::BN>(args, u);
+                const int buf = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
+                if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * C::BN;
+                bool failed = false;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = smem_u32(stages + stage * C::kStageBytes);
+                    const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                                    : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                                    : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty_bar[stage]);  // stage reusable once these MMAs finish
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (failed) break;
+                umma_commit(&accf_bar[buf]);  // accumulator ready for the epilogue
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;                // TMEM lane quarter of this warp
+        const int row_in_tile = 32 * q + lane;
+        int it = 0;
+        int sbuf = 0;
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+            const WorkUnit w = decode_unit<C::BN>(args, u);
+            const int buf = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            const bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after_sync();
+            const int row = w.m0 + row_in_tile;
+            const bool row_ok = row < args.M;
+            const bool warp_rows = (w.m0 + 32 * q) < args.M;
+            float rsc = 1.0f;
+            if (C::EPI == kEpiFwdW1) rsc = rs[buf * 128 + row_in_tile];
+            if (C::EPI == kEpiDgradH) rsc = row_ok ? args.rstd_in[row] : 0.0f;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
+
+#pragma unroll 1
+            for (int c = 0; c < C::kNumChunks; ++c) {
+                const int col0 = w.n0 + c * C::kChunkCols;
+                if (col0 >= args.N) break;
+                // operands read from global memory by the fused epilogues (issued
+                // first so their latency overlaps the TMEM load)
+                uint4 aux[8];
+                if (C::EPI == kEpiFwdW2 || C::EPI == kEpiDgradH) {
+                    const uint16_t *p = args.aux + static_cast<int64_t>(row) * args.ld_aux + col0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (row_ok && col0 + 8 * j < args.N) aux[j] = ld_global_nc_v4(p + 8 * j);
+                        else aux[j] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                float cs[32];
+                if (C::EPI == kEpiAccF32ColScale) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 g = make_uint4(0, 0, 0, 0);
+                        if (col0 + 8 * j < args.N) g = ld_global_nc_v4(args.colscale + col0 + 8 * j);
+                        cs[8 * j + 0] = bf16_lo(g.x); cs[8 * j + 1] = bf16_hi(g.x);
+                        cs[8 * j + 2] = bf16_lo(g.y); cs[8 * j + 3] = bf16_hi(g.y);
+                        cs[8 * j + 4] = bf16_lo(g.z); cs[8 * j + 5] = bf16_hi(g.z);
+                        cs[8 * j + 6] = bf16_lo(g.w); cs[8 * j + 7] = bf16_hi(g.w);
+                    }
+                }
+                float v0[32], v1[32];
+                if (C::kOutBf16) tmem_load_64cols(t_row + c * C::kChunkCols, v0, v1);
+                else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
+
+                // the staging buffers of two chunks ago must have been read by TMA
+                if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+                __syncwarp();
+                uint8_t *st0 = staging + ((q * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
+                uint8_t *st1 = staging + ((q * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
+                const uint32_t s0 = smem_u32(st0) + lane * 128;
+                const uint32_t s1 = smem_u32(st1) + lane * 128;
+                const uint32_t sw = static_cast<uint32_t>(lane & 7);
+
+                if (C::kOutBf16) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float e[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) e[i] = (j < 4) ? v0[8 * j + i] : v1[8 * (j - 4) + i];
+                        uint32_t o[4], o2[4];
+                        if (C::EPI == kEpiFwdW1) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float h0 = rsc * e[2 * i], h1 = rsc * e[2 * i + 1];
+                                o[i] = pack_bf16x2(h0, h1);
+                                const float r0 = h0 > 0.0f ? h0 : 0.0f, r1 = h1 > 0.0f ? h1 : 0.0f;
+                                o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                            }
+                        } else if (C::EPI == kEpiFwdW2) {
+                            const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                o[i] = pack_bf16x2(bf16_lo(xs[i]) + e[2 * i], bf16_hi(xs[i]) + e[2 * i + 1]);
+                        } else {  // kEpiDgradH
+                            const uint32_t hs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float g0 = bf16_lo(hs[i]), g1 = bf16_hi(hs[i]);
+                                const float d0 = g0 > 0.0f ? rsc * e[2 * i] * (2.0f * g0) : 0.0f;
+                                const float d1 = g1 > 0.0f ? rsc * e[2 * i + 1] * (2.0f * g1) : 0.0f;
+                                o[i] = pack_bf16x2(d0, d1);
+                            }
+                        }
+                        const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
+                        st_shared_v4(s0 + off, o[0], o[1], o[2], o[3]);
+                        if (C::kNumOut == 2) st_shared_v4(s1 + off, o2[0], o2[1], o2[2], o2[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float e[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            e[i] = v0[4 * j + i];
+                            if (C::EPI == kEpiAccF32ColScale) e[i] *= cs[4 * j + i];
+                        }
+                        const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
+                        st_shared_v4(s0 + off, __float_as_uint(e[0]), __float_as_uint(e[1]),
+                                     __float_as_uint(e[2]), __float_as_uint(e[3]));
+                    }
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp_rows) {
+                        const int r0 = w.m0 + 32 * q;
+                        if (C::kReduce) {
+                            tma_reduce_add_2d(&tmC0, st0, col0, r0);
+                        } else {
+                            tma_store_2d(&tmC0, st0, col0, r0);
+                            if (C::kNumOut == 2) tma_store_2d(&tmC1, st1, col0, r0);
+                        }
+                    }
+                    bulk_commit_group();
+                }
+                sbuf ^= 1;
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce_bar[buf]);  // TMEM buffer free again
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    } else if (C::kNorm) {
+        // ------------------------------------------- RMSNorm prologue (fwd W1)
+        const int r = 32 * (warp - 6) + lane;  // row of the tile
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
+            const WorkUnit w = decode_unit<C::BN>(args, u);
+            const int buf = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            float ss = 0.0f;
+            bool ok = true;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                ok = mbar_wait(&full_bar[stage], phase, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                const uint32_t rowaddr = smem_u32(stages + stage * C::kStageBytes) + r * 128;
+#pragma unroll
+                for (int cidx = 0; cidx < 8; ++cidx)
+                    ss += sumsq_bf16x8(ld_shared_v4(rowaddr + ((static_cast<uint32_t>(cidx) ^ sw) << 4)));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[stage]);
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ok = mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const float rstd = 1.0f / sqrtf(ss * args.inv_k + args.eps);
+            rs[buf * 128 + r] = rstd;
+            const int row = w.m0 + r;
+            if (w.n_blk == 0 && row < args.M) args.rstd_out[row] = rstd;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accf_bar[buf]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D tensor map of a row-major array [outer][inner] with 128-byte swizzle.
+inline bool make_map_2d(CUtensorMap *m, const void *ptr, bool f32, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const uint64_t esz = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * esz};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Builds the tensor maps and launches one GEMM of configuration C.
+template <class C>
+int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
+                GemmArgs a, int num_sms, cudaStream_t stream) {
+    CUtensorMap mA, mB, mC0, mC1;
+    bool ok = true;
+    ok &= C::A_MN ? make_map_2d(&mA, A, false, M, K, 64, 64) : make_map_2d(&mA, A, false, K, M, 64, kBM);
+    ok &= C::B_MN ? make_map_2d(&mB, B, false, N, K, 64, 64) : make_map_2d(&mB, B, false, K, N, 64, C::BN);
+    if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, false, N, M, 64, 32);
+    else ok &= make_map_2d(&mC0, C0, true, N, M, 32, 32);
+    if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, false, N, M, 64, 32);
+    else mC1 = mC0;
+    if (!ok) return MLPBLK_ECUDA;
+
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.m_tiles = (M + kBM - 1) / kBM;
+    a.n_tiles = (N + C::BN - 1) / C::BN;
+    a.k_blocks = (K + kBK - 1) / kBK;
+    const int tiles = a.m_tiles * a.n_tiles;
+    int splits = 1;
+    if (C::kReduce && tiles < num_sms) {
+        splits = num_sms / tiles;
+        if (splits > a.k_blocks) splits = a.k_blocks;
+        if (splits < 1) splits = 1;
+    }
+    a.kb_per_split = (a.k_blocks + splits - 1) / splits;
+    a.splits = (a.k_blocks + a.kb_per_split - 1) / a.kb_per_split;  // every split has work
+    a.num_units = tiles * a.splits;
+    if (a.group_m <= 0) a.group_m = 16;
+    const int grid = a.num_units < num_sms ? a.num_units : num_sms;
+
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return MLPBLK_ECUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return MLPBLK_ECUDA;
+        attr_set[dev] = 1;
+    }
+    gemm_tc_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, mC0, mC1, a);
+    return cudaGetLastError() == cudaSuccess ? MLPBLK_OK : MLPBLK_ECUDA;
+}
+
+// BN choice: 256 unless the N extent is small or BN=128 fills the SMs much better.
+inline int choose_bn(int M, int N, int num_sms) {
+    if (N <= 128) return 128;
+    const int mt = (M + kBM - 1) / kBM;
+    auto eff = [&](int bn) {
+        const int tiles = mt * ((N + bn - 1) / bn);
+        const int waves = (tiles + num_sms - 1) / num_sms;
+        // useful fraction of the SM-waves, with a mild preference for wide tiles
+        return static_cast<double>(tiles) / (static_cast<double>(waves) * num_sms) *
+               (bn == 256 ? 1.0 : 0.9) * (static_cast<double>(N) / (((N + bn - 1) / bn) * bn));
+    };
+    return eff(128) > eff(256) ? 128 : 256;
+}
+
+}  // namespace mlpblk

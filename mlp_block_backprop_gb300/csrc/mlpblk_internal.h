@@ -1,0 +1,94 @@
+// mlpblk_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mlpblk.h"
+
+namespace mlpblk {
+
+// A bounded device-side wait gives up after this long (two seconds).  Kernels of
+// this library run for milliseconds, so only a broken pipeline gets here.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Each translation unit that runs kernels with bounded waits has its own device
+// error word (internal linkage); mlpblk_last_error() collects all of them.
+static __device__ int g_device_error;
+
+// Epilogues of the tensor-core GEMM D[M,N] = sum_k A[m,k] B[n,k].
+enum Epilogue : int {
+    kEpiFwdW1 = 0,    // h = rstd*acc, a = relu(h)^2 (bf16 x2); rstd from A in-kernel
+    kEpiFwdW2 = 1,    // y = x + acc (bf16); x read from global
+    kEpiDgradH = 2,   // dh_s = rstd * acc * 2 relu(h) (bf16); h, rstd read from global
+    kEpiStoreF32 = 3, // out = acc (fp32)
+    kEpiAccF32 = 4,   // out += acc (fp32, TMA reduce-add)
+    kEpiAccF32ColScale = 5,  // out += colscale[n] * acc (fp32, TMA reduce-add)
+};
+
+// Arguments of one GEMM launch (the tensor maps travel separately).
+struct GemmArgs {
+    int M, N, K;
+    int m_tiles, n_tiles, k_blocks;
+    int splits, kb_per_split;
+    int num_units;             // m_tiles * n_tiles * splits
+    int group_m;               // raster: this many M tiles sweep N together
+    const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
+    int ld_aux;
+    const float *rstd_in;      // DgradH: per-row rstd
+    float *rstd_out;           // FwdW1: per-row rstd written by the n-tile-0 CTAs
+    const uint16_t *colscale;  // AccF32ColScale: bf16 per-column scale (gamma)
+    float inv_k;               // FwdW1: 1/d
+    float eps;                 // FwdW1: RMSNorm epsilon
+};
+
+// Operand / output views handed to the GEMM launcher (row-major 2-D tensors).
+struct Mat {
+    const void *ptr;
+    int64_t rows, cols;  // logical shape of the stored array
+};
+
+// Host: launch one tensor-core GEMM.  A is [M,K] (K-major: stored [M][K]) or
+// MN-major (stored [K][M]); B likewise with N.  Returns an MLPBLK_* code.
+int launch_gemm_tc(int epi, bool a_mn, bool b_mn, int M, int N, int K,
+                   const void *A, const void *B, void *C0, void *C1, const GemmArgs &extra,
+                   int num_sms, cudaStream_t stream);
+int take_device_error_gemm();
+
+// Host: row/element kernels (rowops.cu).  All return MLPBLK_* codes.
+int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, int64_t F,
+                      int64_t d, cudaStream_t s);
+int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps,
+                    cudaStream_t s);
+int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
+                       const float *rstd, const void *gamma, void *dx, float *dgamma_part,
+                       int64_t T, int64_t d, int parts, cudaStream_t s);
+int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
+                           cudaStream_t s);
+int launch_fill_zero(float *p, int64_t n, cudaStream_t s);
+int launch_scale(float *p, int64_t n, float sc, cudaStream_t s);
+
+// Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
+// A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].
+struct SimtEpi {
+    const float *aux;       // FwdW2: x;  DgradH: h   (row-major [M][N])
+    const float *rstd;      // FwdW1, DgradH
+    const float *colscale;  // AccF32ColScale
+};
+int launch_gemm_simt(int epi, int M, int N, int K, const float *A, int64_t sam, int64_t sak,
+                     const float *B, int64_t sbn, int64_t sbk, float *C0, float *C1,
+                     const SimtEpi &e, cudaStream_t s);
+
+// Norm-backward partial count for T rows (fixed, device independent).
+inline int norm_bwd_parts(int64_t T) {
+    int64_t p = (T + 15) / 16;
+    if (p > 512) p = 512;
+    if (p < 1) p = 1;
+    return static_cast<int>(p);
+}
+
+constexpr int64_t kMaxNormD = 4096;  // RMSNorm backward keeps a row's dgamma share in registers
+
+}  // namespace mlpblk

@@ -1,0 +1,108 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports every
+entry point include/mlpblk.h declares, and rejects bad arguments before it
+enqueues anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mb():
+    from mlp_block_backprop_gb300.build import build_library
+    build_library()
+    import mlp_block_backprop_gb300
+    return mlp_block_backprop_gb300
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mlpblk_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(mb):
+    declared = _declared()
+    assert {"mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads"} <= declared
+    lib = ctypes.CDLL(mb.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert set(mb.EXPORTED) <= declared
+
+
+def test_version_and_strerror(mb):
+    assert mb.mlpblk_version() >= 100
+    for code in range(0, 7):
+        assert mb.strerror(code)
+    assert "unknown" in mb.strerror(99)
+
+
+def test_workspace_size(mb):
+    d = mb.make_desc(8192, 768, 3072)
+    ws = mb.mlpblk_workspace_size(d)
+    # backward scratch: dh (bf16 T x F), dn (fp32 T x d), dgamma partials
+    assert ws >= 8192 * 3072 * 2 + 8192 * 768 * 4
+    assert ws % 256 == 0
+    assert mb.mlpblk_workspace_size(mb.make_desc(8, 100, 64)) == 0       # d not a multiple of 8
+    assert mb.mlpblk_workspace_size(mb.make_desc(-1, 64, 64)) == 0
+    assert mb.mlpblk_workspace_size(mb.make_desc(8, 64, 64, dtype=7)) == 0
+    assert mb.mlpblk_workspace_size(mb.make_desc(8, 64, 64, eps=float("nan"))) == 0
+    assert mb.mlpblk_workspace_size(mb.make_desc(8, 8192, 64)) == 0      # beyond the norm kernel's width
+    assert mb.mlpblk_workspace_size(mb.make_desc(1 << 20, 4096, 4096)) == 0  # index range
+
+
+def _fwd(mb, desc, ptrs, ws_bytes=1 << 40):
+    return mb.lib.mlpblk_forward(ctypes.byref(desc), *ptrs, ws_bytes, None)
+
+
+def test_forward_argument_errors_need_no_device(mb):
+    good = [0x10000 * (i + 1) for i in range(9)]  # aligned, never dereferenced
+    d = mb.make_desc(64, 128, 256)
+    bad_null = list(good)
+    bad_null[0] = None
+    assert _fwd(mb, d, bad_null) == mb.MLPBLK_EINVAL
+    bad_align = list(good)
+    bad_align[3] += 8
+    assert _fwd(mb, d, bad_align) == mb.MLPBLK_EINVAL
+    alias = list(good)
+    alias[4] = alias[0]  # y == x
+    assert _fwd(mb, d, alias) == mb.MLPBLK_EINVAL
+    assert _fwd(mb, d, good, ws_bytes=16) == mb.MLPBLK_EWORKSPACE
+    assert _fwd(mb, mb.make_desc(64, 100, 256), good) == mb.MLPBLK_ENOTSUP
+    assert _fwd(mb, mb.make_desc(64, 128, 256, dtype=3), good) == mb.MLPBLK_ENOTSUP
+    assert _fwd(mb, mb.make_desc(64, 128, 256, eps=-1.0), good) == mb.MLPBLK_EINVAL
+    assert mb.lib.mlpblk_forward(None, *good, 1 << 40, None) == mb.MLPBLK_EINVAL
+    # an empty microbatch is valid and does nothing, whatever the pointers
+    assert _fwd(mb, mb.make_desc(0, 128, 256), [None] * 9) == mb.MLPBLK_OK
+
+
+def test_backward_and_grad_argument_errors_need_no_device(mb):
+    good = [0x10000 * (i + 1) for i in range(13)]
+    d = mb.make_desc(64, 128, 256)
+    args = list(good)
+    args[9] = args[9] + 4  # dgamma misaligned
+    assert mb.lib.mlpblk_backward(ctypes.byref(d), *args, 1 << 40, None) == mb.MLPBLK_EINVAL
+    args = list(good)
+    args[8] = args[0]  # dx == dy
+    assert mb.lib.mlpblk_backward(ctypes.byref(d), *args, 1 << 40, None) == mb.MLPBLK_EINVAL
+    assert mb.lib.mlpblk_backward(ctypes.byref(d), *good, 0, None) == mb.MLPBLK_EWORKSPACE
+    assert mb.lib.mlpblk_backward(ctypes.byref(mb.make_desc(0, 128, 256)), *([None] * 13), 0,
+                                  None) == mb.MLPBLK_OK
+    assert mb.lib.mlpblk_zero_grads(ctypes.byref(d), None, 0x10000, 0x20000, None) == mb.MLPBLK_EINVAL
+    assert mb.lib.mlpblk_scale_grads(ctypes.byref(d), 0x10000, 0x20000, 0x30000, float("inf"),
+                                     None) == mb.MLPBLK_EINVAL
+
+
+def test_grad_buffers_are_float32_by_contract():
+    """The gradient accumulators are declared float32: the bf16 loss of a small
+    contribution next to a large running sum is why."""
+    src = open(os.path.join(ROOT, "include", "mlpblk.h")).read()
+    assert re.search(r"float\s*\*dgamma,\s*float\s*\*dw1,\s*float\s*\*dw2", src)
