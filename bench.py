@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Forward + backward of the pre-norm residual ReLU² MLP block on GB300.
+
+One step = the whole hot path over one batch of synthetic input: zero_grads,
+then forward and backward of every microbatch (fp32 += gradient accumulation),
+then scale_grads where the workload has one.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the float64 oracle on the host cores on a bounded token
+sample of the same workload (the only other place this script runs the oracle
+is the cpu_baseline leg).  Under torchrun each rank runs an independent replica
+(the block has no cross-rank step in this build); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "fwd+bwd block TFLOP/s & tokens/s at 1 GB300; % of BF16 tensor peak / HBM BW"
+DEFAULT_WORKLOAD = "large_accum2"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+GEMM_KINDS = ("gemm_fwd_w1", "gemm_fwd_w2", "gemm_dgrad_h", "gemm_wgrad_w2", "gemm_dgrad_n",
+              "gemm_wgrad_w1")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ----------------------------------------------------------------- distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 7:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        power = [num(r[2]) or 0.0 for r in rows]
+        pmax = max(power) if power else 0.0
+        loaded = [num(r[0]) for r, p in zip(rows, power) if p >= 0.5 * pmax and num(r[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": num(rows[0][1]),
+                "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------- our arm
+
+def csrc_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "mlp_block_backprop_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (profiles/traffic.md: 'traffic <kernel> <workload>
+    <bytes> csrc=<hash>')."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    cur = csrc_hash()
+    for line in open(path):
+        f = line.split()
+        if len(f) == 5 and f[0] == "traffic" and f[1] == kernel and f[2] == workload:
+            if f[4] == f"csrc={cur}":
+                return float(f[3])
+    return None
+
+
+def algorithmic_work(kind, T, d, F, parts):
+    """(amount, unit) per launch: FLOP for the GEMMs, bytes for the HBM-bound kernels."""
+    if kind in GEMM_KINDS:
+        return 2.0 * T * d * F, "flop"
+    if kind == "norm_bwd":
+        # x, dy (bf16) and dn (fp32) read, dx (bf16) written, rstd read, partials written
+        return T * d * (2 + 2 + 4 + 2) + 4.0 * T + 4.0 * parts * d + 2.0 * d, "byte"
+    if kind == "fold_gamma":
+        return 2.0 * F * d * 2 + 2.0 * d, "byte"
+    if kind == "zero_grads":
+        return 4.0 * (2 * F * d + d) / 3.0, "byte"
+    if kind == "scale_grads":
+        return 8.0 * (2 * F * d + d) / 3.0, "byte"
+    if kind == "dgamma_reduce":
+        return 4.0 * parts * d + 8.0 * d, "byte"
+    return None, None
+
+
+def run_ours(args, dist, peaks):
+    import torch
+
+    import mlp_block_backprop_gb300 as mb
+
+    torch.cuda.set_device(dist.local_rank)
+    inp = synth.config_inputs(args.workload)
+    T, d, F, n_mb = inp.tokens, inp.d, inp.ffn, inp.n_mb
+    dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+    dev = "cuda"
+    to = lambda a: torch.from_numpy(a).to(dev).to(dt)
+    bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps)
+    bb.gamma.copy_(to(inp.gamma))
+    bb.w1.copy_(to(inp.w1))
+    bb.w2.copy_(to(inp.w2))
+    xs = [to(x) for x in inp.x]
+    dys = [to(g) for g in inp.dy]
+    desc = bb.desc
+
+    def step(x_list, dy_list, dx_out=None, host_x=None, host_dy=None):
+        mb.mlpblk_zero_grads(desc, bb.dgamma, bb.dw1, bb.dw2)
+        for i in range(n_mb):
+            if host_x is not None:
+                x_list[i].copy_(host_x[i], non_blocking=True)
+                dy_list[i].copy_(host_dy[i], non_blocking=True)
+            mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
+            mb.mlpblk_backward(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a, bb.rstd,
+                               bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+            if dx_out is not None:
+                dx_out[i].copy_(bb.dx, non_blocking=True)
+        if inp.grad_scale is not None:
+            mb.mlpblk_scale_grads(desc, bb.dgamma, bb.dw1, bb.dw2, inp.grad_scale)
+
+    for _ in range(args.warmup):
+        step(xs, dys)
+    torch.cuda.synchronize()
+    if mb.mlpblk_last_error() != mb.MLPBLK_OK:
+        raise RuntimeError("device error during warm-up")
+
+    launches_per_step = 3 + n_mb * 9 + (3 if inp.grad_scale is not None else 0)
+    trace = mb.KernelTrace(args.steps * launches_per_step + 8)
+    clocks = ClockSampler(dist.local_rank)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with trace:
+        start.record()
+        for _ in range(args.steps):
+            step(xs, dys)
+        end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    ms_total = dist.max(start.elapsed_time(end))
+    if mb.mlpblk_last_error() != mb.MLPBLK_OK:
+        raise RuntimeError("device error in the timed region")
+    ms_step = ms_total / args.steps
+    flop_step = synth.block_flops(T, d, F, n_mb)
+    value = dist.world * flop_step / (ms_step * 1e-3) / 1e12
+    tokens_s = dist.world * T * n_mb / (ms_step * 1e-3)
+
+    # per-kernel breakdown from the trace (CUDA events on the launch stream)
+    per = {}
+    for kind, ms in trace.durations():
+        e = per.setdefault(kind, [0, 0.0])
+        e[0] += 1
+        e[1] += ms
+    total_k = sum(v[1] for v in per.values())
+    kernels = {k: {"launches": v[0], "total_ms": round(v[1], 4), "mean_us": round(1e3 * v[1] / v[0], 2),
+                   "share": round(v[1] / total_k, 4)} for k, v in sorted(per.items(), key=lambda kv: -kv[1][1])}
+    import ctypes  # noqa: F401
+    parts = min(max(1, (T + 15) // 16), 512, 2 * torch.cuda.get_device_properties(0).multi_processor_count)
+
+    def roofline(kind):
+        if kind not in per:
+            return None
+        amount, unit = algorithmic_work(kind, T, d, F, parts)
+        mean_s = per[kind][1] / per[kind][0] * 1e-3
+        traffic = recorded_traffic(args.workload, kind)
+        if unit == "flop":
+            peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+            ach = amount / mean_s / 1e12
+            return {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
+                    "algorithmic_per_launch": amount, "peak_source": f"{peaks['source']} sustained bf16",
+                    "mean_launch_us": round(mean_s * 1e6, 2)}
+        peak = peaks["hbm_gbs"]
+        ach = amount / mean_s / 1e9
+        return {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": traffic, "algorithmic_per_launch": amount,
+                "peak_source": f"{peaks['source']} copy bandwidth", "mean_launch_us": round(mean_s * 1e6, 2)}
+
+    dominant = max(per, key=lambda k: per[k][1])
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype,
+        "data": "synthetic (seeded numpy normals, bf16-rounded; no dataset)",
+        "config": {"workload": args.workload, "tokens_per_microbatch": T, "microbatches": n_mb,
+                   "d_model": d, "ffn": F, "shape": synth.CONFIGS[args.workload]["shape"],
+                   "flop_per_step": flop_step,
+                   "l2": "inputs larger than L2 (working set %.1f GB per replica)" % (
+                       (bb.ws.numel() + sum(t.numel() * t.element_size() for t in
+                        [bb.w1, bb.w2, bb.h, bb.a, bb.dw1, bb.dw2] + xs + dys)) / 1e9),
+                   "parallelism": "replicas" if dist.world > 1 else "single"},
+        "tokens_per_s": round(tokens_s, 1),
+        "frac_of_peak": {"sustained": round(value / dist.world / peaks.get("bf16_tflops_sustained", 1.0), 4),
+                         "burst": round(value / dist.world / peaks.get("bf16_tflops", 1.0), 4)},
+        "roofline": roofline(dominant),
+        "roofline_hbm": roofline("norm_bwd"),
+        "kernels": kernels,
+        "gpu_launches": trace.count,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        k_e2e = max(3, min(args.steps, 20))
+        hx = [torch.from_numpy(x).to(dt).pin_memory() for x in inp.x]
+        hdy = [torch.from_numpy(g).to(dt).pin_memory() for g in inp.dy]
+        hdx = [torch.empty(T, d, dtype=dt).pin_memory() for _ in range(n_mb)]
+        bx = [torch.empty_like(x) for x in xs]
+        bdy = [torch.empty_like(g) for g in dys]
+        step(bx, bdy, hdx, hx, hdy)
+        torch.cuda.synchronize()
+        dist.barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        s2.record()
+        for _ in range(k_e2e):
+            step(bx, bdy, hdx, hx, hdy)
+        e2.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        dist.barrier()
+        ms_e2e = dist.max(max(s2.elapsed_time(e2), wall * 1e3)) / k_e2e
+        elt = 2 if inp.dtype == "bf16" else 4
+        result["e2e"] = {"value": round(dist.world * flop_step / (ms_e2e * 1e-3) / 1e12, 2),
+                         "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4), "steps": k_e2e,
+                         "h2d_bytes_per_step": n_mb * 2 * T * d * elt,
+                         "d2h_bytes_per_step": n_mb * T * d * elt,
+                         "path": "pinned host x, dy -> device; mlpblk_forward/backward; dx -> pinned host"}
+    return result, inp
+
+
+# --------------------------------------------------------- oracle on the host
+
+def oracle_sample(inp, tokens, steps=1):
+    """Times the float64 oracle on the first `tokens` tokens of every microbatch
+    (all weights, all gradient buffers).  Returns seconds per step."""
+    import oracle
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        grads = oracle.new_grads(inp.d, inp.ffn)
+        for x, dy in zip(inp.x, inp.dy):
+            xs, dys = x[:tokens], dy[:tokens]
+            y, h, a, r = oracle.forward(xs, inp.gamma, inp.w1, inp.w2, inp.eps)
+            oracle.backward(dys, xs, inp.gamma, inp.w1, inp.w2, h, r, grads)
+        if inp.grad_scale is not None:
+            oracle.scale_grads(grads, inp.grad_scale)
+    return (time.perf_counter() - t0) / steps
+
+
+def host_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def calibrate_tokens(inp, target_s, lo=8):
+    n = min(lo, inp.tokens)
+    t = oracle_sample(inp, n)
+    while t < target_s / 4 and n < inp.tokens:
+        n = min(inp.tokens, n * 4)
+        t = oracle_sample(inp, n)
+    # cost ~ fixed + per-token; extrapolate linearly from the last measurement
+    want = int(n * target_s / max(t, 1e-6))
+    return max(lo, min(inp.tokens, want))
+
+
+def cpu_baseline(inp, target_s=15.0):
+    tok = calibrate_tokens(inp, target_s)
+    sec = oracle_sample(inp, tok)
+    flop = synth.block_flops(tok, inp.d, inp.ffn, inp.n_mb)
+    return {"value": round(flop / sec / 1e12, 6), "unit": "TFLOP/s", "cores": host_threads(),
+            "kind": "oracle", "seconds": round(sec, 3),
+            "sample": f"first {tok} tokens of each of the {inp.n_mb} microbatch(es), all weights "
+                      f"(float64 numpy, block FLOP of the sample / wall time)",
+            "tokens_per_s": round(tok * inp.n_mb / sec, 2)}
+
+
+def run_reference(args, dist):
+    inp = synth.config_inputs(args.workload)
+    budget = 120.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    tok = calibrate_tokens(inp, per_step)
+    for _ in range(args.warmup):
+        oracle_sample(inp, tok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(inp, tok)
+    sec = (time.perf_counter() - t0) / args.steps
+    flop = synth.block_flops(tok, inp.d, inp.ffn, inp.n_mb)
+    value = flop / sec / 1e12
+    sample = (f"first {tok} tokens of each of the {inp.n_mb} microbatch(es) per step, all weights "
+              f"(float64 numpy oracle on the host)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy normals)",
+            "config": {"workload": args.workload, "tokens_per_microbatch_sampled": tok,
+                       "microbatches": inp.n_mb, "d_model": inp.d, "ffn": inp.ffn},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # host-only arm: rank 0 runs it, the other ranks have nothing to do
+        if int(os.environ.get("RANK", "0")) == 0:
+            class _Solo:
+                world = int(os.environ.get("WORLD_SIZE", "1"))
+            print(json.dumps(run_reference(args, _Solo())), flush=True)
+        return
+    dist = Dist()
+    peaks = load_peaks()
+    result, inp = run_ours(args, dist, peaks)
+    if dist.rank == 0:
+        if dist.world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(inp)
+        print(json.dumps(result), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -140,6 +140,41 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
  */
 int mlpblk_last_error(void);
 
+/*
+ * Kernel timing hook for profiling harnesses (CUDA events, no profiler needed).
+ * Kinds reported for each kernel launch the library makes:
+ */
+#define MLPBLK_KERNEL_FOLD_GAMMA      1  /* W1g = W1 * gamma (forward)               */
+#define MLPBLK_KERNEL_GEMM_FWD_W1     2  /* h, a = RMSNorm(x) . W1^T, relu^2         */
+#define MLPBLK_KERNEL_GEMM_FWD_W2     3  /* y = x + a . W2^T                          */
+#define MLPBLK_KERNEL_GEMM_DGRAD_H    4  /* dh = (dy . W2) * 2 relu(h)                */
+#define MLPBLK_KERNEL_GEMM_WGRAD_W2   5  /* dW2 += dy^T . a                           */
+#define MLPBLK_KERNEL_GEMM_DGRAD_N    6  /* dn = dh . W1                              */
+#define MLPBLK_KERNEL_GEMM_WGRAD_W1   7  /* dW1 += dh^T . n                           */
+#define MLPBLK_KERNEL_NORM_BWD        8  /* RMSNorm backward + residual, dgamma parts */
+#define MLPBLK_KERNEL_DGAMMA_REDUCE   9  /* dgamma += sum of parts                    */
+#define MLPBLK_KERNEL_ZERO_GRADS     10
+#define MLPBLK_KERNEL_SCALE_GRADS    11
+#define MLPBLK_KERNEL_RSTD           12  /* fp32 element type only                    */
+
+/*
+ * mlpblk_trace_begin: from now on, launch i of this library records
+ * events[2i] on its stream just before the kernel and events[2i+1] just after
+ * it, and stores its MLPBLK_KERNEL_* kind in kinds[i], for i < capacity; later
+ * launches are not recorded.  events (2*capacity cudaEvent_t handles created by
+ * the caller) and kinds (capacity ints, host memory) stay owned by the caller
+ * and must outlive the trace.  One trace at a time per process; not
+ * thread-safe.  Returns MLPBLK_EINVAL for NULL arrays or capacity < 1.
+ * mlpblk_trace_end: stops recording and returns how many launches were
+ * recorded (may exceed capacity: the launches beyond it were only counted).
+ */
+int mlpblk_trace_begin(void **events, int *kinds, int capacity);
+int mlpblk_trace_end(void);
+
+/* The CUDA runtime's message for the most recent failing CUDA call made inside
+ * the library (behind an MLPBLK_ECUDA), or "no CUDA error recorded". */
+const char *mlpblk_cuda_error_string(void);
+
 /* Static, NUL-terminated description of an MLPBLK_* code. */
 const char *mlpblk_strerror(int code);
 

@@ -27,13 +27,21 @@ MLPBLK_BF16 = 1
 MLPBLK_FP32 = 2
 
 EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads",
-            "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version")
+            "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version",
+            "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string")
+
+KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dgrad_h",
+                5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
+                9: "dgamma_reduce", 10: "zero_grads", 11: "scale_grads", 12: "rstd"}
 
 
 class MlpBlkError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
-        super().__init__(f"{where}: status {code} ({strerror(code)})")
+        extra = ""
+        if code == MLPBLK_ECUDA:
+            extra = "; CUDA: " + lib.mlpblk_cuda_error_string().decode()
+        super().__init__(f"{where}: status {code} ({strerror(code)}{extra})")
 
 
 class Desc(ctypes.Structure):
@@ -65,6 +73,12 @@ def _load():
     lib.mlpblk_strerror.restype = ctypes.c_char_p
     lib.mlpblk_version.argtypes = []
     lib.mlpblk_version.restype = i32
+    lib.mlpblk_trace_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int), i32]
+    lib.mlpblk_trace_begin.restype = i32
+    lib.mlpblk_cuda_error_string.argtypes = []
+    lib.mlpblk_cuda_error_string.restype = ctypes.c_char_p
+    lib.mlpblk_trace_end.argtypes = []
+    lib.mlpblk_trace_end.restype = i32
     return lib
 
 
@@ -140,6 +154,38 @@ def mlpblk_last_error() -> int:
 
 def mlpblk_version() -> int:
     return int(lib.mlpblk_version())
+
+
+class KernelTrace:
+    """Records CUDA events around every kernel the library launches while active
+    (mlpblk_trace_begin/end); durations() then gives (kind name, ms) per launch."""
+
+    def __init__(self, capacity):
+        import torch
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:  # torch creates the CUDA event on its first record
+            e.record()
+        torch.cuda.synchronize()
+        if any(not e.cuda_event for e in self.events):
+            raise RuntimeError("torch did not create the CUDA events for the kernel trace")
+        self._handles = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self._kinds = (ctypes.c_int * capacity)()
+        self.count = 0
+
+    def __enter__(self):
+        _check(lib.mlpblk_trace_begin(self._handles, self._kinds, self.capacity), "mlpblk_trace_begin")
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(lib.mlpblk_trace_end())
+        return False
+
+    def durations(self):
+        """[(kind name, milliseconds)] of the recorded launches (call after a sync)."""
+        n = min(self.count, self.capacity)
+        return [(KERNEL_NAMES.get(self._kinds[i], str(self._kinds[i])),
+                 self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(n)]
 
 
 class BlockBuffers:

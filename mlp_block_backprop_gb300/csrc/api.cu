@@ -22,6 +22,10 @@ int take_device_error_gemm_fwd();
 int take_device_error_gemm_bwd();
 }  // namespace mlpblk
 
+namespace mlpblk {
+int g_last_cuda_error = 0;
+}  // namespace mlpblk
+
 using namespace mlpblk;
 
 namespace {
@@ -67,7 +71,7 @@ WsLayout ws_layout(const mlpblk_desc *d) {
 int device_sms(int *sms) {
     static int cached[64] = {0};  // 0 unknown, -1 unsupported, else SM count
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
+    if (cuda_status(cudaGetDevice(&dev)) != MLPBLK_OK || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
     if (cached[dev] == 0) {
         int major = 0, minor = 0, n = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -86,6 +90,32 @@ int device_sms(int *sms) {
         const int rc_ = (expr);       \
         if (rc_ != MLPBLK_OK) return rc_; \
     } while (0)
+
+// Launch trace (mlpblk_trace_begin/end): caller-owned events around each launch.
+struct Trace {
+    cudaEvent_t *events = nullptr;
+    int *kinds = nullptr;
+    int capacity = 0;
+    int count = 0;
+    bool on = false;
+} g_trace;
+
+// Runs one launcher, bracketed by the trace events when a trace is active.
+template <class F>
+int traced(int kind, cudaStream_t s, F &&launch) {
+    if (!g_trace.on) return launch();
+    const int i = g_trace.count++;
+    const bool rec = i < g_trace.capacity;
+    if (rec) {
+        g_trace.kinds[i] = kind;
+        MLPBLK_TRY(cuda_status(cudaEventRecord(g_trace.events[2 * i], s)));
+    }
+    MLPBLK_TRY(launch());
+    if (rec) MLPBLK_TRY(cuda_status(cudaEventRecord(g_trace.events[2 * i + 1], s)));
+    return MLPBLK_OK;
+}
+
+#define MLPBLK_LAUNCH(kind, stream, call) MLPBLK_TRY(traced(kind, stream, [&]() { return (call); }))
 
 int norm_parts(int64_t T, int sms) {
     int p = norm_bwd_parts(T);
@@ -136,26 +166,26 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *w1g = ws + l.w1g;
 
-    MLPBLK_TRY(launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s, launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
     if (desc->dtype == MLPBLK_BF16) {
         GemmArgs g1 = {};
         g1.rstd_out = rstd_saved;
         g1.inv_k = 1.0f / static_cast<float>(d);
         g1.eps = desc->eps;
-        MLPBLK_TRY(launch_gemm_tc_fwd(kEpiFwdW1, (int)T, (int)F, (int)d, x, w1g, h_saved, a_saved, g1, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_tc_fwd(kEpiFwdW1, (int)T, (int)F, (int)d, x, w1g, h_saved, a_saved, g1, sms, s));
         GemmArgs g2 = {};
         g2.aux = static_cast<const uint16_t *>(x);
         g2.ld_aux = (int)d;
-        MLPBLK_TRY(launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
     } else {
         const float *xf = static_cast<const float *>(x);
-        MLPBLK_TRY(launch_rstd_f32(xf, rstd_saved, T, d, desc->eps, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_RSTD, s, launch_rstd_f32(xf, rstd_saved, T, d, desc->eps, s));
         SimtEpi e1 = {nullptr, rstd_saved, nullptr};
-        MLPBLK_TRY(launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, xf, d, 1,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, xf, d, 1,
                                     static_cast<const float *>(w1g), d, 1,
                                     static_cast<float *>(h_saved), static_cast<float *>(a_saved), e1, s));
         SimtEpi e2 = {xf, nullptr, nullptr};
-        MLPBLK_TRY(launch_gemm_simt(kEpiFwdW2, (int)T, (int)d, (int)F,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_simt(kEpiFwdW2, (int)T, (int)d, (int)F,
                                     static_cast<const float *>(a_saved), F, 1,
                                     static_cast<const float *>(w2), F, 1, static_cast<float *>(y),
                                     nullptr, e2, s));
@@ -191,33 +221,33 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
         gd.aux = static_cast<const uint16_t *>(h_saved);
         gd.ld_aux = (int)F;
         gd.rstd_in = rstd_saved;
-        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
         GemmArgs gw2 = {};
-        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
         GemmArgs gn = {};
-        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);
-        MLPBLK_TRY(launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
     } else {
         const float *dyf = static_cast<const float *>(dy);
         const float *xf = static_cast<const float *>(x);
         const float *dhf = static_cast<const float *>(dh_s);
         SimtEpi ed = {static_cast<const float *>(h_saved), rstd_saved, nullptr};
-        MLPBLK_TRY(launch_gemm_simt(kEpiDgradH, (int)T, (int)F, (int)d, dyf, d, 1,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_simt(kEpiDgradH, (int)T, (int)F, (int)d, dyf, d, 1,
                                     static_cast<const float *>(w2), 1, F, static_cast<float *>(dh_s),
                                     nullptr, ed, s));
         SimtEpi e0 = {nullptr, nullptr, nullptr};
-        MLPBLK_TRY(launch_gemm_simt(kEpiAccF32, (int)d, (int)F, (int)T, dyf, 1, d,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_simt(kEpiAccF32, (int)d, (int)F, (int)T, dyf, 1, d,
                                     static_cast<const float *>(a_saved), 1, F, dw2, nullptr, e0, s));
-        MLPBLK_TRY(launch_gemm_simt(kEpiStoreF32, (int)T, (int)d, (int)F, dhf, F, 1,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_simt(kEpiStoreF32, (int)T, (int)d, (int)F, dhf, F, 1,
                                     static_cast<const float *>(w1), 1, d, dn_s, nullptr, e0, s));
         SimtEpi ec = {nullptr, nullptr, static_cast<const float *>(gamma)};
-        MLPBLK_TRY(launch_gemm_simt(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dhf, 1, F, xf, 1, d,
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_simt(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dhf, 1, F, xf, 1, d,
                                     dw1, nullptr, ec, s));
     }
-    MLPBLK_TRY(launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, parts, s));
-    MLPBLK_TRY(launch_dgamma_finalize(part, parts, dgamma, d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
 }
 
@@ -226,9 +256,9 @@ int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float 
     if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t d = desc->d_model, F = desc->ffn;
-    MLPBLK_TRY(launch_fill_zero(dgamma, d, s));
-    MLPBLK_TRY(launch_fill_zero(dw1, F * d, s));
-    MLPBLK_TRY(launch_fill_zero(dw2, F * d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dgamma, d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dw1, F * d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dw2, F * d, s));
     return MLPBLK_OK;
 }
 
@@ -239,14 +269,34 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
     if (!isfinite(sc)) return MLPBLK_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t d = desc->d_model, F = desc->ffn;
-    MLPBLK_TRY(launch_scale(dgamma, d, sc, s));
-    MLPBLK_TRY(launch_scale(dw1, F * d, sc, s));
-    MLPBLK_TRY(launch_scale(dw2, F * d, sc, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dgamma, d, sc, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dw1, F * d, sc, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dw2, F * d, sc, s));
     return MLPBLK_OK;
 }
 
+int mlpblk_trace_begin(void **events, int *kinds, int capacity) {
+    if (!events || !kinds || capacity < 1) return MLPBLK_EINVAL;
+    g_trace.events = reinterpret_cast<cudaEvent_t *>(events);
+    g_trace.kinds = kinds;
+    g_trace.capacity = capacity;
+    g_trace.count = 0;
+    g_trace.on = true;
+    return MLPBLK_OK;
+}
+
+int mlpblk_trace_end(void) {
+    g_trace.on = false;
+    return g_trace.count;
+}
+
+const char *mlpblk_cuda_error_string(void) {
+    if (g_last_cuda_error == 0) return "no CUDA error recorded";
+    return cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda_error));
+}
+
 int mlpblk_last_error(void) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return MLPBLK_ECUDA;
+    if (cuda_status(cudaDeviceSynchronize()) != MLPBLK_OK) return MLPBLK_ECUDA;
     const int a = take_device_error_gemm_fwd();
     const int b = take_device_error_gemm_bwd();
     return a != MLPBLK_OK ? a : b;

@@ -471,13 +471,13 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return MLPBLK_ECUDA;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
-            return MLPBLK_ECUDA;
+        const int rc = cuda_status(cudaFuncSetAttribute(
+            gemm_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+        if (rc != MLPBLK_OK) return rc;
         attr_set[dev] = 1;
     }
     gemm_tc_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, mC0, mC1, a);
-    return cudaGetLastError() == cudaSuccess ? MLPBLK_OK : MLPBLK_ECUDA;
+    return launch_status();
 }
 
 // BN choice: 256 unless the N extent is small or BN=128 fills the SMs much better.

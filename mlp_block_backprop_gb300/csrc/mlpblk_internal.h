@@ -14,6 +14,20 @@ namespace mlpblk {
 // this library run for milliseconds, so only a broken pipeline gets here.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Host: the most recent failing CUDA runtime status seen by the library
+// (reported by mlpblk_cuda_error_string).
+extern int g_last_cuda_error;
+
+// Host: MLPBLK_OK if `e` is cudaSuccess, else records it and returns MLPBLK_ECUDA.
+inline int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MLPBLK_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return MLPBLK_ECUDA;
+}
+
+// Host: status of the kernel launch just made.
+inline int launch_status() { return cuda_status(cudaGetLastError()); }
+
 // Each translation unit that runs kernels with bounded waits has its own device
 // error word (internal linkage); mlpblk_last_error() collects all of them.
 static __device__ int g_device_error;

@@ -237,7 +237,7 @@ int grid_for(int64_t work_items, int threads) {
     return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
-int status() { return cudaGetLastError() == cudaSuccess ? MLPBLK_OK : MLPBLK_ECUDA; }
+int status() { return launch_status(); }
 
 template <class E, int NCH>
 int run_norm_bwd(const void *x, const float *dn_s, const void *dy, const float *rstd,

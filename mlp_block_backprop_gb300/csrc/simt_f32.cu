@@ -97,7 +97,7 @@ int launch_gemm_simt(int epi, int M, int N, int K, const float *A, int64_t sam, 
 #undef MLPBLK_SIMT
         default: return MLPBLK_EINVAL;
     }
-    return cudaGetLastError() == cudaSuccess ? MLPBLK_OK : MLPBLK_ECUDA;
+    return launch_status();
 }
 
 }  // namespace mlpblk

@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def mb():
-    from mlp_block_backprop_gb300.build import build_library
-    build_library()
+    import __graft_entry__
+    __graft_entry__.build()
     import mlp_block_backprop_gb300
     return mlp_block_backprop_gb300
 

@@ -42,7 +42,8 @@ def test_small_bf16_accum4_config():
 @pytest.mark.parametrize("shape", [
     (333, 200, 328),    # ragged in every GEMM dimension, several tiles
     (129, 64, 264),     # one row past a tile; K below one stage in the W1 GEMM
-    (1, 8, 8),          # smallest sizes
+    (1, 256, 512),      # a single token
+    (40, 8, 8),         # the narrowest widths (one 16-byte row)
     (77, 136, 1032),    # ffn spans five 256-wide tiles with a ragged tail
     (520, 520, 520),
 ])
