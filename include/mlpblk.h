@@ -141,6 +141,44 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
 int mlpblk_last_error(void);
 
 /*
+ * RMSNorm backward with the residual gradient, for callers that cannot give
+ * the library any device scratch memory.  The paper has no counterpart to this
+ * entry point: it is the row kernel of mlpblk_backward offered on its own.
+ *
+ * Who needs it: code that runs inside a host engine which owns all device
+ * memory and plans every buffer once at start-up, and gives its extensions no
+ * way to allocate (a cudaMalloc there breaks the memory plan and can fail with
+ * out-of-memory in the middle of a step); and code on threads that must not
+ * stall on the implicit device synchronisation cudaMalloc and cudaFree can
+ * cause.  This call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Its scratch (the per-block dgamma partial sums)
+ * is a fixed 4 MiB array inside the library, held by every GPU that loads the
+ * library until the process exits.
+ *
+ *   in : x[T,d], dy[T,d], gamma[d] (desc->dtype), dn[T,d] float32 = the gradient
+ *        of the normalised output n = x * r * gamma, rstd[T] float32 = r
+ *   out: dx[T,d]     = dy + r * (g - xh * mean_k(g * xh)),  xh = x*r, g = dn*gamma
+ *                                                                        (written)
+ *        dgamma[d]  += sum_t dn[t,k] * xh[t,k]                float32 (accumulated)
+ * Limits: d_model a multiple of 8 and at most 4096 (MLPBLK_ENOTSUP beyond: one
+ * partial row must fit the array); any tokens >= 0 (at most
+ * min(512, 1048576 / d_model) partial rows are used; with more tokens each
+ * partial row sums more of them).
+ * desc->ffn and desc->eps are not used.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call shares the one array and each call overwrites
+ * the part it reads, so nothing needs clearing, but calls that overlap on the
+ * GPU (other streams, other threads) race on it and must be serialised by the
+ * caller.  Pointers are device pointers, 16-byte aligned.  Returns an MLPBLK_*
+ * code.
+ */
+int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, const float *dn,
+                                    const void *dy, const void *gamma, const float *rstd,
+                                    void *dx, float *dgamma, void *stream);
+
+/*
  * Kernel timing hook for profiling harnesses (CUDA events, no profiler needed).
  * Kinds reported for each kernel launch the library makes:
  */

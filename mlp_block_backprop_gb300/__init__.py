@@ -28,7 +28,8 @@ MLPBLK_FP32 = 2
 
 EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads",
             "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version",
-            "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string")
+            "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
+            "mlpblk_rmsnorm_backward_noalloc")
 
 KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dgrad_h",
                 5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
@@ -75,6 +76,8 @@ def _load():
     lib.mlpblk_version.restype = i32
     lib.mlpblk_trace_begin.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int), i32]
     lib.mlpblk_trace_begin.restype = i32
+    lib.mlpblk_rmsnorm_backward_noalloc.argtypes = [pd] + [vp] * 8
+    lib.mlpblk_rmsnorm_backward_noalloc.restype = i32
     lib.mlpblk_cuda_error_string.argtypes = []
     lib.mlpblk_cuda_error_string.restype = ctypes.c_char_p
     lib.mlpblk_trace_end.argtypes = []
@@ -146,6 +149,14 @@ def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):
 def mlpblk_scale_grads(desc, dgamma, dw1, dw2, s, stream=None):
     _check(lib.mlpblk_scale_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2), float(s),
                                   _stream(stream)), "mlpblk_scale_grads")
+
+
+def mlpblk_rmsnorm_backward_noalloc(desc, x, dn, dy, gamma, rstd, dx, dgamma, stream=None):
+    """RMSNorm backward + residual gradient with no workspace argument, for
+    callers that cannot allocate device scratch (see include/mlpblk.h)."""
+    _check(lib.mlpblk_rmsnorm_backward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(dn), _ptr(dy),
+                                               _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+                                               _stream(stream)), "mlpblk_rmsnorm_backward_noalloc")
 
 
 def mlpblk_last_error() -> int:

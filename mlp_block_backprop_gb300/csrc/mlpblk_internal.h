@@ -81,6 +81,11 @@ int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *
                        int64_t T, int64_t d, int parts, cudaStream_t s);
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
                            cudaStream_t s);
+// Same row kernel, fed the plain gradient dn of the normalised output (the rstd
+// scale is applied inside the kernel).
+int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
+                                const float *rstd, const void *gamma, void *dx, float *dgamma_part,
+                                int64_t T, int64_t d, int parts, cudaStream_t s);
 int launch_fill_zero(float *p, int64_t n, cudaStream_t s);
 int launch_scale(float *p, int64_t n, float sc, cudaStream_t s);
 

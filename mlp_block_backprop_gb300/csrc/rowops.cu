@@ -113,7 +113,9 @@ __global__ void rstd_f32_kernel(const float *__restrict__ x, float *__restrict__
 // registers for all of the CTA's rows, then the CTA adds its warps' shares in
 // warp order and writes one partial row; dgamma_finalize adds the partials in
 // CTA order, so the result does not depend on timing.
-template <class T, int NCH>
+// kScaleDn = true takes the plain gradient dn of the normalised output and
+// applies the row's rstd to it in the kernel (dn_s = rstd * dn).
+template <class T, int NCH, bool kScaleDn = false>
 __global__ void __launch_bounds__(kRowThreads)
 rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, const T *__restrict__ dy,
                    const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
@@ -143,6 +145,7 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
     for (int64_t t = t0 + warp; t < t1; t += kRowThreads / 32) {
         const T *xr = x + t * d;
         const float *nr = dn_s + t * d;
+        const float rr = kScaleDn ? rstd[t] : 1.0f;
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
@@ -151,6 +154,10 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
                 float xv[8], nv[8];
                 Io8<T>::load(xr + c, xv);
                 Io8<float>::load(nr + c, nv);
+                if (kScaleDn) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nv[i] *= rr;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) s += g_s[c + i] * nv[i] * xv[i];
             }
@@ -167,6 +174,10 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
                 float xv[8], nv[8], gv[8], o[8];
                 Io8<T>::load(xr + c, xv);
                 Io8<float>::load(nr + c, nv);
+                if (kScaleDn) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nv[i] *= rr;
+                }
                 Io8<T>::load(dyr + c, gv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -239,25 +250,25 @@ int grid_for(int64_t work_items, int threads) {
 
 int status() { return launch_status(); }
 
-template <class E, int NCH>
+template <class E, int NCH, bool kScaleDn = false>
 int run_norm_bwd(const void *x, const float *dn_s, const void *dy, const float *rstd,
                  const void *gamma, void *dx, float *part, int64_t T, int64_t d, int parts,
                  cudaStream_t s) {
     const int64_t rows_per_cta = (T + parts - 1) / parts;
     const size_t smem = static_cast<size_t>(2 * d) * sizeof(float);
-    rmsnorm_bwd_kernel<E, NCH><<<parts, kRowThreads, smem, s>>>(
+    rmsnorm_bwd_kernel<E, NCH, kScaleDn><<<parts, kRowThreads, smem, s>>>(
         static_cast<const E *>(x), dn_s, static_cast<const E *>(dy), rstd,
         static_cast<const E *>(gamma), static_cast<E *>(dx), part, T, d, rows_per_cta);
     return status();
 }
 
-template <class E>
+template <class E, bool kScaleDn = false>
 int dispatch_norm_bwd(const void *x, const float *dn_s, const void *dy, const float *rstd,
                       const void *gamma, void *dx, float *part, int64_t T, int64_t d, int parts,
                       cudaStream_t s) {
     const int64_t nch = (d + 255) / 256;
 #define MLPBLK_NB(N) \
-    if (nch <= N) return run_norm_bwd<E, N>(x, dn_s, dy, rstd, gamma, dx, part, T, d, parts, s)
+    if (nch <= N) return run_norm_bwd<E, N, kScaleDn>(x, dn_s, dy, rstd, gamma, dx, part, T, d, parts, s)
     MLPBLK_NB(1);
     MLPBLK_NB(2);
     MLPBLK_NB(3);
@@ -298,6 +309,14 @@ int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *
     if (dtype == MLPBLK_BF16)
         return dispatch_norm_bwd<uint16_t>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
     return dispatch_norm_bwd<float>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
+}
+
+int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
+                                const float *rstd, const void *gamma, void *dx, float *dgamma_part,
+                                int64_t T, int64_t d, int parts, cudaStream_t s) {
+    if (dtype == MLPBLK_BF16)
+        return dispatch_norm_bwd<uint16_t, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
+    return dispatch_norm_bwd<float, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
 }
 
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {
