@@ -106,23 +106,23 @@ int traced(int kind, cudaStream_t s, F &&launch) {
     if (!g_trace.on) return launch();
     const int i = g_trace.count++;
     const bool rec = i < g_trace.capacity;
+    // under stream capture the records become external event nodes, which keep
+    // their timestamps when the graph is replayed
+    unsigned int flags = cudaEventRecordDefault;
     if (rec) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        MLPBLK_TRY(cuda_status(cudaStreamIsCapturing(s, &cs)));
+        if (cs == cudaStreamCaptureStatusActive) flags = cudaEventRecordExternal;
         g_trace.kinds[i] = kind;
-        MLPBLK_TRY(cuda_status(cudaEventRecord(g_trace.events[2 * i], s)));
+        MLPBLK_TRY(cuda_status(cudaEventRecordWithFlags(g_trace.events[2 * i], s, flags)));
     }
     MLPBLK_TRY(launch());
-    if (rec) MLPBLK_TRY(cuda_status(cudaEventRecord(g_trace.events[2 * i + 1], s)));
+    if (rec) MLPBLK_TRY(cuda_status(cudaEventRecordWithFlags(g_trace.events[2 * i + 1], s, flags)));
     return MLPBLK_OK;
 }
 
 #define MLPBLK_LAUNCH(kind, stream, call) MLPBLK_TRY(traced(kind, stream, [&]() { return (call); }))
 
-int norm_parts(int64_t T, int sms) {
-    int p = norm_bwd_parts(T);
-    if (p > 2 * sms) p = 2 * sms;
-    if (p > kMaxParts) p = kMaxParts;
-    return p;
-}
 
 }  // namespace
 
@@ -214,7 +214,7 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
     void *dh_s = ws + l.dh;
     float *dn_s = reinterpret_cast<float *>(ws + l.dn);
     float *part = reinterpret_cast<float *>(ws + l.part);
-    const int parts = norm_parts(T, sms);
+    int parts = 0;  // dgamma partial rows written by the norm kernel
 
     if (desc->dtype == MLPBLK_BF16) {
         GemmArgs gd = {};
@@ -246,7 +246,7 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_simt(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dhf, 1, F, xf, 1, d,
                                     dw1, nullptr, ec, s));
     }
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
 }
@@ -256,9 +256,8 @@ int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float 
     if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t d = desc->d_model, F = desc->ffn;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dgamma, d, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dw1, F * d, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_fill_zero(dw2, F * d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s,
+                  launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, F * d, s));
     return MLPBLK_OK;
 }
 
@@ -269,9 +268,8 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
     if (!isfinite(sc)) return MLPBLK_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t d = desc->d_model, F = desc->ffn;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dgamma, d, sc, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dw1, F * d, sc, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s, launch_scale(dw2, F * d, sc, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s,
+                  launch_grads(false, sc, dgamma, d, dw1, F * d, dw2, F * d, s));
     return MLPBLK_OK;
 }
 

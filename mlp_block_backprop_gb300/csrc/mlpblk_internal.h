@@ -76,18 +76,23 @@ int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, i
                       int64_t d, cudaStream_t s);
 int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps,
                     cudaStream_t s);
+// RMSNorm backward rows; writes at most max_parts dgamma partial rows of d
+// floats to dgamma_part and returns their count in *parts_out.
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
-                       int64_t T, int64_t d, int parts, cudaStream_t s);
+                       int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
                            cudaStream_t s);
 // Same row kernel, fed the plain gradient dn of the normalised output (the rstd
 // scale is applied inside the kernel).
 int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
                                 const float *rstd, const void *gamma, void *dx, float *dgamma_part,
-                                int64_t T, int64_t d, int parts, cudaStream_t s);
-int launch_fill_zero(float *p, int64_t n, cudaStream_t s);
-int launch_scale(float *p, int64_t n, float sc, cudaStream_t s);
+                                int64_t T, int64_t d, int max_parts, int *parts_out,
+                                cudaStream_t s);
+// zero_grads (zero = true) or scale_grads of three float32 buffers of n0, n1,
+// n2 elements (multiples of 4, 16-byte aligned) in one launch.
+int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,
+                 int64_t n2, cudaStream_t s);
 
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].
@@ -99,14 +104,6 @@ struct SimtEpi {
 int launch_gemm_simt(int epi, int M, int N, int K, const float *A, int64_t sam, int64_t sak,
                      const float *B, int64_t sbn, int64_t sbk, float *C0, float *C1,
                      const SimtEpi &e, cudaStream_t s);
-
-// Norm-backward partial count for T rows (fixed, device independent).
-inline int norm_bwd_parts(int64_t T) {
-    int64_t p = (T + 15) / 16;
-    if (p > 512) p = 512;
-    if (p < 1) p = 1;
-    return static_cast<int>(p);
-}
 
 constexpr int64_t kMaxNormD = 4096;  // RMSNorm backward keeps a row's dgamma share in registers
 

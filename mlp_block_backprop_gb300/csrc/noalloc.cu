@@ -65,14 +65,14 @@ extern "C" int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const vo
     float *scratch = nullptr;
     const int rc = device_setup(&dev, &scratch, &sms);
     if (rc != MLPBLK_OK) return rc;
-    int parts = norm_bwd_parts(T);
-    if (parts > 2 * sms) parts = 2 * sms;
-    if (parts > kScratchFloats / d) parts = static_cast<int>(kScratchFloats / d);
+    int max_parts = 512;
+    if (max_parts > kScratchFloats / d) max_parts = static_cast<int>(kScratchFloats / d);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // every one of the `parts` partial rows is written before it is read, so
     // nothing left in the array by an earlier call reaches the result
+    int parts = 0;
     const int r1 = launch_rmsnorm_bwd_unscaled(desc->dtype, x, dn, dy, rstd, gamma, dx, scratch, T,
-                                               d, parts, s);
+                                               d, max_parts, &parts, s);
     if (r1 != MLPBLK_OK) return r1;
     return launch_dgamma_finalize(scratch, parts, dgamma, d, s);
 }

@@ -10,7 +10,7 @@ namespace mlpblk {
 
 namespace {
 
-constexpr int kRowThreads = 256;  // 8 warps, one row per warp at a time
+constexpr int kRowThreads = 256;
 
 __device__ __forceinline__ float bf(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -103,135 +103,216 @@ __global__ void rstd_f32_kernel(const float *__restrict__ x, float *__restrict__
     }
 }
 
-// RMSNorm backward with the residual gradient, one warp per row.  Inputs carry
-// the per-row scale already: dn_s = rstd * dn (from the dgrad GEMM).  With
+// 8 consecutive elements kept in their storage type (bf16: one 16-byte register
+// quad), widened to float on use; keeps the norm kernel at two CTAs per SM.
+template <class T>
+struct Chunk;
+
+template <>
+struct Chunk<uint16_t> {
+    uint4 u;
+    __device__ void load(const uint16_t *p) { u = __ldg(reinterpret_cast<const uint4 *>(p)); }
+    __device__ void zero() { u = make_uint4(0, 0, 0, 0); }
+    __device__ float operator[](int i) const {
+        const uint32_t w = i < 2 ? u.x : (i < 4 ? u.y : (i < 6 ? u.z : u.w));
+        return (i & 1) ? bf(w >> 16) : bf(w & 0xFFFFu);
+    }
+};
+
+template <>
+struct Chunk<float> {
+    float4 a, b;
+    __device__ void load(const float *p) {
+        a = __ldg(reinterpret_cast<const float4 *>(p));
+        b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ void zero() { a = b = make_float4(0.0f, 0.0f, 0.0f, 0.0f); }
+    __device__ float operator[](int i) const {
+        const float4 &v = i < 4 ? a : b;
+        const int k = i & 3;
+        return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+    }
+};
+
+// RMSNorm backward with the residual gradient.  The gradient input carries the
+// per-row scale already, dn_s = rstd * dn (the dgrad GEMM writes it that way);
+// kScaleDn = true instead takes the plain dn and applies rstd here.  With
 // x_hat = x*r and g = dn*gamma the backward of n = x*r*gamma is
 //   dx = dy + r*(g - x_hat*mean_k(g*x_hat)) = dy + gamma*dn_s - x*c,
 //   c  = r^2 * mean_k(gamma * dn_s * x),
 //   dgamma[k] += sum_t dn[t,k]*x_hat[t,k] = sum_t dn_s[t,k]*x[t,k].
-// Lane l owns the 8-column chunks l, l+32, ...; its share of dgamma stays in
-// registers for all of the CTA's rows, then the CTA adds its warps' shares in
-// warp order and writes one partial row; dgamma_finalize adds the partials in
-// CTA order, so the result does not depend on timing.
-// kScaleDn = true takes the plain gradient dn of the normalised output and
-// applies the row's rstd to it in the kernel (dn_s = rstd * dn).
-template <class T, int NCH, bool kScaleDn = false>
-__global__ void __launch_bounds__(kRowThreads)
+//
+// A row is shared by a group of G threads (a power of two, 8..256); thread l of
+// the group owns the 8-column chunks l, l+G, ..., l+(CPT-1)G, keeps them in
+// registers between the row reduction and the dx pass (so no element is read
+// twice), and keeps gamma and its dgamma share for those columns in registers
+// for all rows of the CTA.  256/G rows are in flight per CTA.  The row sum is a
+// shuffle butterfly plus, for G > 32, a shared-memory sum over the group's warps
+// in warp order; the CTA's row groups then add their dgamma shares in group
+// order and the CTA writes one partial row.  Every sum has a fixed order.
+template <class T, int CPT, bool kScaleDn>
+__global__ void __launch_bounds__(kRowThreads, (CPT <= 3 ? 2 : 1))
 rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, const T *__restrict__ dy,
                    const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
-                   float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta) {
+                   float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta,
+                   int G) {
     extern __shared__ float sm[];
-    float *g_s = sm;        // gamma as float [d]
-    float *red = sm + d;    // dgamma share of the CTA [d]
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    for (int64_t i = threadIdx.x * 8; i < d; i += kRowThreads * 8) {
-        float v[8];
-        Io8<T>::load(gamma + i, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g_s[i + j] = v[j];
-    }
-    __syncthreads();
+    const int R = kRowThreads / G;
+    const int grp = threadIdx.x / G;
+    const int gl = threadIdx.x - grp * G;
+    const int chunks = static_cast<int>(d / 8);
+    const float inv_d = 1.0f / static_cast<float>(d);
 
-    float acc[NCH][8];
+    Chunk<T> gch[CPT];
+    float acc[CPT][8];
 #pragma unroll
-    for (int j = 0; j < NCH; ++j)
+    for (int j = 0; j < CPT; ++j) {
+        const int q = gl + G * j;
+        if (q < chunks) gch[j].load(gamma + 8 * q);
+        else gch[j].zero();
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+    }
 
     const int64_t t0 = blockIdx.x * rows_per_cta;
     const int64_t t1 = min(T_rows, t0 + rows_per_cta);
-    const float inv_d = 1.0f / static_cast<float>(d);
-    for (int64_t t = t0 + warp; t < t1; t += kRowThreads / 32) {
-        const T *xr = x + t * d;
-        const float *nr = dn_s + t * d;
-        const float rr = kScaleDn ? rstd[t] : 1.0f;
+    int parity = 0;
+    for (int64_t base = t0; base < t1; base += R, parity ^= 1) {
+        const int64_t t = base + grp;
+        const bool valid = t < t1;
+        const float r = valid ? rstd[t] : 0.0f;
+        Chunk<T> xch[CPT], ych[CPT];
+        Chunk<float> nch[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int q = gl + G * j;
+            if (valid && q < chunks) {
+                xch[j].load(x + t * d + 8 * q);
+                nch[j].load(dn_s + t * d + 8 * q);
+                ych[j].load(dy + t * d + 8 * q);
+            } else {
+                xch[j].zero();
+                nch[j].zero();
+                ych[j].zero();
+            }
+        }
+        const float nscale = kScaleDn ? r : 1.0f;
         float s = 0.0f;
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-            const int64_t c = (lane + 32 * j) * 8;
-            if (c < d) {
-                float xv[8], nv[8];
-                Io8<T>::load(xr + c, xv);
-                Io8<float>::load(nr + c, nv);
-                if (kScaleDn) {
+        for (int j = 0; j < CPT; ++j)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nv[i] *= rr;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s += g_s[c + i] * nv[i] * xv[i];
-            }
+            for (int i = 0; i < 8; ++i) s += gch[j][i] * (nch[j][i] * nscale) * xch[j][i];
+        for (int o = (G < 32 ? G : 32) / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (G > 32) {
+            float *rs = sm + parity * (R * 8);  // a group spans at most 8 warps
+            if ((threadIdx.x & 31) == 0) rs[grp * 8 + (gl >> 5)] = s;
+            __syncthreads();
+            s = 0.0f;
+            for (int w = 0; w < G / 32; ++w) s += rs[grp * 8 + w];
         }
-        s = warp_sum(s);
-        const float r = rstd[t];
         const float cr = r * r * s * inv_d;
-        const T *dyr = dy + t * d;
-        T *dxr = dx + t * d;
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-            const int64_t c = (lane + 32 * j) * 8;
-            if (c < d) {
-                float xv[8], nv[8], gv[8], o[8];
-                Io8<T>::load(xr + c, xv);
-                Io8<float>::load(nr + c, nv);
-                if (kScaleDn) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) nv[i] *= rr;
-                }
-                Io8<T>::load(dyr + c, gv);
+        for (int j = 0; j < CPT; ++j) {
+            const int q = gl + G * j;
+            if (valid && q < chunks) {
+                float o[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    o[i] = gv[i] + g_s[c + i] * nv[i] - xv[i] * cr;
-                    acc[j][i] += nv[i] * xv[i];
+                    const float nv = nch[j][i] * nscale;
+                    const float xv = xch[j][i];
+                    o[i] = ych[j][i] + gch[j][i] * nv - xv * cr;
+                    acc[j][i] += nv * xv;
                 }
-                Io8<T>::store(dxr + c, o);
+                Io8<T>::store(dx + t * d + 8 * q, o);
             }
         }
     }
 
-    // CTA share of dgamma: warps add in order 0, 1, ..., 7.
-    for (int w = 0; w < kRowThreads / 32; ++w) {
-        if (warp == w) {
+    float *out = dg_part + blockIdx.x * d;
+    if (R == 1) {
 #pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-                const int64_t c = (lane + 32 * j) * 8;
-                if (c < d) {
+        for (int j = 0; j < CPT; ++j) {
+            const int q = gl + G * j;
+            if (q < chunks) Io8<float>::store(out + 8 * q, acc[j]);
+        }
+    } else {
+        __syncthreads();
+        float *red = sm;  // [R][d]
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) red[c + i] = (w == 0 ? 0.0f : red[c + i]) + acc[j][i];
-                }
-            }
+        for (int j = 0; j < CPT; ++j) {
+            const int q = gl + G * j;
+            if (q < chunks) Io8<float>::store(red + grp * d + 8 * q, acc[j]);
         }
         __syncthreads();
+        for (int64_t i = threadIdx.x; i < d; i += kRowThreads) {
+            float v = 0.0f;
+            for (int g2 = 0; g2 < R; ++g2) v += red[g2 * d + i];
+            out[i] = v;
+        }
     }
-    float *out = dg_part + blockIdx.x * d;
-    for (int64_t i = threadIdx.x; i < d; i += kRowThreads) out[i] = red[i];
 }
 
-// dgamma[k] += sum_p part[p][k], p in increasing order.
-__global__ void dgamma_finalize_kernel(const float *__restrict__ part, int parts,
-                                       float *__restrict__ dgamma, int64_t d) {
-    const int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (k >= d) return;
-    float s = 0.0f;
-    for (int p = 0; p < parts; ++p) s += part[p * d + k];
-    dgamma[k] += s;
+// dgamma[k] += sum of the partial rows.  A CTA covers 128 columns with 32
+// slices: slice s adds partial rows s, s+32, ... in increasing order (4 columns
+// per thread), then slice 0 adds the 32 slice sums in slice order.
+__global__ void __launch_bounds__(1024)
+dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restrict__ dgamma,
+                       int64_t d) {
+    __shared__ float4 red[32][33];
+    const int lane = threadIdx.x & 31;
+    const int slice = threadIdx.x >> 5;
+    const int64_t col = blockIdx.x * 128 + lane * 4;
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (col < d) {
+#pragma unroll 4
+        for (int p = slice; p < parts; p += 32) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(part + p * d + col));
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+    }
+    red[slice][lane] = s;
+    __syncthreads();
+    if (slice == 0 && col < d) {
+        float4 t = red[0][lane];
+        for (int i = 1; i < 32; ++i) {
+            const float4 v = red[i][lane];
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        float4 *g = reinterpret_cast<float4 *>(dgamma + col);
+        float4 o = *g;
+        o.x += t.x;
+        o.y += t.y;
+        o.z += t.z;
+        o.w += t.w;
+        *g = o;
+    }
 }
 
-__global__ void fill_zero_kernel(float4 *p, int64_t n4) {
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        p[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-}
-
-__global__ void scale_kernel(float4 *p, int64_t n4, float s) {
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+// The three gradient buffers in one launch: p_b[i] = 0 (kZero) or p_b[i] *= s,
+// over the concatenated float4 index space of the buffers.
+template <bool kZero>
+__global__ void grads_kernel(float4 *p0, int64_t n0, float4 *p1, int64_t n1, float4 *p2,
+                             int64_t n2, float s) {
+    const int64_t n = n0 + n1 + n2;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float4 v = p[i];
-        v.x *= s;
-        v.y *= s;
-        v.z *= s;
-        v.w *= s;
-        p[i] = v;
+        float4 *p = i < n0 ? p0 + i : (i < n0 + n1 ? p1 + (i - n0) : p2 + (i - n0 - n1));
+        if (kZero) {
+            *p = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else {
+            float4 v = *p;
+            v.x *= s;
+            v.y *= s;
+            v.z *= s;
+            v.w *= s;
+            *p = v;
+        }
     }
 }
 
@@ -250,35 +331,70 @@ int grid_for(int64_t work_items, int threads) {
 
 int status() { return launch_status(); }
 
-template <class E, int NCH, bool kScaleDn = false>
-int run_norm_bwd(const void *x, const float *dn_s, const void *dy, const float *rstd,
-                 const void *gamma, void *dx, float *part, int64_t T, int64_t d, int parts,
-                 cudaStream_t s) {
-    const int64_t rows_per_cta = (T + parts - 1) / parts;
-    const size_t smem = static_cast<size_t>(2 * d) * sizeof(float);
-    rmsnorm_bwd_kernel<E, NCH, kScaleDn><<<parts, kRowThreads, smem, s>>>(
-        static_cast<const E *>(x), dn_s, static_cast<const E *>(dy), rstd,
-        static_cast<const E *>(gamma), static_cast<E *>(dx), part, T, d, rows_per_cta);
+// Row-group shape of the norm backward for width d: chunks per thread (1..4)
+// and group size G (power of two, 8..256) with the fewest masked chunk slots.
+void norm_shape(int64_t d, int *cpt_out, int *g_out) {
+    const int chunks = static_cast<int>(d / 8);
+    int best_c = 0, best_g = 0, best_waste = 1 << 30;
+    for (int c = 1; c <= 4; ++c) {
+        const int need = (chunks + c - 1) / c;
+        int g = 8;
+        while (g < need) g <<= 1;
+        if (g > kRowThreads) continue;
+        const int waste = g * c - chunks;
+        if (waste < best_waste) {
+            best_waste = waste;
+            best_c = c;
+            best_g = g;
+        }
+    }
+    *cpt_out = best_c;
+    *g_out = best_g;
+}
+
+// One CTA per resident slot (at most max_parts), rows split in whole multiples
+// of the rows in flight; the number of CTAs (= dgamma partial rows) is returned.
+template <class E, int CPT, bool kScaleDn>
+int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
+                 const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
+                 int *parts_out, int G, cudaStream_t s) {
+    const int R = kRowThreads / G;
+    const int64_t floats = R > 1 ? (R * d > 2 * R * 8 ? R * d : 2 * R * 8) : 2 * 8;
+    const size_t smem = floats * sizeof(float);
+    int occ = 0;
+    const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, rmsnorm_bwd_kernel<E, CPT, kScaleDn>, kRowThreads, smem));
+    if (rc != MLPBLK_OK) return rc;
+    int64_t parts = static_cast<int64_t>(occ > 0 ? occ : 1) * sm_count();
+    if (parts > max_parts) parts = max_parts;
+    const int64_t groups = (T + R - 1) / R;
+    if (parts > groups) parts = groups;
+    if (parts < 1) parts = 1;
+    const int64_t rows_per_cta = ((T + parts - 1) / parts + R - 1) / R * R;
+    parts = (T + rows_per_cta - 1) / rows_per_cta;
+    *parts_out = static_cast<int>(parts);
+    rmsnorm_bwd_kernel<E, CPT, kScaleDn><<<static_cast<int>(parts), kRowThreads, smem, s>>>(
+        static_cast<const E *>(x), dn, static_cast<const E *>(dy), rstd,
+        static_cast<const E *>(gamma), static_cast<E *>(dx), part, T, d, rows_per_cta, G);
     return status();
 }
 
-template <class E, bool kScaleDn = false>
-int dispatch_norm_bwd(const void *x, const float *dn_s, const void *dy, const float *rstd,
-                      const void *gamma, void *dx, float *part, int64_t T, int64_t d, int parts,
-                      cudaStream_t s) {
-    const int64_t nch = (d + 255) / 256;
-#define MLPBLK_NB(N) \
-    if (nch <= N) return run_norm_bwd<E, N, kScaleDn>(x, dn_s, dy, rstd, gamma, dx, part, T, d, parts, s)
-    MLPBLK_NB(1);
-    MLPBLK_NB(2);
-    MLPBLK_NB(3);
-    MLPBLK_NB(4);
-    MLPBLK_NB(6);
-    MLPBLK_NB(8);
-    MLPBLK_NB(12);
-    MLPBLK_NB(16);
+template <class E, bool kScaleDn>
+int dispatch_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
+                      const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
+                      int *parts_out, cudaStream_t s) {
+    int cpt = 0, G = 0;
+    norm_shape(d, &cpt, &G);
+#define MLPBLK_NB(C) \
+    return run_norm_bwd<E, C, kScaleDn>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, s)
+    switch (cpt) {
+        case 1: MLPBLK_NB(1);
+        case 2: MLPBLK_NB(2);
+        case 3: MLPBLK_NB(3);
+        case 4: MLPBLK_NB(4);
+        default: return MLPBLK_ENOTSUP;
+    }
 #undef MLPBLK_NB
-    return MLPBLK_ENOTSUP;
 }
 
 }  // namespace
@@ -305,34 +421,37 @@ int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps
 
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
-                       int64_t T, int64_t d, int parts, cudaStream_t s) {
+                       int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
     if (dtype == MLPBLK_BF16)
-        return dispatch_norm_bwd<uint16_t>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
-    return dispatch_norm_bwd<float>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
+        return dispatch_norm_bwd<uint16_t, false>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d,
+                                                  max_parts, parts_out, s);
+    return dispatch_norm_bwd<float, false>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
+                                           parts_out, s);
 }
 
 int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
                                 const float *rstd, const void *gamma, void *dx, float *dgamma_part,
-                                int64_t T, int64_t d, int parts, cudaStream_t s) {
+                                int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
     if (dtype == MLPBLK_BF16)
-        return dispatch_norm_bwd<uint16_t, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
-    return dispatch_norm_bwd<float, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, parts, s);
+        return dispatch_norm_bwd<uint16_t, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d,
+                                                 max_parts, parts_out, s);
+    return dispatch_norm_bwd<float, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
+                                          parts_out, s);
 }
 
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {
-    dgamma_finalize_kernel<<<static_cast<int>((d + 255) / 256), 256, 0, s>>>(part, parts, dgamma, d);
+    dgamma_finalize_kernel<<<static_cast<int>((d + 127) / 128), 1024, 0, s>>>(part, parts, dgamma, d);
     return status();
 }
 
-int launch_fill_zero(float *p, int64_t n, cudaStream_t s) {
-    const int64_t n4 = n / 4;
-    fill_zero_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<float4 *>(p), n4);
-    return status();
-}
-
-int launch_scale(float *p, int64_t n, float sc, cudaStream_t s) {
-    const int64_t n4 = n / 4;
-    scale_kernel<<<grid_for(n4, 256), 256, 0, s>>>(reinterpret_cast<float4 *>(p), n4, sc);
+int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,
+                 int64_t n2, cudaStream_t s) {
+    const int64_t a = n0 / 4, b = n1 / 4, c = n2 / 4;
+    const int grid = grid_for(a + b + c, 256);
+    float4 *q0 = reinterpret_cast<float4 *>(p0), *q1 = reinterpret_cast<float4 *>(p1),
+           *q2 = reinterpret_cast<float4 *>(p2);
+    if (zero) grads_kernel<true><<<grid, 256, 0, s>>>(q0, a, q1, b, q2, c, 0.0f);
+    else grads_kernel<false><<<grid, 256, 0, s>>>(q0, a, q1, b, q2, c, sc);
     return status();
 }
 
