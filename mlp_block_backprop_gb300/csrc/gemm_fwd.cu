@@ -8,7 +8,7 @@ namespace mlpblk {
 
 int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    const int bn = choose_bn(M, N, num_sms);
+    const int bn = choose_bn(M, N, K, false, num_sms);
     if (epi == kEpiFwdW1) {
         return bn == 256
                    ? run_gemm_tc<GemmCfg<256, kEpiFwdW1, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s)

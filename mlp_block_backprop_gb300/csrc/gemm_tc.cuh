@@ -481,15 +481,24 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
 }
 
 // BN choice: 256 unless the N extent is small or BN=128 fills the SMs much better.
-inline int choose_bn(int M, int N, int num_sms) {
+// A 128-wide tile feeds the tensor core half as long per staged byte, so it is
+// taken only when it clearly wins on SM fill.  `split_k` GEMMs (the fp32 +=
+// epilogues) count the K splits that fill idle SMs.
+inline int choose_bn(int M, int N, int K, bool split_k, int num_sms) {
     if (N <= 128) return 128;
     const int mt = (M + kBM - 1) / kBM;
+    const int kb = (K + kBK - 1) / kBK;
     auto eff = [&](int bn) {
-        const int tiles = mt * ((N + bn - 1) / bn);
+        int tiles = mt * ((N + bn - 1) / bn);
+        if (split_k && tiles < num_sms) {
+            int s = num_sms / tiles;
+            if (s > kb) s = kb;
+            if (s > 1) tiles *= s;
+        }
         const int waves = (tiles + num_sms - 1) / num_sms;
         // useful fraction of the SM-waves, with a mild preference for wide tiles
         return static_cast<double>(tiles) / (static_cast<double>(waves) * num_sms) *
-               (bn == 256 ? 1.0 : 0.9) * (static_cast<double>(N) / (((N + bn - 1) / bn) * bn));
+               (bn == 256 ? 1.0 : 0.75) * (static_cast<double>(N) / (((N + bn - 1) / bn) * bn));
     };
     return eff(128) > eff(256) ? 128 : 256;
 }
