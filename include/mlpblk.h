@@ -209,6 +209,18 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 int mlpblk_trace_begin(void **events, int *kinds, int capacity);
 int mlpblk_trace_end(void);
 
+/*
+ * Failure-detection test hook.  MLPBLK_TEST_FAULT_SKIP_LOADS makes the W1 GEMM
+ * of the next bf16 mlpblk_forward issue none of its operand loads: its pipeline
+ * waits then run out after their bound (about 2 s), the kernel unwinds (TMEM
+ * freed, no trap) and MLPBLK_ETIMEOUT is recorded for mlpblk_last_error(); that
+ * forward's outputs are not valid, and the context stays usable.  One-shot; not
+ * thread-safe.  Returns MLPBLK_EINVAL for an unknown fault.
+ */
+#define MLPBLK_TEST_FAULT_NONE        0
+#define MLPBLK_TEST_FAULT_SKIP_LOADS  1
+int mlpblk_set_test_fault(int fault);
+
 /* The CUDA runtime's message for the most recent failing CUDA call made inside
  * the library (behind an MLPBLK_ECUDA), or "no CUDA error recorded". */
 const char *mlpblk_cuda_error_string(void);

@@ -29,7 +29,9 @@ MLPBLK_FP32 = 2
 EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads",
             "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version",
             "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
-            "mlpblk_rmsnorm_backward_noalloc")
+            "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault")
+MLPBLK_TEST_FAULT_NONE = 0
+MLPBLK_TEST_FAULT_SKIP_LOADS = 1
 
 KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dgrad_h",
                 5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
@@ -78,6 +80,8 @@ def _load():
     lib.mlpblk_trace_begin.restype = i32
     lib.mlpblk_rmsnorm_backward_noalloc.argtypes = [pd] + [vp] * 8
     lib.mlpblk_rmsnorm_backward_noalloc.restype = i32
+    lib.mlpblk_set_test_fault.argtypes = [i32]
+    lib.mlpblk_set_test_fault.restype = i32
     lib.mlpblk_cuda_error_string.argtypes = []
     lib.mlpblk_cuda_error_string.restype = ctypes.c_char_p
     lib.mlpblk_trace_end.argtypes = []
@@ -157,6 +161,10 @@ def mlpblk_rmsnorm_backward_noalloc(desc, x, dn, dy, gamma, rstd, dx, dgamma, st
     _check(lib.mlpblk_rmsnorm_backward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(dn), _ptr(dy),
                                                _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
                                                _stream(stream)), "mlpblk_rmsnorm_backward_noalloc")
+
+
+def mlpblk_set_test_fault(fault: int) -> None:
+    _check(lib.mlpblk_set_test_fault(int(fault)), "mlpblk_set_test_fault")
 
 
 def mlpblk_last_error() -> int:

@@ -100,6 +100,15 @@ struct Trace {
     bool on = false;
 } g_trace;
 
+// One-shot test fault (mlpblk_set_test_fault): consumed by the next bf16 forward.
+int g_test_fault = 0;
+
+int take_test_fault() {
+    const int f = g_test_fault;
+    g_test_fault = 0;
+    return f == MLPBLK_TEST_FAULT_SKIP_LOADS ? 1 : 0;
+}
+
 // Runs one launcher, bracketed by the trace events when a trace is active.
 template <class F>
 int traced(int kind, cudaStream_t s, F &&launch) {
@@ -172,6 +181,7 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
         g1.rstd_out = rstd_saved;
         g1.inv_k = 1.0f / static_cast<float>(d);
         g1.eps = desc->eps;
+        g1.skip_loads = take_test_fault();
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_tc_fwd(kEpiFwdW1, (int)T, (int)F, (int)d, x, w1g, h_saved, a_saved, g1, sms, s));
         GemmArgs g2 = {};
         g2.aux = static_cast<const uint16_t *>(x);
@@ -270,6 +280,12 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
     const int64_t d = desc->d_model, F = desc->ffn;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s,
                   launch_grads(false, sc, dgamma, d, dw1, F * d, dw2, F * d, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_set_test_fault(int fault) {
+    if (fault != MLPBLK_TEST_FAULT_NONE && fault != MLPBLK_TEST_FAULT_SKIP_LOADS) return MLPBLK_EINVAL;
+    g_test_fault = fault;
     return MLPBLK_OK;
 }
 

@@ -144,7 +144,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !args.skip_loads) {
             int stage = 0;
             uint32_t phase = 0;
             for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {

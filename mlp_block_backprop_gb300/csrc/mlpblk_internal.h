@@ -56,6 +56,7 @@ struct GemmArgs {
     const uint16_t *colscale;  // AccF32ColScale: bf16 per-column scale (gamma)
     float inv_k;               // FwdW1: 1/d
     float eps;                 // FwdW1: RMSNorm epsilon
+    int skip_loads;            // test fault: the producer issues no loads (waits run out)
 };
 
 // Operand / output views handed to the GEMM launcher (row-major 2-D tensors).
