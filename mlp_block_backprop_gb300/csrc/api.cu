@@ -8,6 +8,7 @@
 //                  -> RMSNorm backward rows (dx, dgamma partials) -> dgamma (+=)
 // The fp32 element type runs the same sequence on CUDA cores.
 #include <math.h>
+#include <stdlib.h>
 
 #include <new>
 
@@ -100,6 +101,21 @@ struct Trace {
     bool on = false;
 } g_trace;
 
+}  // namespace
+
+namespace mlpblk {
+bool rms_in_gemm() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_RMS_IN_GEMM");
+        v = (e && e[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+}  // namespace mlpblk
+
+namespace {
+
 // One-shot test fault (mlpblk_set_test_fault): consumed by the next bf16 forward.
 int g_test_fault = 0;
 
@@ -175,21 +191,31 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *w1g = ws + l.w1g;
 
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s, launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
+    const bool stats_in_gemm = desc->dtype == MLPBLK_BF16 && rms_in_gemm();
+    if (stats_in_gemm)
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s, launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
+    else
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                      launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, w1, gamma, w1g, F, s));
     if (desc->dtype == MLPBLK_BF16) {
         GemmArgs g1 = {};
-        g1.rstd_out = rstd_saved;
-        g1.inv_k = 1.0f / static_cast<float>(d);
-        g1.eps = desc->eps;
+        if (stats_in_gemm) {
+            g1.rstd_out = rstd_saved;
+            g1.inv_k = 1.0f / static_cast<float>(d);
+            g1.eps = desc->eps;
+        } else {
+            g1.rstd_in = rstd_saved;
+        }
         g1.skip_loads = take_test_fault();
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_tc_fwd(kEpiFwdW1, (int)T, (int)F, (int)d, x, w1g, h_saved, a_saved, g1, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                      launch_gemm_tc_fwd(stats_in_gemm ? kEpiFwdW1 : kEpiFwdW1Pre, (int)T, (int)F, (int)d,
+                                         x, w1g, h_saved, a_saved, g1, sms, s));
         GemmArgs g2 = {};
         g2.aux = static_cast<const uint16_t *>(x);
         g2.ld_aux = (int)d;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
     } else {
         const float *xf = static_cast<const float *>(x);
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_RSTD, s, launch_rstd_f32(xf, rstd_saved, T, d, desc->eps, s));
         SimtEpi e1 = {nullptr, rstd_saved, nullptr};
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, xf, d, 1,
                                     static_cast<const float *>(w1g), d, 1,

@@ -7,22 +7,32 @@
 //   wgrad W1: dW1 += (dh_s^T . x) * gamma[col]            (both operands MN-major)
 // dh_s = rstd*dh and dn_s = rstd*dn carry the per-row RMSNorm scale, so the
 // normalised input n never has to be stored or rebuilt: dh^T.n = (dh_s^T.x)*gamma.
+#include <stdlib.h>
+
 #include "gemm_tc.cuh"
 
 namespace mlpblk {
 
 int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    const int bn = choose_bn(M, N, K, epi == kEpiAccF32 || epi == kEpiAccF32ColScale, num_sms);
-#define MLPBLK_RUN(E, AMN, BMN)                                                                    \
-    return bn == 256                                                                               \
-               ? run_gemm_tc<GemmCfg<256, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s)  \
-               : run_gemm_tc<GemmCfg<128, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+    const bool split_k = epi == kEpiAccF32 || epi == kEpiAccF32ColScale;
+    // Pair tiles for the dgrad GEMMs; the wgrad GEMMs (both operands MN-major)
+    // measured slower in pair mode and keep single-CTA tiles.
+    const int mode = choose_tile(M, N, K, split_k, num_sms, pair_tiles_enabled() && !split_k);
+#define MLPBLK_RUN(E, AMN, BMN)                                                                         \
+    switch (mode) {                                                                                     \
+        case kTilePair256:                                                                              \
+            return run_gemm_tc<GemmCfg<256, E, AMN, BMN, true>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
+        case kTile256:                                                                                  \
+            return run_gemm_tc<GemmCfg<256, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s);   \
+        default:                                                                                        \
+            return run_gemm_tc<GemmCfg<128, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s);   \
+    }
     switch (epi) {
-        case kEpiDgradH: MLPBLK_RUN(kEpiDgradH, false, true);
-        case kEpiStoreF32: MLPBLK_RUN(kEpiStoreF32, false, true);
-        case kEpiAccF32: MLPBLK_RUN(kEpiAccF32, true, true);
-        case kEpiAccF32ColScale: MLPBLK_RUN(kEpiAccF32ColScale, true, true);
+        case kEpiDgradH: MLPBLK_RUN(kEpiDgradH, false, true)
+        case kEpiStoreF32: MLPBLK_RUN(kEpiStoreF32, false, true)
+        case kEpiAccF32: MLPBLK_RUN(kEpiAccF32, true, true)
+        case kEpiAccF32ColScale: MLPBLK_RUN(kEpiAccF32ColScale, true, true)
         default: return MLPBLK_EINVAL;
     }
 #undef MLPBLK_RUN

@@ -1,24 +1,34 @@
 // gemm_fwd.cu -- tensor-core GEMMs of the block forward.
-//   W1 GEMM: acc = x . (W1*gamma)^T; rstd from the x stages (RMSNorm prologue);
-//            epilogue h = rstd*acc, a = relu(h)^2      ("Kernel 3: Dense ReLU2 ...")
+//   W1 GEMM: acc = x . (W1*gamma)^T, epilogue h = rstd*acc, a = relu(h)^2
+//            ("Kernel 3: Dense ReLU2 ..."); rstd comes from the preceding
+//            statistics pass (kEpiFwdW1Pre) or from the GEMM's own RMSNorm
+//            prologue warps reading the x stages (kEpiFwdW1)
 //   W2 GEMM: y = x + a . W2^T                           (residual add in the epilogue)
+#include <stdlib.h>
+
 #include "gemm_tc.cuh"
 
 namespace mlpblk {
 
 int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    const int bn = choose_bn(M, N, K, false, num_sms);
-    if (epi == kEpiFwdW1) {
-        return bn == 256
-                   ? run_gemm_tc<GemmCfg<256, kEpiFwdW1, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
-                   : run_gemm_tc<GemmCfg<128, kEpiFwdW1, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s);
+    // Pair tiles except for the W1 GEMM with the in-kernel RMSNorm prologue: in
+    // pair mode its shared-memory reads slow the partner SM's operand reads
+    // (measured 2.3x slower), so that variant keeps single-CTA tiles.
+    const int mode = choose_tile(M, N, K, false, num_sms, pair_tiles_enabled() && epi != kEpiFwdW1);
+#define MLPBLK_RUN(E)                                                                                   \
+    switch (mode) {                                                                                     \
+        case kTilePair256:                                                                              \
+            return run_gemm_tc<GemmCfg<256, E, false, false, true>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
+        case kTile256:                                                                                  \
+            return run_gemm_tc<GemmCfg<256, E, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
+        default:                                                                                        \
+            return run_gemm_tc<GemmCfg<128, E, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
     }
-    if (epi == kEpiFwdW2) {
-        return bn == 256
-                   ? run_gemm_tc<GemmCfg<256, kEpiFwdW2, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
-                   : run_gemm_tc<GemmCfg<128, kEpiFwdW2, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s);
-    }
+    if (epi == kEpiFwdW1) { MLPBLK_RUN(kEpiFwdW1) }
+    if (epi == kEpiFwdW1Pre) { MLPBLK_RUN(kEpiFwdW1Pre) }
+    if (epi == kEpiFwdW2) { MLPBLK_RUN(kEpiFwdW2) }
+#undef MLPBLK_RUN
     return MLPBLK_EINVAL;
 }
 

@@ -8,41 +8,57 @@
 // transposed products of the backward pass (g.B and A^T.g of the MatMul rule of
 // "Reverse-mode automatic differentiation", section 5) need no transpose copies.
 //
-// CTA layout (one CTA per SM, persistent over output tiles):
+// CTA layout (persistent over output tiles):
 //   warp 0      TMA producer: A/B tiles -> shared-memory ring of kStages stages
-//   warp 1      owns TMEM; one lane issues tcgen05.mma (128 x BN x 16 per step)
+//   warp 1      owns TMEM; one lane issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
 //   warps 6..9  (forward W1 only) RMSNorm prologue: sum of x^2 per row, read from
 //               the A stages already in shared memory, gives rstd for the epilogue
 // The accumulator is double buffered in TMEM (2 x BN columns) so the epilogue of
 // one tile overlaps the main loop of the next.
+//
+// Two tile modes:
+//   single (PAIR = false): one CTA per SM computes a 128 x BN tile.
+//   pair   (PAIR = true):  a cluster of two CTAs on two SMs computes a 256 x BN
+//     tile with tcgen05.mma.cta_group::2.  Each CTA loads its 128 rows of A and
+//     BN/2 rows of B; the leader CTA (rank 0) issues the MMAs, which read both
+//     CTAs' shared memory; each CTA's TMEM receives its own 128 rows.  Per SM this
+//     stages half of B per unit of tensor work, which is what keeps the tensor
+//     core fed when the stage refill rate, not the MMA, is the limit.
 #pragma once
 
 #include "ptx.cuh"
 
 namespace mlpblk {
 
-constexpr int kBM = 128;      // tile rows (UMMA M)
+constexpr int kBM = 128;      // rows per CTA (UMMA M per CTA)
 constexpr int kBK = 64;       // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;    // K per tcgen05.mma for 16-bit inputs
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
+// Accumulator buffers of a pair tile (256 TMEM columns each): two, so the
+// epilogue of one tile overlaps the main loop of the next.
+constexpr int kPairAccBufs = 2;
 
-template <int BN_, int EPI_, bool A_MN_, bool B_MN_>
+template <int BN_, int EPI_, bool A_MN_, bool B_MN_, bool PAIR_ = false>
 struct GemmCfg {
-    static constexpr int BN = BN_;
+    static constexpr int BN = BN_;               // tile width (of the pair tile in pair mode)
     static constexpr int EPI = EPI_;
     static constexpr bool A_MN = A_MN_;
     static constexpr bool B_MN = B_MN_;
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // rows of one output tile
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;    // rows of B staged per CTA
     static constexpr bool kNorm = (EPI == kEpiFwdW1);
-    static constexpr bool kOutBf16 = (EPI == kEpiFwdW1 || EPI == kEpiFwdW2 || EPI == kEpiDgradH);
+    static constexpr bool kReluSq = (EPI == kEpiFwdW1 || EPI == kEpiFwdW1Pre);  // h and a out
+    static constexpr bool kOutBf16 = (kReluSq || EPI == kEpiFwdW2 || EPI == kEpiDgradH);
     static constexpr bool kReduce = (EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
-    static constexpr int kNumOut = (EPI == kEpiFwdW1) ? 2 : 1;
+    static constexpr int kNumOut = kReluSq ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
     static constexpr int kStagingBufs = 2;
     static constexpr int kThreads = kNorm ? 320 : 192;
     static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kBBytes = kBRows * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStagingBytes = 4 * kNumOut * kStagingBufs * 4096;
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
@@ -51,21 +67,24 @@ struct GemmCfg {
         (kSmemLimit - kAlignSlack - kCtrlBytes - kStagingBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSmemBytes = kAlignSlack + kCtrlBytes + kStagingBytes + kStages * kStageBytes;
-    static constexpr uint32_t kTmemCols = 2 * BN;
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+    // TMEM accumulator buffers (pair tiles: see kPairAccBufs)
+    static constexpr int kAccBufs = PAIR ? kPairAccBufs : 2;
+    static constexpr uint32_t kTmemCols = kAccBufs * BN;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN, A_MN, B_MN);
     static_assert(kStages >= 2, "not enough shared memory for a pipeline");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory over budget");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+    static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
 };
 
 struct WorkUnit {
-    int m0, n0, n_blk, kb0, kb1;
+    int m0, n0, n_blk, kb0, kb1;  // m0, n0: origin of the (pair) output tile
 };
 
 // Unit u -> (split, tile); tiles are rastered in groups of group_m M-tiles that
 // sweep all N-tiles together, so CTAs running at the same time share operand
 // tiles in L2.  The split index is outermost for the same reason.
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ WorkUnit decode_unit(const GemmArgs &a, int u) {
     const int tiles = a.m_tiles * a.n_tiles;
     const int split = u / tiles;
@@ -78,7 +97,7 @@ __device__ __forceinline__ WorkUnit decode_unit(const GemmArgs &a, int u) {
     WorkUnit w;
     const int m_blk = first_m + r % gm;
     w.n_blk = r / gm;
-    w.m0 = m_blk * kBM;
+    w.m0 = m_blk * TILE_M;
     w.n0 = w.n_blk * BN;
     w.kb0 = split * a.kb_per_split;
     w.kb1 = min(a.k_blocks, w.kb0 + a.kb_per_split);
@@ -114,15 +133,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr uint32_t kNormArrivals = C::kNorm ? 4u : 0u;
+    // pair mode: rank in the CTA pair, the pair's index and count
+    const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit0 = C::PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int unit_step = C::PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full_bar[s], 1);
+            // pair mode, leader: its producer's arrive (+ the peer's "A landed"
+            // notice when the peer's A stage carries the RMSNorm reads)
+            mbar_init(&full_bar[s], 1 + ((C::PAIR && C::kNorm && leader) ? 1u : 0u));
             mbar_init(&empty_bar[s], 1 + kNormArrivals);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1 + kNormArrivals);
-            mbar_init(&acce_bar[b], 4);
+            // the leader's MMA reuses a TMEM buffer once both CTAs' epilogues drained it
+            mbar_init(&acce_bar[b], (C::PAIR && leader) ? 8 : 4);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -133,9 +160,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_tensormap(&tmC0);
         if (C::kNumOut == 2) prefetch_tensormap(&tmC1);
     }
+    if (C::PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::kTmemCols);
-        tmem_relinquish_alloc_permit();
+        if (C::PAIR) {
+            tmem_alloc_pair(tmem_slot, C::kTmemCols);
+            tmem_relinquish_alloc_permit_pair();
+        } else {
+            tmem_alloc(tmem_slot, C::kTmemCols);
+            tmem_relinquish_alloc_permit();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -147,26 +180,55 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0 && !args.skip_loads) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
-                const WorkUnit w = decode_unit<C::BN>(args, u);
+            for (int u = unit0; u < args.num_units; u += unit_step) {
+                const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+                const int a_row = w.m0 + static_cast<int>(rank) * kBM;       // this CTA's A rows
+                const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows;  // this CTA's B rows
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) goto producer_done;
                     uint8_t *sa = stages + stage * C::kStageBytes;
                     uint8_t *sb = sa + C::kABytes;
-                    mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
                     const int k0 = kb * kBK;
-                    if (C::A_MN) {
-                        tma_load_2d(&tmA, &full_bar[stage], sa, w.m0, k0);
-                        tma_load_2d(&tmA, &full_bar[stage], sa + 8192, w.m0 + 64, k0);
+                    // where this CTA's A and B loads signal completion
+                    uint32_t bar_a = smem_u32(&full_bar[stage]), bar_b = bar_a;
+                    bool a_pair = false, b_pair = false;
+                    if (!C::PAIR) {
+                        mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+                    } else if (leader) {
+                        // the leader's barrier collects both CTAs' bytes, except the
+                        // peer's A when the peer's own RMSNorm warps wait for it
+                        mbar_arrive_expect_tx(&full_bar[stage], C::kNorm ? C::kStageBytes + C::kBBytes
+                                                                         : 2 * C::kStageBytes);
                     } else {
-                        tma_load_2d(&tmA, &full_bar[stage], sa, k0, w.m0);
+                        const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                        b_pair = true;
+                        bar_b = leader_full;
+                        if (C::kNorm) {
+                            mbar_arrive_expect_tx(&full_bar[stage], C::kABytes);
+                        } else {
+                            a_pair = true;
+                            bar_a = leader_full;
+                        }
+                    }
+                    if (C::A_MN) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa + j * 8192, a_row + 64 * j, k0);
+                            else tma_load_2d(&tmA, &full_bar[stage], sa + j * 8192, a_row + 64 * j, k0);
+                        }
+                    } else {
+                        if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa, k0, a_row);
+                        else tma_load_2d(&tmA, &full_bar[stage], sa, k0, a_row);
                     }
                     if (C::B_MN) {
 #pragma unroll
-                        for (int j = 0; j < C::BN / 64; ++j)
-                            tma_load_2d(&tmB, &full_bar[stage], sb + j * 8192, w.n0 + 64 * j, k0);
+                        for (int j = 0; j < C::kBRows / 64; ++j) {
+                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * 8192, b_row + 64 * j, k0);
+                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * 8192, b_row + 64 * j, k0);
+                        }
                     } else {
-                        tma_load_2d(&tmB, &full_bar[stage], sb, k0, w.n0);
+                        if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb, k0, b_row);
+                        else tma_load_2d(&tmB, &full_bar[stage], sb, k0, b_row);
                     }
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -179,14 +241,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-                const WorkUnit w = decode_unit<C::BN>(args, u);
-                const int buf = it & 1;
-                const uint32_t aph = (it >> 1) & 1;
+            for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
+                const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+                const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+                const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * C::BN;
@@ -205,16 +267,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
                         const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
                                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, C::kIdesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                        if (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, acc);
+                        else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
                     }
-                    umma_commit(&empty_bar[stage]);  // stage reusable once these MMAs finish
+                    // the stage is reusable (in both CTAs) once these MMAs finish
+                    if (C::PAIR) umma_commit_pair(&empty_bar[stage], 3);
+                    else umma_commit(&empty_bar[stage]);
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (failed) break;
-                umma_commit(&accf_bar[buf]);  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue(s)
+                if (C::PAIR) umma_commit_pair(&accf_bar[buf], 3);
+                else umma_commit(&accf_bar[buf]);
             }
         }
         __syncwarp();
@@ -222,21 +290,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;                // TMEM lane quarter of this warp
         const int row_in_tile = 32 * q + lane;
+        const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
         int it = 0;
         int sbuf = 0;
-        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-            const WorkUnit w = decode_unit<C::BN>(args, u);
-            const int buf = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+        for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
+            const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+            const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
+            const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+            const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
             const bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after_sync();
-            const int row = w.m0 + row_in_tile;
+            const int row = m0 + row_in_tile;
             const bool row_ok = row < args.M;
-            const bool warp_rows = (w.m0 + 32 * q) < args.M;
+            const bool warp_rows = (m0 + 32 * q) < args.M;
             float rsc = 1.0f;
             if (C::EPI == kEpiFwdW1) rsc = rs[buf * 128 + row_in_tile];
-            if (C::EPI == kEpiDgradH) rsc = row_ok ? args.rstd_in[row] : 0.0f;
+            if (C::EPI == kEpiDgradH || C::EPI == kEpiFwdW1Pre) rsc = row_ok ? args.rstd_in[row] : 0.0f;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
 
 #pragma unroll 1
@@ -286,7 +356,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                         for (int i = 0; i < 8; ++i) e[i] = (j < 4) ? v0[8 * j + i] : v1[8 * (j - 4) + i];
                         uint32_t o[4], o2[4];
-                        if (C::EPI == kEpiFwdW1) {
+                        if (C::kReluSq) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float h0 = rsc * e[2 * i], h1 = rsc * e[2 * i + 1];
@@ -331,7 +401,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 __syncwarp();
                 if (lane == 0) {
                     if (warp_rows) {
-                        const int r0 = w.m0 + 32 * q;
+                        const int r0 = m0 + 32 * q;
                         if (C::kReduce) {
                             tma_reduce_add_2d(&tmC0, st0, col0, r0);
                         } else {
@@ -345,26 +415,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acce_bar[buf]);  // TMEM buffer free again
+            if (lane == 0) {
+                mbar_arrive(&acce_bar[buf]);  // TMEM buffer free again
+                if (C::PAIR && !leader) mbar_arrive_cluster(leader_acce0 + buf * 8);
+            }
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     } else if (C::kNorm) {
         // ------------------------------------------- RMSNorm prologue (fwd W1)
-        const int r = 32 * (warp - 6) + lane;  // row of the tile
+        const int r = 32 * (warp - 6) + lane;  // row of this CTA's 128 rows
         const uint32_t sw = static_cast<uint32_t>(r & 7);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
-        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x, ++it) {
-            const WorkUnit w = decode_unit<C::BN>(args, u);
-            const int buf = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+        for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
+            const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+            const int m0 = w.m0 + static_cast<int>(rank) * kBM;
+            const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+            const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
             float ss = 0.0f;
             bool ok = true;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 ok = mbar_wait(&full_bar[stage], phase, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
+                // pair mode: the peer's A stage has landed; tell the leader's MMA
+                if (C::PAIR && !leader && warp == 6 && lane == 0)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&full_bar[stage]), 0));
                 const uint32_t rowaddr = smem_u32(stages + stage * C::kStageBytes) + r * 128;
 #pragma unroll
                 for (int cidx = 0; cidx < 8; ++cidx)
@@ -381,7 +458,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!__all_sync(0xffffffffu, ok)) break;
             const float rstd = 1.0f / sqrtf(ss * args.inv_k + args.eps);
             rs[buf * 128 + r] = rstd;
-            const int row = w.m0 + r;
+            const int row = m0 + r;
             if (w.n_blk == 0 && row < args.M) args.rstd_out[row] = rstd;
             __syncwarp();
             if (lane == 0) mbar_arrive(&accf_bar[buf]);
@@ -390,9 +467,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     tc_fence_before_sync();
     __syncthreads();
+    if (C::PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs may touch it
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        if (C::PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 
@@ -433,30 +512,33 @@ inline bool make_map_2d(CUtensorMap *m, const void *ptr, bool f32, uint64_t inne
     return r == CUDA_SUCCESS;
 }
 
-// Builds the tensor maps and launches one GEMM of configuration C.
+// Builds the tensor maps and launches one GEMM of configuration C.  Pair mode
+// launches clusters of two CTAs, one pair per two SMs.
 template <class C>
 int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
                 GemmArgs a, int num_sms, cudaStream_t stream) {
     CUtensorMap mA, mB, mC0, mC1;
     bool ok = true;
     ok &= C::A_MN ? make_map_2d(&mA, A, false, M, K, 64, 64) : make_map_2d(&mA, A, false, K, M, 64, kBM);
-    ok &= C::B_MN ? make_map_2d(&mB, B, false, N, K, 64, 64) : make_map_2d(&mB, B, false, K, N, 64, C::BN);
+    ok &= C::B_MN ? make_map_2d(&mB, B, false, N, K, 64, 64)
+                  : make_map_2d(&mB, B, false, K, N, 64, C::kBRows);
     if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, false, N, M, 64, 32);
     else ok &= make_map_2d(&mC0, C0, true, N, M, 32, 32);
     if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, false, N, M, 64, 32);
     else mC1 = mC0;
     if (!ok) return MLPBLK_ECUDA;
 
+    const int slots = C::PAIR ? num_sms / 2 : num_sms;  // concurrent tile workers
     a.M = M;
     a.N = N;
     a.K = K;
-    a.m_tiles = (M + kBM - 1) / kBM;
+    a.m_tiles = (M + C::kTileM - 1) / C::kTileM;
     a.n_tiles = (N + C::BN - 1) / C::BN;
     a.k_blocks = (K + kBK - 1) / kBK;
     const int tiles = a.m_tiles * a.n_tiles;
     int splits = 1;
-    if (C::kReduce && tiles < num_sms) {
-        splits = num_sms / tiles;
+    if (C::kReduce && tiles < slots) {
+        splits = slots / tiles;
         if (splits > a.k_blocks) splits = a.k_blocks;
         if (splits < 1) splits = 1;
     }
@@ -464,7 +546,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.splits = (a.k_blocks + a.kb_per_split - 1) / a.kb_per_split;  // every split has work
     a.num_units = tiles * a.splits;
     if (a.group_m <= 0) a.group_m = 16;
-    const int grid = a.num_units < num_sms ? a.num_units : num_sms;
+    const int workers = a.num_units < slots ? a.num_units : slots;
 
     static int attr_set[64] = {0};
     int dev = 0;
@@ -476,31 +558,71 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
         if (rc != MLPBLK_OK) return rc;
         attr_set[dev] = 1;
     }
-    gemm_tc_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, mC0, mC1, a);
-    return launch_status();
+    if (!C::PAIR) {
+        gemm_tc_kernel<C><<<workers, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, mC0, mC1, a);
+        return launch_status();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * workers, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<C>, mA, mB, mC0, mC1, a));
 }
 
-// BN choice: 256 unless the N extent is small or BN=128 fills the SMs much better.
-// A 128-wide tile feeds the tensor core half as long per staged byte, so it is
-// taken only when it clearly wins on SM fill.  `split_k` GEMMs (the fp32 +=
-// epilogues) count the K splits that fill idle SMs.
-inline int choose_bn(int M, int N, int K, bool split_k, int num_sms) {
-    if (N <= 128) return 128;
-    const int mt = (M + kBM - 1) / kBM;
+// Tile modes a GEMM can launch with.
+enum TileMode : int { kTile128 = 0, kTile256 = 1, kTilePair256 = 2 };
+
+// Pair tiles are used when MLPBLK_PAIR_TILES is not "0" (default on).
+inline bool pair_tiles_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_PAIR_TILES");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
+// Tile choice: estimated useful fraction of the SM-waves times the tensor-core
+// efficiency of the tile shape (per staged byte a 128-wide tile feeds the tensor
+// core half as long as a 256-wide one, and a pair tile half again less B per
+// SM).  `split_k` GEMMs (the fp32 += epilogues) count the K splits that fill
+// idle SMs.
+inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, bool allow_pair) {
+    // MLPBLK_TILE=128|256|pair forces one mode (tests run every mode through the
+    // same parity suite)
+    static int forced = -2;
+    if (forced == -2) {
+        const char *e = getenv("MLPBLK_TILE");
+        forced = !e ? -1 : (e[0] == 'p' ? kTilePair256 : (e[0] == '1' ? kTile128 : kTile256));
+    }
+    if (forced >= 0) return (forced == kTilePair256 && !allow_pair) ? kTile256 : forced;
     const int kb = (K + kBK - 1) / kBK;
-    auto eff = [&](int bn) {
-        int tiles = mt * ((N + bn - 1) / bn);
-        if (split_k && tiles < num_sms) {
-            int s = num_sms / tiles;
+    auto eff = [&](int tile_m, int bn, int slots, double shape_eff) {
+        int tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
+        if (split_k && tiles < slots) {
+            int s = slots / tiles;
             if (s > kb) s = kb;
             if (s > 1) tiles *= s;
         }
-        const int waves = (tiles + num_sms - 1) / num_sms;
-        // useful fraction of the SM-waves, with a mild preference for wide tiles
-        return static_cast<double>(tiles) / (static_cast<double>(waves) * num_sms) *
-               (bn == 256 ? 1.0 : 0.75) * (static_cast<double>(N) / (((N + bn - 1) / bn) * bn));
+        const int waves = (tiles + slots - 1) / slots;
+        const double fill = static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
+        const double n_use = static_cast<double>(N) / (((N + bn - 1) / bn) * bn);
+        const double m_use = static_cast<double>(M) / (((M + tile_m - 1) / tile_m) * tile_m);
+        return fill * n_use * m_use * shape_eff;
     };
-    return eff(128) > eff(256) ? 128 : 256;
+    const double e128 = eff(kBM, 128, num_sms, 0.70);
+    const double e256 = eff(kBM, 256, num_sms, 0.92);
+    const double ep = allow_pair ? eff(2 * kBM, 256, num_sms / 2, 1.0) : 0.0;
+    if (ep >= e256 && ep >= e128) return kTilePair256;
+    return e256 >= e128 ? kTile256 : kTile128;
 }
 
 }  // namespace mlpblk

@@ -40,6 +40,7 @@ enum Epilogue : int {
     kEpiStoreF32 = 3, // out = acc (fp32)
     kEpiAccF32 = 4,   // out += acc (fp32, TMA reduce-add)
     kEpiAccF32ColScale = 5,  // out += colscale[n] * acc (fp32, TMA reduce-add)
+    kEpiFwdW1Pre = 6, // h = rstd*acc, a = relu(h)^2 (bf16 x2); rstd read from global
 };
 
 // Arguments of one GEMM launch (the tensor maps travel separately).
@@ -77,6 +78,12 @@ int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, i
                       int64_t d, cudaStream_t s);
 int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps,
                     cudaStream_t s);
+// Forward statistics pass: rstd[T] of x and W1g = W1 * gamma in one launch.
+int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,
+                     const void *w1, const void *gamma, void *w1g, int64_t F, cudaStream_t s);
+// RMSNorm statistics inside the W1 GEMM (its prologue warps) when
+// MLPBLK_RMS_IN_GEMM=1; by default the statistics pass computes rstd.
+bool rms_in_gemm();
 // RMSNorm backward rows; writes at most max_parts dgamma partial rows of d
 // floats to dgamma_part and returns their count in *parts_out.
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,

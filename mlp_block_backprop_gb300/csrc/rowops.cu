@@ -82,6 +82,49 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// The forward's statistics pass, one launch with two jobs.  Blocks below
+// row_blocks: rstd[t] = 1/sqrt(mean_k x[t,k]^2 + eps), one warp per row (the
+// per-row statistic of RMSNorm; the normalisation itself is applied by the W1
+// GEMM, gamma through its B operand and rstd in its epilogue).  The other
+// blocks: W1g = W1 * gamma (8 elements per thread).
+template <class T>
+__global__ void __launch_bounds__(256)
+norm_prep_kernel(const T *__restrict__ x, float *__restrict__ rstd, int64_t T_rows, int64_t d,
+                 float eps, const T *__restrict__ w1, const T *__restrict__ gamma,
+                 T *__restrict__ w1g, int64_t groups, int row_blocks) {
+    if (static_cast<int>(blockIdx.x) < row_blocks) {
+        const int lane = threadIdx.x & 31;
+        const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+        const int64_t nw = (static_cast<int64_t>(row_blocks) * blockDim.x) >> 5;
+        const float inv_d = 1.0f / static_cast<float>(d);
+        for (int64_t t = wid; t < T_rows; t += nw) {
+            const T *row = x + t * d;
+            float ss = 0.0f;
+            for (int64_t c = lane * 8; c < d; c += 256) {
+                float v[8];
+                Io8<T>::load(row + c, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) rstd[t] = 1.0f / sqrtf(ss * inv_d + eps);
+        }
+        return;
+    }
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x - row_blocks) * blockDim.x;
+    for (int64_t g = (blockIdx.x - row_blocks) * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+         g < groups; g += nthreads) {
+        const int64_t e = g * 8;
+        const int64_t k = e % d;
+        float w[8], s[8];
+        Io8<T>::load(w1 + e, w);
+        Io8<T>::load(gamma + k, s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] *= s[i];
+        Io8<T>::store(w1g + e, w);
+    }
+}
+
 // rstd[t] = 1/sqrt(mean_k x[t,k]^2 + eps) for the fp32 path (the bf16 path
 // computes it inside the W1 GEMM).  One warp per row.
 __global__ void rstd_f32_kernel(const float *__restrict__ x, float *__restrict__ rstd, int64_t T,
@@ -411,6 +454,26 @@ int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, i
         fold_gamma_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(w1),
                                                      static_cast<const float *>(gamma),
                                                      static_cast<float *>(w1g), groups, d);
+    return status();
+}
+
+int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,
+                     const void *w1, const void *gamma, void *w1g, int64_t F, cudaStream_t s) {
+    const int64_t groups = F * d / 8;
+    int64_t rb = (T * 32 + 255) / 256;  // one warp per row
+    const int64_t rb_cap = static_cast<int64_t>(sm_count()) * 4;
+    if (rb > rb_cap) rb = rb_cap;
+    if (rb < 1) rb = 1;
+    const int fold_blocks = grid_for(groups, 256);
+    const int grid = static_cast<int>(rb) + fold_blocks;
+    if (dtype == MLPBLK_BF16)
+        norm_prep_kernel<uint16_t><<<grid, 256, 0, s>>>(
+            static_cast<const uint16_t *>(x), rstd, T, d, eps, static_cast<const uint16_t *>(w1),
+            static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(w1g), groups, static_cast<int>(rb));
+    else
+        norm_prep_kernel<float><<<grid, 256, 0, s>>>(
+            static_cast<const float *>(x), rstd, T, d, eps, static_cast<const float *>(w1),
+            static_cast<const float *>(gamma), static_cast<float *>(w1g), groups, static_cast<int>(rb));
     return status();
 }
 
