@@ -16,26 +16,31 @@ namespace mlpblk {
 int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
     const bool split_k = epi == kEpiAccF32 || epi == kEpiAccF32ColScale;
-    // Pair tiles for the dgrad GEMMs; the wgrad GEMMs (both operands MN-major)
-    // measured slower in pair mode and keep single-CTA tiles.
-    const int mode = choose_tile(M, N, K, split_k, num_sms, pair_tiles_enabled() && !split_k);
-#define MLPBLK_RUN(E, AMN, BMN)                                                                         \
-    switch (mode) {                                                                                     \
-        case kTilePair256:                                                                              \
-            return run_gemm_tc<GemmCfg<256, E, AMN, BMN, true>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
-        case kTile256:                                                                                  \
-            return run_gemm_tc<GemmCfg<256, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s);   \
-        default:                                                                                        \
-            return run_gemm_tc<GemmCfg<128, E, AMN, BMN>>(M, N, K, A, B, C0, C1, extra, num_sms, s);   \
+    // B is MN-major in every backward GEMM, so only 256-wide pairs exist; the
+    // wgrad GEMMs (both operands MN-major) measured faster with single-CTA tiles.
+    const int pairs = (pair_tiles_enabled() && !split_k) ? kAllowPair256 : 0;
+    const int mode = choose_tile(M, N, K, split_k, num_sms, pairs);
+#define MLPBLK_RUN_MODE(E, AMN, BNV, PAIRV) \
+    return run_gemm_tc<GemmCfg<BNV, E, AMN, true, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+#define MLPBLK_RUN_SINGLE(E, AMN)                           \
+    switch (mode) {                                         \
+        case kTile256: MLPBLK_RUN_MODE(E, AMN, 256, false); \
+        case kTile192: MLPBLK_RUN_MODE(E, AMN, 192, false); \
+        default: MLPBLK_RUN_MODE(E, AMN, 128, false);       \
     }
+#define MLPBLK_RUN(E, AMN)                                                   \
+    if (mode == kTilePair256) { MLPBLK_RUN_MODE(E, AMN, 256, true); }       \
+    MLPBLK_RUN_SINGLE(E, AMN)
     switch (epi) {
-        case kEpiDgradH: MLPBLK_RUN(kEpiDgradH, false, true)
-        case kEpiStoreF32: MLPBLK_RUN(kEpiStoreF32, false, true)
-        case kEpiAccF32: MLPBLK_RUN(kEpiAccF32, true, true)
-        case kEpiAccF32ColScale: MLPBLK_RUN(kEpiAccF32ColScale, true, true)
+        case kEpiDgradH: { MLPBLK_RUN(kEpiDgradH, false) }
+        case kEpiStoreF32: { MLPBLK_RUN(kEpiStoreF32, false) }
+        case kEpiAccF32: { MLPBLK_RUN_SINGLE(kEpiAccF32, true) }
+        case kEpiAccF32ColScale: { MLPBLK_RUN_SINGLE(kEpiAccF32ColScale, true) }
         default: return MLPBLK_EINVAL;
     }
 #undef MLPBLK_RUN
+#undef MLPBLK_RUN_SINGLE
+#undef MLPBLK_RUN_MODE
 }
 
 int take_device_error_gemm_bwd() {

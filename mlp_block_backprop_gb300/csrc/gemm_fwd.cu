@@ -12,23 +12,34 @@ namespace mlpblk {
 
 int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    // Pair tiles except for the W1 GEMM with the in-kernel RMSNorm prologue: in
-    // pair mode its shared-memory reads slow the partner SM's operand reads
-    // (measured 2.3x slower), so that variant keeps single-CTA tiles.
-    const int mode = choose_tile(M, N, K, false, num_sms, pair_tiles_enabled() && epi != kEpiFwdW1);
-#define MLPBLK_RUN(E)                                                                                   \
-    switch (mode) {                                                                                     \
-        case kTilePair256:                                                                              \
-            return run_gemm_tc<GemmCfg<256, E, false, false, true>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
-        case kTile256:                                                                                  \
-            return run_gemm_tc<GemmCfg<256, E, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
-        default:                                                                                        \
-            return run_gemm_tc<GemmCfg<128, E, false, false>>(M, N, K, A, B, C0, C1, extra, num_sms, s); \
+    // Both operands are K-major here, so both pair widths are possible; the W1
+    // GEMM with the in-kernel RMSNorm prologue keeps single-CTA tiles (in pair
+    // mode its shared-memory reads slow the partner SM's operand reads:
+    // measured 2.3x slower).
+    const int pairs = (pair_tiles_enabled() && epi != kEpiFwdW1) ? (kAllowPair256 | kAllowPair192) : 0;
+    const int mode = choose_tile(M, N, K, false, num_sms, pairs);
+#define MLPBLK_RUN_MODE(E, BNV, PAIRV) \
+    return run_gemm_tc<GemmCfg<BNV, E, false, false, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+#define MLPBLK_RUN(E)                                         \
+    switch (mode) {                                           \
+        case kTilePair256: MLPBLK_RUN_MODE(E, 256, true);     \
+        case kTilePair192: MLPBLK_RUN_MODE(E, 192, true);     \
+        case kTile256: MLPBLK_RUN_MODE(E, 256, false);        \
+        case kTile192: MLPBLK_RUN_MODE(E, 192, false);        \
+        default: MLPBLK_RUN_MODE(E, 128, false);              \
     }
-    if (epi == kEpiFwdW1) { MLPBLK_RUN(kEpiFwdW1) }
+    if (epi == kEpiFwdW1) {
+        // single-CTA modes only (see above)
+        switch (mode) {
+            case kTile256: MLPBLK_RUN_MODE(kEpiFwdW1, 256, false);
+            case kTile192: MLPBLK_RUN_MODE(kEpiFwdW1, 192, false);
+            default: MLPBLK_RUN_MODE(kEpiFwdW1, 128, false);
+        }
+    }
     if (epi == kEpiFwdW1Pre) { MLPBLK_RUN(kEpiFwdW1Pre) }
     if (epi == kEpiFwdW2) { MLPBLK_RUN(kEpiFwdW2) }
 #undef MLPBLK_RUN
+#undef MLPBLK_RUN_MODE
     return MLPBLK_EINVAL;
 }
 

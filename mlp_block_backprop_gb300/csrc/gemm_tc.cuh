@@ -61,20 +61,29 @@ struct GemmCfg {
     static constexpr int kBBytes = kBRows * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStagingBytes = 4 * kNumOut * kStagingBufs * 4096;
+    // epilogues that read a [M][N] bf16 operand (x for the residual, h for the
+    // gate) prefetch each warp's 32 rows of the next tile into shared memory
+    static constexpr bool kAux = (EPI == kEpiFwdW2 || EPI == kEpiDgradH);
+    static constexpr int kAuxBytes = kAux ? 4 * kNumChunks * 4096 : 0;
+    static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre);  // rstd from memory
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
     static constexpr int kAlignSlack = 1024;
     static constexpr int kStagesRaw =
-        (kSmemLimit - kAlignSlack - kCtrlBytes - kStagingBytes) / kStageBytes;
+        (kSmemLimit - kAlignSlack - kCtrlBytes - kStagingBytes - kAuxBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kSmemBytes = kAlignSlack + kCtrlBytes + kStagingBytes + kStages * kStageBytes;
+    static constexpr int kSmemBytes =
+        kAlignSlack + kCtrlBytes + kStagingBytes + kAuxBytes + kStages * kStageBytes;
     // TMEM accumulator buffers (pair tiles: see kPairAccBufs)
     static constexpr int kAccBufs = PAIR ? kPairAccBufs : 2;
-    static constexpr uint32_t kTmemCols = kAccBufs * BN;
+    // TMEM columns allocated: a power of two >= the accumulators' columns
+    static constexpr uint32_t kTmemCols = kAccBufs * BN <= 256 ? 256u : 512u;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN, A_MN, B_MN);
     static_assert(kStages >= 2, "not enough shared memory for a pipeline");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory over budget");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-    static_assert(!PAIR || BN == 256, "pair tiles are 256 x 256");
+    // a pair stages BN/2 rows of B per CTA; MN-major B is staged in 64-wide
+    // swizzle blocks, so there BN/2 must be a multiple of 64
+    static_assert(!PAIR || BN == 256 || (BN == 192 && !B_MN), "pair tiles are 256 x 256 or 256 x 192");
 };
 
 struct WorkUnit {
@@ -116,16 +125,18 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-               const GemmArgs args) {
+               const __grid_constant__ CUtensorMap tmAux, const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *stages = smem;
     uint8_t *staging = smem + C::kStages * C::kStageBytes;
-    uint8_t *ctrl = staging + C::kStagingBytes;
+    uint8_t *aux_smem = staging + C::kStagingBytes;  // [4 warps][chunks][32 rows][128 B]
+    uint8_t *ctrl = aux_smem + C::kAuxBytes;
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ctrl);
     uint64_t *empty_bar = full_bar + C::kStages;
     uint64_t *accf_bar = empty_bar + C::kStages;
     uint64_t *acce_bar = accf_bar + 2;
+    uint64_t *aux_bar = acce_bar + 2;  // one per epilogue warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
     float *rs = reinterpret_cast<float *>(ctrl + 1024);  // [2][128], forward W1 only
@@ -151,6 +162,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // the leader's MMA reuses a TMEM buffer once both CTAs' epilogues drained it
             mbar_init(&acce_bar[b], (C::PAIR && leader) ? 8 : 4);
         }
+        for (int w = 0; w < 4; ++w) mbar_init(&aux_bar[w], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,6 +171,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmC0);
         if (C::kNumOut == 2) prefetch_tensormap(&tmC1);
+        if (C::kAux) prefetch_tensormap(&tmAux);
     }
     if (C::PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
     if (warp == 1) {
@@ -174,6 +187,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel's tail; operands and outputs
+    // are touched only after it has completed
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -291,38 +308,64 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int q = warp & 3;                // TMEM lane quarter of this warp
         const int row_in_tile = 32 * q + lane;
         const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
+        uint8_t *aux_w = aux_smem + q * C::kNumChunks * 4096;  // this warp's 32 rows
+        // The next tile's operands of this warp (its 32 rows of x or h into
+        // shared memory by TMA, its rows' rstd into a register) are fetched as
+        // soon as the current tile no longer needs them, so their latency
+        // overlaps the main loop instead of the epilogue.
+        bool aux_pending = false;  // a prefetch copy issued and not yet waited for
+        auto prefetch = [&](int u_next, float &rsc_next) {
+            const WorkUnit wn = decode_unit<C::BN, C::kTileM>(args, u_next);
+            const int r0 = wn.m0 + static_cast<int>(rank) * kBM + 32 * q;
+            if (C::kRowScale) rsc_next = (r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f;
+            if (C::kAux && lane == 0) {
+                int nch = 0;
+                for (int c = 0; c < C::kNumChunks; ++c)
+                    if (wn.n0 + c * C::kChunkCols < args.N) ++nch;
+                mbar_arrive_expect_tx(&aux_bar[q], nch * 4096);
+                aux_pending = true;
+                for (int c = 0; c < nch; ++c)
+                    tma_load_2d(&tmAux, &aux_bar[q], aux_w + c * 4096, wn.n0 + c * C::kChunkCols, r0);
+            }
+        };
         int it = 0;
         int sbuf = 0;
+        uint32_t aux_phase = 0;
+        float rsc_pre = 1.0f;
+        if (unit0 < args.num_units) prefetch(unit0, rsc_pre);
         for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
             const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
             const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
             const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
             const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
-            const bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
+            bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
+            if (C::kAux && ok) {
+                ok = mbar_wait(&aux_bar[q], aux_phase, abort_flag);
+                if (ok) {
+                    aux_pending = false;
+                    aux_phase ^= 1u;
+                }
+            }
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after_sync();
-            const int row = m0 + row_in_tile;
-            const bool row_ok = row < args.M;
             const bool warp_rows = (m0 + 32 * q) < args.M;
             float rsc = 1.0f;
             if (C::EPI == kEpiFwdW1) rsc = rs[buf * 128 + row_in_tile];
-            if (C::EPI == kEpiDgradH || C::EPI == kEpiFwdW1Pre) rsc = row_ok ? args.rstd_in[row] : 0.0f;
+            if (C::kRowScale) rsc = rsc_pre;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
 
 #pragma unroll 1
             for (int c = 0; c < C::kNumChunks; ++c) {
                 const int col0 = w.n0 + c * C::kChunkCols;
                 if (col0 >= args.N) break;
-                // operands read from global memory by the fused epilogues (issued
-                // first so their latency overlaps the TMEM load)
+                // the fused epilogues' [M][N] operand: this row's 64 values of the
+                // chunk, from the swizzled shared copy (zero beyond M and N)
                 uint4 aux[8];
-                if (C::EPI == kEpiFwdW2 || C::EPI == kEpiDgradH) {
-                    const uint16_t *p = args.aux + static_cast<int64_t>(row) * args.ld_aux + col0;
+                if (C::kAux) {
+                    const uint32_t arow = smem_u32(aux_w + c * 4096) + lane * 128;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (row_ok && col0 + 8 * j < args.N) aux[j] = ld_global_nc_v4(p + 8 * j);
-                        else aux[j] = make_uint4(0, 0, 0, 0);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        aux[j] = ld_shared_v4(arow + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4));
                 }
                 float cs[32];
                 if (C::EPI == kEpiAccF32ColScale) {
@@ -419,8 +462,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 mbar_arrive(&acce_bar[buf]);  // TMEM buffer free again
                 if (C::PAIR && !leader) mbar_arrive_cluster(leader_acce0 + buf * 8);
             }
+            // every lane is done with this tile's shared operand copy
+            if (u + unit_step < args.num_units) prefetch(u + unit_step, rsc_pre);
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (lane == 0) {
+            bulk_wait_group<0>();
+            if (C::kAux && aux_pending) mbar_drain(&aux_bar[q], aux_phase);
+        }
         __syncwarp();
     } else if (C::kNorm) {
         // ------------------------------------------- RMSNorm prologue (fwd W1)
@@ -517,7 +565,7 @@ inline bool make_map_2d(CUtensorMap *m, const void *ptr, bool f32, uint64_t inne
 template <class C>
 int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
                 GemmArgs a, int num_sms, cudaStream_t stream) {
-    CUtensorMap mA, mB, mC0, mC1;
+    CUtensorMap mA, mB, mC0, mC1, mAux;
     bool ok = true;
     ok &= C::A_MN ? make_map_2d(&mA, A, false, M, K, 64, 64) : make_map_2d(&mA, A, false, K, M, 64, kBM);
     ok &= C::B_MN ? make_map_2d(&mB, B, false, N, K, 64, 64)
@@ -526,6 +574,9 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     else ok &= make_map_2d(&mC0, C0, true, N, M, 32, 32);
     if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, false, N, M, 64, 32);
     else mC1 = mC0;
+    // the epilogue's [M][N] operand (row stride N), in the output chunks' boxes
+    if (C::kAux) ok &= a.aux != nullptr && a.ld_aux == N && make_map_2d(&mAux, a.aux, false, N, M, 64, 32);
+    else mAux = mC0;
     if (!ok) return MLPBLK_ECUDA;
 
     const int slots = C::PAIR ? num_sms / 2 : num_sms;  // concurrent tile workers
@@ -558,27 +609,28 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
         if (rc != MLPBLK_OK) return rc;
         attr_set[dev] = 1;
     }
-    if (!C::PAIR) {
-        gemm_tc_kernel<C><<<workers, C::kThreads, C::kSmemBytes, stream>>>(mA, mB, mC0, mC1, a);
-        return launch_status();
-    }
+    if (!C::PAIR)
+        return launch_pdl(gemm_tc_kernel<C>, dim3(workers), dim3(C::kThreads), C::kSmemBytes, stream,
+                          mA, mB, mC0, mC1, mAux, a);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * workers, 1, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<C>, mA, mB, mC0, mC1, a));
+    cfg.numAttrs = 2;
+    return cuda_status(cudaLaunchKernelEx(&cfg, gemm_tc_kernel<C>, mA, mB, mC0, mC1, mAux, a));
 }
 
 // Tile modes a GEMM can launch with.
-enum TileMode : int { kTile128 = 0, kTile256 = 1, kTilePair256 = 2 };
+enum TileMode : int { kTile128 = 0, kTile192 = 1, kTile256 = 2, kTilePair192 = 3, kTilePair256 = 4 };
 
 // Pair tiles are used when MLPBLK_PAIR_TILES is not "0" (default on).
 inline bool pair_tiles_enabled() {
@@ -590,20 +642,31 @@ inline bool pair_tiles_enabled() {
     return v == 1;
 }
 
+// Pair modes a GEMM may use (bit mask).
+constexpr int kAllowPair256 = 1;
+constexpr int kAllowPair192 = 2;  // only with a K-major B operand
+
 // Tile choice: estimated useful fraction of the SM-waves times the tensor-core
 // efficiency of the tile shape (per staged byte a 128-wide tile feeds the tensor
-// core half as long as a 256-wide one, and a pair tile half again less B per
+// core half as long as a 256-wide one, and a pair tile stages half of B per
 // SM).  `split_k` GEMMs (the fp32 += epilogues) count the K splits that fill
 // idle SMs.
-inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, bool allow_pair) {
-    // MLPBLK_TILE=128|256|pair forces one mode (tests run every mode through the
-    // same parity suite)
+inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, int allow_pairs) {
+    // MLPBLK_TILE=128|192|256|pair|pair192 forces one mode where the GEMM
+    // allows it (tests run every mode through the same parity suite)
     static int forced = -2;
     if (forced == -2) {
         const char *e = getenv("MLPBLK_TILE");
-        forced = !e ? -1 : (e[0] == 'p' ? kTilePair256 : (e[0] == '1' ? kTile128 : kTile256));
+        if (!e) forced = -1;
+        else if (e[0] == 'p') forced = (e[4] == '1') ? kTilePair192 : kTilePair256;
+        else if (e[0] == '1') forced = e[1] == '9' ? kTile192 : kTile128;
+        else forced = kTile256;
     }
-    if (forced >= 0) return (forced == kTilePair256 && !allow_pair) ? kTile256 : forced;
+    if (forced >= 0) {
+        if (forced == kTilePair256 && !(allow_pairs & kAllowPair256)) return kTile256;
+        if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) return kTile192;
+        return forced;
+    }
     const int kb = (K + kBK - 1) / kBK;
     auto eff = [&](int tile_m, int bn, int slots, double shape_eff) {
         int tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
@@ -618,11 +681,19 @@ inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, bool allo
         const double m_use = static_cast<double>(M) / (((M + tile_m - 1) / tile_m) * tile_m);
         return fill * n_use * m_use * shape_eff;
     };
-    const double e128 = eff(kBM, 128, num_sms, 0.70);
-    const double e256 = eff(kBM, 256, num_sms, 0.92);
-    const double ep = allow_pair ? eff(2 * kBM, 256, num_sms / 2, 1.0) : 0.0;
-    if (ep >= e256 && ep >= e128) return kTilePair256;
-    return e256 >= e128 ? kTile256 : kTile128;
+    double best = eff(kBM, 128, num_sms, 0.70);
+    int mode = kTile128;
+    auto consider = [&](int m, double e) {
+        if (e > best) {
+            best = e;
+            mode = m;
+        }
+    };
+    consider(kTile192, eff(kBM, 192, num_sms, 0.85));
+    consider(kTile256, eff(kBM, 256, num_sms, 0.92));
+    if (allow_pairs & kAllowPair192) consider(kTilePair192, eff(2 * kBM, 192, num_sms / 2, 0.96));
+    if (allow_pairs & kAllowPair256) consider(kTilePair256, eff(2 * kBM, 256, num_sms / 2, 1.0));
+    return mode;
 }
 
 }  // namespace mlpblk

@@ -28,6 +28,46 @@ inline int cuda_status(cudaError_t e) {
 // Host: status of the kernel launch just made.
 inline int launch_status() { return cuda_status(cudaGetLastError()); }
 
+// Programmatic dependent launch.  Kernels of this library are launched so that
+// the next kernel in the stream may start while this one finishes.  Every
+// kernel calls griddep_wait() before its first global-memory access: it returns
+// once the preceding kernel has completed and its writes are visible
+// (immediately when there is none).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled (it still waits in
+// griddep_wait for this kernel's completion before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Both, at the top of a kernel that has no set-up worth overlapping.
+__device__ __forceinline__ void griddep_enter() {
+    griddep_launch_dependents();
+    griddep_wait();
+}
+
+// Host: launches `kernel` on `s` with programmatic stream serialisation, so it
+// may be scheduled while the previous kernel of the stream finishes (every
+// kernel of the library waits for its predecessor before touching memory).
+template <class... KArgs, class... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...));
+}
+
 // Each translation unit that runs kernels with bounded waits has its own device
 // error word (internal linkage); mlpblk_last_error() collects all of them.
 static __device__ int g_device_error;

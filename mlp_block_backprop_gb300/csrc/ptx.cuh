@@ -80,6 +80,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Waits (bounded, ignoring the abort flag) for copies this thread issued to
+// land, so that none writes shared memory after an aborted kernel has exited.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 <= kWaitLimitNs) {
+    }
+}
+
 // -------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

@@ -63,6 +63,7 @@ struct Io8<float> {
 template <class T>
 __global__ void fold_gamma_kernel(const T *__restrict__ w1, const T *__restrict__ gamma,
                                   T *__restrict__ w1g, int64_t groups, int64_t d) {
+    griddep_enter();
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t e = g * 8;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(256)
 norm_prep_kernel(const T *__restrict__ x, float *__restrict__ rstd, int64_t T_rows, int64_t d,
                  float eps, const T *__restrict__ w1, const T *__restrict__ gamma,
                  T *__restrict__ w1g, int64_t groups, int row_blocks) {
+    griddep_enter();
     if (static_cast<int>(blockIdx.x) < row_blocks) {
         const int lane = threadIdx.x & 31;
         const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -129,6 +131,7 @@ norm_prep_kernel(const T *__restrict__ x, float *__restrict__ rstd, int64_t T_ro
 // computes it inside the W1 GEMM).  One warp per row.
 __global__ void rstd_f32_kernel(const float *__restrict__ x, float *__restrict__ rstd, int64_t T,
                                 int64_t d, float eps) {
+    griddep_enter();
     const int lane = threadIdx.x & 31;
     const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -200,6 +203,7 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
                    float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta,
                    int G) {
     extern __shared__ float sm[];
+    griddep_enter();
     const int R = kRowThreads / G;
     const int grp = threadIdx.x / G;
     const int gl = threadIdx.x - grp * G;
@@ -302,6 +306,7 @@ __global__ void __launch_bounds__(1024)
 dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restrict__ dgamma,
                        int64_t d) {
     __shared__ float4 red[32][33];
+    griddep_enter();
     const int lane = threadIdx.x & 31;
     const int slice = threadIdx.x >> 5;
     const int64_t col = blockIdx.x * 128 + lane * 4;
@@ -342,6 +347,7 @@ dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restr
 template <bool kZero>
 __global__ void grads_kernel(float4 *p0, int64_t n0, float4 *p1, int64_t n1, float4 *p2,
                              int64_t n2, float s) {
+    griddep_enter();
     const int64_t n = n0 + n1 + n2;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -416,10 +422,10 @@ int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rs
     const int64_t rows_per_cta = ((T + parts - 1) / parts + R - 1) / R * R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    rmsnorm_bwd_kernel<E, CPT, kScaleDn><<<static_cast<int>(parts), kRowThreads, smem, s>>>(
-        static_cast<const E *>(x), dn, static_cast<const E *>(dy), rstd,
-        static_cast<const E *>(gamma), static_cast<E *>(dx), part, T, d, rows_per_cta, G);
-    return status();
+    return launch_pdl(rmsnorm_bwd_kernel<E, CPT, kScaleDn>, dim3(static_cast<unsigned>(parts)),
+                      dim3(kRowThreads), smem, s, static_cast<const E *>(x), dn,
+                      static_cast<const E *>(dy), rstd, static_cast<const E *>(gamma),
+                      static_cast<E *>(dx), part, T, d, rows_per_cta, G);
 }
 
 template <class E, bool kScaleDn>
@@ -447,14 +453,12 @@ int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, i
     const int64_t groups = F * d / 8;
     const int grid = grid_for(groups, 256);
     if (dtype == MLPBLK_BF16)
-        fold_gamma_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(w1),
-                                                        static_cast<const uint16_t *>(gamma),
-                                                        static_cast<uint16_t *>(w1g), groups, d);
-    else
-        fold_gamma_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(w1),
-                                                     static_cast<const float *>(gamma),
-                                                     static_cast<float *>(w1g), groups, d);
-    return status();
+        return launch_pdl(fold_gamma_kernel<uint16_t>, dim3(grid), dim3(256), 0, s,
+                          static_cast<const uint16_t *>(w1), static_cast<const uint16_t *>(gamma),
+                          static_cast<uint16_t *>(w1g), groups, d);
+    return launch_pdl(fold_gamma_kernel<float>, dim3(grid), dim3(256), 0, s,
+                      static_cast<const float *>(w1), static_cast<const float *>(gamma),
+                      static_cast<float *>(w1g), groups, d);
 }
 
 int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,
@@ -467,19 +471,18 @@ int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d
     const int fold_blocks = grid_for(groups, 256);
     const int grid = static_cast<int>(rb) + fold_blocks;
     if (dtype == MLPBLK_BF16)
-        norm_prep_kernel<uint16_t><<<grid, 256, 0, s>>>(
-            static_cast<const uint16_t *>(x), rstd, T, d, eps, static_cast<const uint16_t *>(w1),
-            static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(w1g), groups, static_cast<int>(rb));
-    else
-        norm_prep_kernel<float><<<grid, 256, 0, s>>>(
-            static_cast<const float *>(x), rstd, T, d, eps, static_cast<const float *>(w1),
-            static_cast<const float *>(gamma), static_cast<float *>(w1g), groups, static_cast<int>(rb));
-    return status();
+        return launch_pdl(norm_prep_kernel<uint16_t>, dim3(grid), dim3(256), 0, s,
+                          static_cast<const uint16_t *>(x), rstd, T, d, eps,
+                          static_cast<const uint16_t *>(w1), static_cast<const uint16_t *>(gamma),
+                          static_cast<uint16_t *>(w1g), groups, static_cast<int>(rb));
+    return launch_pdl(norm_prep_kernel<float>, dim3(grid), dim3(256), 0, s,
+                      static_cast<const float *>(x), rstd, T, d, eps, static_cast<const float *>(w1),
+                      static_cast<const float *>(gamma), static_cast<float *>(w1g), groups,
+                      static_cast<int>(rb));
 }
 
 int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps, cudaStream_t s) {
-    rstd_f32_kernel<<<grid_for(T * 32, 256), 256, 0, s>>>(x, rstd, T, d, eps);
-    return status();
+    return launch_pdl(rstd_f32_kernel, dim3(grid_for(T * 32, 256)), dim3(256), 0, s, x, rstd, T, d, eps);
 }
 
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
@@ -503,8 +506,8 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
 }
 
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {
-    dgamma_finalize_kernel<<<static_cast<int>((d + 127) / 128), 1024, 0, s>>>(part, parts, dgamma, d);
-    return status();
+    return launch_pdl(dgamma_finalize_kernel, dim3(static_cast<unsigned>((d + 127) / 128)), dim3(1024), 0,
+                      s, part, parts, dgamma, d);
 }
 
 int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,
@@ -513,9 +516,8 @@ int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t 
     const int grid = grid_for(a + b + c, 256);
     float4 *q0 = reinterpret_cast<float4 *>(p0), *q1 = reinterpret_cast<float4 *>(p1),
            *q2 = reinterpret_cast<float4 *>(p2);
-    if (zero) grads_kernel<true><<<grid, 256, 0, s>>>(q0, a, q1, b, q2, c, 0.0f);
-    else grads_kernel<false><<<grid, 256, 0, s>>>(q0, a, q1, b, q2, c, sc);
-    return status();
+    if (zero) return launch_pdl(grads_kernel<true>, dim3(grid), dim3(256), 0, s, q0, a, q1, b, q2, c, 0.0f);
+    return launch_pdl(grads_kernel<false>, dim3(grid), dim3(256), 0, s, q0, a, q1, b, q2, c, sc);
 }
 
 }  // namespace mlpblk

@@ -20,6 +20,7 @@ gemm_simt_kernel(const float *__restrict__ A, int64_t sam, int64_t sak, const fl
                  float *__restrict__ C1, SimtEpi e) {
     __shared__ float As[kTk][kTile + 4];
     __shared__ float Bs[kTk][kTile + 4];
+    griddep_enter();
     const int tx = threadIdx.x % 16;
     const int ty = threadIdx.x / 16;
     const int m0 = blockIdx.y * kTile;
@@ -87,7 +88,7 @@ int launch_gemm_simt(int epi, int M, int N, int K, const float *A, int64_t sam, 
     dim3 grid((N + kTile - 1) / kTile, (M + kTile - 1) / kTile);
     switch (epi) {
 #define MLPBLK_SIMT(E) \
-    case E: gemm_simt_kernel<E><<<grid, 256, 0, s>>>(A, sam, sak, B, sbn, sbk, M, N, K, C0, C1, e); break
+    case E: return launch_pdl(gemm_simt_kernel<E>, grid, dim3(256), 0, s, A, sam, sak, B, sbn, sbk, M, N, K, C0, C1, e)
         MLPBLK_SIMT(kEpiFwdW1);
         MLPBLK_SIMT(kEpiFwdW2);
         MLPBLK_SIMT(kEpiDgradH);
