@@ -55,16 +55,19 @@ struct GemmCfg {
     static constexpr int kNumOut = kReluSq ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
-    static constexpr int kStagingBufs = 2;
     static constexpr int kThreads = kNorm ? 320 : 192;
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = kBRows * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStagingBytes = 4 * kNumOut * kStagingBufs * 4096;
     // epilogues that read a [M][N] bf16 operand (x for the residual, h for the
-    // gate) prefetch each warp's 32 rows of the next tile into shared memory
+    // gate) prefetch each warp's 32 rows of the next tile into shared memory and
+    // stage their output in place of it, so they need no staging buffers
     static constexpr bool kAux = (EPI == kEpiFwdW2 || EPI == kEpiDgradH);
     static constexpr int kAuxBytes = kAux ? 4 * kNumChunks * 4096 : 0;
+    // output staging per epilogue warp and output: double buffered, except for
+    // the two-output W1 epilogue, whose shared memory goes to a deeper pipeline
+    static constexpr int kStagingBufs = kNumOut == 2 ? 1 : 2;
+    static constexpr int kStagingBytes = kAux ? 0 : 4 * kNumOut * kStagingBufs * 4096;
     static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre);  // rstd from memory
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
     static constexpr int kAlignSlack = 1024;
@@ -384,10 +387,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
 
                 // the staging buffers of two chunks ago must have been read by TMA
-                if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
-                __syncwarp();
-                uint8_t *st0 = staging + ((q * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
-                uint8_t *st1 = staging + ((q * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
+                // the staging buffer written kStagingBufs chunks ago must have been
+                // read by its TMA store (in-place staging: this chunk's operand copy,
+                // already in registers, is not stored from before this tile ends)
+                if (!C::kAux) {
+                    if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+                    __syncwarp();
+                }
+                uint8_t *st0 = C::kAux ? aux_w + c * 4096
+                                       : staging + ((q * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
+                uint8_t *st1 = C::kAux ? st0
+                                       : staging + ((q * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
                 const uint32_t s0 = smem_u32(st0) + lane * 128;
                 const uint32_t s1 = smem_u32(st1) + lane * 128;
                 const uint32_t sw = static_cast<uint32_t>(lane & 7);
@@ -454,13 +464,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     bulk_commit_group();
                 }
-                sbuf ^= 1;
+                sbuf = C::kStagingBufs == 2 ? sbuf ^ 1 : 0;
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&acce_bar[buf]);  // TMEM buffer free again
-                if (C::PAIR && !leader) mbar_arrive_cluster(leader_acce0 + buf * 8);
+                // TMEM buffer free again (every tcgen05.ld of it has completed)
+                mbar_arrive_relaxed(&acce_bar[buf]);
+                if (C::PAIR && !leader) mbar_arrive_cluster_relaxed(leader_acce0 + buf * 8);
+                // in-place staging: the stores must have read the operand buffers
+                // before the next tile's operands are loaded into them
+                if (C::kAux) bulk_wait_group_read<0>();
             }
             // every lane is done with this tile's shared operand copy
             if (u + unit_step < args.num_units) prefetch(u + unit_step, rsc_pre);
