@@ -52,8 +52,12 @@ int check_desc(const mlpblk_desc *d) {
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-    int64_t w1g, dh, dn, part, total;
+    int64_t w1g, dh, dn, part, sk_partial, sk_flags, total;
 };
+
+// Stream-K flag sets, one per tensor-core GEMM that can split a tile; each set
+// is zeroed by the kernel launched just before that GEMM.
+enum SkFlagSet : int { kSetFwdW1 = 0, kSetFwdW2 = 1, kSetDgradH = 2, kSetDgradN = 3, kSkSets = 4 };
 
 WsLayout ws_layout(const mlpblk_desc *d) {
     const int64_t elt = d->dtype == MLPBLK_BF16 ? 2 : 4;
@@ -64,7 +68,10 @@ WsLayout ws_layout(const mlpblk_desc *d) {
     l.dn = align256(d->tokens * d->ffn * elt);
     l.part = l.dn + align256(d->tokens * d->d_model * 4);
     const int64_t bwd = l.part + align256(static_cast<int64_t>(kMaxParts) * d->d_model * 4);
-    l.total = fwd > bwd ? fwd : bwd;
+    // the GEMMs' stream-K partial sums and flags, apart from everything above
+    l.sk_partial = fwd > bwd ? fwd : bwd;
+    l.sk_flags = l.sk_partial + align256(static_cast<int64_t>(kMaxSkSlots) * kSkSlotFloats * 4);
+    l.total = l.sk_flags + align256(static_cast<int64_t>(kSkSets) * kSkFlagsPerSet * 4);
     return l;
 }
 
@@ -190,13 +197,16 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     void *w1g = ws + l.w1g;
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
 
     const bool stats_in_gemm = desc->dtype == MLPBLK_BF16 && rms_in_gemm();
     if (stats_in_gemm)
         MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s, launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
     else
         MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
-                      launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, w1, gamma, w1g, F, s));
+                      launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, w1, gamma, w1g, F,
+                                       sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
     if (desc->dtype == MLPBLK_BF16) {
         GemmArgs g1 = {};
         if (stats_in_gemm) {
@@ -207,12 +217,17 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
             g1.rstd_in = rstd_saved;
         }
         g1.skip_loads = take_test_fault();
+        g1.sk_partial = sk_partial;
+        g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+        g1.zero_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
                       launch_gemm_tc_fwd(stats_in_gemm ? kEpiFwdW1 : kEpiFwdW1Pre, (int)T, (int)F, (int)d,
                                          x, w1g, h_saved, a_saved, g1, sms, s));
         GemmArgs g2 = {};
         g2.aux = static_cast<const uint16_t *>(x);
         g2.ld_aux = (int)d;
+        g2.sk_partial = sk_partial;
+        g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
     } else {
         const float *xf = static_cast<const float *>(x);
@@ -250,17 +265,26 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
     void *dh_s = ws + l.dh;
     float *dn_s = reinterpret_cast<float *>(ws + l.dn);
     float *part = reinterpret_cast<float *>(ws + l.part);
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
     int parts = 0;  // dgamma partial rows written by the norm kernel
 
     if (desc->dtype == MLPBLK_BF16) {
+        // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's
+        GemmArgs gw2 = {};
+        gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
         GemmArgs gd = {};
         gd.aux = static_cast<const uint16_t *>(h_saved);
         gd.ld_aux = (int)F;
         gd.rstd_in = rstd_saved;
+        gd.sk_partial = sk_partial;
+        gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+        gd.zero_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
-        GemmArgs gw2 = {};
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
         GemmArgs gn = {};
+        gn.sk_partial = sk_partial;
+        gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);

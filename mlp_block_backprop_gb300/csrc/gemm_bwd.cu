@@ -15,11 +15,9 @@ namespace mlpblk {
 
 int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    const bool split_k = epi == kEpiAccF32 || epi == kEpiAccF32ColScale;
-    // B is MN-major in every backward GEMM, so only 256-wide pairs exist; the
-    // wgrad GEMMs (both operands MN-major) measured faster with single-CTA tiles.
-    const int pairs = (pair_tiles_enabled() && !split_k) ? kAllowPair256 : 0;
-    const int mode = choose_tile(M, N, K, split_k, num_sms, pairs);
+    // B is MN-major in every backward GEMM, so only 256-wide pairs exist
+    const int pairs = pair_tiles_enabled() ? kAllowPair256 : 0;
+    const int mode = choose_tile(M, N, streamk_enabled(), num_sms, pairs);
 #define MLPBLK_RUN_MODE(E, AMN, BNV, PAIRV) \
     return run_gemm_tc<GemmCfg<BNV, E, AMN, true, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
 #define MLPBLK_RUN_SINGLE(E, AMN)                           \
@@ -34,8 +32,8 @@ int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *
     switch (epi) {
         case kEpiDgradH: { MLPBLK_RUN(kEpiDgradH, false) }
         case kEpiStoreF32: { MLPBLK_RUN(kEpiStoreF32, false) }
-        case kEpiAccF32: { MLPBLK_RUN_SINGLE(kEpiAccF32, true) }
-        case kEpiAccF32ColScale: { MLPBLK_RUN_SINGLE(kEpiAccF32ColScale, true) }
+        case kEpiAccF32: { MLPBLK_RUN(kEpiAccF32, true) }
+        case kEpiAccF32ColScale: { MLPBLK_RUN(kEpiAccF32ColScale, true) }
         default: return MLPBLK_EINVAL;
     }
 #undef MLPBLK_RUN

@@ -17,7 +17,8 @@ int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *
     // mode its shared-memory reads slow the partner SM's operand reads:
     // measured 2.3x slower).
     const int pairs = (pair_tiles_enabled() && epi != kEpiFwdW1) ? (kAllowPair256 | kAllowPair192) : 0;
-    const int mode = choose_tile(M, N, K, false, num_sms, pairs);
+    // the in-kernel prologue needs whole tiles (all of K) per segment
+    const int mode = choose_tile(M, N, epi != kEpiFwdW1 && streamk_enabled(), num_sms, pairs);
 #define MLPBLK_RUN_MODE(E, BNV, PAIRV) \
     return run_gemm_tc<GemmCfg<BNV, E, false, false, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
 #define MLPBLK_RUN(E)                                         \

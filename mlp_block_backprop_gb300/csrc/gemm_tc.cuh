@@ -82,6 +82,9 @@ struct GemmCfg {
     static constexpr uint32_t kTmemCols = kAccBufs * BN <= 256 ? 256u : 512u;
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN, A_MN, B_MN);
     static_assert(kStages >= 2, "not enough shared memory for a pipeline");
+    // a split tile's owner copies one partial sum (128 x BN fp32) into the
+    // pipeline stages, which its last segment has finished with
+    static_assert(kStages * kStageBytes >= 4 * BN * 128, "stages cannot hold a partial tile");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory over budget");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
     // a pair stages BN/2 rows of B per CTA; MN-major B is staged in 64-wide
@@ -89,31 +92,64 @@ struct GemmCfg {
     static_assert(!PAIR || BN == 256 || (BN == 192 && !B_MN), "pair tiles are 256 x 256 or 256 x 192");
 };
 
-struct WorkUnit {
-    int m0, n0, n_blk, kb0, kb1;  // m0, n0: origin of the (pair) output tile
+// One segment of a worker's work: k-blocks [kb0, kb1) of one output tile.
+struct Seg {
+    int tile, m0, n0, n_blk, kb0, kb1;  // m0, n0: origin of the (pair) output tile
 };
 
-// Unit u -> (split, tile); tiles are rastered in groups of group_m M-tiles that
-// sweep all N-tiles together, so CTAs running at the same time share operand
-// tiles in L2.  The split index is outermost for the same reason.
+// First stream-K iteration of worker w (iterations of the tiles after dp_tiles,
+// k-block fastest).
+__device__ __forceinline__ int sk_begin(const GemmArgs &a, int w) {
+    return min(w * a.sk_base + min(w, a.sk_rem), a.sk_total);
+}
+
+// A worker's segments in order: its whole tiles w, w + workers, ... below
+// dp_tiles, then its stream-K range, cut at tile boundaries.  Only the first
+// stream-K segment can start inside a tile, and only the last can end inside
+// one, so a worker writes at most one partial and owns at most one split tile.
+struct SegIter {
+    int worker, j, n_dp, pos, end;
+};
+
+__device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
+    SegIter it;
+    it.worker = worker;
+    it.j = 0;
+    it.n_dp = a.dp_tiles / a.workers;
+    it.pos = sk_begin(a, worker);
+    it.end = sk_begin(a, worker + 1);
+    return it;
+}
+
+// Tiles are rastered in groups of group_m M-tiles that sweep all N-tiles
+// together, so tiles in flight at the same time share operand tiles in L2.
 template <int BN, int TILE_M>
-__device__ __forceinline__ WorkUnit decode_unit(const GemmArgs &a, int u) {
-    const int tiles = a.m_tiles * a.n_tiles;
-    const int split = u / tiles;
-    const int t = u - split * tiles;
+__device__ __forceinline__ bool seg_next(const GemmArgs &a, SegIter &it, Seg &s) {
+    int t;
+    if (it.j < it.n_dp) {
+        t = it.worker + it.j * a.workers;
+        s.kb0 = 0;
+        s.kb1 = a.k_blocks;
+        ++it.j;
+    } else if (it.pos < it.end) {
+        const int tt = it.pos / a.k_blocks;
+        s.kb0 = it.pos - tt * a.k_blocks;
+        s.kb1 = min(a.k_blocks, s.kb0 + (it.end - it.pos));
+        it.pos += s.kb1 - s.kb0;
+        t = a.dp_tiles + tt;
+    } else {
+        return false;
+    }
+    s.tile = t;
     const int group = a.group_m * a.n_tiles;
     const int g = t / group;
     const int first_m = g * a.group_m;
     const int gm = min(a.m_tiles - first_m, a.group_m);
     const int r = t - g * group;
-    WorkUnit w;
-    const int m_blk = first_m + r % gm;
-    w.n_blk = r / gm;
-    w.m0 = m_blk * TILE_M;
-    w.n0 = w.n_blk * BN;
-    w.kb0 = split * a.kb_per_split;
-    w.kb1 = min(a.k_blocks, w.kb0 + a.kb_per_split);
-    return w;
+    s.n_blk = r / gm;
+    s.m0 = (first_m + r % gm) * TILE_M;
+    s.n0 = s.n_blk * BN;
+    return true;
 }
 
 __device__ __forceinline__ float sq(float v) { return v * v; }
@@ -150,8 +186,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // pair mode: rank in the CTA pair, the pair's index and count
     const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const int unit0 = C::PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int unit_step = C::PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int worker = C::PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int slot = static_cast<int>(blockIdx.x);  // this CTA's stream-K partial slot
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -194,14 +230,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // are touched only after it has completed
     griddep_launch_dependents();
     griddep_wait();
+    // the next GEMM's stream-K flags start from zero (it runs after this one)
+    if (blockIdx.x == 0 && warp == 0 && args.zero_flags)
+        for (int i = lane; i < kSkFlagsPerSet; i += 32) args.zero_flags[i] = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !args.skip_loads) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int u = unit0; u < args.num_units; u += unit_step) {
-                const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+            SegIter si = seg_begin(args, worker);
+            Seg w;
+            while (seg_next<C::BN, C::kTileM>(args, si, w)) {
                 const int a_row = w.m0 + static_cast<int>(rank) * kBM;       // this CTA's A rows
                 const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows;  // this CTA's B rows
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -265,8 +305,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
-                const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+            SegIter si = seg_begin(args, worker);
+            Seg w;
+            for (; seg_next<C::BN, C::kTileM>(args, si, w); ++it) {
                 const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
                 const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
@@ -312,16 +353,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int row_in_tile = 32 * q + lane;
         const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
         uint8_t *aux_w = aux_smem + q * C::kNumChunks * 4096;  // this warp's 32 rows
-        // The next tile's operands of this warp (its 32 rows of x or h into
+        constexpr int kUnits = C::BN / 32;  // 32-column units of a partial-slot row
+        constexpr int kSlotsPerWorker = C::PAIR ? 2 : 1;
+        // This warp's part of stream-K partial slot `sl`: 32-column unit u, vector
+        // j, lane -> float4 ((q * kUnits + u) * 8 + j) * 32 + lane, so that every
+        // warp-wide access is 512 contiguous bytes.
+        auto part_ptr = [&](int sl, int u, int j) {
+            return args.sk_partial + static_cast<size_t>(sl) * kSkSlotFloats +
+                   ((static_cast<size_t>(q * kUnits + u) * 8 + j) * 32 + lane) * 4;
+        };
+        // The next segment's operands of this warp (its 32 rows of x or h into
         // shared memory by TMA, its rows' rstd into a register) are fetched as
-        // soon as the current tile no longer needs them, so their latency
-        // overlaps the main loop instead of the epilogue.
+        // soon as the current segment no longer needs them, so their latency
+        // overlaps the main loop instead of the epilogue.  A segment that only
+        // writes a partial sum needs neither.
         bool aux_pending = false;  // a prefetch copy issued and not yet waited for
-        auto prefetch = [&](int u_next, float &rsc_next) {
-            const WorkUnit wn = decode_unit<C::BN, C::kTileM>(args, u_next);
+        auto prefetch = [&](const Seg &wn, float &rsc_next) {
             const int r0 = wn.m0 + static_cast<int>(rank) * kBM + 32 * q;
             if (C::kRowScale) rsc_next = (r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f;
-            if (C::kAux && lane == 0) {
+            if (C::kAux && wn.kb0 == 0 && lane == 0) {
                 int nch = 0;
                 for (int c = 0; c < C::kNumChunks; ++c)
                     if (wn.n0 + c * C::kChunkCols < args.N) ++nch;
@@ -335,18 +385,51 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int sbuf = 0;
         uint32_t aux_phase = 0;
         float rsc_pre = 1.0f;
-        if (unit0 < args.num_units) prefetch(unit0, rsc_pre);
-        for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
-            const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+        SegIter si = seg_begin(args, worker);
+        Seg w;
+        bool have = seg_next<C::BN, C::kTileM>(args, si, w);
+        if (have) prefetch(w, rsc_pre);
+        for (; have; ++it) {
+            // The fused epilogues are nonlinear in the sum over k, so a tile split
+            // between workers is finished by the worker holding its first k-blocks
+            // (in its last segment); the others (in their first segment) leave
+            // fp32 partial sums, which it adds before the fused math.  Reduce
+            // epilogues are linear: every segment adds into the output as it is.
+            const bool head = w.kb0 == 0;
+            const bool to_partial = !C::kReduce && !head;
+            const bool fixup = !C::kReduce && head && w.kb1 < args.k_blocks;
             const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
             const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
             const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
             bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
-            if (C::kAux && ok) {
+            if (C::kAux && head && ok) {
                 ok = mbar_wait(&aux_bar[q], aux_phase, abort_flag);
                 if (ok) {
                     aux_pending = false;
                     aux_phase ^= 1u;
+                }
+            }
+            // a split tile's contributors: the next workers whose ranges start in it
+            int cw_end = worker + 1;
+            if (fixup) {
+                const int tile_end = (w.tile - args.dp_tiles + 1) * args.k_blocks;
+                while (cw_end < args.workers && sk_begin(args, cw_end) < tile_end) ++cw_end;
+                for (int cw = worker + 1; cw < cw_end && ok; ++cw)
+                    ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * 4 + q],
+                                   abort_flag);
+                // The first contributor's partial (this warp's kUnits x 4 KB) comes
+                // into the pipeline stages with one bulk copy: this is the worker's
+                // last segment, and its MMAs, which read the stages, have completed.
+                if (ok && lane == 0) {
+                    fence_proxy_async_global();
+                    mbar_arrive_expect_tx(&aux_bar[q], kUnits * 4096);
+                    bulk_copy_g2s(stages + q * kUnits * 4096,
+                                  part_ptr((worker + 1) * kSlotsPerWorker + static_cast<int>(rank), 0, 0) - lane * 4,
+                                  kUnits * 4096, &aux_bar[q]);
+                }
+                if (ok) {
+                    ok = mbar_wait(&aux_bar[q], aux_phase, abort_flag);
+                    if (ok) aux_phase ^= 1u;
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -361,6 +444,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int c = 0; c < C::kNumChunks; ++c) {
                 const int col0 = w.n0 + c * C::kChunkCols;
                 if (col0 >= args.N) break;
+                constexpr int kChunkUnits = C::kChunkCols / 32;
+                float v0[32], v1[32];
+                if (C::kOutBf16) tmem_load_64cols(t_row + c * C::kChunkCols, v0, v1);
+                else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
+                if (to_partial) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        st_global_v4(part_ptr(slot, c * kChunkUnits, j), v0[4 * j], v0[4 * j + 1],
+                                     v0[4 * j + 2], v0[4 * j + 3]);
+                        if (kChunkUnits == 2)
+                            st_global_v4(part_ptr(slot, c * kChunkUnits + 1, j), v1[4 * j], v1[4 * j + 1],
+                                         v1[4 * j + 2], v1[4 * j + 3]);
+                    }
+                    continue;
+                }
+                if (fixup) {
+                    const uint32_t ps = smem_u32(stages + q * kUnits * 4096) + lane * 16;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 p = ld_shared_v4(ps + ((c * kChunkUnits) * 8 + j) * 512);
+                        v0[4 * j] += __uint_as_float(p.x); v0[4 * j + 1] += __uint_as_float(p.y);
+                        v0[4 * j + 2] += __uint_as_float(p.z); v0[4 * j + 3] += __uint_as_float(p.w);
+                        if (kChunkUnits == 2) {
+                            const uint4 p1 = ld_shared_v4(ps + ((c * kChunkUnits + 1) * 8 + j) * 512);
+                            v1[4 * j] += __uint_as_float(p1.x); v1[4 * j + 1] += __uint_as_float(p1.y);
+                            v1[4 * j + 2] += __uint_as_float(p1.z); v1[4 * j + 3] += __uint_as_float(p1.w);
+                        }
+                    }
+                    // further contributors (ranges shorter than a tile): from L2
+                    for (int cw = worker + 2; cw < cw_end; ++cw) {
+                        const int sl = cw * kSlotsPerWorker + static_cast<int>(rank);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 p = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits, j));
+                            v0[4 * j] += p.x; v0[4 * j + 1] += p.y; v0[4 * j + 2] += p.z; v0[4 * j + 3] += p.w;
+                            if (kChunkUnits == 2) {
+                                const float4 p1 = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits + 1, j));
+                                v1[4 * j] += p1.x; v1[4 * j + 1] += p1.y; v1[4 * j + 2] += p1.z; v1[4 * j + 3] += p1.w;
+                            }
+                        }
+                    }
+                }
                 // the fused epilogues' [M][N] operand: this row's 64 values of the
                 // chunk, from the swizzled shared copy (zero beyond M and N)
                 uint4 aux[8];
@@ -382,11 +507,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         cs[8 * j + 6] = bf16_lo(g.w); cs[8 * j + 7] = bf16_hi(g.w);
                     }
                 }
-                float v0[32], v1[32];
-                if (C::kOutBf16) tmem_load_64cols(t_row + c * C::kChunkCols, v0, v1);
-                else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
 
-                // the staging buffers of two chunks ago must have been read by TMA
                 // the staging buffer written kStagingBufs chunks ago must have been
                 // read by its TMA store (in-place staging: this chunk's operand copy,
                 // already in registers, is not stored from before this tile ends)
@@ -473,11 +594,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 mbar_arrive_relaxed(&acce_bar[buf]);
                 if (C::PAIR && !leader) mbar_arrive_cluster_relaxed(leader_acce0 + buf * 8);
                 // in-place staging: the stores must have read the operand buffers
-                // before the next tile's operands are loaded into them
+                // before the next segment's operands are loaded into them
                 if (C::kAux) bulk_wait_group_read<0>();
             }
-            // every lane is done with this tile's shared operand copy
-            if (u + unit_step < args.num_units) prefetch(u + unit_step, rsc_pre);
+            if (to_partial) {
+                // every lane's partial stores are visible before the flag is (after
+                // the TMEM release, so the main loop does not wait for the stores)
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(&args.sk_flags[slot * 4 + q], 1);
+            }
+            // every lane is done with this segment's shared operand copy
+            have = seg_next<C::BN, C::kTileM>(args, si, w);
+            if (have) prefetch(w, rsc_pre);
         }
         if (lane == 0) {
             bulk_wait_group<0>();
@@ -491,8 +620,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
-        for (int u = unit0; u < args.num_units; u += unit_step, ++it) {
-            const WorkUnit w = decode_unit<C::BN, C::kTileM>(args, u);
+        SegIter si = seg_begin(args, worker);  // whole tiles only (no stream-K)
+        Seg w;
+        for (; seg_next<C::BN, C::kTileM>(args, si, w); ++it) {
             const int m0 = w.m0 + static_cast<int>(rank) * kBM;
             const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
             const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -574,6 +704,16 @@ inline bool make_map_2d(CUtensorMap *m, const void *ptr, bool f32, uint64_t inne
     return r == CUDA_SUCCESS;
 }
 
+// Stream-K scheduling is used unless MLPBLK_STREAMK=0 (whole tiles only).
+inline bool streamk_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_STREAMK");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 // Builds the tensor maps and launches one GEMM of configuration C.  Pair mode
 // launches clusters of two CTAs, one pair per two SMs.
 template <class C>
@@ -593,7 +733,11 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     else mAux = mC0;
     if (!ok) return MLPBLK_ECUDA;
 
-    const int slots = C::PAIR ? num_sms / 2 : num_sms;  // concurrent tile workers
+    // concurrent tile workers: one CTA (pair) per SM (pair of SMs), at most one
+    // stream-K partial slot per CTA
+    const int cta_per_worker = C::PAIR ? 2 : 1;
+    int slots = (num_sms < kMaxSkSlots ? num_sms : kMaxSkSlots) / cta_per_worker;
+    if (slots < 1) slots = 1;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -601,17 +745,30 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.n_tiles = (N + C::BN - 1) / C::BN;
     a.k_blocks = (K + kBK - 1) / kBK;
     const int tiles = a.m_tiles * a.n_tiles;
-    int splits = 1;
-    if (C::kReduce && tiles < slots) {
-        splits = slots / tiles;
-        if (splits > a.k_blocks) splits = a.k_blocks;
-        if (splits < 1) splits = 1;
-    }
-    a.kb_per_split = (a.k_blocks + splits - 1) / splits;
-    a.splits = (a.k_blocks + a.kb_per_split - 1) / a.kb_per_split;  // every split has work
-    a.num_units = tiles * a.splits;
+    const int kb = a.k_blocks;
+    a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = 16;
-    const int workers = a.num_units < slots ? a.num_units : slots;
+    int workers = slots;
+    const bool sk = !C::kNorm && streamk_enabled() && (C::kReduce || (a.sk_partial && a.sk_flags));
+    if (!sk || tiles % workers == 0) {
+        // whole tiles: full rounds dealt round robin, the last tiles one each
+        if (tiles < workers) workers = tiles;
+        a.dp_tiles = tiles / workers * workers;
+        a.sk_base = kb;
+        a.sk_rem = 0;
+        a.sk_total = (tiles - a.dp_tiles) * kb;
+    } else {
+        // whole-tile rounds while more than two remain; the last one to two
+        // rounds' k-blocks are split evenly, so every worker ends together
+        const int full = tiles / workers;
+        a.dp_tiles = full >= 2 ? (full - 1) * workers : 0;
+        const int iters = (tiles - a.dp_tiles) * kb;
+        if (a.dp_tiles == 0 && iters < 4 * workers) workers = (iters + 3) / 4;  // >= ~4 k-blocks each
+        a.sk_base = iters / workers;
+        a.sk_rem = iters % workers;
+        a.sk_total = iters;
+    }
+    a.workers = workers;
 
     static int attr_set[64] = {0};
     int dev = 0;
@@ -660,12 +817,12 @@ inline bool pair_tiles_enabled() {
 constexpr int kAllowPair256 = 1;
 constexpr int kAllowPair192 = 2;  // only with a K-major B operand
 
-// Tile choice: estimated useful fraction of the SM-waves times the tensor-core
-// efficiency of the tile shape (per staged byte a 128-wide tile feeds the tensor
-// core half as long as a 256-wide one, and a pair tile stages half of B per
-// SM).  `split_k` GEMMs (the fp32 += epilogues) count the K splits that fill
-// idle SMs.
-inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, int allow_pairs) {
+// Tile choice: the tensor-core efficiency of the tile shape (per staged byte a
+// 128-wide tile feeds the tensor core half as long as a 256-wide one, and a
+// pair tile stages half of B per SM) times the used fraction of the edge tiles,
+// and -- for whole-tile schedules only -- of the last round of tiles (a
+// stream-K schedule balances the rounds).
+inline int choose_tile(int M, int N, bool stream_k, int num_sms, int allow_pairs) {
     // MLPBLK_TILE=128|192|256|pair|pair192 forces one mode where the GEMM
     // allows it (tests run every mode through the same parity suite)
     static int forced = -2;
@@ -681,16 +838,10 @@ inline int choose_tile(int M, int N, int K, bool split_k, int num_sms, int allow
         if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) return kTile192;
         return forced;
     }
-    const int kb = (K + kBK - 1) / kBK;
     auto eff = [&](int tile_m, int bn, int slots, double shape_eff) {
-        int tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
-        if (split_k && tiles < slots) {
-            int s = slots / tiles;
-            if (s > kb) s = kb;
-            if (s > 1) tiles *= s;
-        }
+        const int tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
         const int waves = (tiles + slots - 1) / slots;
-        const double fill = static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
+        const double fill = stream_k ? 1.0 : static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
         const double n_use = static_cast<double>(N) / (((N + bn - 1) / bn) * bn);
         const double m_use = static_cast<double>(M) / (((M + tile_m - 1) / tile_m) * tile_m);
         return fill * n_use * m_use * shape_eff;

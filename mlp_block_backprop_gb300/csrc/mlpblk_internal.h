@@ -84,12 +84,25 @@ enum Epilogue : int {
 };
 
 // Arguments of one GEMM launch (the tensor maps travel separately).
+// Stream-K partial accumulators: one slot of 128 x 256 fp32 per CTA, and per
+// slot one flag word per epilogue warp.
+constexpr int kMaxSkSlots = 160;
+constexpr int kSkSlotFloats = 128 * 256;
+constexpr int kSkFlagsPerSet = kMaxSkSlots * 4;
+
 struct GemmArgs {
     int M, N, K;
     int m_tiles, n_tiles, k_blocks;
-    int splits, kb_per_split;
-    int num_units;             // m_tiles * n_tiles * splits
+    int tiles;                 // m_tiles * n_tiles
     int group_m;               // raster: this many M tiles sweep N together
+    // Schedule over `workers` persistent workers (CTAs, or CTA pairs): tiles
+    // [0, dp_tiles) are dealt whole, round robin; the sk_total k-block
+    // iterations of tiles [dp_tiles, tiles) are cut into contiguous ranges of
+    // sk_base (+1 for the first sk_rem workers) each ("stream-K").
+    int workers, dp_tiles, sk_base, sk_rem, sk_total;
+    float *sk_partial;         // kMaxSkSlots slots of kSkSlotFloats: split-tile partial sums
+    int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
+    int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
     const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
     int ld_aux;
     const float *rstd_in;      // DgradH: per-row rstd
@@ -120,7 +133,8 @@ int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps
                     cudaStream_t s);
 // Forward statistics pass: rstd[T] of x and W1g = W1 * gamma in one launch.
 int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,
-                     const void *w1, const void *gamma, void *w1g, int64_t F, cudaStream_t s);
+                     const void *w1, const void *gamma, void *w1g, int64_t F, int *zero_flags,
+                     int zero_count, cudaStream_t s);
 // RMSNorm statistics inside the W1 GEMM (its prologue warps) when
 // MLPBLK_RMS_IN_GEMM=1; by default the statistics pass computes rstd.
 bool rms_in_gemm();

@@ -403,6 +403,64 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
     return v;
 }
 
+// ------------------------------------------------- flags between CTAs (global)
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *flag == 1 (acquire), with the same bound and abort protocol as
+// mbar_wait.  Returns false when the wait gave up.
+__device__ __forceinline__ bool flag_wait(const int *flag, volatile int *abort) {
+    if (ld_acquire_gpu(flag) == 1) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_gpu(flag) == 1) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            record_device_error(MLPBLK_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Orders this thread's earlier generic-proxy accesses (e.g. an acquire of a
+// flag) before its later async-proxy accesses of global memory (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Untiled bulk copy global -> this CTA's shared memory; completion is signalled
+// on `bar` (tx bytes).  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// 16-byte load cached in L2 only (data another SM wrote during this kernel).
+__device__ __forceinline__ float4 ld_global_cg_v4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 // Named barrier over `nthreads` threads (multiple of 32), id 1..15.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

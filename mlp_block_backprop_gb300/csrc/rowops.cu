@@ -92,8 +92,11 @@ template <class T>
 __global__ void __launch_bounds__(256)
 norm_prep_kernel(const T *__restrict__ x, float *__restrict__ rstd, int64_t T_rows, int64_t d,
                  float eps, const T *__restrict__ w1, const T *__restrict__ gamma,
-                 T *__restrict__ w1g, int64_t groups, int row_blocks) {
+                 T *__restrict__ w1g, int64_t groups, int row_blocks, int *zero_flags, int zero_count) {
     griddep_enter();
+    // the following GEMM's stream-K flags start from zero
+    if (zero_flags && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_flags[i] = 0;
     if (static_cast<int>(blockIdx.x) < row_blocks) {
         const int lane = threadIdx.x & 31;
         const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -462,7 +465,8 @@ int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, i
 }
 
 int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,
-                     const void *w1, const void *gamma, void *w1g, int64_t F, cudaStream_t s) {
+                     const void *w1, const void *gamma, void *w1g, int64_t F, int *zero_flags,
+                     int zero_count, cudaStream_t s) {
     const int64_t groups = F * d / 8;
     int64_t rb = (T * 32 + 255) / 256;  // one warp per row
     const int64_t rb_cap = static_cast<int64_t>(sm_count()) * 4;
@@ -474,11 +478,12 @@ int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d
         return launch_pdl(norm_prep_kernel<uint16_t>, dim3(grid), dim3(256), 0, s,
                           static_cast<const uint16_t *>(x), rstd, T, d, eps,
                           static_cast<const uint16_t *>(w1), static_cast<const uint16_t *>(gamma),
-                          static_cast<uint16_t *>(w1g), groups, static_cast<int>(rb));
+                          static_cast<uint16_t *>(w1g), groups, static_cast<int>(rb), zero_flags,
+                          zero_count);
     return launch_pdl(norm_prep_kernel<float>, dim3(grid), dim3(256), 0, s,
                       static_cast<const float *>(x), rstd, T, d, eps, static_cast<const float *>(w1),
                       static_cast<const float *>(gamma), static_cast<float *>(w1g), groups,
-                      static_cast<int>(rb));
+                      static_cast<int>(rb), zero_flags, zero_count);
 }
 
 int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps, cudaStream_t s) {
