@@ -346,6 +346,10 @@ def run_ours(args, dist, peaks):
                          "burst": round(value / dist.world / peaks.get("bf16_tflops", 1.0), 4)},
         "roofline": roofline(dominant),
         "roofline_hbm": roofline("norm_bwd"),
+        # every kernel kind against its own roof: tensor peak for the GEMMs, copy
+        # bandwidth for the HBM-bound kernels (same live event durations)
+        "roofline_per_kernel": {k: {f: r[f] for f in ("bound", "achieved", "unit", "frac", "mean_launch_us")}
+                                for k in per for r in [roofline(k)] if r is not None},
         "kernels": kernels,
         "kernel_trace": {"how": "second replay of the same K steps with a CUDA event pair around "
                                 "every launch (on the launch stream)",
