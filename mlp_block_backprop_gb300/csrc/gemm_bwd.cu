@@ -17,9 +17,13 @@ int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
     // B is MN-major in every backward GEMM, so only 256-wide pairs exist
     const int pairs = pair_tiles_enabled() ? kAllowPair256 : 0;
-    const int mode = choose_tile(M, N, streamk_enabled(), num_sms, pairs);
+    const bool reduce = epi == kEpiAccF32 || epi == kEpiAccF32ColScale;
+    const int choice = choose_tile(M, N, K, streamk_enabled(), reduce, num_sms, pairs);
+    const int mode = choice & ~kUseStreamK;
+    GemmArgs args = extra;
+    args.whole_tiles = (choice & kUseStreamK) ? 0 : 1;
 #define MLPBLK_RUN_MODE(E, AMN, BNV, PAIRV) \
-    return run_gemm_tc<GemmCfg<BNV, E, AMN, true, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+    return run_gemm_tc<GemmCfg<BNV, E, AMN, true, PAIRV>>(M, N, K, A, B, C0, C1, args, num_sms, s)
 #define MLPBLK_RUN_SINGLE(E, AMN)                           \
     switch (mode) {                                         \
         case kTile256: MLPBLK_RUN_MODE(E, AMN, 256, false); \

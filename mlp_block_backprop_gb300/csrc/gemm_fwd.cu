@@ -18,9 +18,12 @@ int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *
     // measured 2.3x slower).
     const int pairs = (pair_tiles_enabled() && epi != kEpiFwdW1) ? (kAllowPair256 | kAllowPair192) : 0;
     // the in-kernel prologue needs whole tiles (all of K) per segment
-    const int mode = choose_tile(M, N, epi != kEpiFwdW1 && streamk_enabled(), num_sms, pairs);
+    const int choice = choose_tile(M, N, K, epi != kEpiFwdW1 && streamk_enabled(), false, num_sms, pairs);
+    const int mode = choice & ~kUseStreamK;
+    GemmArgs args = extra;
+    args.whole_tiles = (choice & kUseStreamK) ? 0 : 1;
 #define MLPBLK_RUN_MODE(E, BNV, PAIRV) \
-    return run_gemm_tc<GemmCfg<BNV, E, false, false, PAIRV>>(M, N, K, A, B, C0, C1, extra, num_sms, s)
+    return run_gemm_tc<GemmCfg<BNV, E, false, false, PAIRV>>(M, N, K, A, B, C0, C1, args, num_sms, s)
 #define MLPBLK_RUN(E)                                         \
     switch (mode) {                                           \
         case kTilePair256: MLPBLK_RUN_MODE(E, 256, true);     \

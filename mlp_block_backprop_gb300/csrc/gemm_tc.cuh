@@ -749,7 +749,8 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = 16;
     int workers = slots;
-    const bool sk = !C::kNorm && streamk_enabled() && (C::kReduce || (a.sk_partial && a.sk_flags));
+    const bool sk = !C::kNorm && !a.whole_tiles && streamk_enabled() &&
+                    (C::kReduce || (a.sk_partial && a.sk_flags));
     if (!sk || tiles % workers == 0) {
         // whole tiles: full rounds dealt round robin, the last tiles one each
         if (tiles < workers) workers = tiles;
@@ -817,14 +818,21 @@ inline bool pair_tiles_enabled() {
 constexpr int kAllowPair256 = 1;
 constexpr int kAllowPair192 = 2;  // only with a K-major B operand
 
-// Tile choice: the tensor-core efficiency of the tile shape (per staged byte a
-// 128-wide tile feeds the tensor core half as long as a 256-wide one, and a
-// pair tile stages half of B per SM) times the used fraction of the edge tiles,
-// and -- for whole-tile schedules only -- of the last round of tiles (a
-// stream-K schedule balances the rounds).
-inline int choose_tile(int M, int N, bool stream_k, int num_sms, int allow_pairs) {
+// Tile and schedule choice.  Cost, per worker, in units of one 128 x 128 x 64
+// MMA step per SM: k-blocks per worker x the tile's MMA work per SM / the shape's
+// efficiency.  The efficiencies are measured ones (k-block time of each shape on
+// the 120M-class block, where the k-loop waits on operand data: a 256 x 256 pair
+// stages the fewest bytes per MMA).  Whole tiles: ceil(tiles / workers) rounds of
+// a tile's k-loop.  Stream-K: the k-blocks spread evenly, plus the split tiles'
+// fix-up (flag wait, partial copy; ~3 us, and ~2 us more per extra contributor
+// when a worker's range is shorter than a tile), which the fp32 += epilogues do
+// not need.  Returns the mode, with kUseStreamK set when stream-K wins.
+constexpr int kUseStreamK = 0x100;
+
+inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int num_sms, int allow_pairs) {
     // MLPBLK_TILE=128|192|256|pair|pair192 forces one mode where the GEMM
-    // allows it (tests run every mode through the same parity suite)
+    // allows it (tests run every mode through the same parity suite); the
+    // schedule is still chosen by cost
     static int forced = -2;
     if (forced == -2) {
         const char *e = getenv("MLPBLK_TILE");
@@ -833,32 +841,38 @@ inline int choose_tile(int M, int N, bool stream_k, int num_sms, int allow_pairs
         else if (e[0] == '1') forced = e[1] == '9' ? kTile192 : kTile128;
         else forced = kTile256;
     }
-    if (forced >= 0) {
-        if (forced == kTilePair256 && !(allow_pairs & kAllowPair256)) return kTile256;
-        if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) return kTile192;
-        return forced;
-    }
-    auto eff = [&](int tile_m, int bn, int slots, double shape_eff) {
-        const int tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
-        const int waves = (tiles + slots - 1) / slots;
-        const double fill = stream_k ? 1.0 : static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
-        const double n_use = static_cast<double>(N) / (((N + bn - 1) / bn) * bn);
-        const double m_use = static_cast<double>(M) / (((M + tile_m - 1) / tile_m) * tile_m);
-        return fill * n_use * m_use * shape_eff;
-    };
-    double best = eff(kBM, 128, num_sms, 0.70);
-    int mode = kTile128;
-    auto consider = [&](int m, double e) {
-        if (e > best) {
-            best = e;
-            mode = m;
+    if (forced == kTilePair256 && !(allow_pairs & kAllowPair256)) forced = kTile256;
+    if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) forced = kTile192;
+    const int64_t kb = (K + kBK - 1) / kBK;
+    double best = 1e300;
+    int choice = kTile128;
+    auto consider = [&](int mode, int tile_m, int bn, int cta_per_worker, double shape_eff) {
+        if (forced >= 0 && mode != forced) return;
+        int workers = (num_sms < kMaxSkSlots ? num_sms : kMaxSkSlots) / cta_per_worker;
+        if (workers < 1) workers = 1;
+        const int64_t tiles = static_cast<int64_t>((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
+        const double unit = static_cast<double>(tile_m / cta_per_worker) * bn / (128.0 * 128.0) / shape_eff;
+        const double dp = static_cast<double>((tiles + workers - 1) / workers) * kb * unit;
+        if (dp < best) {
+            best = dp;
+            choice = mode;
+        }
+        if (!sk_allowed || tiles % workers == 0) return;
+        const int64_t per = (tiles * kb + workers - 1) / workers;
+        double fix = reduce ? 2.0 : 17.0;
+        if (!reduce && per < kb) fix += 10.0 * static_cast<double>((kb + per - 1) / per - 1);
+        const double sk = static_cast<double>(per) * unit + fix;
+        if (sk < best) {
+            best = sk;
+            choice = mode | kUseStreamK;
         }
     };
-    consider(kTile192, eff(kBM, 192, num_sms, 0.85));
-    consider(kTile256, eff(kBM, 256, num_sms, 0.92));
-    if (allow_pairs & kAllowPair192) consider(kTilePair192, eff(2 * kBM, 192, num_sms / 2, 0.96));
-    if (allow_pairs & kAllowPair256) consider(kTilePair256, eff(2 * kBM, 256, num_sms / 2, 1.0));
-    return mode;
+    consider(kTile128, kBM, 128, 1, 0.55);
+    consider(kTile192, kBM, 192, 1, 0.76);
+    consider(kTile256, kBM, 256, 1, 0.90);
+    if (allow_pairs & kAllowPair192) consider(kTilePair192, 2 * kBM, 192, 2, 0.75);
+    if (allow_pairs & kAllowPair256) consider(kTilePair256, 2 * kBM, 256, 2, 1.0);
+    return choice;
 }
 
 }  // namespace mlpblk

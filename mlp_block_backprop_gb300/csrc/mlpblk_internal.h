@@ -103,6 +103,7 @@ struct GemmArgs {
     float *sk_partial;         // kMaxSkSlots slots of kSkSlotFloats: split-tile partial sums
     int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
+    int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
     int ld_aux;
     const float *rstd_in;      // DgradH: per-row rstd
