@@ -75,9 +75,10 @@ typedef struct {
 /*
  * Bytes of device workspace that mlpblk_forward and mlpblk_backward need for
  * `desc` (one size serves both).  Returns 0 for an invalid descriptor.  The
- * workspace holds scratch only (gamma-folded W1, the rstd-scaled dh, dn, and
- * the per-block dgamma partials); its contents need not be preserved between
- * calls, but two calls in flight at once must not share one workspace.
+ * workspace holds scratch only (gamma-folded W1, the rstd-scaled dh, dn, the
+ * per-block dgamma partials, and the GEMMs' stream-K partial sums and flags,
+ * which every call initialises itself); its contents need not be preserved
+ * between calls, but two calls in flight at once must not share one workspace.
  */
 size_t mlpblk_workspace_size(const mlpblk_desc *desc);
 
@@ -182,7 +183,7 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
  * Kernel timing hook for profiling harnesses (CUDA events, no profiler needed).
  * Kinds reported for each kernel launch the library makes:
  */
-#define MLPBLK_KERNEL_FOLD_GAMMA      1  /* W1g = W1 * gamma (forward)               */
+#define MLPBLK_KERNEL_FOLD_GAMMA      1  /* statistics pass: rstd, W1g = W1 * gamma  */
 #define MLPBLK_KERNEL_GEMM_FWD_W1     2  /* h, a = RMSNorm(x) . W1^T, relu^2         */
 #define MLPBLK_KERNEL_GEMM_FWD_W2     3  /* y = x + a . W2^T                          */
 #define MLPBLK_KERNEL_GEMM_DGRAD_H    4  /* dh = (dy . W2) * 2 relu(h)                */
@@ -193,7 +194,7 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_DGAMMA_REDUCE   9  /* dgamma += sum of parts                    */
 #define MLPBLK_KERNEL_ZERO_GRADS     10
 #define MLPBLK_KERNEL_SCALE_GRADS    11
-#define MLPBLK_KERNEL_RSTD           12  /* fp32 element type only                    */
+#define MLPBLK_KERNEL_RSTD           12  /* reserved (no launch uses it)              */
 
 /*
  * mlpblk_trace_begin: from now on, launch i of this library records

@@ -12,10 +12,17 @@
 //   warp 0      TMA producer: A/B tiles -> shared-memory ring of kStages stages
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
-//   warps 6..9  (forward W1 only) RMSNorm prologue: sum of x^2 per row, read from
-//               the A stages already in shared memory, gives rstd for the epilogue
+//   warps 6..9  (the in-GEMM RMSNorm variant of the forward W1 GEMM only) sum of
+//               x^2 per row, read from the A stages already in shared memory,
+//               gives rstd for the epilogue
 // The accumulator is double buffered in TMEM (2 x BN columns) so the epilogue of
 // one tile overlaps the main loop of the next.
+//
+// Work is a list of segments per worker (a CTA, or a CTA pair): whole tiles dealt
+// round robin, then optionally a contiguous range of the remaining tiles' k-blocks
+// ("stream-K", see SegIter), so every worker ends at the same time.  A tile split
+// between workers is finished by the one holding its first k-blocks from the
+// others' fp32 partial sums; the fp32 += epilogues simply add every segment.
 //
 // Two tile modes:
 //   single (PAIR = false): one CTA per SM computes a 128 x BN tile.
