@@ -51,6 +51,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--variant", default="saving", choices=["saving", "recompute"],
+                   help="saving: h and a saved by the forward; recompute: x and rstd saved, h and a "
+                        "rebuilt by one more W1 GEMM in the backward")
     return p.parse_args()
 
 
@@ -207,7 +210,8 @@ def run_ours(args, dist, peaks):
     dt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
     dev = "cuda"
     to = lambda a: torch.from_numpy(a).to(dev).to(dt)
-    bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps)
+    recompute = args.variant == "recompute"
+    bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps, recompute=recompute)
     bb.gamma.copy_(to(inp.gamma))
     bb.w1.copy_(to(inp.w1))
     bb.w2.copy_(to(inp.w2))
@@ -221,9 +225,14 @@ def run_ours(args, dist, peaks):
             if host_x is not None:
                 x_list[i].copy_(host_x[i], non_blocking=True)
                 dy_list[i].copy_(host_dy[i], non_blocking=True)
-            mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
-            mb.mlpblk_backward(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a, bb.rstd,
-                               bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+            if recompute:
+                mb.mlpblk_forward_recompute(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.rstd, bb.ws)
+                mb.mlpblk_backward_recompute(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.rstd,
+                                             bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+            else:
+                mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
+                mb.mlpblk_backward(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a, bb.rstd,
+                                   bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
             if dx_out is not None:
                 dx_out[i].copy_(bb.dx, non_blocking=True)
         if inp.grad_scale is not None:
@@ -235,7 +244,7 @@ def run_ours(args, dist, peaks):
     if mb.mlpblk_last_error() != mb.MLPBLK_OK:
         raise RuntimeError("device error during warm-up")
 
-    launches_per_step = 1 + n_mb * 9 + (1 if inp.grad_scale is not None else 0)
+    launches_per_step = 1 + n_mb * (11 if recompute else 9) + (1 if inp.grad_scale is not None else 0)
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
     clocks = ClockSampler(dist.local_rank)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -336,9 +345,16 @@ def run_ours(args, dist, peaks):
         "config": {"workload": args.workload, "tokens_per_microbatch": T, "microbatches": n_mb,
                    "d_model": d, "ffn": F, "shape": synth.CONFIGS[args.workload]["shape"],
                    "flop_per_step": flop_step,
+                   "variant": args.variant,
+                   # the recompute variant runs one more W1 GEMM per microbatch; the
+                   # metric stays the algorithmic 12*T*d*F per microbatch
+                   "executed_flop_per_step": flop_step * 7 // 6 if recompute else flop_step,
+                   "saved_activation_bytes_per_microbatch": (T * d * (2 if inp.dtype == "bf16" else 4) + 4 * T
+                                                             + (0 if recompute else
+                                                                2 * T * F * (2 if inp.dtype == "bf16" else 4))),
                    "l2": "inputs larger than L2 (working set %.1f GB per replica)" % (
                        (bb.ws.numel() + sum(t.numel() * t.element_size() for t in
-                        [bb.w1, bb.w2, bb.h, bb.a, bb.dw1, bb.dw2] + xs + dys)) / 1e9),
+                        [bb.w1, bb.w2, bb.h, bb.a, bb.dw1, bb.dw2] + xs + dys if t is not None)) / 1e9),
                    "parallelism": "replicas" if dist.world > 1 else "single",
                    "launch": launch_mode},
         "tokens_per_s": round(tokens_s, 1),

@@ -118,6 +118,42 @@ int mlpblk_backward(const mlpblk_desc *desc,
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Recompute variant: save x and rstd only, and rebuild h and a at the start of
+ * the backward ("Nemotron Kernels From Inference To Backpropagation" -- Part II:
+ * training must preserve or later recompute what reverse mode needs, and an
+ * engine states what is saved and what is recomputed; "grow_a_language_model_
+ * backprop" -- saved tensors dominate activation memory).  It trades the
+ * 2*T*F*elt bytes of saved h and a per block for one more W1 GEMM
+ * (2*T*d*F FLOP) in the backward; h and a live in the workspace only while a
+ * call runs, so one workspace serves every block of a model.
+ *
+ * mlpblk_workspace_size_recompute: bytes of workspace both recompute calls
+ * need (larger than mlpblk_workspace_size by the T x F h and a).  0 for an
+ * invalid descriptor.
+ *
+ * mlpblk_forward_recompute: y and rstd_saved exactly as mlpblk_forward writes
+ * them (same kernels and schedule, the W1 epilogue writing a alone into the
+ * workspace; bf16 keeps no h at all).
+ *
+ * mlpblk_backward_recompute: recomputes h and a from x, W1, gamma and
+ * rstd_saved with the forward's W1 GEMM (the same bits the forward produced),
+ * then runs mlpblk_backward's kernels; dx written, dgamma/dw1/dw2 += as there.
+ * Argument rules and return codes as for mlpblk_forward / mlpblk_backward.
+ */
+size_t mlpblk_workspace_size_recompute(const mlpblk_desc *desc);
+
+int mlpblk_forward_recompute(const mlpblk_desc *desc,
+                             const void *x, const void *gamma, const void *w1, const void *w2,
+                             void *y, float *rstd_saved,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_backward_recompute(const mlpblk_desc *desc,
+                              const void *dy, const void *x, const void *gamma,
+                              const void *w1, const void *w2, const float *rstd_saved,
+                              void *dx, float *dgamma, float *dw1, float *dw2,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --
  * accumulation across microbatches): dgamma[d], dw1[F,d], dw2[d,F] = 0 (float32).
  * desc->tokens is ignored.  Returns an MLPBLK_* code.

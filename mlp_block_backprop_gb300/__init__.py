@@ -29,7 +29,8 @@ MLPBLK_FP32 = 2
 EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpblk_zero_grads",
             "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version",
             "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
-            "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault")
+            "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault",
+            "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute")
 MLPBLK_TEST_FAULT_NONE = 0
 MLPBLK_TEST_FAULT_SKIP_LOADS = 1
 
@@ -66,6 +67,12 @@ def _load():
     lib.mlpblk_forward.restype = i32
     lib.mlpblk_backward.argtypes = [pd] + [vp] * 13 + [sz, vp]
     lib.mlpblk_backward.restype = i32
+    lib.mlpblk_workspace_size_recompute.argtypes = [pd]
+    lib.mlpblk_workspace_size_recompute.restype = sz
+    lib.mlpblk_forward_recompute.argtypes = [pd] + [vp] * 7 + [sz, vp]
+    lib.mlpblk_forward_recompute.restype = i32
+    lib.mlpblk_backward_recompute.argtypes = [pd] + [vp] * 11 + [sz, vp]
+    lib.mlpblk_backward_recompute.restype = i32
     lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_zero_grads.restype = i32
     lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
@@ -145,6 +152,27 @@ def mlpblk_backward(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx
     _check(rc, "mlpblk_backward")
 
 
+def mlpblk_workspace_size_recompute(desc: Desc) -> int:
+    return int(lib.mlpblk_workspace_size_recompute(ctypes.byref(desc)))
+
+
+def mlpblk_forward_recompute(desc, x, gamma, w1, w2, y, rstd_saved, workspace, workspace_bytes=None,
+                             stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_forward_recompute(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
+                                      _ptr(y), _ptr(rstd_saved), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_forward_recompute")
+
+
+def mlpblk_backward_recompute(desc, dy, x, gamma, w1, w2, rstd_saved, dx, dgamma, dw1, dw2, workspace,
+                              workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_backward_recompute(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1),
+                                       _ptr(w2), _ptr(rstd_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1),
+                                       _ptr(dw2), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_backward_recompute")
+
+
 def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):
     _check(lib.mlpblk_zero_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
                                  _stream(stream)), "mlpblk_zero_grads")
@@ -209,9 +237,11 @@ class KernelTrace:
 
 class BlockBuffers:
     """Device buffers of one block for microbatches of up to `tokens` rows:
-    parameters, saved tensors, outputs, fp32 gradient buffers and workspace."""
+    parameters, saved tensors, outputs, fp32 gradient buffers and workspace.
+    recompute=True uses the recompute variant (no h and a buffers; a larger
+    workspace holds them during each call)."""
 
-    def __init__(self, tokens, d_model, ffn, dtype="bf16", eps=1e-6, device="cuda"):
+    def __init__(self, tokens, d_model, ffn, dtype="bf16", eps=1e-6, device="cuda", recompute=False):
         import torch
         self.torch = torch
         self.dt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -226,23 +256,32 @@ class BlockBuffers:
         self.x = torch.empty(T, d, dtype=self.dt, **e)
         self.dy = torch.empty(T, d, dtype=self.dt, **e)
         self.y = torch.empty(T, d, dtype=self.dt, **e)
-        self.h = torch.empty(T, F, dtype=self.dt, **e)
-        self.a = torch.empty(T, F, dtype=self.dt, **e)
+        self.recompute = recompute
+        self.h = None if recompute else torch.empty(T, F, dtype=self.dt, **e)
+        self.a = None if recompute else torch.empty(T, F, dtype=self.dt, **e)
         self.rstd = torch.empty(T, dtype=torch.float32, **e)
         self.dx = torch.empty(T, d, dtype=self.dt, **e)
         self.dgamma = torch.zeros(d, dtype=torch.float32, **e)
         self.dw1 = torch.zeros(F, d, dtype=torch.float32, **e)
         self.dw2 = torch.zeros(d, F, dtype=torch.float32, **e)
-        ws = mlpblk_workspace_size(self.desc)
+        ws = (mlpblk_workspace_size_recompute if recompute else mlpblk_workspace_size)(self.desc)
         if ws == 0:
             raise MlpBlkError(MLPBLK_EINVAL, "mlpblk_workspace_size")
         self.ws = torch.empty(ws, dtype=torch.uint8, **e)
 
     def forward(self, stream=None):
+        if self.recompute:
+            mlpblk_forward_recompute(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.rstd,
+                                     self.ws, stream=stream)
+            return
         mlpblk_forward(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.h, self.a,
                        self.rstd, self.ws, stream=stream)
 
     def backward(self, stream=None):
+        if self.recompute:
+            mlpblk_backward_recompute(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.rstd,
+                                      self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)
+            return
         mlpblk_backward(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a,
                         self.rstd, self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)
 

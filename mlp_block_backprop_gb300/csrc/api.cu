@@ -52,24 +52,33 @@ int check_desc(const mlpblk_desc *d) {
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-    int64_t w1g, dh, dn, part, sk_partial, sk_flags, total;
+    int64_t w1g, dh, h, a, dn, part, sk_partial, sk_flags, total;
 };
 
 // Stream-K flag sets, one per tensor-core GEMM that can split a tile; each set
 // is zeroed by the kernel launched just before that GEMM.
 enum SkFlagSet : int { kSetFwdW1 = 0, kSetFwdW2 = 1, kSetDgradH = 2, kSetDgradN = 3, kSkSets = 4 };
 
-WsLayout ws_layout(const mlpblk_desc *d) {
+// Workspace regions.  W1*gamma (forward, and the recompute backward's first
+// GEMM) shares its region with dh_s (backward).  `recompute` adds the T x F
+// h and a that the recompute variant keeps in the workspace instead of saving.
+WsLayout ws_layout(const mlpblk_desc *d, bool recompute) {
     const int64_t elt = d->dtype == MLPBLK_BF16 ? 2 : 4;
+    const int64_t tf = align256(d->tokens * d->ffn * elt);
+    const int64_t fd = align256(d->ffn * d->d_model * elt);
     WsLayout l;
     l.w1g = 0;
-    const int64_t fwd = align256(d->ffn * d->d_model * elt);
     l.dh = 0;
-    l.dn = align256(d->tokens * d->ffn * elt);
+    int64_t off = recompute ? (tf > fd ? tf : fd) : tf;
+    l.h = recompute ? off : -1;
+    if (recompute) off += tf;
+    l.a = recompute ? off : -1;
+    if (recompute) off += tf;
+    l.dn = off;
     l.part = l.dn + align256(d->tokens * d->d_model * 4);
     const int64_t bwd = l.part + align256(static_cast<int64_t>(kMaxParts) * d->d_model * 4);
     // the GEMMs' stream-K partial sums and flags, apart from everything above
-    l.sk_partial = fwd > bwd ? fwd : bwd;
+    l.sk_partial = fd > bwd ? fd : bwd;
     l.sk_flags = l.sk_partial + align256(static_cast<int64_t>(kMaxSkSlots) * kSkSlotFloats * 4);
     l.total = l.sk_flags + align256(static_cast<int64_t>(kSkSets) * kSkFlagsPerSet * 4);
     return l;
@@ -177,32 +186,23 @@ const char *mlpblk_strerror(int code) {
 
 size_t mlpblk_workspace_size(const mlpblk_desc *desc) {
     if (check_desc(desc) != MLPBLK_OK) return 0;
-    return static_cast<size_t>(ws_layout(desc).total);
+    return static_cast<size_t>(ws_layout(desc, false).total);
 }
 
-int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1,
-                   const void *w2, void *y, void *h_saved, void *a_saved, float *rstd_saved,
-                   void *workspace, size_t workspace_bytes, void *stream) {
-    MLPBLK_TRY(check_desc(desc));
-    if (desc->tokens == 0) return MLPBLK_OK;
-    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) ||
-        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(workspace))
-        return MLPBLK_EINVAL;
-    if (y == x) return MLPBLK_EINVAL;
-    const WsLayout l = ws_layout(desc);
-    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
-    int sms = 0;
-    MLPBLK_TRY(device_sms(&sms));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    void *w1g = ws + l.w1g;
-    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
-    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+}  // extern "C"
 
-    const bool stats_in_gemm = desc->dtype == MLPBLK_BF16 && rms_in_gemm();
+namespace {
+
+// The forward's launches.  h_out may be null on the bf16 path (a_only: the
+// recompute variant's forward, whose W1 epilogue writes a alone).
+int forward_impl(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1,
+                 const void *w2, void *y, void *h_out, void *a_out, float *rstd_saved, void *w1g,
+                 float *sk_partial, int *sk_flags, int sms, cudaStream_t s, bool a_only) {
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    const bool stats_in_gemm = desc->dtype == MLPBLK_BF16 && !a_only && rms_in_gemm();
     if (stats_in_gemm)
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s, launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                      launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, nullptr, 0, s));
     else
         MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
                       launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, w1, gamma, w1g, F,
@@ -220,55 +220,39 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
         g1.sk_partial = sk_partial;
         g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
         g1.zero_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
+        const int epi1 = a_only ? kEpiFwdW1A : (stats_in_gemm ? kEpiFwdW1 : kEpiFwdW1Pre);
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
-                      launch_gemm_tc_fwd(stats_in_gemm ? kEpiFwdW1 : kEpiFwdW1Pre, (int)T, (int)F, (int)d,
-                                         x, w1g, h_saved, a_saved, g1, sms, s));
+                      launch_gemm_tc_fwd(epi1, (int)T, (int)F, (int)d, x, w1g, a_only ? a_out : h_out,
+                                         a_only ? nullptr : a_out, g1, sms, s));
         GemmArgs g2 = {};
         g2.aux = static_cast<const uint16_t *>(x);
         g2.ld_aux = (int)d;
         g2.sk_partial = sk_partial;
         g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_saved, w2, y, nullptr, g2, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_tc_fwd(kEpiFwdW2, (int)T, (int)d, (int)F, a_out, w2, y, nullptr, g2, sms, s));
     } else {
         const float *xf = static_cast<const float *>(x);
         SimtEpi e1 = {nullptr, rstd_saved, nullptr};
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s, launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, xf, d, 1,
                                     static_cast<const float *>(w1g), d, 1,
-                                    static_cast<float *>(h_saved), static_cast<float *>(a_saved), e1, s));
+                                    static_cast<float *>(h_out), static_cast<float *>(a_out), e1, s));
         SimtEpi e2 = {xf, nullptr, nullptr};
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s, launch_gemm_simt(kEpiFwdW2, (int)T, (int)d, (int)F,
-                                    static_cast<const float *>(a_saved), F, 1,
+                                    static_cast<const float *>(a_out), F, 1,
                                     static_cast<const float *>(w2), F, 1, static_cast<float *>(y),
                                     nullptr, e2, s));
     }
     return MLPBLK_OK;
 }
 
-int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
-                    const void *w1, const void *w2, const void *h_saved, const void *a_saved,
-                    const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
-                    void *workspace, size_t workspace_bytes, void *stream) {
-    MLPBLK_TRY(check_desc(desc));
-    if (desc->tokens == 0) return MLPBLK_OK;
-    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
-        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(dx) ||
-        !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
-        return MLPBLK_EINVAL;
-    if (dx == dy || dx == x) return MLPBLK_EINVAL;
-    const WsLayout l = ws_layout(desc);
-    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
-    int sms = 0;
-    MLPBLK_TRY(device_sms(&sms));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The backward's launches, from saved (or recomputed) h and a.
+int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                  const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                  const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                  void *dh_s, float *dn_s, float *part, float *sk_partial, int *sk_flags, int sms,
+                  cudaStream_t s) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    void *dh_s = ws + l.dh;
-    float *dn_s = reinterpret_cast<float *>(ws + l.dn);
-    float *part = reinterpret_cast<float *>(ws + l.part);
-    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
-    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
     int parts = 0;  // dgamma partial rows written by the norm kernel
-
     if (desc->dtype == MLPBLK_BF16) {
         // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's
         GemmArgs gw2 = {};
@@ -309,6 +293,125 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
     MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1,
+                   const void *w2, void *y, void *h_saved, void *a_saved, float *rstd_saved,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) ||
+        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, false);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return forward_impl(desc, x, gamma, w1, w2, y, h_saved, a_saved, rstd_saved, ws + l.w1g,
+                        reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
+                        sms, static_cast<cudaStream_t>(stream), false);
+}
+
+int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                    const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                    const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
+        !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(dx) ||
+        !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, false);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return backward_impl(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
+                         ws + l.dh, reinterpret_cast<float *>(ws + l.dn), reinterpret_cast<float *>(ws + l.part),
+                         reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
+                         sms, static_cast<cudaStream_t>(stream));
+}
+
+size_t mlpblk_workspace_size_recompute(const mlpblk_desc *desc) {
+    if (check_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(ws_layout(desc, true).total);
+}
+
+int mlpblk_forward_recompute(const mlpblk_desc *desc, const void *x, const void *gamma,
+                             const void *w1, const void *w2, void *y, float *rstd_saved,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) ||
+        !aligned16(rstd_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, true);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // bf16: the W1 epilogue writes a alone; fp32: h goes to scratch
+    const bool bf16 = desc->dtype == MLPBLK_BF16;
+    return forward_impl(desc, x, gamma, w1, w2, y, bf16 ? nullptr : ws + l.h, ws + l.a, rstd_saved,
+                        ws + l.w1g, reinterpret_cast<float *>(ws + l.sk_partial),
+                        reinterpret_cast<int *>(ws + l.sk_flags), sms, static_cast<cudaStream_t>(stream), bf16);
+}
+
+int mlpblk_backward_recompute(const mlpblk_desc *desc, const void *dy, const void *x,
+                              const void *gamma, const void *w1, const void *w2,
+                              const float *rstd_saved, void *dx, float *dgamma, float *dw1,
+                              float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
+        !aligned16(rstd_saved) || !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) ||
+        !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, true);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *w1g = ws + l.w1g;
+    void *h = ws + l.h;
+    void *a = ws + l.a;
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    // h and a again, from x and the saved rstd: the forward's W1 GEMM (same
+    // configuration and schedule, so the same bits)
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                  launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, sk_flags + kSetFwdW1 * kSkFlagsPerSet,
+                                    kSkFlagsPerSet, s));
+    if (desc->dtype == MLPBLK_BF16) {
+        GemmArgs g1 = {};
+        g1.rstd_in = rstd_saved;
+        g1.sk_partial = sk_partial;
+        g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                      launch_gemm_tc_fwd(kEpiFwdW1Pre, (int)T, (int)F, (int)d, x, w1g, h, a, g1, sms, s));
+    } else {
+        SimtEpi e1 = {nullptr, rstd_saved, nullptr};
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                      launch_gemm_simt(kEpiFwdW1, (int)T, (int)F, (int)d, static_cast<const float *>(x), d, 1,
+                                       static_cast<const float *>(w1g), d, 1, static_cast<float *>(h),
+                                       static_cast<float *>(a), e1, s));
+    }
+    // dh_s takes the W1*gamma region, which the GEMM above was the last to read
+    return backward_impl(desc, dy, x, gamma, w1, w2, h, a, rstd_saved, dx, dgamma, dw1, dw2, ws + l.dh,
+                         reinterpret_cast<float *>(ws + l.dn), reinterpret_cast<float *>(ws + l.part),
+                         sk_partial, sk_flags, sms, s);
 }
 
 int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {

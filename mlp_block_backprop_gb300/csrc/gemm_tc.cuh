@@ -56,10 +56,11 @@ struct GemmCfg {
     static constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // rows of one output tile
     static constexpr int kBRows = PAIR ? BN / 2 : BN;    // rows of B staged per CTA
     static constexpr bool kNorm = (EPI == kEpiFwdW1);
-    static constexpr bool kReluSq = (EPI == kEpiFwdW1 || EPI == kEpiFwdW1Pre);  // h and a out
+    static constexpr bool kReluSq = (EPI == kEpiFwdW1 || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A);
+    static constexpr bool kAOnly = (EPI == kEpiFwdW1A);  // a out only (h is not kept)
     static constexpr bool kOutBf16 = (kReluSq || EPI == kEpiFwdW2 || EPI == kEpiDgradH);
     static constexpr bool kReduce = (EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
-    static constexpr int kNumOut = kReluSq ? 2 : 1;
+    static constexpr int kNumOut = (kReluSq && !kAOnly) ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
     static constexpr int kThreads = kNorm ? 320 : 192;
@@ -75,7 +76,7 @@ struct GemmCfg {
     // the two-output W1 epilogue, whose shared memory goes to a deeper pipeline
     static constexpr int kStagingBufs = kNumOut == 2 ? 1 : 2;
     static constexpr int kStagingBytes = kAux ? 0 : 4 * kNumOut * kStagingBufs * 4096;
-    static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre);  // rstd from memory
+    static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A);
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
     static constexpr int kAlignSlack = 1024;
     static constexpr int kStagesRaw =
@@ -541,9 +542,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float h0 = rsc * e[2 * i], h1 = rsc * e[2 * i + 1];
-                                o[i] = pack_bf16x2(h0, h1);
                                 const float r0 = h0 > 0.0f ? h0 : 0.0f, r1 = h1 > 0.0f ? h1 : 0.0f;
-                                o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                                if (C::kAOnly) {
+                                    o[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                                } else {
+                                    o[i] = pack_bf16x2(h0, h1);
+                                    o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                                }
                             }
                         } else if (C::EPI == kEpiFwdW2) {
                             const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};

@@ -81,6 +81,7 @@ enum Epilogue : int {
     kEpiAccF32 = 4,   // out += acc (fp32, TMA reduce-add)
     kEpiAccF32ColScale = 5,  // out += colscale[n] * acc (fp32, TMA reduce-add)
     kEpiFwdW1Pre = 6, // h = rstd*acc, a = relu(h)^2 (bf16 x2); rstd read from global
+    kEpiFwdW1A = 7,   // a = relu(rstd*acc)^2 only (bf16); rstd read from global
 };
 
 // Arguments of one GEMM launch (the tensor maps travel separately).
@@ -129,7 +130,7 @@ int take_device_error_gemm();
 
 // Host: row/element kernels (rowops.cu).  All return MLPBLK_* codes.
 int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, int64_t F,
-                      int64_t d, cudaStream_t s);
+                      int64_t d, int *zero_flags, int zero_count, cudaStream_t s);
 int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps,
                     cudaStream_t s);
 // Forward statistics pass: rstd[T] of x and W1g = W1 * gamma in one launch.

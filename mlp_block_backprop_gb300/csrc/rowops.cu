@@ -62,8 +62,12 @@ struct Io8<float> {
 // 8 consecutive elements (d is a multiple of 8, so a group never crosses rows).
 template <class T>
 __global__ void fold_gamma_kernel(const T *__restrict__ w1, const T *__restrict__ gamma,
-                                  T *__restrict__ w1g, int64_t groups, int64_t d) {
+                                  T *__restrict__ w1g, int64_t groups, int64_t d, int *zero_flags,
+                                  int zero_count) {
     griddep_enter();
+    // the following GEMM's stream-K flags start from zero
+    if (zero_flags && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_flags[i] = 0;
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t e = g * 8;
@@ -452,16 +456,16 @@ int dispatch_norm_bwd(const void *x, const float *dn, const void *dy, const floa
 }  // namespace
 
 int launch_fold_gamma(int dtype, const void *w1, const void *gamma, void *w1g, int64_t F,
-                      int64_t d, cudaStream_t s) {
+                      int64_t d, int *zero_flags, int zero_count, cudaStream_t s) {
     const int64_t groups = F * d / 8;
     const int grid = grid_for(groups, 256);
     if (dtype == MLPBLK_BF16)
         return launch_pdl(fold_gamma_kernel<uint16_t>, dim3(grid), dim3(256), 0, s,
                           static_cast<const uint16_t *>(w1), static_cast<const uint16_t *>(gamma),
-                          static_cast<uint16_t *>(w1g), groups, d);
+                          static_cast<uint16_t *>(w1g), groups, d, zero_flags, zero_count);
     return launch_pdl(fold_gamma_kernel<float>, dim3(grid), dim3(256), 0, s,
                       static_cast<const float *>(w1), static_cast<const float *>(gamma),
-                      static_cast<float *>(w1g), groups, d);
+                      static_cast<float *>(w1g), groups, d, zero_flags, zero_count);
 }
 
 int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d, float eps,

@@ -101,6 +101,34 @@ def test_backward_and_grad_argument_errors_need_no_device(mb):
                                      None) == mb.MLPBLK_EINVAL
 
 
+def test_recompute_argument_errors_need_no_device(mb):
+    d = mb.make_desc(64, 128, 256)
+    assert mb.lib.mlpblk_workspace_size_recompute(ctypes.byref(d)) >= (
+        mb.lib.mlpblk_workspace_size(ctypes.byref(d)) + 2 * 64 * 256 * 2)
+    assert mb.lib.mlpblk_workspace_size_recompute(ctypes.byref(mb.make_desc(8, 100, 64))) == 0
+    fwd = [0x10000 * (i + 1) for i in range(7)]
+    f = lambda args, ws=1 << 40: mb.lib.mlpblk_forward_recompute(ctypes.byref(d), *args, ws, None)
+    bad = list(fwd)
+    bad[5] = None  # rstd
+    assert f(bad) == mb.MLPBLK_EINVAL
+    alias = list(fwd)
+    alias[4] = alias[0]  # y == x
+    assert f(alias) == mb.MLPBLK_EINVAL
+    # the saving path's workspace is too small for the recompute variant
+    assert f(fwd, mb.lib.mlpblk_workspace_size(ctypes.byref(d))) == mb.MLPBLK_EWORKSPACE
+    bwd = [0x10000 * (i + 1) for i in range(11)]
+    b = lambda args, ws=1 << 40: mb.lib.mlpblk_backward_recompute(ctypes.byref(d), *args, ws, None)
+    bad = list(bwd)
+    bad[7] += 4  # dgamma misaligned
+    assert b(bad) == mb.MLPBLK_EINVAL
+    alias = list(bwd)
+    alias[6] = alias[1]  # dx == x
+    assert b(alias) == mb.MLPBLK_EINVAL
+    assert b(bwd, 16) == mb.MLPBLK_EWORKSPACE
+    empty = ctypes.byref(mb.make_desc(0, 128, 256))
+    assert mb.lib.mlpblk_backward_recompute(empty, *([None] * 11), 0, None) == mb.MLPBLK_OK
+
+
 def test_grad_buffers_are_float32_by_contract():
     """The gradient accumulators are declared float32: the bf16 loss of a small
     contribution next to a large running sum is why."""
