@@ -51,6 +51,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--optimizer", action="store_true",
+                   help="end each step with the optimizer-side kernels: global gradient norm, "
+                        "clip scale, fused AdamW on float32 master weights")
     p.add_argument("--variant", default="saving", choices=["saving", "recompute"],
                    help="saving: h and a saved by the forward; recompute: x and rstd saved, h and a "
                         "rebuilt by one more W1 GEMM in the backward")
@@ -196,6 +199,13 @@ def algorithmic_work(kind, T, d, F, parts):
         return 8.0 * (2 * F * d + d), "byte"
     if kind == "dgamma_reduce":
         return 4.0 * parts * d + 8.0 * d, "byte"
+    if kind == "grad_norm":
+        return 4.0 * (2 * F * d + d), "byte"
+    if kind == "clip_grads":
+        return 8.0 * (2 * F * d + d), "byte"
+    if kind == "adamw":
+        # master, grad, m, v read; master, m, v written (fp32); bf16 working copy written
+        return 30.0 * (2 * F * d + d), "byte"
     return None, None
 
 
@@ -218,6 +228,16 @@ def run_ours(args, dist, peaks):
     xs = [to(x) for x in inp.x]
     dys = [to(g) for g in inp.dy]
     desc = bb.desc
+    if args.optimizer:
+        # float32 master weights and AdamW moments; the bf16 weights are the working copy
+        masters = {k: torch.from_numpy(a.astype("float32")).to(dev) for k, a in
+                   (("gamma", inp.gamma), ("w1", inp.w1), ("w2", inp.w2))}
+        moments = {k: (torch.zeros_like(t), torch.zeros_like(t)) for k, t in masters.items()}
+        norm_scale = torch.zeros(2, dtype=torch.float32, device=dev)
+        hp = mb.AdamW(1e-4, 0.9, 0.95, 1e-8, 0.1)
+        opt_params = [(masters["gamma"], bb.gamma, bb.dgamma, *moments["gamma"], False),
+                      (masters["w1"], bb.w1, bb.dw1, *moments["w1"], True),
+                      (masters["w2"], bb.w2, bb.dw2, *moments["w2"], True)]
 
     def step(x_list, dy_list, dx_out=None, host_x=None, host_dy=None):
         mb.mlpblk_zero_grads(desc, bb.dgamma, bb.dw1, bb.dw2)
@@ -237,6 +257,11 @@ def run_ours(args, dist, peaks):
                 dx_out[i].copy_(bb.dx, non_blocking=True)
         if inp.grad_scale is not None:
             mb.mlpblk_scale_grads(desc, bb.dgamma, bb.dw1, bb.dw2, inp.grad_scale)
+        if args.optimizer:
+            # a CUDA graph keeps the step number it was captured with; the update's
+            # cost does not depend on it
+            mb.mlpblk_grad_norm(desc, bb.dgamma, bb.dw1, bb.dw2, 1.0, norm_scale[0:1], norm_scale[1:2], bb.ws)
+            mb.mlpblk_adamw_step(opt_params, hp, 1, bb.code, grad_scale=norm_scale[1:2])
 
     for _ in range(args.warmup):
         step(xs, dys)
@@ -244,7 +269,8 @@ def run_ours(args, dist, peaks):
     if mb.mlpblk_last_error() != mb.MLPBLK_OK:
         raise RuntimeError("device error during warm-up")
 
-    launches_per_step = 1 + n_mb * (11 if recompute else 9) + (1 if inp.grad_scale is not None else 0)
+    launches_per_step = (1 + n_mb * (11 if recompute else 9) + (1 if inp.grad_scale is not None else 0)
+                         + (3 if args.optimizer else 0))
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
     clocks = ClockSampler(dist.local_rank)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -321,6 +347,8 @@ def run_ours(args, dist, peaks):
         if kind not in per:
             return None
         amount, unit = algorithmic_work(kind, T, d, F, parts)
+        if amount is None:  # a launch with no bandwidth or FLOP roof of its own (a scalar finalize)
+            return None
         mean_s = per[kind][1] / per[kind][0] * 1e-3
         traffic = recorded_traffic(args.workload, kind)
         if unit == "flop":
@@ -346,6 +374,7 @@ def run_ours(args, dist, peaks):
                    "d_model": d, "ffn": F, "shape": synth.CONFIGS[args.workload]["shape"],
                    "flop_per_step": flop_step,
                    "variant": args.variant,
+                   "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch
                    "executed_flop_per_step": flop_step * 7 // 6 if recompute else flop_step,

@@ -154,6 +154,59 @@ int mlpblk_backward_recompute(const mlpblk_desc *desc,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Optimizer-side steps after the accumulation loop ("grow_a_language_model_
+ * backprop" -- the two-stage gradient-norm kernels and the gradient scale used
+ * for clipping; "optimizer state": AdamW holds a first and a second moment per
+ * weight; "Losing small gradient contributions in BF16": the state an update
+ * accumulates into stays float32).  All asynchronous on `stream`; the norm and
+ * the clip scale stay on the device, so clipping needs no host round trip.
+ *
+ * mlpblk_grad_norm: norm_out[0] = sqrt(sum of g^2 over dgamma[d], dw1[F,d],
+ *   dw2[d,F]) and clip_scale_out[0] = min(1, max_norm / (norm + 1e-6)), both
+ *   float32 device scalars (either may be NULL, not both).  Per-CTA partial sums
+ *   (float32 with compensation, then float64) go to `workspace`
+ *   (>= mlpblk_workspace_size(desc) bytes) and are added in a fixed order.
+ *   max_norm > 0 and finite.  desc->tokens is ignored.
+ *
+ * mlpblk_clip_grads: dgamma, dw1, dw2 *= clip_scale[0] (a device scalar, e.g.
+ *   the one mlpblk_grad_norm wrote).
+ *
+ * mlpblk_adamw_step: one AdamW update (decoupled weight decay; Loshchilov &
+ *   Hutter, "Decoupled Weight Decay Regularization", Algorithm 2) of `count`
+ *   tensors, `step` >= 1 counting updates:
+ *     g <- g * grad_scale[0] (if grad_scale is not NULL), w <- w * (1 - lr*wd)
+ *     (tensors with decay != 0), m <- b1*m + (1-b1)*g, v <- b2*v + (1-b2)*g^2,
+ *     w <- w - lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
+ *   on the float32 master weights, then weight = w in `dtype` (MLPBLK_BF16:
+ *   rounded to nearest even; weight may be NULL).  master, grad, m, v 16-byte
+ *   aligned, weight 8-byte (bf16) / 16-byte (fp32) aligned, n a positive
+ *   multiple of 4; grads are read only.  Returns MLPBLK_EINVAL on bad
+ *   hyper-parameters (0 <= beta < 1, lr >= 0, eps >= 0, wd >= 0, finite).
+ */
+typedef struct {
+    float       *master;  /* float32 master weights [n] (updated)                 */
+    void        *weight;  /* working copy in `dtype` [n] (written) or NULL         */
+    const float *grad;    /* float32 gradient [n]                                  */
+    float       *m, *v;   /* AdamW first and second moments [n] (updated)         */
+    int64_t      n;       /* elements                                             */
+    int32_t      decay;   /* nonzero: apply the weight decay to this tensor        */
+} mlpblk_param;
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} mlpblk_adamw;
+
+int mlpblk_grad_norm(const mlpblk_desc *desc, const float *dgamma, const float *dw1,
+                     const float *dw2, float max_norm, float *norm_out, float *clip_scale_out,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_clip_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2,
+                      const float *clip_scale, void *stream);
+
+int mlpblk_adamw_step(const mlpblk_param *params, int count, const mlpblk_adamw *hp,
+                      int64_t step, int dtype, const float *grad_scale, void *stream);
+
+/*
  * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --
  * accumulation across microbatches): dgamma[d], dw1[F,d], dw2[d,F] = 0 (float32).
  * desc->tokens is ignored.  Returns an MLPBLK_* code.
@@ -231,6 +284,10 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_ZERO_GRADS     10
 #define MLPBLK_KERNEL_SCALE_GRADS    11
 #define MLPBLK_KERNEL_RSTD           12  /* reserved (no launch uses it)              */
+#define MLPBLK_KERNEL_GRAD_NORM      13  /* per-CTA partial sums of g^2               */
+#define MLPBLK_KERNEL_CLIP_GRADS     14  /* g *= clip scale (device scalar)           */
+#define MLPBLK_KERNEL_ADAMW          15  /* fused AdamW update                        */
+#define MLPBLK_KERNEL_GRAD_NORM_FINAL 16 /* partials -> norm and clip scale           */
 
 /*
  * mlpblk_trace_begin: from now on, launch i of this library records

@@ -30,13 +30,15 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_scale_grads", "mlpblk_last_error", "mlpblk_strerror", "mlpblk_version",
             "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
             "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault",
-            "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute")
+            "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute",
+            "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step")
 MLPBLK_TEST_FAULT_NONE = 0
 MLPBLK_TEST_FAULT_SKIP_LOADS = 1
 
 KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dgrad_h",
                 5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
-                9: "dgamma_reduce", 10: "zero_grads", 11: "scale_grads", 12: "rstd"}
+                9: "dgamma_reduce", 10: "zero_grads", 11: "scale_grads", 12: "rstd",
+                13: "grad_norm", 14: "clip_grads", 15: "adamw", 16: "grad_norm_final"}
 
 
 class MlpBlkError(RuntimeError):
@@ -52,6 +54,18 @@ class Desc(ctypes.Structure):
     """mlpblk_desc: shape of one microbatch through one block."""
     _fields_ = [("tokens", ctypes.c_int64), ("d_model", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class Param(ctypes.Structure):
+    """mlpblk_param: one tensor of an AdamW update."""
+    _fields_ = [("master", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("m", ctypes.c_void_p), ("v", ctypes.c_void_p), ("n", ctypes.c_int64), ("decay", ctypes.c_int32)]
+
+
+class AdamW(ctypes.Structure):
+    """mlpblk_adamw: AdamW hyper-parameters."""
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
 
 
 def _load():
@@ -73,6 +87,12 @@ def _load():
     lib.mlpblk_forward_recompute.restype = i32
     lib.mlpblk_backward_recompute.argtypes = [pd] + [vp] * 11 + [sz, vp]
     lib.mlpblk_backward_recompute.restype = i32
+    lib.mlpblk_grad_norm.argtypes = [pd, vp, vp, vp, f32, vp, vp, vp, sz, vp]
+    lib.mlpblk_grad_norm.restype = i32
+    lib.mlpblk_clip_grads.argtypes = [pd, vp, vp, vp, vp, vp]
+    lib.mlpblk_clip_grads.restype = i32
+    lib.mlpblk_adamw_step.argtypes = [ctypes.POINTER(Param), i32, ctypes.POINTER(AdamW), ctypes.c_int64, i32, vp, vp]
+    lib.mlpblk_adamw_step.restype = i32
     lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_zero_grads.restype = i32
     lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
@@ -171,6 +191,30 @@ def mlpblk_backward_recompute(desc, dy, x, gamma, w1, w2, rstd_saved, dx, dgamma
                                        _ptr(w2), _ptr(rstd_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1),
                                        _ptr(dw2), _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "mlpblk_backward_recompute")
+
+
+def mlpblk_grad_norm(desc, dgamma, dw1, dw2, max_norm, norm_out, clip_scale_out, workspace,
+                     workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_grad_norm(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2), float(max_norm),
+                              _ptr(norm_out), _ptr(clip_scale_out), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_grad_norm")
+
+
+def mlpblk_clip_grads(desc, dgamma, dw1, dw2, clip_scale, stream=None):
+    rc = lib.mlpblk_clip_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2), _ptr(clip_scale),
+                               _stream(stream))
+    _check(rc, "mlpblk_clip_grads")
+
+
+def mlpblk_adamw_step(params, hp, step, dtype, grad_scale=None, stream=None):
+    """params: sequence of (master, weight, grad, m, v, decay) tensors/flags; hp: AdamW."""
+    arr = (Param * len(params))()
+    for i, (master, weight, grad, m, v, decay) in enumerate(params):
+        arr[i] = Param(_ptr(master), _ptr(weight), _ptr(grad), _ptr(m), _ptr(v), master.numel(), int(decay))
+    rc = lib.mlpblk_adamw_step(arr, len(params), ctypes.byref(hp), int(step), int(dtype), _ptr(grad_scale),
+                               _stream(stream))
+    _check(rc, "mlpblk_adamw_step")
 
 
 def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):

@@ -414,6 +414,68 @@ int mlpblk_backward_recompute(const mlpblk_desc *desc, const void *dy, const voi
                          sk_partial, sk_flags, sms, s);
 }
 
+int mlpblk_grad_norm(const mlpblk_desc *desc, const float *dgamma, const float *dw1, const float *dw2,
+                     float max_norm, float *norm_out, float *clip_scale_out, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (!norm_out && !clip_scale_out) return MLPBLK_EINVAL;
+    if ((norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 3u)) ||
+        (clip_scale_out && (reinterpret_cast<uintptr_t>(clip_scale_out) & 3u)))
+        return MLPBLK_EINVAL;
+    if (!(max_norm > 0.0f) || !isfinite(max_norm)) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, false);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    const int64_t d = desc->d_model, F = desc->ffn;
+    const int64_t part_bytes = static_cast<int64_t>(kMaxParts) * d * 4;
+    const int max_parts = static_cast<int>(part_bytes / 8 < 1024 ? part_bytes / 8 : 1024);
+    double *partial = reinterpret_cast<double *>(static_cast<uint8_t *>(workspace) + l.part);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int parts = 0;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GRAD_NORM, s,
+                  launch_grad_norm_partial(dgamma, d, dw1, F * d, dw2, F * d, partial, max_parts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GRAD_NORM_FINAL, s,
+                  launch_grad_norm_final(partial, parts, max_norm, norm_out, clip_scale_out, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_clip_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, const float *clip_scale,
+                      void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
+    if (!clip_scale || (reinterpret_cast<uintptr_t>(clip_scale) & 3u)) return MLPBLK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t d = desc->d_model, F = desc->ffn;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_CLIP_GRADS, s, launch_clip_grads(dgamma, d, dw1, F * d, dw2, F * d, clip_scale, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_adamw_step(const mlpblk_param *params, int count, const mlpblk_adamw *hp, int64_t step, int dtype,
+                      const float *grad_scale, void *stream) {
+    if (!params || count < 1 || count > 1024 || !hp || step < 1) return MLPBLK_EINVAL;
+    if (dtype != MLPBLK_BF16 && dtype != MLPBLK_FP32) return MLPBLK_ENOTSUP;
+    const float vals[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    for (float v : vals)
+        if (!isfinite(v) || v < 0.0f) return MLPBLK_EINVAL;
+    if (!(hp->beta1 < 1.0f) || !(hp->beta2 < 1.0f)) return MLPBLK_EINVAL;
+    if (grad_scale && (reinterpret_cast<uintptr_t>(grad_scale) & 3u)) return MLPBLK_EINVAL;
+    const uintptr_t walign = dtype == MLPBLK_BF16 ? 7u : 15u;
+    AdamTensor t[1024];
+    for (int i = 0; i < count; ++i) {
+        const mlpblk_param &p = params[i];
+        if (!aligned16(p.master) || !aligned16(p.grad) || !aligned16(p.m) || !aligned16(p.v)) return MLPBLK_EINVAL;
+        if (p.weight && (reinterpret_cast<uintptr_t>(p.weight) & walign)) return MLPBLK_EINVAL;
+        if (p.n <= 0 || p.n % 4 != 0) return MLPBLK_EINVAL;
+        t[i] = AdamTensor{p.master, p.weight, p.grad, p.m, p.v, p.n, p.decay != 0};
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ADAMW, s,
+                  launch_adamw(t, count, hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, step,
+                               dtype == MLPBLK_BF16, grad_scale, s));
+    return MLPBLK_OK;
+}
+
 int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {
     MLPBLK_TRY(check_desc(desc));
     if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;

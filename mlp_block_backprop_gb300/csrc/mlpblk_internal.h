@@ -158,6 +158,25 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
 int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,
                  int64_t n2, cudaStream_t s);
 
+// Host: optimizer-side kernels (optim.cu).  Tensor sizes in elements, multiples
+// of 4, 16-byte aligned.
+struct AdamTensor {
+    float *master;       // fp32 master weights (updated)
+    void *weight;        // working copy in the block's element type (written), or null
+    const float *grad;   // fp32 gradient
+    float *m, *v;        // moments (updated)
+    int64_t n;
+    int decay;           // apply the weight decay to this tensor
+};
+int launch_grad_norm_partial(const float *g0, int64_t n0, const float *g1, int64_t n1, const float *g2,
+                             int64_t n2, double *partial, int max_parts, int *parts_out, cudaStream_t s);
+int launch_grad_norm_final(const double *partial, int parts, float max_norm, float *norm_out, float *scale_out,
+                           cudaStream_t s);
+int launch_clip_grads(float *g0, int64_t n0, float *g1, int64_t n1, float *g2, int64_t n2, const float *scale,
+                      cudaStream_t s);
+int launch_adamw(const AdamTensor *tensors, int count, float lr, float beta1, float beta2, float eps,
+                 float weight_decay, int64_t step, bool bf16, const float *grad_scale, cudaStream_t s);
+
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].
 struct SimtEpi {

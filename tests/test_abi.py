@@ -129,6 +129,33 @@ def test_recompute_argument_errors_need_no_device(mb):
     assert mb.lib.mlpblk_backward_recompute(empty, *([None] * 11), 0, None) == mb.MLPBLK_OK
 
 
+def test_optimizer_argument_errors_need_no_device(mb):
+    d = mb.make_desc(1, 128, 256)
+    g = [0x10000, 0x20000, 0x30000]
+    ws = 1 << 40
+    norm = lambda *a: mb.lib.mlpblk_grad_norm(ctypes.byref(d), *a)
+    assert norm(*g, 1.0, None, None, 0x40000, ws, None) == mb.MLPBLK_EINVAL        # no output
+    assert norm(*g, 0.0, 0x50000, None, 0x40000, ws, None) == mb.MLPBLK_EINVAL     # max_norm 0
+    assert norm(*g, float("nan"), 0x50000, None, 0x40000, ws, None) == mb.MLPBLK_EINVAL
+    assert norm(g[0] + 4, g[1], g[2], 1.0, 0x50000, None, 0x40000, ws, None) == mb.MLPBLK_EINVAL
+    assert norm(*g, 1.0, 0x50002, None, 0x40000, ws, None) == mb.MLPBLK_EINVAL    # misaligned scalar
+    assert norm(*g, 1.0, 0x50000, None, 0x40000, 16, None) == mb.MLPBLK_EWORKSPACE
+    assert mb.lib.mlpblk_clip_grads(ctypes.byref(d), *g, None, None) == mb.MLPBLK_EINVAL
+    p = mb.Param(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 64, 1)
+    hp = mb.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.1)
+    step = lambda params, n, h, t=1, dt=mb.MLPBLK_BF16: mb.lib.mlpblk_adamw_step(params, n, h, t, dt, None, None)
+    arr = (mb.Param * 1)(p)
+    assert step(arr, 0, ctypes.byref(hp)) == mb.MLPBLK_EINVAL                      # no tensors
+    assert step(arr, 1, ctypes.byref(hp), t=0) == mb.MLPBLK_EINVAL                 # step counts from 1
+    assert step(arr, 1, ctypes.byref(hp), dt=9) == mb.MLPBLK_ENOTSUP
+    assert step(arr, 1, ctypes.byref(mb.AdamW(1e-3, 1.0, 0.999, 1e-8, 0.0))) == mb.MLPBLK_EINVAL
+    assert step(arr, 1, ctypes.byref(mb.AdamW(-1e-3, 0.9, 0.999, 1e-8, 0.0))) == mb.MLPBLK_EINVAL
+    bad = (mb.Param * 1)(mb.Param(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 66, 1))   # n % 4
+    assert step(bad, 1, ctypes.byref(hp)) == mb.MLPBLK_EINVAL
+    bad = (mb.Param * 1)(mb.Param(0x10008, 0x20000, 0x30000, 0x40000, 0x50000, 64, 1))   # master align
+    assert step(bad, 1, ctypes.byref(hp)) == mb.MLPBLK_EINVAL
+
+
 def test_grad_buffers_are_float32_by_contract():
     """The gradient accumulators are declared float32: the bf16 loss of a small
     contribution next to a large running sum is why."""
