@@ -54,6 +54,9 @@ def parse_args():
     p.add_argument("--optimizer", action="store_true",
                    help="end each step with the optimizer-side kernels: global gradient norm, "
                         "clip scale, fused AdamW on float32 master weights")
+    p.add_argument("--rmsnorm", default="stats", choices=["stats", "prologue"],
+                   help="stats: rstd from one statistics pass ahead of the W1 GEMM (default); prologue: "
+                        "rstd summed inside the W1 GEMM from its staged x tiles")
     p.add_argument("--variant", default="saving", choices=["saving", "recompute"],
                    help="saving: h and a saved by the forward; recompute: x and rstd saved, h and a "
                         "rebuilt by one more W1 GEMM in the backward")
@@ -221,6 +224,8 @@ def run_ours(args, dist, peaks):
     dev = "cuda"
     to = lambda a: torch.from_numpy(a).to(dev).to(dt)
     recompute = args.variant == "recompute"
+    mb.mlpblk_set_rmsnorm_mode(mb.MLPBLK_RMSNORM_IN_W1_PROLOGUE if args.rmsnorm == "prologue"
+                               else mb.MLPBLK_RMSNORM_STATS_PASS)
     bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps, recompute=recompute)
     bb.gamma.copy_(to(inp.gamma))
     bb.w1.copy_(to(inp.w1))
@@ -374,6 +379,7 @@ def run_ours(args, dist, peaks):
                    "d_model": d, "ffn": F, "shape": synth.CONFIGS[args.workload]["shape"],
                    "flop_per_step": flop_step,
                    "variant": args.variant,
+                   "rmsnorm": args.rmsnorm,
                    "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch

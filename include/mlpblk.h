@@ -311,6 +311,24 @@ int mlpblk_trace_end(void);
  * forward's outputs are not valid, and the context stays usable.  One-shot; not
  * thread-safe.  Returns MLPBLK_EINVAL for an unknown fault.
  */
+#define MLPBLK_RMSNORM_STATS_PASS      0
+#define MLPBLK_RMSNORM_IN_W1_PROLOGUE  1
+/*
+ * Where the bf16 forward computes the RMSNorm statistic rstd[t] ("Setup: The
+ * Shared Transformer Shell": the norm feeds the W1 projection):
+ *   MLPBLK_RMSNORM_STATS_PASS (default): one HBM pass over x ahead of the W1
+ *     GEMM computes rstd and, in the same launch, W1*gamma; the GEMM applies
+ *     rstd in its epilogue and runs 256 x 256 pair tiles.
+ *   MLPBLK_RMSNORM_IN_W1_PROLOGUE: four extra warps of the W1 GEMM sum x^2 per
+ *     row from the x tiles already staged in shared memory for the MMAs (no
+ *     extra pass over x; W1*gamma still takes one pass over W1).  Whole-tile
+ *     schedule only (every tile needs all of K for its rows' sums).
+ * Same results up to float32 summation order.  Process-wide; applies to later
+ * mlpblk_forward calls (the recompute variant always uses the statistics
+ * pass).  Returns MLPBLK_EINVAL for an unknown mode.
+ */
+int mlpblk_set_rmsnorm_mode(int mode);
+
 #define MLPBLK_TEST_FAULT_NONE        0
 #define MLPBLK_TEST_FAULT_SKIP_LOADS  1
 int mlpblk_set_test_fault(int fault);

@@ -31,7 +31,9 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
             "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault",
             "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute",
-            "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step")
+            "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step", "mlpblk_set_rmsnorm_mode")
+MLPBLK_RMSNORM_STATS_PASS = 0
+MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
 MLPBLK_TEST_FAULT_SKIP_LOADS = 1
 
@@ -107,6 +109,8 @@ def _load():
     lib.mlpblk_trace_begin.restype = i32
     lib.mlpblk_rmsnorm_backward_noalloc.argtypes = [pd] + [vp] * 8
     lib.mlpblk_rmsnorm_backward_noalloc.restype = i32
+    lib.mlpblk_set_rmsnorm_mode.argtypes = [i32]
+    lib.mlpblk_set_rmsnorm_mode.restype = i32
     lib.mlpblk_set_test_fault.argtypes = [i32]
     lib.mlpblk_set_test_fault.restype = i32
     lib.mlpblk_cuda_error_string.argtypes = []
@@ -233,6 +237,10 @@ def mlpblk_rmsnorm_backward_noalloc(desc, x, dn, dy, gamma, rstd, dx, dgamma, st
     _check(lib.mlpblk_rmsnorm_backward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(dn), _ptr(dy),
                                                _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
                                                _stream(stream)), "mlpblk_rmsnorm_backward_noalloc")
+
+
+def mlpblk_set_rmsnorm_mode(mode: int) -> None:
+    _check(lib.mlpblk_set_rmsnorm_mode(int(mode)), "mlpblk_set_rmsnorm_mode")
 
 
 def mlpblk_set_test_fault(fault: int) -> None:

@@ -120,13 +120,16 @@ struct Trace {
 }  // namespace
 
 namespace mlpblk {
+// Where the forward's RMSNorm statistic is computed (mlpblk_set_rmsnorm_mode);
+// the environment variable MLPBLK_RMS_IN_GEMM=1 sets the initial mode.
+int g_rms_mode = -1;
+
 bool rms_in_gemm() {
-    static int v = -1;
-    if (v < 0) {
+    if (g_rms_mode < 0) {
         const char *e = getenv("MLPBLK_RMS_IN_GEMM");
-        v = (e && e[0] == '1') ? 1 : 0;
+        g_rms_mode = (e && e[0] == '1') ? MLPBLK_RMSNORM_IN_W1_PROLOGUE : MLPBLK_RMSNORM_STATS_PASS;
     }
-    return v == 1;
+    return g_rms_mode == MLPBLK_RMSNORM_IN_W1_PROLOGUE;
 }
 }  // namespace mlpblk
 
@@ -495,6 +498,12 @@ int mlpblk_scale_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float
     const int64_t d = desc->d_model, F = desc->ffn;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_SCALE_GRADS, s,
                   launch_grads(false, sc, dgamma, d, dw1, F * d, dw2, F * d, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_set_rmsnorm_mode(int mode) {
+    if (mode != MLPBLK_RMSNORM_STATS_PASS && mode != MLPBLK_RMSNORM_IN_W1_PROLOGUE) return MLPBLK_EINVAL;
+    g_rms_mode = mode;
     return MLPBLK_OK;
 }
 

@@ -13,11 +13,8 @@ namespace mlpblk {
 
 int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *B, void *C0,
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
-    // Both operands are K-major here, so both pair widths are possible; the W1
-    // GEMM with the in-kernel RMSNorm prologue keeps single-CTA tiles (in pair
-    // mode its shared-memory reads slow the partner SM's operand reads:
-    // measured 2.3x slower).
-    const int pairs = (pair_tiles_enabled() && epi != kEpiFwdW1) ? (kAllowPair256 | kAllowPair192) : 0;
+    // Both operands are K-major here, so both pair widths are possible
+    const int pairs = pair_tiles_enabled() ? (kAllowPair256 | kAllowPair192) : 0;
     // the in-kernel prologue needs whole tiles (all of K) per segment
     const int choice = choose_tile(M, N, K, epi != kEpiFwdW1 && streamk_enabled(), false, num_sms, pairs);
     const int mode = choice & ~kUseStreamK;
@@ -33,14 +30,7 @@ int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *
         case kTile192: MLPBLK_RUN_MODE(E, 192, false);        \
         default: MLPBLK_RUN_MODE(E, 128, false);              \
     }
-    if (epi == kEpiFwdW1) {
-        // single-CTA modes only (see above)
-        switch (mode) {
-            case kTile256: MLPBLK_RUN_MODE(kEpiFwdW1, 256, false);
-            case kTile192: MLPBLK_RUN_MODE(kEpiFwdW1, 192, false);
-            default: MLPBLK_RUN_MODE(kEpiFwdW1, 128, false);
-        }
-    }
+    if (epi == kEpiFwdW1) { MLPBLK_RUN(kEpiFwdW1) }
     if (epi == kEpiFwdW1Pre) { MLPBLK_RUN(kEpiFwdW1Pre) }
     if (epi == kEpiFwdW1A) { MLPBLK_RUN(kEpiFwdW1A) }
     if (epi == kEpiFwdW2) { MLPBLK_RUN(kEpiFwdW2) }

@@ -13,8 +13,9 @@
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
 //   warps 6..9  (the in-GEMM RMSNorm variant of the forward W1 GEMM only) sum of
-//               x^2 per row, read from the A stages already in shared memory,
-//               gives rstd for the epilogue
+//               x^2 per row, read from each A stage once its MMAs have completed
+//               (then the stage goes back to the producer), gives rstd for the
+//               epilogue; works with pair tiles, each CTA summing its own rows
 // The accumulator is double buffered in TMEM (2 x BN columns) so the epilogue of
 // one tile overlaps the main loop of the next.
 //
@@ -184,6 +185,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t *accf_bar = empty_bar + C::kStages;
     uint64_t *acce_bar = accf_bar + 2;
     uint64_t *aux_bar = acce_bar + 2;  // one per epilogue warp
+    // in-GEMM RMSNorm: stage s's MMAs have completed, so its x tile may be read
+    // by the norm warps (who then release the stage to the producer)
+    uint64_t *consumed_bar = aux_bar + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
     float *rs = reinterpret_cast<float *>(ctrl + 1024);  // [2][128], forward W1 only
@@ -199,10 +203,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            // pair mode, leader: its producer's arrive (+ the peer's "A landed"
-            // notice when the peer's A stage carries the RMSNorm reads)
-            mbar_init(&full_bar[s], 1 + ((C::PAIR && C::kNorm && leader) ? 1u : 0u));
+            mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1 + kNormArrivals);
+            if (C::kNorm) mbar_init(&consumed_bar[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1 + kNormArrivals);
@@ -263,20 +266,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (!C::PAIR) {
                         mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
                     } else if (leader) {
-                        // the leader's barrier collects both CTAs' bytes, except the
-                        // peer's A when the peer's own RMSNorm warps wait for it
-                        mbar_arrive_expect_tx(&full_bar[stage], C::kNorm ? C::kStageBytes + C::kBBytes
-                                                                         : 2 * C::kStageBytes);
+                        // the leader's barrier collects both CTAs' bytes
+                        mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageBytes);
                     } else {
                         const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
-                        b_pair = true;
-                        bar_b = leader_full;
-                        if (C::kNorm) {
-                            mbar_arrive_expect_tx(&full_bar[stage], C::kABytes);
-                        } else {
-                            a_pair = true;
-                            bar_a = leader_full;
-                        }
+                        a_pair = b_pair = true;
+                        bar_a = bar_b = leader_full;
                     }
                     if (C::A_MN) {
 #pragma unroll
@@ -341,8 +336,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
                     }
                     // the stage is reusable (in both CTAs) once these MMAs finish
+                    // (and, in-GEMM RMSNorm, once the norm warps have read its x)
                     if (C::PAIR) umma_commit_pair(&empty_bar[stage], 3);
                     else umma_commit(&empty_bar[stage]);
+                    if (C::kNorm) {
+                        if (C::PAIR) umma_commit_pair(&consumed_bar[stage], 3);
+                        else umma_commit(&consumed_bar[stage]);
+                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -641,11 +641,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             float ss = 0.0f;
             bool ok = true;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                ok = mbar_wait(&full_bar[stage], phase, abort_flag);
+                // the x tile is read after the MMAs that used it completed (they
+                // read it from this CTA's shared memory, in pair mode too); the
+                // producer refills the stage once these reads are done
+                ok = mbar_wait(&consumed_bar[stage], phase, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
-                // pair mode: the peer's A stage has landed; tell the leader's MMA
-                if (C::PAIR && !leader && warp == 6 && lane == 0)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&full_bar[stage]), 0));
                 const uint32_t rowaddr = smem_u32(stages + stage * C::kStageBytes) + r * 128;
 #pragma unroll
                 for (int cidx = 0; cidx < 8; ++cidx)
