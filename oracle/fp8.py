@@ -35,7 +35,11 @@ Readings (the pages name E4M3 but give no recipe):
   same quantised a, dy, dh and n';
 * everything else (h, the gate, the RMSNorm statistic and backward, the residual
   paths, the += gradients) is as in the bf16 block: h and dh are rounded to bf16
-  where the bf16 path rounds them; the accumulators are float32 on the GPU and
+  where the bf16 path rounds them, and the gate reads the kept (bf16) h ("Kernel
+  3: Dense ReLU2 ...": the reverse kernel applies the branch to the preserved
+  input of ReLU^2) -- here, unlike in the bf16 block, that matters: dh is
+  quantised next, and a difference of one bf16 step in dh moves an E4M3 code in
+  about one element in sixteen; the accumulators are float32 on the GPU and
   float64 here.
 """
 
@@ -113,7 +117,10 @@ def backward(dy, x, gamma, w1, w2, h, a_q, n_q, r, grads):
     dy_q, _ = quantize(dy)
     w2_q, _ = quantize(w2)
     da = dy_q @ w2_q                                          # [T, F]
-    dh = da * 2.0 * np.where(h > 0, h, 0.0)                   # d relu(h)^2 / dh
+    # the gate reads h as the forward keeps it (bf16): the reverse kernel applies
+    # the branch to the preserved input of ReLU^2
+    hk = round_to_bf16(np.asarray(h, dtype=np.float32))
+    dh = da * 2.0 * np.where(hk > 0, hk, 0.0)                 # d relu(h)^2 / dh
     dh_q, _ = quantize(round_to_bf16(dh.astype(np.float32)))
     grads["dw2"] += dy_q.T @ a_q
     w1_q, _ = quantize(w1)
