@@ -57,6 +57,9 @@ def parse_args():
     p.add_argument("--rmsnorm", default="stats", choices=["stats", "prologue"],
                    help="stats: rstd from one statistics pass ahead of the W1 GEMM (default); prologue: "
                         "rstd summed inside the W1 GEMM from its staged x tiles")
+    p.add_argument("--precision", default="bf16", choices=["bf16", "fp8"],
+                   help="bf16: the block's GEMMs on bf16 operands; fp8: the E4M3-operand variant "
+                        "(per-tensor scales, fp32 accumulators)")
     p.add_argument("--variant", default="saving", choices=["saving", "recompute"],
                    help="saving: h and a saved by the forward; recompute: x and rstd saved, h and a "
                         "rebuilt by one more W1 GEMM in the backward")
@@ -202,6 +205,10 @@ def algorithmic_work(kind, T, d, F, parts):
         return 8.0 * (2 * F * d + d), "byte"
     if kind == "dgamma_reduce":
         return 4.0 * parts * d + 8.0 * d, "byte"
+    if kind in ("quant_amax", "quant_scale", "quant_apply"):
+        return None, None  # one launch per quantised tensor, of different sizes
+    if kind == "norm_quant":
+        return 2.0 * T * d + 1.0 * T * d + 4.0 * T, "byte"
     if kind == "grad_norm":
         return 4.0 * (2 * F * d + d), "byte"
     if kind == "clip_grads":
@@ -226,7 +233,10 @@ def run_ours(args, dist, peaks):
     recompute = args.variant == "recompute"
     mb.mlpblk_set_rmsnorm_mode(mb.MLPBLK_RMSNORM_IN_W1_PROLOGUE if args.rmsnorm == "prologue"
                                else mb.MLPBLK_RMSNORM_STATS_PASS)
-    bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps, recompute=recompute)
+    fp8 = args.precision == "fp8"
+    if fp8 and (recompute or inp.dtype != "bf16"):
+        raise SystemExit("--precision fp8 needs a bf16 workload and the saving variant")
+    bb = mb.BlockBuffers(T, d, F, dtype=inp.dtype, eps=inp.eps, recompute=recompute, fp8=fp8)
     bb.gamma.copy_(to(inp.gamma))
     bb.w1.copy_(to(inp.w1))
     bb.w2.copy_(to(inp.w2))
@@ -250,7 +260,12 @@ def run_ours(args, dist, peaks):
             if host_x is not None:
                 x_list[i].copy_(host_x[i], non_blocking=True)
                 dy_list[i].copy_(host_dy[i], non_blocking=True)
-            if recompute:
+            if fp8:
+                mb.mlpblk_forward_fp8(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a8, bb.n8, bb.rstd,
+                                      bb.scales, bb.ws)
+                mb.mlpblk_backward_fp8(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a8, bb.n8,
+                                       bb.rstd, bb.scales, bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+            elif recompute:
                 mb.mlpblk_forward_recompute(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.rstd, bb.ws)
                 mb.mlpblk_backward_recompute(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.rstd,
                                              bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
@@ -274,7 +289,7 @@ def run_ours(args, dist, peaks):
     if mb.mlpblk_last_error() != mb.MLPBLK_OK:
         raise RuntimeError("device error during warm-up")
 
-    launches_per_step = (1 + n_mb * (11 if recompute else 9) + (1 if inp.grad_scale is not None else 0)
+    launches_per_step = (1 + n_mb * (30 if fp8 else 11 if recompute else 9) + (1 if inp.grad_scale is not None else 0)
                          + (3 if args.optimizer else 0))
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
     clocks = ClockSampler(dist.local_rank)
@@ -358,10 +373,14 @@ def run_ours(args, dist, peaks):
         traffic = recorded_traffic(args.workload, kind)
         if unit == "flop":
             peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+            src = f"{peaks['source']} sustained bf16"
+            if fp8:  # E4M3 contractions: the bf16 measurement times the nominal 4.5 / 2.25 ratio
+                peak = 2.0 * peak
+                src += " x 2 (nominal fp8 / bf16 dense ratio)"
             ach = amount / mean_s / 1e12
             return {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
                     "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
-                    "algorithmic_per_launch": amount, "peak_source": f"{peaks['source']} sustained bf16",
+                    "algorithmic_per_launch": amount, "peak_source": src,
                     "mean_launch_us": round(mean_s * 1e6, 2)}
         peak = peaks["hbm_gbs"]
         ach = amount / mean_s / 1e9
@@ -370,6 +389,7 @@ def run_ours(args, dist, peaks):
                 "peak_source": f"{peaks['source']} copy bandwidth", "mean_launch_us": round(mean_s * 1e6, 2)}
 
     dominant = max(per, key=lambda k: per[k][1])
+    pk_mul = 2.0 if fp8 else 1.0
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -379,22 +399,25 @@ def run_ours(args, dist, peaks):
                    "d_model": d, "ffn": F, "shape": synth.CONFIGS[args.workload]["shape"],
                    "flop_per_step": flop_step,
                    "variant": args.variant,
+                   "precision": args.precision + (" (E4M3 GEMM operands, per-tensor scales)" if fp8 else ""),
                    "rmsnorm": args.rmsnorm,
                    "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch
                    "executed_flop_per_step": flop_step * 7 // 6 if recompute else flop_step,
-                   "saved_activation_bytes_per_microbatch": (T * d * (2 if inp.dtype == "bf16" else 4) + 4 * T
-                                                             + (0 if recompute else
-                                                                2 * T * F * (2 if inp.dtype == "bf16" else 4))),
+                   "saved_activation_bytes_per_microbatch": (
+                       T * d * (2 if inp.dtype == "bf16" else 4) + 4 * T
+                       + (3 * T * F + T * d + 16 if fp8 else 0 if recompute else
+                          2 * T * F * (2 if inp.dtype == "bf16" else 4))),
                    "l2": "inputs larger than L2 (working set %.1f GB per replica)" % (
                        (bb.ws.numel() + sum(t.numel() * t.element_size() for t in
                         [bb.w1, bb.w2, bb.h, bb.a, bb.dw1, bb.dw2] + xs + dys if t is not None)) / 1e9),
                    "parallelism": "replicas" if dist.world > 1 else "single",
                    "launch": launch_mode},
         "tokens_per_s": round(tokens_s, 1),
-        "frac_of_peak": {"sustained": round(value / dist.world / peaks.get("bf16_tflops_sustained", 1.0), 4),
-                         "burst": round(value / dist.world / peaks.get("bf16_tflops", 1.0), 4)},
+        "frac_of_peak": {"sustained": round(value / dist.world / (pk_mul * peaks.get("bf16_tflops_sustained", 1.0)), 4),
+                         "burst": round(value / dist.world / (pk_mul * peaks.get("bf16_tflops", 1.0)), 4),
+                         "peak": "fp8 = 2 x measured bf16 (nominal ratio)" if fp8 else "measured bf16"},
         "roofline": roofline(dominant),
         "roofline_hbm": roofline("norm_bwd"),
         # every kernel kind against its own roof: tensor peak for the GEMMs, copy

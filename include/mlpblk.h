@@ -207,6 +207,41 @@ int mlpblk_adamw_step(const mlpblk_param *params, int count, const mlpblk_adamw 
                       int64_t step, int dtype, const float *grad_scale, void *stream);
 
 /*
+ * FP8-operand variant: the same block with the six GEMMs on E4M3 operands
+ * (tcgen05 kind::f8f6f4, float32 accumulators; "Nemotron Kernels From
+ * Inference To Backpropagation" -- "Where Quantization Fits": quantisation as a
+ * policy for particular tensor edges, higher-precision accumulators kept).
+ * Tensors in and out are bf16 (desc->dtype = MLPBLK_BF16), d_model and ffn
+ * multiples of 16.  Per-tensor scaling: s = amax / 448, codes E4M3(v / s)
+ * nearest-even and saturated, the GEMM epilogue multiplies by the operands'
+ * scales.  Quantised: n' = x * rstd (scale 1, |n'| <= sqrt(d)), W1 * gamma, W2,
+ * a (from its bf16 value), dy, dh (from its bf16 value), W1; everything else as
+ * in mlpblk_forward / mlpblk_backward.
+ *
+ * Saved by the forward for the backward (caller-owned):
+ *   h_saved[T,F] bf16, a8_saved[T,F] E4M3 codes (1 byte), n8_saved[T,d] E4M3
+ *   codes of n', rstd_saved[T] float32, scales_saved[4] float32 (a's scale
+ *   record {amax, 448/amax, amax/448, 0}).
+ * mlpblk_workspace_size_fp8: scratch bytes both calls need; 0 for an invalid or
+ *   unsupported descriptor.
+ */
+size_t mlpblk_workspace_size_fp8(const mlpblk_desc *desc);
+
+int mlpblk_forward_fp8(const mlpblk_desc *desc,
+                       const void *x, const void *gamma, const void *w1, const void *w2,
+                       void *y, void *h_saved, void *a8_saved, void *n8_saved,
+                       float *rstd_saved, float *scales_saved,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_backward_fp8(const mlpblk_desc *desc,
+                        const void *dy, const void *x, const void *gamma,
+                        const void *w1, const void *w2,
+                        const void *h_saved, const void *a8_saved, const void *n8_saved,
+                        const float *rstd_saved, const float *scales_saved,
+                        void *dx, float *dgamma, float *dw1, float *dw2,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --
  * accumulation across microbatches): dgamma[d], dw1[F,d], dw2[d,F] = 0 (float32).
  * desc->tokens is ignored.  Returns an MLPBLK_* code.
@@ -288,6 +323,10 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_CLIP_GRADS     14  /* g *= clip scale (device scalar)           */
 #define MLPBLK_KERNEL_ADAMW          15  /* fused AdamW update                        */
 #define MLPBLK_KERNEL_GRAD_NORM_FINAL 16 /* partials -> norm and clip scale           */
+#define MLPBLK_KERNEL_QUANT_AMAX     17  /* E4M3: per-CTA maxima of |v|               */
+#define MLPBLK_KERNEL_QUANT_SCALE    18  /* E4M3: amax -> scale record                */
+#define MLPBLK_KERNEL_QUANT_APPLY    19  /* E4M3: v -> codes                          */
+#define MLPBLK_KERNEL_NORM_QUANT     20  /* E4M3: rstd and n' = x * rstd              */
 
 /*
  * mlpblk_trace_begin: from now on, launch i of this library records

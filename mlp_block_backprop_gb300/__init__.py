@@ -31,7 +31,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_trace_begin", "mlpblk_trace_end", "mlpblk_cuda_error_string",
             "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault",
             "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute",
-            "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step", "mlpblk_set_rmsnorm_mode")
+            "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step", "mlpblk_set_rmsnorm_mode",
+            "mlpblk_workspace_size_fp8", "mlpblk_forward_fp8", "mlpblk_backward_fp8")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
@@ -40,7 +41,8 @@ MLPBLK_TEST_FAULT_SKIP_LOADS = 1
 KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dgrad_h",
                 5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
                 9: "dgamma_reduce", 10: "zero_grads", 11: "scale_grads", 12: "rstd",
-                13: "grad_norm", 14: "clip_grads", 15: "adamw", 16: "grad_norm_final"}
+                13: "grad_norm", 14: "clip_grads", 15: "adamw", 16: "grad_norm_final",
+                17: "quant_amax", 18: "quant_scale", 19: "quant_apply", 20: "norm_quant"}
 
 
 class MlpBlkError(RuntimeError):
@@ -95,6 +97,12 @@ def _load():
     lib.mlpblk_clip_grads.restype = i32
     lib.mlpblk_adamw_step.argtypes = [ctypes.POINTER(Param), i32, ctypes.POINTER(AdamW), ctypes.c_int64, i32, vp, vp]
     lib.mlpblk_adamw_step.restype = i32
+    lib.mlpblk_workspace_size_fp8.argtypes = [pd]
+    lib.mlpblk_workspace_size_fp8.restype = sz
+    lib.mlpblk_forward_fp8.argtypes = [pd] + [vp] * 10 + [sz, vp]
+    lib.mlpblk_forward_fp8.restype = i32
+    lib.mlpblk_backward_fp8.argtypes = [pd] + [vp] * 14 + [sz, vp]
+    lib.mlpblk_backward_fp8.restype = i32
     lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_zero_grads.restype = i32
     lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
@@ -221,6 +229,29 @@ def mlpblk_adamw_step(params, hp, step, dtype, grad_scale=None, stream=None):
     _check(rc, "mlpblk_adamw_step")
 
 
+def mlpblk_workspace_size_fp8(desc: Desc) -> int:
+    return int(lib.mlpblk_workspace_size_fp8(ctypes.byref(desc)))
+
+
+def mlpblk_forward_fp8(desc, x, gamma, w1, w2, y, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
+                       workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_forward_fp8(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2), _ptr(y),
+                                _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
+                                _ptr(scales_saved), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_forward_fp8")
+
+
+def mlpblk_backward_fp8(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
+                        dx, dgamma, dw1, dw2, workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_backward_fp8(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
+                                 _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
+                                 _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
+                                 _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_backward_fp8")
+
+
 def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):
     _check(lib.mlpblk_zero_grads(ctypes.byref(desc), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
                                  _stream(stream)), "mlpblk_zero_grads")
@@ -293,7 +324,8 @@ class BlockBuffers:
     recompute=True uses the recompute variant (no h and a buffers; a larger
     workspace holds them during each call)."""
 
-    def __init__(self, tokens, d_model, ffn, dtype="bf16", eps=1e-6, device="cuda", recompute=False):
+    def __init__(self, tokens, d_model, ffn, dtype="bf16", eps=1e-6, device="cuda", recompute=False,
+                 fp8=False):
         import torch
         self.torch = torch
         self.dt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -309,19 +341,29 @@ class BlockBuffers:
         self.dy = torch.empty(T, d, dtype=self.dt, **e)
         self.y = torch.empty(T, d, dtype=self.dt, **e)
         self.recompute = recompute
+        self.fp8 = fp8
         self.h = None if recompute else torch.empty(T, F, dtype=self.dt, **e)
-        self.a = None if recompute else torch.empty(T, F, dtype=self.dt, **e)
+        self.a = None if (recompute or fp8) else torch.empty(T, F, dtype=self.dt, **e)
+        if fp8:  # E4M3 codes of a and n' and a's scale record, saved for the backward
+            self.a8 = torch.empty(T, F, dtype=torch.uint8, **e)
+            self.n8 = torch.empty(T, d, dtype=torch.uint8, **e)
+            self.scales = torch.empty(4, dtype=torch.float32, **e)
         self.rstd = torch.empty(T, dtype=torch.float32, **e)
         self.dx = torch.empty(T, d, dtype=self.dt, **e)
         self.dgamma = torch.zeros(d, dtype=torch.float32, **e)
         self.dw1 = torch.zeros(F, d, dtype=torch.float32, **e)
         self.dw2 = torch.zeros(d, F, dtype=torch.float32, **e)
-        ws = (mlpblk_workspace_size_recompute if recompute else mlpblk_workspace_size)(self.desc)
+        ws = (mlpblk_workspace_size_fp8 if fp8 else
+              mlpblk_workspace_size_recompute if recompute else mlpblk_workspace_size)(self.desc)
         if ws == 0:
             raise MlpBlkError(MLPBLK_EINVAL, "mlpblk_workspace_size")
         self.ws = torch.empty(ws, dtype=torch.uint8, **e)
 
     def forward(self, stream=None):
+        if self.fp8:
+            mlpblk_forward_fp8(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.h, self.a8, self.n8,
+                               self.rstd, self.scales, self.ws, stream=stream)
+            return
         if self.recompute:
             mlpblk_forward_recompute(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.rstd,
                                      self.ws, stream=stream)
@@ -330,6 +372,11 @@ class BlockBuffers:
                        self.rstd, self.ws, stream=stream)
 
     def backward(self, stream=None):
+        if self.fp8:
+            mlpblk_backward_fp8(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a8,
+                                self.n8, self.rstd, self.scales, self.dx, self.dgamma, self.dw1, self.dw2, self.ws,
+                                stream=stream)
+            return
         if self.recompute:
             mlpblk_backward_recompute(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.rstd,
                                       self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)

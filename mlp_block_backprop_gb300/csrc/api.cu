@@ -84,6 +84,47 @@ WsLayout ws_layout(const mlpblk_desc *d, bool recompute) {
     return l;
 }
 
+// Workspace of the FP8-operand variant (forward and backward regions overlap
+// where they are never live together).
+struct WsLayoutF8 {
+    int64_t t16;   // a (forward) or dh (backward), bf16 [T, F]
+    int64_t dh8;   // dh in E4M3 [T, F]
+    int64_t w1q;   // W1*gamma (forward) or W1 (backward) in E4M3 [F, d]
+    int64_t w2q;   // W2 in E4M3 [d, F]
+    int64_t dyq;   // dy in E4M3 [T, d]
+    int64_t dn;    // dn_s fp32 [T, d]
+    int64_t part;  // dgamma partials [kMaxParts, d]
+    int64_t amax;  // per-CTA maxima of the amax passes
+    int64_t scales;  // scale records: 0 W1, 1 W2, 2 dy, 3 dh
+    int64_t sk_partial, sk_flags, total;
+};
+
+constexpr int kAmaxParts = 2048;
+
+WsLayoutF8 ws_layout_f8(const mlpblk_desc *dsc) {
+    const int64_t T = dsc->tokens, d = dsc->d_model, F = dsc->ffn;
+    WsLayoutF8 l;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    l.t16 = take(T * F * 2);
+    l.dh8 = take(T * F);
+    l.w1q = take(F * d);
+    l.w2q = take(d * F);
+    l.dyq = take(T * d);
+    l.dn = take(T * d * 4);
+    l.part = take(static_cast<int64_t>(kMaxParts) * d * 4);
+    l.amax = take(kAmaxParts * 4);
+    l.scales = take(4 * 16);
+    l.sk_partial = take(static_cast<int64_t>(kMaxSkSlots) * kSkSlotFloats * 4);
+    l.sk_flags = take(static_cast<int64_t>(kSkSets) * kSkFlagsPerSet * 4);
+    l.total = off;
+    return l;
+}
+
 // Device properties, checked once per device: sm_103 and its SM count.
 int device_sms(int *sms) {
     static int cached[64] = {0};  // 0 unknown, -1 unsupported, else SM count
@@ -479,6 +520,159 @@ int mlpblk_adamw_step(const mlpblk_param *params, int count, const mlpblk_adamw 
     return MLPBLK_OK;
 }
 
+static int check_fp8_desc(const mlpblk_desc *desc) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->dtype != MLPBLK_BF16) return MLPBLK_ENOTSUP;
+    if (desc->d_model % 16 != 0 || desc->ffn % 16 != 0) return MLPBLK_ENOTSUP;  // 16-byte E4M3 rows
+    return MLPBLK_OK;
+}
+
+size_t mlpblk_workspace_size_fp8(const mlpblk_desc *desc) {
+    if (check_fp8_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(ws_layout_f8(desc).total);
+}
+
+int mlpblk_forward_fp8(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1, const void *w2,
+                       void *y, void *h_saved, void *a8_saved, void *n8_saved, float *rstd_saved,
+                       float *scales_saved, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(y) ||
+        !aligned16(h_saved) || !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) ||
+        !aligned16(scales_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *amax = reinterpret_cast<float *>(ws + l.amax);
+    float *sc = reinterpret_cast<float *>(ws + l.scales);  // [4][4]
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    uint8_t *w1q = ws + l.w1q, *w2q = ws + l.w2q;
+    void *a16 = ws + l.t16;
+    int parts = 0;
+    // n' = x * rstd in E4M3 (scale 1) and rstd
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_QUANT, s,
+                  launch_norm_quant(x, rstd_saved, static_cast<uint8_t *>(n8_saved), T, d, desc->eps, s));
+    // W1 * gamma and W2 in E4M3 (the W2 scale record also clears the W1 GEMM's flags)
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w1, gamma, d, F * d, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 0, nullptr, 0, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w1, gamma, d, F * d, sc + 0, w1q, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w2, nullptr, F, d * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, sc + 4, sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w2, nullptr, F, d * F, sc + 4, w2q, s));
+    // h (saved, bf16) and a (bf16, scratch) = relu(h)^2, h = (n' . (W1*gamma)^T) * s_w1
+    GemmArgs g1 = {};
+    g1.deq_b = sc + 0 + 2;
+    g1.sk_partial = sk_partial;
+    g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                  launch_gemm_tc_f8(kEpiFwdW1Pre, (int)T, (int)F, (int)d, n8_saved, w1q, h_saved, a16, g1, sms, s));
+    // a in E4M3 (saved with its scale record; clears the W2 GEMM's flags)
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(a16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet, kSkFlagsPerSet,
+                                    s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s,
+                  launch_apply_e4m3(a16, nullptr, F, T * F, scales_saved, static_cast<uint8_t *>(a8_saved), s));
+    // y = x + (a . W2^T) * s_a * s_w2
+    GemmArgs g2 = {};
+    g2.aux = static_cast<const uint16_t *>(x);
+    g2.ld_aux = (int)d;
+    g2.deq_a = scales_saved + 2;
+    g2.deq_b = sc + 4 + 2;
+    g2.sk_partial = sk_partial;
+    g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s,
+                  launch_gemm_tc_f8(kEpiFwdW2, (int)T, (int)d, (int)F, a8_saved, w2q, y, nullptr, g2, sms, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const void *w1,
+                        const void *w2, const void *h_saved, const void *a8_saved, const void *n8_saved,
+                        const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma, float *dw1,
+                        float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
+        !aligned16(h_saved) || !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) ||
+        !aligned16(scales_saved) || !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) ||
+        !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *amax = reinterpret_cast<float *>(ws + l.amax);
+    float *sc = reinterpret_cast<float *>(ws + l.scales);  // 0 W1, 1 W2, 2 dy, 3 dh
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    uint8_t *w1q = ws + l.w1q, *w2q = ws + l.w2q, *dyq = ws + l.dyq, *dh8 = ws + l.dh8;
+    void *dh16 = ws + l.t16;
+    float *dn_s = reinterpret_cast<float *>(ws + l.dn);
+    float *part = reinterpret_cast<float *>(ws + l.part);
+    int parts = 0;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dy, nullptr, d, T * d, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 8, nullptr, 0, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dy, nullptr, d, T * d, sc + 8, dyq, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w2, nullptr, F, d * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 4, nullptr, 0, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w2, nullptr, F, d * F, sc + 4, w2q, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w1, nullptr, d, F * d, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, sc + 0, sk_flags + kSetDgradH * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w1, nullptr, d, F * d, sc + 0, w1q, s));
+    // dW2 += (dy^T . a) * s_dy * s_a
+    GemmArgs gw2 = {};
+    gw2.deq_a = sc + 8 + 2;
+    gw2.deq_b = scales_saved + 2;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
+                  launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
+    // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
+    GemmArgs gd = {};
+    gd.aux = static_cast<const uint16_t *>(h_saved);
+    gd.ld_aux = (int)F;
+    gd.deq_a = sc + 8 + 2;
+    gd.deq_b = sc + 4 + 2;
+    gd.sk_partial = sk_partial;
+    gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
+                  launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w2q, dh16, nullptr, gd, sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dh16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dh16, nullptr, F, T * F, sc + 12, dh8, s));
+    // dn_s = rstd * (dh . W1) * s_dh * s_w1   (fp32)
+    GemmArgs gn = {};
+    gn.rstd_in = rstd_saved;
+    gn.deq_a = sc + 12 + 2;
+    gn.deq_b = sc + 0 + 2;
+    gn.sk_partial = sk_partial;
+    gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
+                  launch_gemm_tc_f8(kEpiStoreF32, (int)T, (int)d, (int)F, dh8, w1q, dn_s, nullptr, gn, sms, s));
+    // dW1 += gamma[col] * (dh^T . n') * s_dh
+    GemmArgs gw1 = {};
+    gw1.colscale = static_cast<const uint16_t *>(gamma);
+    gw1.deq_a = sc + 12 + 2;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
+                  launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
+                                    sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+    return MLPBLK_OK;
+}
+
 int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {
     MLPBLK_TRY(check_desc(desc));
     if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
@@ -537,7 +731,8 @@ int mlpblk_last_error(void) {
     if (cuda_status(cudaDeviceSynchronize()) != MLPBLK_OK) return MLPBLK_ECUDA;
     const int a = take_device_error_gemm_fwd();
     const int b = take_device_error_gemm_bwd();
-    return a != MLPBLK_OK ? a : b;
+    const int c = take_device_error_gemm_f8();
+    return a != MLPBLK_OK ? a : (b != MLPBLK_OK ? b : c);
 }
 
 }  // extern "C"

@@ -40,20 +40,27 @@
 namespace mlpblk {
 
 constexpr int kBM = 128;      // rows per CTA (UMMA M per CTA)
-constexpr int kBK = 64;       // K per stage: one 128-byte swizzle row of bf16
-constexpr int kUmmaK = 16;    // K per tcgen05.mma for 16-bit inputs
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 // Accumulator buffers of a pair tile (256 TMEM columns each): two, so the
 // epilogue of one tile overlaps the main loop of the next.
 constexpr int kPairAccBufs = 2;
 
-template <int BN_, int EPI_, bool A_MN_, bool B_MN_, bool PAIR_ = false>
+template <int BN_, int EPI_, bool A_MN_, bool B_MN_, bool PAIR_ = false, bool F8_ = false>
 struct GemmCfg {
     static constexpr int BN = BN_;               // tile width (of the pair tile in pair mode)
     static constexpr int EPI = EPI_;
     static constexpr bool A_MN = A_MN_;
     static constexpr bool B_MN = B_MN_;
     static constexpr bool PAIR = PAIR_;
+    // operand element type: bf16 (kind::f16) or E4M3 (kind::f8f6f4).  A stage row
+    // is 128 bytes either way: 64 bf16 or 128 E4M3 values of K, and one MMA
+    // takes 32 bytes of K per row (16 or 32 values)
+    static constexpr bool F8 = F8_;
+    static constexpr int kElem = F8 ? 1 : 2;
+    static constexpr int kBKe = 128 / kElem;       // K values per stage
+    static constexpr int kUmmaKe = 32 / kElem;     // K values per tcgen05.mma
+    static constexpr int kMNBox = 128 / kElem;     // MN values per MN-major box row
+    static constexpr int kMNBoxBytes = kBKe * 128; // one MN-major box: kBKe rows of 128 bytes
     static constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // rows of one output tile
     static constexpr int kBRows = PAIR ? BN / 2 : BN;    // rows of B staged per CTA
     static constexpr bool kNorm = (EPI == kEpiFwdW1);
@@ -65,8 +72,8 @@ struct GemmCfg {
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
     static constexpr int kThreads = kNorm ? 320 : 192;
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = kBRows * kBK * 2;
+    static constexpr int kABytes = kBM * 128;
+    static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     // epilogues that read a [M][N] bf16 operand (x for the residual, h for the
     // gate) prefetch each warp's 32 rows of the next tile into shared memory and
@@ -77,7 +84,9 @@ struct GemmCfg {
     // the two-output W1 epilogue, whose shared memory goes to a deeper pipeline
     static constexpr int kStagingBufs = kNumOut == 2 ? 1 : 2;
     static constexpr int kStagingBytes = kAux ? 0 : 4 * kNumOut * kStagingBufs * 4096;
-    static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A);
+    // per-row scale read from args.rstd_in (1 when that is null)
+    static constexpr bool kRowScale =
+        (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A || EPI == kEpiStoreF32);
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
     static constexpr int kAlignSlack = 1024;
     static constexpr int kStagesRaw =
@@ -89,7 +98,8 @@ struct GemmCfg {
     static constexpr int kAccBufs = PAIR ? kPairAccBufs : 2;
     // TMEM columns allocated: a power of two >= the accumulators' columns
     static constexpr uint32_t kTmemCols = kAccBufs * BN <= 256 ? 256u : 512u;
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN, A_MN, B_MN);
+    static constexpr uint32_t kIdesc = F8 ? idesc_e4m3_f32(kTileM, BN, A_MN, B_MN)
+                                          : idesc_bf16_f32(kTileM, BN, A_MN, B_MN);
     static_assert(kStages >= 2, "not enough shared memory for a pipeline");
     // a split tile's owner copies one partial sum (128 x BN fp32) into the
     // pipeline stages, which its last segment has finished with
@@ -99,6 +109,7 @@ struct GemmCfg {
     // a pair stages BN/2 rows of B per CTA; MN-major B is staged in 64-wide
     // swizzle blocks, so there BN/2 must be a multiple of 64
     static_assert(!PAIR || BN == 256 || (BN == 192 && !B_MN), "pair tiles are 256 x 256 or 256 x 192");
+    static_assert(!B_MN || kBRows % kMNBox == 0, "MN-major B is staged in whole 128-byte box rows");
 };
 
 // One segment of a worker's work: k-blocks [kb0, kb1) of one output tile.
@@ -259,7 +270,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) goto producer_done;
                     uint8_t *sa = stages + stage * C::kStageBytes;
                     uint8_t *sb = sa + C::kABytes;
-                    const int k0 = kb * kBK;
+                    const int k0 = kb * C::kBKe;
                     // where this CTA's A and B loads signal completion
                     uint32_t bar_a = smem_u32(&full_bar[stage]), bar_b = bar_a;
                     bool a_pair = false, b_pair = false;
@@ -275,9 +286,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (C::A_MN) {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa + j * 8192, a_row + 64 * j, k0);
-                            else tma_load_2d(&tmA, &full_bar[stage], sa + j * 8192, a_row + 64 * j, k0);
+                        for (int j = 0; j < kBM / C::kMNBox; ++j) {
+                            if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
+                            else tma_load_2d(&tmA, &full_bar[stage], sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
                         }
                     } else {
                         if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa, k0, a_row);
@@ -285,9 +296,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     if (C::B_MN) {
 #pragma unroll
-                        for (int j = 0; j < C::kBRows / 64; ++j) {
-                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * 8192, b_row + 64 * j, k0);
-                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * 8192, b_row + 64 * j, k0);
+                        for (int j = 0; j < C::kBRows / C::kMNBox; ++j) {
+                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0);
+                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0);
                         }
                     } else {
                         if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb, k0, b_row);
@@ -326,14 +337,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t a_addr = smem_u32(stages + stage * C::kStageBytes);
                     const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * 2048, 8192, 1024)
+                    for (int kk = 0; kk < C::kBKe / C::kUmmaKe; ++kk) {
+                        // K-major: the next 32 bytes of each row; MN-major: the next
+                        // kUmmaKe rows of 128 bytes
+                        const uint32_t mn_step = static_cast<uint32_t>(C::kUmmaKe * 128);
+                        const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * mn_step, C::kMNBoxBytes, 1024)
                                                     : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * 2048, 8192, 1024)
+                        const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * mn_step, C::kMNBoxBytes, 1024)
                                                     : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
                         const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        if (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, acc);
-                        else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
+                        if (C::F8) {
+                            if (C::PAIR) umma_e4m3_pair(d_tmem, ad, bd, C::kIdesc, acc);
+                            else umma_e4m3(d_tmem, ad, bd, C::kIdesc, acc);
+                        } else {
+                            if (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, acc);
+                            else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
+                        }
                     }
                     // the stage is reusable (in both CTAs) once these MMAs finish
                     // (and, in-GEMM RMSNorm, once the norm warps have read its x)
@@ -378,7 +397,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         bool aux_pending = false;  // a prefetch copy issued and not yet waited for
         auto prefetch = [&](const Seg &wn, float &rsc_next) {
             const int r0 = wn.m0 + static_cast<int>(rank) * kBM + 32 * q;
-            if (C::kRowScale) rsc_next = (r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f;
+            if (C::kRowScale)
+                rsc_next = args.rstd_in ? ((r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f) : 1.0f;
             if (C::kAux && wn.kb0 == 0 && lane == 0) {
                 int nch = 0;
                 for (int c = 0; c < C::kNumChunks; ++c)
@@ -393,6 +413,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int sbuf = 0;
         uint32_t aux_phase = 0;
         float rsc_pre = 1.0f;
+        const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
         SegIter si = seg_begin(args, worker);
         Seg w;
         bool have = seg_next<C::BN, C::kTileM>(args, si, w);
@@ -494,6 +515,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                     }
                 }
+                if (C::F8) {
+                    // E4M3 operands: the dequantisation scales of A and B
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v0[i] *= deq;
+                        if (kChunkUnits == 2) v1[i] *= deq;
+                    }
+                }
                 // the fused epilogues' [M][N] operand: this row's 64 values of the
                 // chunk, from the swizzled shared copy (zero beyond M and N)
                 uint4 aux[8];
@@ -577,6 +606,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int i = 0; i < 4; ++i) {
                             e[i] = v0[4 * j + i];
                             if (C::EPI == kEpiAccF32ColScale) e[i] *= cs[4 * j + i];
+                            if (C::EPI == kEpiStoreF32) e[i] *= rsc;
                         }
                         const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
                         st_shared_v4(s0 + off, __float_as_uint(e[0]), __float_as_uint(e[1]),
@@ -699,17 +729,23 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
+// Element types of the tensor maps.
+enum MapType : int { kMapBf16 = 0, kMapF32 = 1, kMapU8 = 2 };
+
 // 2-D tensor map of a row-major array [outer][inner] with 128-byte swizzle.
-inline bool make_map_2d(CUtensorMap *m, const void *ptr, bool f32, uint64_t inner, uint64_t outer,
+inline bool make_map_2d(CUtensorMap *m, const void *ptr, int type, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
-    const uint64_t esz = f32 ? 4 : 2;
+    const uint64_t esz = type == kMapF32 ? 4 : (type == kMapU8 ? 1 : 2);
+    const CUtensorMapDataType dt = type == kMapF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (type == kMapU8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * esz};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    CUresult r = fn(m, dt, 2,
                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -733,15 +769,18 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
                 GemmArgs a, int num_sms, cudaStream_t stream) {
     CUtensorMap mA, mB, mC0, mC1, mAux;
     bool ok = true;
-    ok &= C::A_MN ? make_map_2d(&mA, A, false, M, K, 64, 64) : make_map_2d(&mA, A, false, K, M, 64, kBM);
-    ok &= C::B_MN ? make_map_2d(&mB, B, false, N, K, 64, 64)
-                  : make_map_2d(&mB, B, false, K, N, 64, C::kBRows);
-    if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, false, N, M, 64, 32);
-    else ok &= make_map_2d(&mC0, C0, true, N, M, 32, 32);
-    if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, false, N, M, 64, 32);
+    // operands: 128-byte box rows (kBKe values of K, or kMNBox values of M / N)
+    const int op = C::F8 ? kMapU8 : kMapBf16;
+    ok &= C::A_MN ? make_map_2d(&mA, A, op, M, K, C::kMNBox, C::kBKe)
+                  : make_map_2d(&mA, A, op, K, M, C::kBKe, kBM);
+    ok &= C::B_MN ? make_map_2d(&mB, B, op, N, K, C::kMNBox, C::kBKe)
+                  : make_map_2d(&mB, B, op, K, N, C::kBKe, C::kBRows);
+    if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, kMapBf16, N, M, 64, 32);
+    else ok &= make_map_2d(&mC0, C0, kMapF32, N, M, 32, 32);
+    if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, kMapBf16, N, M, 64, 32);
     else mC1 = mC0;
     // the epilogue's [M][N] operand (row stride N), in the output chunks' boxes
-    if (C::kAux) ok &= a.aux != nullptr && a.ld_aux == N && make_map_2d(&mAux, a.aux, false, N, M, 64, 32);
+    if (C::kAux) ok &= a.aux != nullptr && a.ld_aux == N && make_map_2d(&mAux, a.aux, kMapBf16, N, M, 64, 32);
     else mAux = mC0;
     if (!ok) return MLPBLK_ECUDA;
 
@@ -755,7 +794,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.K = K;
     a.m_tiles = (M + C::kTileM - 1) / C::kTileM;
     a.n_tiles = (N + C::BN - 1) / C::BN;
-    a.k_blocks = (K + kBK - 1) / kBK;
+    a.k_blocks = (K + C::kBKe - 1) / C::kBKe;
     const int tiles = a.m_tiles * a.n_tiles;
     const int kb = a.k_blocks;
     a.tiles = tiles;
@@ -841,7 +880,8 @@ constexpr int kAllowPair192 = 2;  // only with a K-major B operand
 // not need.  Returns the mode, with kUseStreamK set when stream-K wins.
 constexpr int kUseStreamK = 0x100;
 
-inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int num_sms, int allow_pairs) {
+inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int num_sms, int allow_pairs,
+                       int elem_bytes = 2) {
     // MLPBLK_TILE=128|192|256|pair|pair192 forces one mode where the GEMM
     // allows it (tests run every mode through the same parity suite); the
     // schedule is still chosen by cost
@@ -855,7 +895,7 @@ inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int nu
     }
     if (forced == kTilePair256 && !(allow_pairs & kAllowPair256)) forced = kTile256;
     if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) forced = kTile192;
-    const int64_t kb = (K + kBK - 1) / kBK;
+    const int64_t kb = (static_cast<int64_t>(K) * elem_bytes + 127) / 128;  // 128-byte k-blocks
     double best = 1e300;
     int choice = kTile128;
     auto consider = [&](int mode, int tile_m, int bn, int cta_per_worker, double shape_eff) {

@@ -105,6 +105,7 @@ struct GemmArgs {
     int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
+    const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
     const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
     int ld_aux;
     const float *rstd_in;      // DgradH: per-row rstd
@@ -176,6 +177,19 @@ int launch_clip_grads(float *g0, int64_t n0, float *g1, int64_t n1, float *g2, i
                       cudaStream_t s);
 int launch_adamw(const AdamTensor *tensors, int count, float lr, float beta1, float beta2, float eps,
                  float weight_decay, int64_t step, bool bf16, const float *grad_scale, cudaStream_t s);
+
+// Host: E4M3 quantisation (fp8.cu) and the E4M3 GEMMs (gemm_f8.cu).  A scale
+// record is 4 floats {amax, 448 / amax, amax / 448, 0}.  n is a multiple of 8.
+int launch_amax_e4m3(const void *v, const void *colmul, int64_t cols, int64_t n, float *partial, int max_parts,
+                     int *parts_out, cudaStream_t s);
+int launch_scale_e4m3(const float *partial, int parts, float *scale, int *zero_flags, int zero_count,
+                      cudaStream_t s);
+int launch_apply_e4m3(const void *v, const void *colmul, int64_t cols, int64_t n, const float *scale, uint8_t *q,
+                      cudaStream_t s);
+int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_t d, float eps, cudaStream_t s);
+int launch_gemm_tc_f8(int epi, int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
+                      const GemmArgs &extra, int num_sms, cudaStream_t s);
+int take_device_error_gemm_f8();
 
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].

@@ -156,6 +156,26 @@ def test_optimizer_argument_errors_need_no_device(mb):
     assert step(bad, 1, ctypes.byref(hp)) == mb.MLPBLK_EINVAL
 
 
+def test_fp8_argument_errors_need_no_device(mb):
+    d = mb.make_desc(64, 128, 256)
+    assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(d)) > 0
+    assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(mb.make_desc(64, 136, 256))) == 0   # d % 16
+    assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(mb.make_desc(64, 128, 256, dtype=mb.MLPBLK_FP32))) == 0
+    fwd = [0x10000 * (i + 1) for i in range(10)]
+    f = lambda args, ws=1 << 40, dd=d: mb.lib.mlpblk_forward_fp8(ctypes.byref(dd), *args, ws, None)
+    assert f(fwd, dd=mb.make_desc(64, 136, 256)) == mb.MLPBLK_ENOTSUP
+    bad = list(fwd)
+    bad[9] += 4   # scales misaligned
+    assert f(bad) == mb.MLPBLK_EINVAL
+    assert f(fwd, 16) == mb.MLPBLK_EWORKSPACE
+    bwd = [0x10000 * (i + 1) for i in range(14)]
+    b = lambda args, ws=1 << 40: mb.lib.mlpblk_backward_fp8(ctypes.byref(d), *args, ws, None)
+    alias = list(bwd)
+    alias[10] = alias[0]   # dx == dy
+    assert b(alias) == mb.MLPBLK_EINVAL
+    assert b(bwd, 16) == mb.MLPBLK_EWORKSPACE
+
+
 def test_grad_buffers_are_float32_by_contract():
     """The gradient accumulators are declared float32: the bf16 loss of a small
     contribution next to a large running sum is why."""

@@ -1,0 +1,115 @@
+"""The FP8 (E4M3) operand variant against its float64 oracle (oracle.fp8), which
+quantises the same tensors with the same per-tensor scales (GB300 only).
+
+Tolerance: scaled error 2e-2, as for the bf16 block.  The quantisation decisions
+are taken on float32 values on both sides (the same codes wherever the inputs to
+a quantisation agree: W1*gamma, W2, W1 and dy exactly; n', a and dh up to the
+last bits of their float32 sums, which moves a few codes by one step); what
+remains is float32 accumulation and the bf16 roundings of the bf16 block.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import fp8 as fp8_oracle
+from helpers import to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mlp_block_backprop_gb300 as mb  # noqa: F401
+    yield
+    assert mb.mlpblk_last_error() == mb.MLPBLK_OK
+
+
+def _run_fp8(inp):
+    import torch
+    import mlp_block_backprop_gb300 as mb
+    bb = mb.BlockBuffers(inp.tokens, inp.d, inp.ffn, dtype="bf16", eps=inp.eps, fp8=True)
+    bb.gamma.copy_(to_dev(inp.gamma, bb.dt))
+    bb.w1.copy_(to_dev(inp.w1, bb.dt))
+    bb.w2.copy_(to_dev(inp.w2, bb.dt))
+    bb.zero_grads()
+    outs = []
+    for x, dy in zip(inp.x, inp.dy):
+        bb.x.copy_(to_dev(x, bb.dt))
+        bb.dy.copy_(to_dev(dy, bb.dt))
+        bb.forward()
+        bb.backward()
+        outs.append({k: to_np(getattr(bb, k)) for k in ("y", "h", "rstd", "dx")})
+    if inp.grad_scale is not None:
+        bb.scale_grads(inp.grad_scale)
+    torch.cuda.synchronize()
+    grads = {k: to_np(getattr(bb, k)) for k in ("dgamma", "dw1", "dw2")}
+    return outs, grads, bb
+
+
+def _check(inp):
+    outs, grads, _ = _run_fp8(inp)
+    ref_outs, ref_grads = fp8_oracle.run_workload(inp)
+    errs = {}
+    for i, (g, r) in enumerate(zip(outs, ref_outs)):
+        for k, rk in (("y", "y"), ("h", "h"), ("rstd", "r"), ("dx", "dx")):
+            errs[f"{k}[{i}]"] = oracle.scaled_error(g[k], r[rk])
+    for k in ("dgamma", "dw1", "dw2"):
+        errs[k] = oracle.scaled_error(grads[k], ref_grads[k])
+    bad = {k: v for k, v in errs.items() if not (v <= TOL)}
+    assert not bad, f"scaled error above {TOL}: {bad} (all: {errs})"
+    return errs
+
+
+def test_fp8_small_bf16_accum4_config():
+    _check(synth.config_inputs("small_bf16_accum4"))
+
+
+@pytest.mark.parametrize("shape", [
+    (333, 208, 336),    # ragged tokens; several tiles in every GEMM
+    (1, 256, 512),      # one token
+    (77, 144, 1040),    # ffn spans five 256-wide tiles with a tail
+    (520, 528, 528),
+])
+def test_fp8_ragged(shape):
+    T, d, F = shape
+    _check(synth.make_inputs(tokens=T, d=d, ffn=F, dtype="bf16", seed=T + d + F, n_mb=2, eps=1e-5))
+
+
+def test_fp8_saved_codes_and_scale():
+    """The saved a codes are E4M3 bytes whose largest magnitude is 448 (the amax
+    element), and a's scale record is {amax, 448/amax, amax/448, 0}."""
+    import torch
+    inp = synth.make_inputs(tokens=256, d=128, ffn=512, dtype="bf16", seed=3, n_mb=1, eps=1e-6)
+    _, _, bb = _run_fp8(inp)
+    a8 = bb.a8.view(torch.float8_e4m3fn).float()
+    assert float(a8.abs().max()) == 448.0
+    assert float(a8.min()) >= 0.0           # a = relu(h)^2 >= 0
+    sc = bb.scales.cpu().numpy()
+    assert sc[1] == np.float32(448.0) / np.float32(sc[0])
+    assert sc[2] == np.float32(sc[0]) / np.float32(448.0)
+    n8 = bb.n8.view(torch.float8_e4m3fn).float().cpu().numpy()
+    x = inp.x[0].astype(np.float32)
+    r = fp8_oracle.rstd32(inp.x[0], inp.eps)
+    ref = fp8_oracle.e4m3((x * r[:, None]).astype(np.float32))
+    # the codes of n' = x * rstd: equal, except where the two float32 rstd values
+    # (different summation orders) put x * rstd on either side of a rounding
+    # boundary, and there one step apart
+    diff = n8 != ref
+    assert diff.mean() <= 1e-3
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref[diff]), 2.0 ** -6))) - 3)
+    assert np.all(np.abs(n8[diff] - ref[diff]) <= step * (1 + 1e-6))
+
+
+def test_fp8_matches_the_bf16_block_within_fp8_error():
+    inp = synth.make_inputs(tokens=384, d=256, ffn=768, dtype="bf16", seed=21, n_mb=1, eps=1e-6)
+    outs, grads, _ = _run_fp8(inp)
+    ref_outs, ref_grads = oracle.run_workload(inp)
+    assert oracle.scaled_error(outs[0]["y"] - inp.x[0], ref_outs[0]["y"] - inp.x[0]) < 0.15
+    for k in ("dw1", "dw2"):
+        assert oracle.scaled_error(grads[k], ref_grads[k]) < 0.15
