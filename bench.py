@@ -46,7 +46,7 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.CONFIGS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.CONFIGS) + sorted(synth.MOE_CONFIGS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -464,6 +464,116 @@ def run_ours(args, dist, peaks):
 
 # --------------------------------------------------------- oracle on the host
 
+def run_moe(args, dist, peaks):
+    """The routed ReLU^2 expert block: zero_grads + forward + backward per step,
+    timed like run_ours (CUDA graph of the K steps, then a traced replay)."""
+    import torch
+
+    import mlp_block_backprop_gb300 as mb
+
+    torch.cuda.set_device(dist.local_rank)
+    inp = synth.moe_config_inputs(args.workload)
+    T, d, F, E, k = inp.tokens, inp.d, inp.ffn, inp.experts, inp.top_k
+    bb = mb.MoeBuffers(T, d, F, E, k, eps=inp.eps)
+    bf = torch.bfloat16
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dt)
+    bb.gamma.copy_(to(inp.gamma))
+    bb.w1s.copy_(to(inp.w1s))
+    bb.w2s.copy_(to(inp.w2s))
+    bb.x.copy_(to(inp.x))
+    bb.dy.copy_(to(inp.dy))
+    bb.idx.copy_(to(inp.idx, torch.int32))
+    bb.p.copy_(to(inp.p, torch.float32))
+
+    def step():
+        bb.zero_grads()
+        bb.forward()
+        bb.backward()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches = 1 + 9 + 10
+    trace = mb.KernelTrace(args.steps * launches + 8)
+    plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(plain):
+        for _ in range(args.steps):
+            step()
+    traced = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(traced):
+        with trace:
+            for _ in range(args.steps):
+                step()
+    plain.replay()
+    traced.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dist.local_rank)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record()
+    plain.replay()
+    end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    traced.replay()
+    torch.cuda.synchronize()
+    if mb.mlpblk_last_error() != mb.MLPBLK_OK:
+        raise RuntimeError("device error in the timed region")
+    ms_step = dist.max(start.elapsed_time(end)) / args.steps
+    flop_step = synth.moe_flops(T, d, F, k)
+    value = dist.world * flop_step / (ms_step * 1e-3) / 1e12
+    per = {}
+    for kind, ms in trace.durations():
+        e = per.setdefault(kind, [0, 0.0])
+        e[0] += 1
+        e[1] += ms
+    total_k = sum(v[1] for v in per.values())
+    kernels = {kk: {"launches": v[0], "mean_us": round(1e3 * v[1] / v[0], 2), "share": round(v[1] / total_k, 4)}
+               for kk, v in sorted(per.items(), key=lambda kv: -kv[1][1])}
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    gemm = {kk: round(2.0 * T * k * d * F / (per[kk][1] / per[kk][0] * 1e-3) / 1e12 / peak, 4)
+            for kk in per if kk.startswith("gemm_")}
+    # host x, dy, routing in; dx, d_routing_weights out; public calls
+    hx, hdy = torch.from_numpy(inp.x).to(bf).pin_memory(), torch.from_numpy(inp.dy).to(bf).pin_memory()
+    hdx = torch.empty(T, d, dtype=bf).pin_memory()
+    hdp = torch.empty(T, k, dtype=torch.float32).pin_memory()
+    k_e2e = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    s2.record()
+    for _ in range(k_e2e):
+        bb.x.copy_(hx, non_blocking=True)
+        bb.dy.copy_(hdy, non_blocking=True)
+        step()
+        hdx.copy_(bb.dx, non_blocking=True)
+        hdp.copy_(bb.dp, non_blocking=True)
+    e2.record()
+    torch.cuda.synchronize()
+    ms_e2e = max(s2.elapsed_time(e2), (time.perf_counter() - t0) * 1e3) / k_e2e
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy normals, bf16-rounded; uniform random top-k routing; no dataset)",
+        "config": {"workload": args.workload, "tokens": T, "d_model": d, "ffn_per_expert": F, "experts": E,
+                   "top_k": k, "flop_per_step": flop_step, "launch": "cuda_graph",
+                   "parallelism": "replicas" if dist.world > 1 else "single"},
+        "tokens_per_s": round(dist.world * T / (ms_step * 1e-3), 1),
+        "frac_of_peak": {"sustained": round(value / dist.world / peak, 4)},
+        "gemm_frac_of_sustained_peak": gemm,
+        "kernels": kernels,
+        "gpu_launches": trace.count,
+        "e2e": {"value": round(dist.world * flop_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": T * d * 2 + T * k * 4},
+        "clocks": clk,
+    }
+    return result, None
+
+
 def oracle_sample(inp, tokens, steps=1):
     """Times the float64 oracle on the first `tokens` tokens of every microbatch
     (all weights, all gradient buffers).  Returns seconds per step."""
@@ -555,9 +665,12 @@ def main():
         return
     dist = Dist()
     peaks = load_peaks()
-    result, inp = run_ours(args, dist, peaks)
+    if args.workload in synth.MOE_CONFIGS:
+        result, inp = run_moe(args, dist, peaks)
+    else:
+        result, inp = run_ours(args, dist, peaks)
     if dist.rank == 0:
-        if dist.world == 1 and not args.no_cpu_baseline:
+        if dist.world == 1 and not args.no_cpu_baseline and inp is not None:
             result["cpu_baseline"] = cpu_baseline(inp)
         print(json.dumps(result), flush=True)
     dist.close()

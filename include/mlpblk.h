@@ -242,6 +242,49 @@ int mlpblk_backward_fp8(const mlpblk_desc *desc,
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Routed ReLU^2 experts ("Nemotron Kernels From Inference To Backpropagation" --
+ * "Kernel 4: Routed ReLU2 MoE Inference And Backpropagation"): the pre-norm
+ * shell around a mixture of ReLU^2 experts with a given top-k dispatch,
+ *   y[t] = x[t] + sum_j p[t,j] * W2_e relu(W1_e n[t])^2,  e = expert_idx[t,j],
+ * n = RMSNorm(x) as in mlpblk_forward.  The dispatch is held fixed ("Hard
+ * Top-K Has No Ordinary Derivative"); the backward returns d_hidden (dx),
+ * d_routing_weights (dp), d_expert_up (dw1s +=), d_expert_down (dw2s +=) and
+ * dgamma (+=).  bf16 tensors (base.dtype = MLPBLK_BF16), float32 routing
+ * weights and gradients, int32 expert ids; an id outside [0, experts) selects
+ * nothing.  Weights: w1s[E][F][d], w2s[E][d][F].
+ *
+ * Each expert's (token, slot) assignments run as one segment of a grouped GEMM
+ * (segments padded to 256 rows, token order within a segment); every sum has a
+ * fixed order except the weight-gradient accumulation (TMA reduce-add).
+ *
+ * saved: written by the forward, read by the backward (rstd, the dispatch, the
+ * gathered inputs, h, a and the experts' outputs); mlpblk_moe_saved_size bytes.
+ * workspace: scratch; mlpblk_moe_workspace_size bytes.  Both sizes are 0 for an
+ * invalid descriptor (experts 1..256, top_k 1..experts, d_model <= 4096).
+ */
+typedef struct {
+    mlpblk_desc base;   /* tokens, d_model, ffn (per expert), eps, dtype        */
+    int32_t experts;    /* E                                                    */
+    int32_t top_k;      /* k: experts per token                                 */
+} mlpblk_moe_desc;
+
+size_t mlpblk_moe_saved_size(const mlpblk_moe_desc *desc);
+size_t mlpblk_moe_workspace_size(const mlpblk_moe_desc *desc);
+
+int mlpblk_moe_forward(const mlpblk_moe_desc *desc,
+                       const void *x, const void *gamma, const void *w1s, const void *w2s,
+                       const int32_t *expert_idx, const float *routing_weights,
+                       void *y, void *saved, size_t saved_bytes,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_moe_backward(const mlpblk_moe_desc *desc,
+                        const void *dy, const void *x, const void *gamma,
+                        const void *w1s, const void *w2s, const float *routing_weights,
+                        const void *saved, void *dx, float *d_routing_weights,
+                        float *dgamma, float *dw1s, float *dw2s,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --
  * accumulation across microbatches): dgamma[d], dw1[F,d], dw2[d,F] = 0 (float32).
  * desc->tokens is ignored.  Returns an MLPBLK_* code.
@@ -327,6 +370,11 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_QUANT_SCALE    18  /* E4M3: amax -> scale record                */
 #define MLPBLK_KERNEL_QUANT_APPLY    19  /* E4M3: v -> codes                          */
 #define MLPBLK_KERNEL_NORM_QUANT     20  /* E4M3: rstd and n' = x * rstd              */
+#define MLPBLK_KERNEL_MOE_ROUTE      21  /* experts: ranks, segments, row map         */
+#define MLPBLK_KERNEL_MOE_GATHER     22  /* experts: rows in segment order            */
+#define MLPBLK_KERNEL_MOE_COMBINE    23  /* experts: y = x + weighted outputs         */
+#define MLPBLK_KERNEL_MOE_DP         24  /* experts: d_routing_weights                */
+#define MLPBLK_KERNEL_MOE_SCATTER    25  /* experts: dn = sum of the slots' dn        */
 
 /*
  * mlpblk_trace_begin: from now on, launch i of this library records

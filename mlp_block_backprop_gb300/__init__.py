@@ -32,7 +32,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_rmsnorm_backward_noalloc", "mlpblk_set_test_fault",
             "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute",
             "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step", "mlpblk_set_rmsnorm_mode",
-            "mlpblk_workspace_size_fp8", "mlpblk_forward_fp8", "mlpblk_backward_fp8")
+            "mlpblk_workspace_size_fp8", "mlpblk_forward_fp8", "mlpblk_backward_fp8",
+            "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
@@ -42,7 +43,8 @@ KERNEL_NAMES = {1: "fold_gamma", 2: "gemm_fwd_w1", 3: "gemm_fwd_w2", 4: "gemm_dg
                 5: "gemm_wgrad_w2", 6: "gemm_dgrad_n", 7: "gemm_wgrad_w1", 8: "norm_bwd",
                 9: "dgamma_reduce", 10: "zero_grads", 11: "scale_grads", 12: "rstd",
                 13: "grad_norm", 14: "clip_grads", 15: "adamw", 16: "grad_norm_final",
-                17: "quant_amax", 18: "quant_scale", 19: "quant_apply", 20: "norm_quant"}
+                17: "quant_amax", 18: "quant_scale", 19: "quant_apply", 20: "norm_quant",
+                21: "moe_route", 22: "moe_gather", 23: "moe_combine", 24: "moe_dp", 25: "moe_scatter"}
 
 
 class MlpBlkError(RuntimeError):
@@ -58,6 +60,11 @@ class Desc(ctypes.Structure):
     """mlpblk_desc: shape of one microbatch through one block."""
     _fields_ = [("tokens", ctypes.c_int64), ("d_model", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class MoeDesc(ctypes.Structure):
+    """mlpblk_moe_desc: the dense descriptor plus the expert count and top-k."""
+    _fields_ = [("base", Desc), ("experts", ctypes.c_int32), ("top_k", ctypes.c_int32)]
 
 
 class Param(ctypes.Structure):
@@ -103,6 +110,15 @@ def _load():
     lib.mlpblk_forward_fp8.restype = i32
     lib.mlpblk_backward_fp8.argtypes = [pd] + [vp] * 14 + [sz, vp]
     lib.mlpblk_backward_fp8.restype = i32
+    pm = ctypes.POINTER(MoeDesc)
+    lib.mlpblk_moe_saved_size.argtypes = [pm]
+    lib.mlpblk_moe_saved_size.restype = sz
+    lib.mlpblk_moe_workspace_size.argtypes = [pm]
+    lib.mlpblk_moe_workspace_size.restype = sz
+    lib.mlpblk_moe_forward.argtypes = [pm] + [vp] * 8 + [sz, vp, sz, vp]
+    lib.mlpblk_moe_forward.restype = i32
+    lib.mlpblk_moe_backward.argtypes = [pm] + [vp] * 13 + [sz, vp]
+    lib.mlpblk_moe_backward.restype = i32
     lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_zero_grads.restype = i32
     lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
@@ -250,6 +266,78 @@ def mlpblk_backward_fp8(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved,
                                  _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
                                  _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "mlpblk_backward_fp8")
+
+
+def make_moe_desc(tokens, d_model, ffn, experts, top_k, eps=1e-6) -> MoeDesc:
+    return MoeDesc(make_desc(tokens, d_model, ffn, eps, MLPBLK_BF16), int(experts), int(top_k))
+
+
+def mlpblk_moe_saved_size(desc: MoeDesc) -> int:
+    return int(lib.mlpblk_moe_saved_size(ctypes.byref(desc)))
+
+
+def mlpblk_moe_workspace_size(desc: MoeDesc) -> int:
+    return int(lib.mlpblk_moe_workspace_size(ctypes.byref(desc)))
+
+
+def mlpblk_moe_forward(desc, x, gamma, w1s, w2s, expert_idx, routing_weights, y, saved, workspace, stream=None):
+    rc = lib.mlpblk_moe_forward(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(w1s), _ptr(w2s), _ptr(expert_idx),
+                                _ptr(routing_weights), _ptr(y), _ptr(saved), saved.numel(), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(rc, "mlpblk_moe_forward")
+
+
+def mlpblk_moe_backward(desc, dy, x, gamma, w1s, w2s, routing_weights, saved, dx, d_routing_weights, dgamma,
+                        dw1s, dw2s, workspace, stream=None):
+    rc = lib.mlpblk_moe_backward(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1s), _ptr(w2s),
+                                 _ptr(routing_weights), _ptr(saved), _ptr(dx), _ptr(d_routing_weights),
+                                 _ptr(dgamma), _ptr(dw1s), _ptr(dw2s), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(rc, "mlpblk_moe_backward")
+
+
+class MoeBuffers:
+    """Device buffers of one routed-expert block (bf16 tensors, fp32 routing weights
+    and gradients, int32 expert ids)."""
+
+    def __init__(self, tokens, d_model, ffn, experts, top_k, eps=1e-6, device="cuda"):
+        import torch
+        self.desc = make_moe_desc(tokens, d_model, ffn, experts, top_k, eps)
+        T, d, F, E, k = tokens, d_model, ffn, experts, top_k
+        e = dict(device=device)
+        bf = torch.bfloat16
+        self.gamma = torch.empty(d, dtype=bf, **e)
+        self.w1s = torch.empty(E, F, d, dtype=bf, **e)
+        self.w2s = torch.empty(E, d, F, dtype=bf, **e)
+        self.x = torch.empty(T, d, dtype=bf, **e)
+        self.dy = torch.empty(T, d, dtype=bf, **e)
+        self.y = torch.empty(T, d, dtype=bf, **e)
+        self.dx = torch.empty(T, d, dtype=bf, **e)
+        self.idx = torch.empty(T, k, dtype=torch.int32, **e)
+        self.p = torch.empty(T, k, dtype=torch.float32, **e)
+        self.dp = torch.empty(T, k, dtype=torch.float32, **e)
+        self.dgamma = torch.zeros(d, dtype=torch.float32, **e)
+        self.dw1s = torch.zeros(E, F, d, dtype=torch.float32, **e)
+        self.dw2s = torch.zeros(E, d, F, dtype=torch.float32, **e)
+        sv, ws = mlpblk_moe_saved_size(self.desc), mlpblk_moe_workspace_size(self.desc)
+        if sv == 0 or ws == 0:
+            raise MlpBlkError(MLPBLK_EINVAL, "mlpblk_moe_saved_size")
+        self.saved = torch.empty(sv, dtype=torch.uint8, **e)
+        self.ws = torch.empty(ws, dtype=torch.uint8, **e)
+
+    def forward(self, stream=None):
+        mlpblk_moe_forward(self.desc, self.x, self.gamma, self.w1s, self.w2s, self.idx, self.p, self.y, self.saved,
+                           self.ws, stream=stream)
+
+    def backward(self, stream=None):
+        mlpblk_moe_backward(self.desc, self.dy, self.x, self.gamma, self.w1s, self.w2s, self.p, self.saved,
+                            self.dx, self.dp, self.dgamma, self.dw1s, self.dw2s, self.ws, stream=stream)
+
+    def zero_grads(self, stream=None):
+        # the experts' gradients as one block's of ffn E*F (same element counts)
+        d = self.desc
+        flat = make_desc(0, d.base.d_model, d.base.ffn * d.experts)
+        mlpblk_zero_grads(flat, self.dgamma, self.dw1s, self.dw2s, stream=stream)
 
 
 def mlpblk_zero_grads(desc, dgamma, dw1, dw2, stream=None):

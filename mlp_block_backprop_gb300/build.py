@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmlpblk.so")
-SOURCES = ["api.cu", "gemm_fwd.cu", "gemm_bwd.cu", "rowops.cu", "simt_f32.cu", "noalloc.cu", "optim.cu", "fp8.cu", "gemm_f8.cu"]
+SOURCES = ["api.cu", "gemm_fwd.cu", "gemm_bwd.cu", "rowops.cu", "simt_f32.cu", "noalloc.cu", "optim.cu", "fp8.cu", "gemm_f8.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v"]
 

@@ -673,6 +673,216 @@ int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, 
     return MLPBLK_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Buffers of the routed-expert block.  R = the row space of the experts'
+// segments: T*k assignments plus up to 255 padding rows per expert, rounded to 256.
+struct MoeLayout {
+    int64_t R;
+    // saved
+    int64_t rstd, pos, row_token, row_slot, seg, count, rank, rstd_perm, x_perm, h_perm, a_perm, o_perm, saved;
+    // workspace
+    int64_t w1g, do_perm, dh_perm, dn_perm, dn_s, part, ws;
+};
+
+int check_moe_desc(const mlpblk_moe_desc *m) {
+    if (!m) return MLPBLK_EINVAL;
+    MLPBLK_TRY(check_desc(&m->base));
+    if (m->base.dtype != MLPBLK_BF16) return MLPBLK_ENOTSUP;
+    if (m->experts < 1 || m->experts > 256 || m->top_k < 1 || m->top_k > m->experts) return MLPBLK_EINVAL;
+    const int64_t lim = static_cast<int64_t>(1) << 31;
+    const int64_t T = m->base.tokens, d = m->base.d_model, F = m->base.ffn, E = m->experts;
+    if (T * m->top_k + E * 256 >= lim / (d > F ? d : F)) return MLPBLK_EINVAL;
+    if (E * F >= lim / d) return MLPBLK_EINVAL;
+    return MLPBLK_OK;
+}
+
+MoeLayout moe_layout(const mlpblk_moe_desc *m) {
+    const int64_t T = m->base.tokens, d = m->base.d_model, F = m->base.ffn, E = m->experts, k = m->top_k;
+    MoeLayout l;
+    l.R = (T * k + E * 255 + 255) / 256 * 256;
+    int64_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    l.rstd = take(T * 4);
+    l.pos = take(T * k * 4);
+    l.row_token = take(l.R * 4);
+    l.row_slot = take(l.R * 4);
+    l.seg = take((E + 1) * 4);
+    l.count = take(E * 4);
+    l.rank = take(T * k * 4);
+    l.rstd_perm = take(l.R * 4);
+    l.x_perm = take(l.R * d * 2);
+    l.h_perm = take(l.R * F * 2);
+    l.a_perm = take(l.R * F * 2);
+    l.o_perm = take(l.R * d * 2);
+    l.saved = off;
+    // workspace: the forward's W1*gamma and the backward's buffers share it
+    off = 0;
+    const int64_t w1g = align256(E * F * d * 2);
+    l.w1g = 0;
+    l.do_perm = take(l.R * d * 2);
+    l.dh_perm = take(l.R * F * 2);
+    l.dn_perm = take(l.R * d * 4);
+    l.dn_s = take(T * d * 4);
+    l.part = take(static_cast<int64_t>(kMaxParts) * d * 4);
+    l.ws = off > w1g ? off : w1g;
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mlpblk_moe_saved_size(const mlpblk_moe_desc *desc) {
+    if (check_moe_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(moe_layout(desc).saved);
+}
+
+size_t mlpblk_moe_workspace_size(const mlpblk_moe_desc *desc) {
+    if (check_moe_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(moe_layout(desc).ws);
+}
+
+int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *gamma, const void *w1s,
+                       const void *w2s, const int32_t *expert_idx, const float *routing_weights, void *y,
+                       void *saved, size_t saved_bytes, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_moe_desc(desc));
+    if (desc->base.tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(w1s) || !aligned16(w2s) || !aligned16(expert_idx) ||
+        !aligned16(routing_weights) || !aligned16(y) || !aligned16(saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const MoeLayout l = moe_layout(desc);
+    if (saved_bytes < static_cast<size_t>(l.saved) || workspace_bytes < static_cast<size_t>(l.ws))
+        return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->base.tokens, d = desc->base.d_model, F = desc->base.ffn;
+    const int E = desc->experts, k = desc->top_k;
+    uint8_t *sv = static_cast<uint8_t *>(saved);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *rstd = reinterpret_cast<float *>(sv + l.rstd);
+    int *pos = reinterpret_cast<int *>(sv + l.pos);
+    int *row_token = reinterpret_cast<int *>(sv + l.row_token);
+    int *row_slot = reinterpret_cast<int *>(sv + l.row_slot);
+    int *seg = reinterpret_cast<int *>(sv + l.seg);
+    int *count = reinterpret_cast<int *>(sv + l.count);
+    int *rank = reinterpret_cast<int *>(sv + l.rank);
+    float *rstd_perm = reinterpret_cast<float *>(sv + l.rstd_perm);
+    void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
+    void *w1g = ws + l.w1g;
+    // rstd and every expert's W1 * gamma (the experts' W1 as one [E*F, d] matrix)
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                  launch_norm_prep(MLPBLK_BF16, x, rstd, T, d, desc->base.eps, w1s, gamma, w1g, E * F, nullptr, 0, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_clear(row_token, l.R, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_rank(expert_idx, T * k, E, rank, count, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_offsets(count, E, seg, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s,
+                  launch_moe_route_place(expert_idx, rank, seg, T * k, k, E, pos, row_token, row_slot, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_GATHER, s,
+                  launch_moe_gather(x, rstd, row_token, seg, E, l.R, d, x_perm, rstd_perm, s));
+    GemmArgs g1 = {};
+    g1.rstd_in = rstd_perm;
+    g1.grp_mode = kGroupM;
+    g1.grp_count = E;
+    g1.grp_rows = seg;
+    g1.grp_b_off = static_cast<int>(F);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                  launch_gemm_tc_fwd(kEpiFwdW1Pre, (int)l.R, (int)F, (int)d, x_perm, w1g, h_perm, a_perm, g1, sms, s));
+    GemmArgs g2 = {};
+    g2.grp_mode = kGroupM;
+    g2.grp_count = E;
+    g2.grp_rows = seg;
+    g2.grp_b_off = static_cast<int>(d);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s,
+                  launch_gemm_tc_fwd(kEpiStoreBf16, (int)l.R, (int)d, (int)F, a_perm, w2s, o_perm, nullptr, g2, sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_COMBINE, s, launch_moe_combine(x, o_perm, routing_weights, pos, T, k, d, y, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void *x, const void *gamma,
+                        const void *w1s, const void *w2s, const float *routing_weights, const void *saved, void *dx,
+                        float *d_routing_weights, float *dgamma, float *dw1s, float *dw2s, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_moe_desc(desc));
+    if (desc->base.tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1s) || !aligned16(w2s) ||
+        !aligned16(routing_weights) || !aligned16(saved) || !aligned16(dx) || !aligned16(d_routing_weights) ||
+        !aligned16(dgamma) || !aligned16(dw1s) || !aligned16(dw2s) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const MoeLayout l = moe_layout(desc);
+    if (workspace_bytes < static_cast<size_t>(l.ws)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = desc->base.tokens, d = desc->base.d_model, F = desc->base.ffn;
+    const int E = desc->experts, k = desc->top_k;
+    const uint8_t *sv = static_cast<const uint8_t *>(saved);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const float *rstd = reinterpret_cast<const float *>(sv + l.rstd);
+    const int *pos = reinterpret_cast<const int *>(sv + l.pos);
+    const int *row_token = reinterpret_cast<const int *>(sv + l.row_token);
+    const int *row_slot = reinterpret_cast<const int *>(sv + l.row_slot);
+    const int *seg = reinterpret_cast<const int *>(sv + l.seg);
+    const float *rstd_perm = reinterpret_cast<const float *>(sv + l.rstd_perm);
+    const void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
+    void *do_perm = ws + l.do_perm, *dh_perm = ws + l.dh_perm;
+    float *dn_perm = reinterpret_cast<float *>(ws + l.dn_perm);
+    float *dn_s = reinterpret_cast<float *>(ws + l.dn_s);
+    float *part = reinterpret_cast<float *>(ws + l.part);
+    int parts = 0;
+    // d_routing_weights, then each slot's output gradient p * dy in segment order
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_DP, s, launch_moe_routing_grad(dy, o_perm, pos, T, k, d, d_routing_weights, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_GATHER, s,
+                  launch_moe_gather_dout(dy, routing_weights, row_token, row_slot, seg, E, k, l.R, d, do_perm, s));
+    GemmArgs gw2 = {};
+    gw2.grp_mode = kGroupK;
+    gw2.grp_count = E;
+    gw2.grp_rows = seg;
+    gw2.grp_c_off = static_cast<int>(d);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
+                  launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)l.R, do_perm, a_perm, dw2s, nullptr, gw2, sms, s));
+    GemmArgs gd = {};
+    gd.aux = static_cast<const uint16_t *>(h_perm);
+    gd.ld_aux = (int)F;
+    gd.rstd_in = rstd_perm;
+    gd.grp_mode = kGroupM;
+    gd.grp_count = E;
+    gd.grp_rows = seg;
+    gd.grp_b_off = static_cast<int>(d);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
+                  launch_gemm_tc_bwd(kEpiDgradH, (int)l.R, (int)F, (int)d, do_perm, w2s, dh_perm, nullptr, gd, sms, s));
+    GemmArgs gn = {};
+    gn.grp_mode = kGroupM;
+    gn.grp_count = E;
+    gn.grp_rows = seg;
+    gn.grp_b_off = static_cast<int>(F);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
+                  launch_gemm_tc_bwd(kEpiStoreF32, (int)l.R, (int)d, (int)F, dh_perm, w1s, dn_perm, nullptr, gn, sms, s));
+    GemmArgs gw1 = {};
+    gw1.colscale = static_cast<const uint16_t *>(gamma);
+    gw1.grp_mode = kGroupK;
+    gw1.grp_count = E;
+    gw1.grp_rows = seg;
+    gw1.grp_c_off = static_cast<int>(F);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
+                  launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)l.R, dh_perm, x_perm, dw1s, nullptr, gw1,
+                                     sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_SCATTER, s, launch_moe_scatter_dn(dn_perm, pos, T, k, d, dn_s, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s,
+                  launch_rmsnorm_bwd(MLPBLK_BF16, x, dn_s, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+    return MLPBLK_OK;
+}
+
 int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {
     MLPBLK_TRY(check_desc(desc));
     if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;

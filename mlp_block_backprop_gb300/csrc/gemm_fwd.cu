@@ -5,6 +5,7 @@
 //            prologue warps reading the x stages (kEpiFwdW1)
 //   W2 GEMM: y = x + a . W2^T                           (residual add in the epilogue)
 //   W1 GEMM, a only (kEpiFwdW1A): the recompute variant's forward keeps no h
+//   plain bf16 store (kEpiStoreBf16): the routed experts' down projections
 #include <stdlib.h>
 
 #include "gemm_tc.cuh"
@@ -34,6 +35,7 @@ int launch_gemm_tc_fwd(int epi, int M, int N, int K, const void *A, const void *
     if (epi == kEpiFwdW1Pre) { MLPBLK_RUN(kEpiFwdW1Pre) }
     if (epi == kEpiFwdW1A) { MLPBLK_RUN(kEpiFwdW1A) }
     if (epi == kEpiFwdW2) { MLPBLK_RUN(kEpiFwdW2) }
+    if (epi == kEpiStoreBf16) { MLPBLK_RUN(kEpiStoreBf16) }
 #undef MLPBLK_RUN
 #undef MLPBLK_RUN_MODE
     return MLPBLK_EINVAL;

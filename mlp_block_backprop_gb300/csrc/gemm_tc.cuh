@@ -66,7 +66,7 @@ struct GemmCfg {
     static constexpr bool kNorm = (EPI == kEpiFwdW1);
     static constexpr bool kReluSq = (EPI == kEpiFwdW1 || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A);
     static constexpr bool kAOnly = (EPI == kEpiFwdW1A);  // a out only (h is not kept)
-    static constexpr bool kOutBf16 = (kReluSq || EPI == kEpiFwdW2 || EPI == kEpiDgradH);
+    static constexpr bool kOutBf16 = (kReluSq || EPI == kEpiFwdW2 || EPI == kEpiDgradH || EPI == kEpiStoreBf16);
     static constexpr bool kReduce = (EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
     static constexpr int kNumOut = (kReluSq && !kAOnly) ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
@@ -115,6 +115,8 @@ struct GemmCfg {
 // One segment of a worker's work: k-blocks [kb0, kb1) of one output tile.
 struct Seg {
     int tile, m0, n0, n_blk, kb0, kb1;  // m0, n0: origin of the (pair) output tile
+    int crow;  // K-grouped: rows added to the output row (the expert's block of C)
+    int boff;  // M-grouped: the expert's offset into B (rows of a K-major B, K of an MN-major B)
 };
 
 // First stream-K iteration of worker w (iterations of the tiles after dp_tiles,
@@ -127,14 +129,30 @@ __device__ __forceinline__ int sk_begin(const GemmArgs &a, int w) {
 // dp_tiles, then its stream-K range, cut at tile boundaries.  Only the first
 // stream-K segment can start inside a tile, and only the last can end inside
 // one, so a worker writes at most one partial and owns at most one split tile.
+//
+// Grouped GEMMs (the routed experts; whole tiles only):
+//   M-grouped: the rows are the experts' token segments back to back, each padded
+//     to a multiple of 256 rows (grp_rows[e] .. grp_rows[e+1]); the row count is
+//     read from device memory, and a tile's expert selects its slice of B;
+//   K-grouped (weight gradients): expert e's tiles sum over K = its segment's
+//     rows and write the expert's block of C; experts without tokens are skipped.
 struct SegIter {
-    int worker, j, n_dp, pos, end;
+    int worker, j, n_dp, pos, end, m_tiles;
 };
 
+template <int TILE_M>
 __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
     SegIter it;
     it.worker = worker;
     it.j = 0;
+    it.m_tiles = a.m_tiles;
+    if (a.grp_mode != kGroupNone) {
+        if (a.grp_mode == kGroupM) it.m_tiles = a.grp_rows[a.grp_count] / TILE_M;
+        const int total = (a.grp_mode == kGroupM ? it.m_tiles : a.grp_count * a.m_tiles) * a.n_tiles;
+        it.n_dp = total > worker ? (total - worker + a.workers - 1) / a.workers : 0;
+        it.pos = it.end = 0;
+        return it;
+    }
     it.n_dp = a.dp_tiles / a.workers;
     it.pos = sk_begin(a, worker);
     it.end = sk_begin(a, worker + 1);
@@ -143,33 +161,52 @@ __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
 
 // Tiles are rastered in groups of group_m M-tiles that sweep all N-tiles
 // together, so tiles in flight at the same time share operand tiles in L2.
-template <int BN, int TILE_M>
+template <int BN, int TILE_M, int KBE>
 __device__ __forceinline__ bool seg_next(const GemmArgs &a, SegIter &it, Seg &s) {
-    int t;
-    if (it.j < it.n_dp) {
-        t = it.worker + it.j * a.workers;
-        s.kb0 = 0;
-        s.kb1 = a.k_blocks;
-        ++it.j;
-    } else if (it.pos < it.end) {
-        const int tt = it.pos / a.k_blocks;
-        s.kb0 = it.pos - tt * a.k_blocks;
-        s.kb1 = min(a.k_blocks, s.kb0 + (it.end - it.pos));
-        it.pos += s.kb1 - s.kb0;
-        t = a.dp_tiles + tt;
-    } else {
-        return false;
+    while (true) {
+        int t;
+        if (it.j < it.n_dp) {
+            t = it.worker + it.j * a.workers;
+            s.kb0 = 0;
+            s.kb1 = a.k_blocks;
+            ++it.j;
+        } else if (it.pos < it.end) {
+            const int tt = it.pos / a.k_blocks;
+            s.kb0 = it.pos - tt * a.k_blocks;
+            s.kb1 = min(a.k_blocks, s.kb0 + (it.end - it.pos));
+            it.pos += s.kb1 - s.kb0;
+            t = a.dp_tiles + tt;
+        } else {
+            return false;
+        }
+        s.tile = t;
+        s.crow = 0;
+        s.boff = 0;
+        if (a.grp_mode == kGroupK) {
+            const int per = a.m_tiles * a.n_tiles;
+            const int e = t / per;
+            t -= e * per;
+            s.kb0 = a.grp_rows[e] / KBE;
+            s.kb1 = a.grp_rows[e + 1] / KBE;
+            if (s.kb0 == s.kb1) continue;  // an expert without tokens: no tile
+            s.crow = e * a.grp_c_off;
+        }
+        const int mt = it.m_tiles;
+        const int group = a.group_m * a.n_tiles;
+        const int g = t / group;
+        const int first_m = g * a.group_m;
+        const int gm = min(mt - first_m, a.group_m);
+        const int r = t - g * group;
+        s.n_blk = r / gm;
+        s.m0 = (first_m + r % gm) * TILE_M;
+        s.n0 = s.n_blk * BN;
+        if (a.grp_mode == kGroupM) {
+            int e = 0;
+            while (e + 1 < a.grp_count && a.grp_rows[e + 1] <= s.m0) ++e;
+            s.boff = e * a.grp_b_off;
+        }
+        return true;
     }
-    s.tile = t;
-    const int group = a.group_m * a.n_tiles;
-    const int g = t / group;
-    const int first_m = g * a.group_m;
-    const int gm = min(a.m_tiles - first_m, a.group_m);
-    const int r = t - g * group;
-    s.n_blk = r / gm;
-    s.m0 = (first_m + r % gm) * TILE_M;
-    s.n0 = s.n_blk * BN;
-    return true;
 }
 
 __device__ __forceinline__ float sq(float v) { return v * v; }
@@ -261,11 +298,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0 && !args.skip_loads) {
             int stage = 0;
             uint32_t phase = 0;
-            SegIter si = seg_begin(args, worker);
+            SegIter si = seg_begin<C::kTileM>(args, worker);
             Seg w;
-            while (seg_next<C::BN, C::kTileM>(args, si, w)) {
+            while (seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w)) {
                 const int a_row = w.m0 + static_cast<int>(rank) * kBM;       // this CTA's A rows
-                const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows;  // this CTA's B rows
+                // this CTA's B rows (a K-major B's rows carry the expert offset)
+                const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows + (C::B_MN ? 0 : w.boff);
+                const int bk = C::B_MN ? w.boff : 0;  // an MN-major B's K carries it
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) goto producer_done;
                     uint8_t *sa = stages + stage * C::kStageBytes;
@@ -297,8 +336,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (C::B_MN) {
 #pragma unroll
                         for (int j = 0; j < C::kBRows / C::kMNBox; ++j) {
-                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0);
-                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0);
+                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
+                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
                         }
                     } else {
                         if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb, k0, b_row);
@@ -319,9 +358,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            SegIter si = seg_begin(args, worker);
+            SegIter si = seg_begin<C::kTileM>(args, worker);
             Seg w;
-            for (; seg_next<C::BN, C::kTileM>(args, si, w); ++it) {
+            for (; seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w); ++it) {
                 const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
                 const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
                 if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
@@ -414,9 +453,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t aux_phase = 0;
         float rsc_pre = 1.0f;
         const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
-        SegIter si = seg_begin(args, worker);
+        SegIter si = seg_begin<C::kTileM>(args, worker);
         Seg w;
-        bool have = seg_next<C::BN, C::kTileM>(args, si, w);
+        bool have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
         if (have) prefetch(w, rsc_pre);
         for (; have; ++it) {
             // The fused epilogues are nonlinear in the sum over k, so a tile split
@@ -579,6 +618,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                     o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
                                 }
                             }
+                        } else if (C::EPI == kEpiStoreBf16) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
                         } else if (C::EPI == kEpiFwdW2) {
                             const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
 #pragma unroll
@@ -617,7 +659,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 __syncwarp();
                 if (lane == 0) {
                     if (warp_rows) {
-                        const int r0 = m0 + 32 * q;
+                        const int r0 = m0 + 32 * q + w.crow;
                         if (C::kReduce) {
                             tma_reduce_add_2d(&tmC0, st0, col0, r0);
                         } else {
@@ -647,7 +689,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (lane == 0) st_release_gpu(&args.sk_flags[slot * 4 + q], 1);
             }
             // every lane is done with this segment's shared operand copy
-            have = seg_next<C::BN, C::kTileM>(args, si, w);
+            have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
             if (have) prefetch(w, rsc_pre);
         }
         if (lane == 0) {
@@ -662,9 +704,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
-        SegIter si = seg_begin(args, worker);  // whole tiles only (no stream-K)
+        SegIter si = seg_begin<C::kTileM>(args, worker);  // whole tiles only (no stream-K)
         Seg w;
-        for (; seg_next<C::BN, C::kTileM>(args, si, w); ++it) {
+        for (; seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w); ++it) {
             const int m0 = w.m0 + static_cast<int>(rank) * kBM;
             const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
             const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -773,10 +815,15 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     const int op = C::F8 ? kMapU8 : kMapBf16;
     ok &= C::A_MN ? make_map_2d(&mA, A, op, M, K, C::kMNBox, C::kBKe)
                   : make_map_2d(&mA, A, op, K, M, C::kBKe, kBM);
-    ok &= C::B_MN ? make_map_2d(&mB, B, op, N, K, C::kMNBox, C::kBKe)
-                  : make_map_2d(&mB, B, op, K, N, C::kBKe, C::kBRows);
-    if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, kMapBf16, N, M, 64, 32);
-    else ok &= make_map_2d(&mC0, C0, kMapF32, N, M, 32, 32);
+    // grouped GEMMs: B holds every expert's slice (M-grouped), C every expert's
+    // block (K-grouped)
+    const uint64_t groups = a.grp_mode != kGroupNone ? static_cast<uint64_t>(a.grp_count) : 1u;
+    const uint64_t b_outer = a.grp_mode == kGroupM ? groups : 1u;
+    const uint64_t c_rows = static_cast<uint64_t>(M) * (a.grp_mode == kGroupK ? groups : 1u);
+    ok &= C::B_MN ? make_map_2d(&mB, B, op, N, K * b_outer, C::kMNBox, C::kBKe)
+                  : make_map_2d(&mB, B, op, K, N * b_outer, C::kBKe, C::kBRows);
+    if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, kMapBf16, N, c_rows, 64, 32);
+    else ok &= make_map_2d(&mC0, C0, kMapF32, N, c_rows, 32, 32);
     if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, kMapBf16, N, M, 64, 32);
     else mC1 = mC0;
     // the epilogue's [M][N] operand (row stride N), in the output chunks' boxes
@@ -800,9 +847,16 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = 16;
     int workers = slots;
-    const bool sk = !C::kNorm && !a.whole_tiles && streamk_enabled() &&
+    const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode == kGroupNone && streamk_enabled() &&
                     (C::kReduce || (a.sk_partial && a.sk_flags));
-    if (!sk || tiles % workers == 0) {
+    if (a.grp_mode != kGroupNone) {
+        // grouped: whole tiles dealt round robin over a count the kernel reads
+        // from device memory (M-grouped) or over every expert's tiles (K-grouped)
+        const int64_t upper = a.grp_mode == kGroupK ? static_cast<int64_t>(tiles) * a.grp_count : tiles;
+        if (upper < workers) workers = static_cast<int>(upper > 0 ? upper : 1);
+        a.dp_tiles = 0;
+        a.sk_base = a.sk_rem = a.sk_total = 0;
+    } else if (!sk || tiles % workers == 0) {
         // whole tiles: full rounds dealt round robin, the last tiles one each
         if (tiles < workers) workers = tiles;
         a.dp_tiles = tiles / workers * workers;

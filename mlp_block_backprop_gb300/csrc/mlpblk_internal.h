@@ -82,6 +82,7 @@ enum Epilogue : int {
     kEpiAccF32ColScale = 5,  // out += colscale[n] * acc (fp32, TMA reduce-add)
     kEpiFwdW1Pre = 6, // h = rstd*acc, a = relu(h)^2 (bf16 x2); rstd read from global
     kEpiFwdW1A = 7,   // a = relu(rstd*acc)^2 only (bf16); rstd read from global
+    kEpiStoreBf16 = 8,  // out = acc (bf16): the routed experts' outputs
 };
 
 // Arguments of one GEMM launch (the tensor maps travel separately).
@@ -90,6 +91,8 @@ enum Epilogue : int {
 constexpr int kMaxSkSlots = 160;
 constexpr int kSkSlotFloats = 128 * 256;
 constexpr int kSkFlagsPerSet = kMaxSkSlots * 4;
+
+enum GroupMode : int { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
 
 struct GemmArgs {
     int M, N, K;
@@ -106,6 +109,11 @@ struct GemmArgs {
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
+    // grouped GEMMs of the routed experts (kGroupNone otherwise)
+    int grp_mode, grp_count;   // kGroupM / kGroupK; number of experts
+    const int *grp_rows;       // device [grp_count + 1]: padded segment starts (rows)
+    int grp_b_off;             // M-grouped: per-expert offset into B (rows or K)
+    int grp_c_off;             // K-grouped: per-expert rows of C
     const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
     int ld_aux;
     const float *rstd_in;      // DgradH: per-row rstd
@@ -190,6 +198,25 @@ int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_
 int launch_gemm_tc_f8(int epi, int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
                       const GemmArgs &extra, int num_sms, cudaStream_t s);
 int take_device_error_gemm_f8();
+
+// Host: dispatch / combine of the routed experts (moe.cu).  Rows are the
+// experts' segments of (token, slot) assignments, each padded to 256 rows.
+int launch_moe_route_clear(int *row_token, int64_t rows_max, cudaStream_t s);
+int launch_moe_route_rank(const int *idx, int64_t n, int experts, int *rank, int *count, cudaStream_t s);
+int launch_moe_route_offsets(const int *count, int experts, int *seg, cudaStream_t s);
+int launch_moe_route_place(const int *idx, const int *rank, const int *seg, int64_t n, int k, int experts,
+                           int *pos, int *row_token, int *row_slot, cudaStream_t s);
+int launch_moe_gather(const void *x, const float *rstd, const int *row_token, const int *seg, int experts,
+                      int64_t rows_max, int64_t d, void *x_perm, float *rstd_perm, cudaStream_t s);
+int launch_moe_combine(const void *x, const void *o_perm, const float *p, const int *pos, int64_t T, int k,
+                       int64_t d, void *y, cudaStream_t s);
+int launch_moe_routing_grad(const void *dy, const void *o_perm, const int *pos, int64_t T, int k, int64_t d,
+                            float *dp, cudaStream_t s);
+int launch_moe_gather_dout(const void *dy, const float *p, const int *row_token, const int *row_slot,
+                           const int *seg, int experts, int k, int64_t rows_max, int64_t d, void *do_perm,
+                           cudaStream_t s);
+int launch_moe_scatter_dn(const float *dn_perm, const int *pos, int64_t T, int k, int64_t d, float *dn_s,
+                          cudaStream_t s);
 
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].

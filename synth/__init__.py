@@ -126,3 +126,58 @@ def config_inputs(name: str) -> BlockInputs:
 def block_flops(tokens: int, d: int, ffn: int, n_mb: int = 1) -> int:
     """Algorithmic tensor work of one forward+backward: six GEMMs of 2*T*d*ffn each."""
     return 12 * tokens * d * ffn * n_mb
+
+
+# ----------------------------------------------------------- routed experts
+
+MOE_CONFIGS = {
+    # 8 experts of ffn 1024, top-2, on 8192 tokens of width 2048
+    "moe_e8k2": dict(tokens=8192, d=2048, ffn=1024, experts=8, top_k=2, seed=7, dy_std=1e-2),
+}
+
+
+@dataclass
+class MoeInputs:
+    """A routed-expert workload (bf16 storage values; routing weights float32)."""
+    name: str
+    tokens: int
+    d: int
+    ffn: int
+    experts: int
+    top_k: int
+    eps: float
+    gamma: np.ndarray
+    w1s: np.ndarray      # [E, ffn, d]
+    w2s: np.ndarray      # [E, d, ffn]
+    x: np.ndarray
+    dy: np.ndarray
+    idx: np.ndarray      # [T, k] int32, k distinct experts per token
+    p: np.ndarray        # [T, k] float32 in [0.1, 1)
+
+
+def make_moe_inputs(tokens: int, d: int, ffn: int, experts: int, top_k: int, seed: int = 0,
+                    dy_std: float = 1.0, eps: float = EPS, name: str = "custom_moe") -> MoeInputs:
+    """Draw order: gamma, W1 of every expert, W2 of every expert, x, dy, the
+    routing (k distinct experts per token: the first k of a uniformly random
+    ordering), then the weights p ~ U(0.1, 1)."""
+    rng = np.random.default_rng(seed)
+    gamma = _draw(rng, (d,), 1.0, 0.02, "bf16")
+    w1s = _draw(rng, (experts, ffn, d), 0.0, 1.0 / np.sqrt(d), "bf16")
+    w2s = _draw(rng, (experts, d, ffn), 0.0, 1.0 / np.sqrt(ffn), "bf16")
+    x = _draw(rng, (tokens, d), 0.0, 1.0, "bf16")
+    dy = _draw(rng, (tokens, d), 0.0, dy_std, "bf16")
+    idx = np.argsort(rng.random((tokens, experts)), axis=1)[:, :top_k].astype(np.int32)
+    p = rng.uniform(0.1, 1.0, size=(tokens, top_k)).astype(np.float32)
+    return MoeInputs(name=name, tokens=tokens, d=d, ffn=ffn, experts=experts, top_k=top_k, eps=eps,
+                     gamma=gamma, w1s=w1s, w2s=w2s, x=x, dy=dy, idx=idx, p=p)
+
+
+def moe_config_inputs(name: str) -> MoeInputs:
+    c = MOE_CONFIGS[name]
+    return make_moe_inputs(tokens=c["tokens"], d=c["d"], ffn=c["ffn"], experts=c["experts"],
+                           top_k=c["top_k"], seed=c["seed"], dy_std=c["dy_std"], name=name)
+
+
+def moe_flops(tokens: int, d: int, ffn: int, top_k: int) -> int:
+    """Algorithmic tensor work of one forward+backward: six GEMMs per assignment."""
+    return 12 * tokens * top_k * d * ffn

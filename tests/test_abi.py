@@ -176,6 +176,30 @@ def test_fp8_argument_errors_need_no_device(mb):
     assert b(bwd, 16) == mb.MLPBLK_EWORKSPACE
 
 
+def test_moe_argument_errors_need_no_device(mb):
+    d = mb.make_moe_desc(64, 128, 256, 4, 2)
+    assert mb.lib.mlpblk_moe_saved_size(ctypes.byref(d)) > 0
+    assert mb.lib.mlpblk_moe_workspace_size(ctypes.byref(d)) > 0
+    for bad in (mb.make_moe_desc(64, 128, 256, 4, 5), mb.make_moe_desc(64, 128, 256, 0, 1),
+                mb.make_moe_desc(64, 100, 256, 4, 2)):
+        assert mb.lib.mlpblk_moe_saved_size(ctypes.byref(bad)) == 0
+    args = [0x10000 * (i + 1) for i in range(8)]
+    f = lambda a, sv=1 << 40, ws=1 << 40: mb.lib.mlpblk_moe_forward(ctypes.byref(d), *a, sv, 0x900000, ws, None)
+    bad = list(args)
+    bad[4] += 4   # expert ids misaligned
+    assert f(bad) == mb.MLPBLK_EINVAL
+    alias = list(args)
+    alias[6] = alias[0]   # y == x
+    assert f(alias) == mb.MLPBLK_EINVAL
+    assert f(args, sv=16) == mb.MLPBLK_EWORKSPACE
+    bargs = [0x10000 * (i + 1) for i in range(13)]
+    b = lambda a, ws=1 << 40: mb.lib.mlpblk_moe_backward(ctypes.byref(d), *a, ws, None)
+    assert b(bargs, 16) == mb.MLPBLK_EWORKSPACE
+    alias = list(bargs)
+    alias[7] = alias[0]   # dx == dy
+    assert b(alias) == mb.MLPBLK_EINVAL
+
+
 def test_grad_buffers_are_float32_by_contract():
     """The gradient accumulators are declared float32: the bf16 loss of a small
     contribution next to a large running sum is why."""
