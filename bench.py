@@ -164,9 +164,22 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-def csrc_hash():
+# the CUDA sources that hold each kernel's device code and its launch choices
+KERNEL_SOURCES = {
+    **{k: ("gemm_tc.cuh", "ptx.cuh", "gemm_fwd.cu") for k in ("gemm_fwd_w1", "gemm_fwd_w2")},
+    **{k: ("gemm_tc.cuh", "ptx.cuh", "gemm_bwd.cu")
+       for k in ("gemm_wgrad_w2", "gemm_dgrad_h", "gemm_dgrad_n", "gemm_wgrad_w1")},
+    **{k: ("rowops.cu",) for k in ("norm_bwd", "fold_gamma", "dgamma_reduce")},
+}
+
+
+def csrc_hash(kernel=None):
+    """Hash of the kernel's sources (KERNEL_SOURCES), else of every CUDA source."""
+    csrc = os.path.join(ROOT, "mlp_block_backprop_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel)
+    paths = [os.path.join(csrc, n) for n in names] if names else sorted(glob.glob(os.path.join(csrc, "*")))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "mlp_block_backprop_gb300", "csrc", "*"))):
+    for p in paths:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
@@ -179,7 +192,7 @@ def recorded_traffic(workload, kernel):
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    cur = csrc_hash()
+    cur = csrc_hash(kernel)
     for line in open(path):
         f = line.split()
         if len(f) == 5 and f[0] == "traffic" and f[1] == kernel and f[2] == workload:
@@ -493,7 +506,7 @@ def run_moe(args, dist, peaks):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    launches = 1 + 9 + 10
+    launches = 1 + 8 + 7   # zero_grads; forward; backward
     trace = mb.KernelTrace(args.steps * launches + 8)
     plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(plain):
@@ -538,6 +551,8 @@ def run_moe(args, dist, peaks):
             for kk in per if kk.startswith("gemm_")}
     # host x, dy, routing in; dx, d_routing_weights out; public calls
     hx, hdy = torch.from_numpy(inp.x).to(bf).pin_memory(), torch.from_numpy(inp.dy).to(bf).pin_memory()
+    hidx = torch.from_numpy(np.ascontiguousarray(inp.idx, dtype=np.int32)).pin_memory()
+    hp = torch.from_numpy(np.ascontiguousarray(inp.p, dtype=np.float32)).pin_memory()
     hdx = torch.empty(T, d, dtype=bf).pin_memory()
     hdp = torch.empty(T, k, dtype=torch.float32).pin_memory()
     k_e2e = max(3, min(args.steps, 10))
@@ -548,6 +563,8 @@ def run_moe(args, dist, peaks):
     for _ in range(k_e2e):
         bb.x.copy_(hx, non_blocking=True)
         bb.dy.copy_(hdy, non_blocking=True)
+        bb.idx.copy_(hidx, non_blocking=True)
+        bb.p.copy_(hp, non_blocking=True)
         step()
         hdx.copy_(bb.dx, non_blocking=True)
         hdp.copy_(bb.dp, non_blocking=True)
@@ -568,7 +585,7 @@ def run_moe(args, dist, peaks):
         "kernels": kernels,
         "gpu_launches": trace.count,
         "e2e": {"value": round(dist.world * flop_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": T * d * 2 + T * k * 4},
+                "h2d_bytes_per_step": 2 * T * d * 2 + T * k * 8, "d2h_bytes_per_step": T * d * 2 + T * k * 4},
         "clocks": clk,
     }
     return result, None

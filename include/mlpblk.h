@@ -370,11 +370,11 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_QUANT_SCALE    18  /* E4M3: amax -> scale record                */
 #define MLPBLK_KERNEL_QUANT_APPLY    19  /* E4M3: v -> codes                          */
 #define MLPBLK_KERNEL_NORM_QUANT     20  /* E4M3: rstd and n' = x * rstd              */
-#define MLPBLK_KERNEL_MOE_ROUTE      21  /* experts: ranks, segments, row map         */
+#define MLPBLK_KERNEL_MOE_ROUTE      21  /* experts: counts, segments, ranks, row map */
 #define MLPBLK_KERNEL_MOE_GATHER     22  /* experts: rows in segment order            */
 #define MLPBLK_KERNEL_MOE_COMBINE    23  /* experts: y = x + weighted outputs         */
-#define MLPBLK_KERNEL_MOE_DP         24  /* experts: d_routing_weights                */
-#define MLPBLK_KERNEL_MOE_SCATTER    25  /* experts: dn = sum of the slots' dn        */
+#define MLPBLK_KERNEL_MOE_DP         24  /* experts: d_routing_weights and p * dy     */
+#define MLPBLK_KERNEL_MOE_SCATTER    25  /* reserved (dn's slot sum is in NORM_BWD)   */
 
 /*
  * mlpblk_trace_begin: from now on, launch i of this library records

@@ -139,7 +139,15 @@ int device_sms(int *sms) {
         cached[dev] = (major == 10 && minor == 3 && n > 0) ? n : -1;
     }
     if (cached[dev] < 0) return MLPBLK_ENODEV;
-    *sms = cached[dev];
+    // MLPBLK_MAX_SMS caps the SMs the GEMMs spread over (an even count, to leave
+    // SMs to concurrent work); unset, they use every SM
+    static int cap = -1;
+    if (cap < 0) {
+        const char *e = getenv("MLPBLK_MAX_SMS");
+        const int v = e ? atoi(e) : 0;
+        cap = v >= 2 ? (v & ~1) : 0;
+    }
+    *sms = (cap > 0 && cap < cached[dev]) ? cap : cached[dev];
     return MLPBLK_OK;
 }
 
@@ -682,9 +690,10 @@ namespace {
 struct MoeLayout {
     int64_t R;
     // saved
-    int64_t rstd, pos, row_token, row_slot, seg, count, rank, rstd_perm, x_perm, h_perm, a_perm, o_perm, saved;
+    int64_t rstd, pos, row_token, row_slot, seg, count, chunk_count, chunk_base, rstd_perm, x_perm, h_perm, a_perm,
+        o_perm, saved;
     // workspace
-    int64_t w1g, do_perm, dh_perm, dn_perm, dn_s, part, ws;
+    int64_t w1g, do_perm, dh_perm, dn_perm, part, ws;
 };
 
 int check_moe_desc(const mlpblk_moe_desc *m) {
@@ -715,7 +724,8 @@ MoeLayout moe_layout(const mlpblk_moe_desc *m) {
     l.row_slot = take(l.R * 4);
     l.seg = take((E + 1) * 4);
     l.count = take(E * 4);
-    l.rank = take(T * k * 4);
+    l.chunk_count = take(moe_route_chunks(T * k) * E * 4);
+    l.chunk_base = take(moe_route_chunks(T * k) * E * 4);
     l.rstd_perm = take(l.R * 4);
     l.x_perm = take(l.R * d * 2);
     l.h_perm = take(l.R * F * 2);
@@ -729,7 +739,6 @@ MoeLayout moe_layout(const mlpblk_moe_desc *m) {
     l.do_perm = take(l.R * d * 2);
     l.dh_perm = take(l.R * F * 2);
     l.dn_perm = take(l.R * d * 4);
-    l.dn_s = take(T * d * 4);
     l.part = take(static_cast<int64_t>(kMaxParts) * d * 4);
     l.ws = off > w1g ? off : w1g;
     return l;
@@ -774,18 +783,18 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     int *row_slot = reinterpret_cast<int *>(sv + l.row_slot);
     int *seg = reinterpret_cast<int *>(sv + l.seg);
     int *count = reinterpret_cast<int *>(sv + l.count);
-    int *rank = reinterpret_cast<int *>(sv + l.rank);
+    int *chunk_count = reinterpret_cast<int *>(sv + l.chunk_count);
+    int *chunk_base = reinterpret_cast<int *>(sv + l.chunk_base);
     float *rstd_perm = reinterpret_cast<float *>(sv + l.rstd_perm);
     void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
     void *w1g = ws + l.w1g;
     // rstd and every expert's W1 * gamma (the experts' W1 as one [E*F, d] matrix)
     MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
                   launch_norm_prep(MLPBLK_BF16, x, rstd, T, d, desc->base.eps, w1s, gamma, w1g, E * F, nullptr, 0, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_clear(row_token, l.R, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_rank(expert_idx, T * k, E, rank, count, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s, launch_moe_route_offsets(count, E, seg, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s,
-                  launch_moe_route_place(expert_idx, rank, seg, T * k, k, E, pos, row_token, row_slot, s));
+    for (int step = 0; step < moe_route_launches(T * k); ++step)
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s,
+                      launch_moe_route(expert_idx, T * k, k, E, chunk_count, chunk_base, count, seg, pos, row_token,
+                                       row_slot, step, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_GATHER, s,
                   launch_moe_gather(x, rstd, row_token, seg, E, l.R, d, x_perm, rstd_perm, s));
     GemmArgs g1 = {};
@@ -829,20 +838,18 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const float *rstd = reinterpret_cast<const float *>(sv + l.rstd);
     const int *pos = reinterpret_cast<const int *>(sv + l.pos);
-    const int *row_token = reinterpret_cast<const int *>(sv + l.row_token);
-    const int *row_slot = reinterpret_cast<const int *>(sv + l.row_slot);
     const int *seg = reinterpret_cast<const int *>(sv + l.seg);
+    const int *count = reinterpret_cast<const int *>(sv + l.count);
     const float *rstd_perm = reinterpret_cast<const float *>(sv + l.rstd_perm);
     const void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
     void *do_perm = ws + l.do_perm, *dh_perm = ws + l.dh_perm;
     float *dn_perm = reinterpret_cast<float *>(ws + l.dn_perm);
-    float *dn_s = reinterpret_cast<float *>(ws + l.dn_s);
     float *part = reinterpret_cast<float *>(ws + l.part);
     int parts = 0;
-    // d_routing_weights, then each slot's output gradient p * dy in segment order
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_DP, s, launch_moe_routing_grad(dy, o_perm, pos, T, k, d, d_routing_weights, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_GATHER, s,
-                  launch_moe_gather_dout(dy, routing_weights, row_token, row_slot, seg, E, k, l.R, d, do_perm, s));
+    // d_routing_weights and each slot's output gradient p * dy in segment order
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_DP, s,
+                  launch_moe_dout(dy, o_perm, routing_weights, pos, count, seg, T, k, E, d, d_routing_weights, do_perm,
+                                  s));
     GemmArgs gw2 = {};
     gw2.grp_mode = kGroupK;
     gw2.grp_count = E;
@@ -876,9 +883,10 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)l.R, dh_perm, x_perm, dw1s, nullptr, gw1,
                                      sms, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_SCATTER, s, launch_moe_scatter_dn(dn_perm, pos, T, k, d, dn_s, s));
+    // the slots' dn meet at n (sum rule) inside the RMSNorm backward
     MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s,
-                  launch_rmsnorm_bwd(MLPBLK_BF16, x, dn_s, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts, s));
+                  launch_rmsnorm_bwd_gather(x, dn_perm, pos, k, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts,
+                                            s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
 }

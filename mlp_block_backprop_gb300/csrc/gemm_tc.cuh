@@ -804,6 +804,17 @@ inline bool streamk_enabled() {
     return v == 1;
 }
 
+// M tiles per raster group: MLPBLK_GROUP_M (1..64) when set, else 16.
+inline int raster_group_m() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_GROUP_M");
+        const int g = e ? atoi(e) : 0;
+        v = (g >= 1 && g <= 64) ? g : 16;
+    }
+    return v;
+}
+
 // Builds the tensor maps and launches one GEMM of configuration C.  Pair mode
 // launches clusters of two CTAs, one pair per two SMs.
 template <class C>
@@ -845,7 +856,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     const int tiles = a.m_tiles * a.n_tiles;
     const int kb = a.k_blocks;
     a.tiles = tiles;
-    if (a.group_m <= 0) a.group_m = 16;
+    if (a.group_m <= 0) a.group_m = raster_group_m();
     int workers = slots;
     const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode == kGroupNone && streamk_enabled() &&
                     (C::kReduce || (a.sk_partial && a.sk_flags));
@@ -950,6 +961,8 @@ inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int nu
     if (forced == kTilePair256 && !(allow_pairs & kAllowPair256)) forced = kTile256;
     if (forced == kTilePair192 && !(allow_pairs & kAllowPair192)) forced = kTile192;
     const int64_t kb = (static_cast<int64_t>(K) * elem_bytes + 127) / 128;  // 128-byte k-blocks
+    const int64_t operand_bytes = (static_cast<int64_t>(M) + N) * K * elem_bytes;
+    constexpr int64_t kL2Budget = 64ll << 20;  // half of the 129 MB L2
     double best = 1e300;
     int choice = kTile128;
     auto consider = [&](int mode, int tile_m, int bn, int cta_per_worker, double shape_eff) {
@@ -967,6 +980,15 @@ inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int nu
         const int64_t per = (tiles * kb + workers - 1) / workers;
         double fix = reduce ? 2.0 : 17.0;
         if (!reduce && per < kb) fix += 10.0 * static_cast<double>((kb + per - 1) / per - 1);
+        // The split phase's workers run at unrelated k offsets, so tiles that
+        // share operand panels no longer read them from L2 at about the same
+        // time: with operands well beyond L2 each split k-block costs ~30% more
+        // (DRAM reads of the 4096 x 16384 block's K = 16384 GEMMs: 2.7 GB with
+        // the split phase, 1.45 GB with whole tiles only)
+        const int64_t full = tiles / workers;
+        const int64_t split_tiles = tiles - (full >= 2 ? (full - 1) * workers : 0);
+        if (operand_bytes > kL2Budget)
+            fix += 0.3 * static_cast<double>(split_tiles * kb) / workers * unit;
         const double sk = static_cast<double>(per) * unit + fix;
         if (sk < best) {
             best = sk;

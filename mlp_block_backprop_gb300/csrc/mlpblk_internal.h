@@ -158,6 +158,11 @@ int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t 
                            cudaStream_t s);
 // Same row kernel, fed the plain gradient dn of the normalised output (the rstd
 // scale is applied inside the kernel).
+// Routed experts, bf16: row t's dn_s is the sum of the rows pos[t*k + j] of
+// dn_rows (slot order; pos < 0 adds nothing).
+int launch_rmsnorm_bwd_gather(const void *x, const float *dn_rows, const int *pos, int k, const void *dy,
+                              const float *rstd, const void *gamma, void *dx, float *dgamma_part, int64_t T,
+                              int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
                                 const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                                 int64_t T, int64_t d, int max_parts, int *parts_out,
@@ -201,22 +206,23 @@ int take_device_error_gemm_f8();
 
 // Host: dispatch / combine of the routed experts (moe.cu).  Rows are the
 // experts' segments of (token, slot) assignments, each padded to 256 rows.
-int launch_moe_route_clear(int *row_token, int64_t rows_max, cudaStream_t s);
-int launch_moe_route_rank(const int *idx, int64_t n, int experts, int *rank, int *count, cudaStream_t s);
-int launch_moe_route_offsets(const int *count, int experts, int *seg, cudaStream_t s);
-int launch_moe_route_place(const int *idx, const int *rank, const int *seg, int64_t n, int k, int experts,
-                           int *pos, int *row_token, int *row_slot, cudaStream_t s);
+constexpr int kMoeRouteChunk = 1024;  // routing entries per CTA
+inline int64_t moe_route_chunks(int64_t n) { return (n + kMoeRouteChunk - 1) / kMoeRouteChunk; }
+// Up to kMoeRouteSingleMax entries, routing is one launch (one CTA); beyond, three:
+// step 0: per-chunk counts, 1: scan and segment offsets, 2: ranks, rows and the
+// row map.  chunk_count and chunk_base hold moe_route_chunks(n) * experts ints.
+constexpr int64_t kMoeRouteSingleMax = 65536;
+int moe_route_launches(int64_t n);
+int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *chunk_base,
+                     int *count, int *seg, int *pos, int *row_token, int *row_slot, int step, cudaStream_t s);
 int launch_moe_gather(const void *x, const float *rstd, const int *row_token, const int *seg, int experts,
                       int64_t rows_max, int64_t d, void *x_perm, float *rstd_perm, cudaStream_t s);
 int launch_moe_combine(const void *x, const void *o_perm, const float *p, const int *pos, int64_t T, int k,
                        int64_t d, void *y, cudaStream_t s);
-int launch_moe_routing_grad(const void *dy, const void *o_perm, const int *pos, int64_t T, int k, int64_t d,
-                            float *dp, cudaStream_t s);
-int launch_moe_gather_dout(const void *dy, const float *p, const int *row_token, const int *row_slot,
-                           const int *seg, int experts, int k, int64_t rows_max, int64_t d, void *do_perm,
-                           cudaStream_t s);
-int launch_moe_scatter_dn(const float *dn_perm, const int *pos, int64_t T, int k, int64_t d, float *dn_s,
-                          cudaStream_t s);
+// d_routing_weights and the slots' output gradients p * dy in segment order
+int launch_moe_dout(const void *dy, const void *o_perm, const float *p, const int *pos, const int *count,
+                    const int *seg, int64_t T, int k, int experts, int64_t d, float *dp, void *do_perm,
+                    cudaStream_t s);
 
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].

@@ -7,7 +7,8 @@
 // token order, each expert's segment padded to a multiple of 256 rows, so the
 // experts' GEMMs run as grouped GEMMs over one row space (gemm_tc.cuh, M- and
 // K-grouped).  Every order is fixed: ranks follow (token, slot) order, the
-// combine and the dn scatter add slots in slot order.
+// combine and the RMSNorm backward's dn gather (rowops.cu) add slots in slot
+// order.
 #include "mlpblk_internal.h"
 
 namespace mlpblk {
@@ -16,6 +17,8 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 constexpr int kSegPad = 256;
+constexpr int kChunk = kMoeRouteChunk;  // routing entries per CTA (8 warps x 128)
+constexpr int kMaxExperts = 256;
 
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -36,73 +39,209 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
 
-// Block e: rank[i] = number of entries idx[i'] == e with i' < i (row-major
-// (token, slot) order) for every i with idx[i] == e; count[e] = their number.
-// Entries outside [0, experts) belong to no expert.
+// Routing runs in three launches over chunks of kChunk (token, slot) entries:
+// route_count (one CTA per chunk: the chunk's entries per expert), route_scan
+// (one CTA: each chunk's first rank per expert, the experts' counts and padded
+// segment offsets) and route_place (one CTA per chunk: every entry's rank in
+// (token, slot) order, its row, and the row -> (token, slot) map).
+
+// chunk_count[b][e] = entries of chunk b with idx == e.  Entries outside
+// [0, experts) belong to no expert.
 __global__ void __launch_bounds__(kRouteThreads)
-route_rank_kernel(const int *__restrict__ idx, int64_t n, int experts, int *__restrict__ rank,
-                  int *__restrict__ count) {
-    __shared__ int warp_sums[kRouteThreads / 32];
+route_count_kernel(const int *__restrict__ idx, int64_t n, int experts, int *__restrict__ chunk_count) {
+    __shared__ int cnt[kMaxExperts];
     griddep_enter();
-    const int e = blockIdx.x;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int running = 0;
-    for (int64_t base = 0; base < n; base += kRouteThreads) {
-        const int64_t i = base + threadIdx.x;
-        const bool hit = i < n && idx[i] == e;
-        const unsigned ballot = __ballot_sync(0xffffffffu, hit);
-        const int before = __popc(ballot & ((1u << lane) - 1u));
-        if (lane == 0) warp_sums[wid] = __popc(ballot);
-        __syncthreads();
-        int prefix = 0, total = 0;
-        for (int w = 0; w < kRouteThreads / 32; ++w) {
-            if (w < wid) prefix += warp_sums[w];
-            total += warp_sums[w];
-        }
-        if (hit) rank[i] = running + prefix + before;
-        running += total;
-        __syncthreads();
+    for (int e = threadIdx.x; e < experts; e += kRouteThreads) cnt[e] = 0;
+    __syncthreads();
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int64_t i1 = min(n, i0 + kChunk);
+    for (int64_t i = i0 + threadIdx.x; i < i1; i += kRouteThreads) {
+        const int e = idx[i];
+        if (e >= 0 && e < experts) atomicAdd(&cnt[e], 1);
     }
-    if (threadIdx.x == 0) count[e] = running;
+    __syncthreads();
+    for (int e = threadIdx.x; e < experts; e += kRouteThreads)
+        chunk_count[static_cast<int64_t>(blockIdx.x) * experts + e] = cnt[e];
 }
 
-// seg[e] = sum over e' < e of count[e'] rounded up to 256; seg[experts] = rows used.
-__global__ void route_offsets_kernel(const int *__restrict__ count, int experts, int *__restrict__ seg) {
+// chunk_base[b][e] = sum over b' < b of chunk_count[b'][e]; count[e] = the
+// expert's entries; seg[e] = sum over e' < e of count[e'] rounded up to 256,
+// seg[experts] = the rows in use.
+__global__ void __launch_bounds__(kRouteThreads)
+route_scan_kernel(const int *__restrict__ chunk_count, int chunks, int experts, int *__restrict__ chunk_base,
+                  int *__restrict__ count, int *__restrict__ seg) {
+    __shared__ int tot[kMaxExperts];
     griddep_enter();
+    for (int e = threadIdx.x; e < experts; e += kRouteThreads) {
+        int run = 0;
+        for (int b = 0; b < chunks; ++b) {
+            const int64_t at = static_cast<int64_t>(b) * experts + e;
+            chunk_base[at] = run;
+            run += chunk_count[at];
+        }
+        tot[e] = run;
+        count[e] = run;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
         int off = 0;
         for (int e = 0; e < experts; ++e) {
             seg[e] = off;
-            off += (count[e] + kSegPad - 1) / kSegPad * kSegPad;
+            off += (tot[e] + kSegPad - 1) / kSegPad * kSegPad;
         }
         seg[experts] = off;
     }
 }
 
-// row_token[r] = -1 (a padding row until an assignment claims it).
-__global__ void route_clear_kernel(int *__restrict__ row_token, int64_t rows) {
+// CTA b places chunk b.  Warp w walks its kChunk/8 entries in groups of 32 in
+// order; lanes with the same expert (match_any) take consecutive ranks, so an
+// entry's rank counts the entries of its expert before it in (token, slot)
+// order.  pos[i] = seg[e] + rank (-1 for an entry that selects nothing),
+// row_token / row_slot of that row; padding rows get row_token = -1.
+__global__ void __launch_bounds__(kRouteThreads)
+route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, const int *__restrict__ chunk_base,
+                   const int *__restrict__ count, const int *__restrict__ seg, int *__restrict__ pos,
+                   int *__restrict__ row_token, int *__restrict__ row_slot) {
+    constexpr int kWarps = kRouteThreads / 32;
+    constexpr int kPerWarp = kChunk / kWarps;
+    __shared__ int wcnt[kWarps][kMaxExperts];
     griddep_enter();
-    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
-         r += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        row_token[r] = -1;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kWarps * experts; i += kRouteThreads) wcnt[i / experts][i % experts] = 0;
+    __syncthreads();
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kChunk + wid * kPerWarp;
+    const unsigned lt = (1u << lane) - 1u;
+    // pass 1: this warp's entries per expert
+    for (int g = 0; g < kPerWarp; g += 32) {
+        const int64_t i = w0 + g + lane;
+        int e = i < n ? idx[i] : -1;
+        if (e < 0 || e >= experts) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // the warp's first rank per expert: the chunk's, plus the warps before it
+    for (int e = threadIdx.x; e < experts; e += kRouteThreads) {
+        int run = chunk_base[static_cast<int64_t>(blockIdx.x) * experts + e];
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = wcnt[w][e];
+            wcnt[w][e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // pass 2: ranks in order
+    for (int g = 0; g < kPerWarp; g += 32) {
+        const int64_t i = w0 + g + lane;
+        int e = i < n ? idx[i] : -1;
+        if (e < 0 || e >= experts) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int base = e >= 0 ? wcnt[wid][e] : 0;
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] = base + __popc(peers);
+        __syncwarp();
+        if (i < n) {
+            if (e < 0) {
+                pos[i] = -1;
+            } else {
+                const int p = seg[e] + base + __popc(peers & lt);
+                pos[i] = p;
+                row_token[p] = static_cast<int>(i / k);
+                row_slot[p] = static_cast<int>(i % k);
+            }
+        }
+    }
+    // padding rows: expert e's rows [seg[e] + count[e], seg[e + 1])
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kRouteThreads + threadIdx.x;
+         q < static_cast<int64_t>(experts) * kSegPad; q += static_cast<int64_t>(gridDim.x) * kRouteThreads) {
+        const int e = static_cast<int>(q / kSegPad);
+        const int r = seg[e] + count[e] + static_cast<int>(q % kSegPad);
+        if (r < seg[e + 1]) {
+            row_token[r] = -1;
+            row_slot[r] = 0;
+        }
+    }
 }
 
-// pos[i] = seg[idx[i]] + rank[i]; row_token / row_slot of that row.
-__global__ void route_place_kernel(const int *__restrict__ idx, const int *__restrict__ rank,
-                                   const int *__restrict__ seg, int64_t n, int k, int experts,
-                                   int *__restrict__ pos, int *__restrict__ row_token, int *__restrict__ row_slot) {
+// All of routing in one CTA of kSingleThreads (up to kSingleMax entries): warp w
+// takes a contiguous range of entries; per-warp counts, a per-expert scan over
+// the warps, the segment offsets, then the ordered ranks as in route_place.
+constexpr int kSingleThreads = 1024;
+constexpr int kSingleWarps = kSingleThreads / 32;
+
+__global__ void __launch_bounds__(kSingleThreads)
+route_single_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, int *__restrict__ count,
+                    int *__restrict__ seg, int *__restrict__ pos, int *__restrict__ row_token,
+                    int *__restrict__ row_slot) {
+    __shared__ int wcnt[kSingleWarps][kMaxExperts];
+    __shared__ int segs[kMaxExperts + 1];
+    __shared__ int tot[kMaxExperts];
     griddep_enter();
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int e = idx[i];
-        if (e < 0 || e >= experts) {
-            pos[i] = -1;
-            continue;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kSingleWarps * experts; i += kSingleThreads) wcnt[i / experts][i % experts] = 0;
+    __syncthreads();
+    const int64_t per = ((n + kSingleWarps - 1) / kSingleWarps + 31) / 32 * 32;
+    const int64_t w0 = wid * per;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t g = 0; g < per; g += 32) {
+        const int64_t i = w0 + g + lane;
+        int e = i < n ? idx[i] : -1;
+        if (e < 0 || e >= experts) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < experts; e += kSingleThreads) {
+        int run = 0;
+        for (int w = 0; w < kSingleWarps; ++w) {
+            const int c = wcnt[w][e];
+            wcnt[w][e] = run;
+            run += c;
         }
-        const int p = seg[e] + rank[i];
-        pos[i] = p;
-        row_token[p] = static_cast<int>(i / k);
-        row_slot[p] = static_cast<int>(i % k);
+        tot[e] = run;
+        count[e] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int off = 0;
+        for (int e = 0; e < experts; ++e) {
+            segs[e] = off;
+            seg[e] = off;
+            off += (tot[e] + kSegPad - 1) / kSegPad * kSegPad;
+        }
+        segs[experts] = off;
+        seg[experts] = off;
+    }
+    __syncthreads();
+    for (int64_t g = 0; g < per; g += 32) {
+        const int64_t i = w0 + g + lane;
+        int e = i < n ? idx[i] : -1;
+        if (e < 0 || e >= experts) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int base = e >= 0 ? wcnt[wid][e] : 0;
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] = base + __popc(peers);
+        __syncwarp();
+        if (i < n) {
+            if (e < 0) {
+                pos[i] = -1;
+            } else {
+                const int p = segs[e] + base + __popc(peers & lt);
+                pos[i] = p;
+                row_token[p] = static_cast<int>(i / k);
+                row_slot[p] = static_cast<int>(i % k);
+            }
+        }
+    }
+    for (int q = threadIdx.x; q < experts * kSegPad; q += kSingleThreads) {
+        const int e = q / kSegPad;
+        const int r = segs[e] + tot[e] + q % kSegPad;
+        if (r < segs[e + 1]) {
+            row_token[r] = -1;
+            row_slot[r] = 0;
+        }
     }
 }
 
@@ -117,6 +256,7 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const float *
     for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
          r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
         const int t = row_token[r];
+#pragma unroll 4
         for (int64_t c = lane * 8; c < d; c += 256) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (t >= 0) v = __ldg(reinterpret_cast<const uint4 *>(x + t * d + c));
@@ -154,77 +294,48 @@ __global__ void combine_kernel(const uint16_t *__restrict__ x, const uint16_t *_
     }
 }
 
-// One warp per (token, slot): dp[t,j] = <dy[t], o_perm[pos[t,j]]> (lane sums, then
-// a fixed shuffle tree).
-__global__ void routing_grad_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ o_perm,
-                                    const int *__restrict__ pos, int64_t n, int k, int64_t d,
-                                    float *__restrict__ dp) {
+// One warp per (token, slot) entry i = t*k + j with row r = pos[i]:
+//   dp[i] = <dy[t], o_perm[r]>  (lane sums, then a fixed shuffle tree),
+//   do_perm[r] = p[i] * dy[t]   (bf16);
+// dp[i] = 0 for an entry that selects nothing.  Warps past the entries zero the
+// padding rows of do_perm (expert e's rows [seg[e] + count[e], seg[e + 1])).
+__global__ void dout_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ o_perm,
+                            const float *__restrict__ p, const int *__restrict__ pos,
+                            const int *__restrict__ count, const int *__restrict__ seg, int64_t n, int k,
+                            int experts, int64_t d, float *__restrict__ dp, uint16_t *__restrict__ do_perm) {
     griddep_enter();
     const int lane = threadIdx.x & 31;
-    for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; i < n;
+    const int64_t items = n + static_cast<int64_t>(experts) * kSegPad;
+    for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; i < items;
          i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        if (i >= n) {
+            const int e = static_cast<int>((i - n) / kSegPad);
+            const int r = seg[e] + count[e] + static_cast<int>((i - n) % kSegPad);
+            if (r < seg[e + 1])
+                for (int64_t c = lane * 8; c < d; c += 256)
+                    *reinterpret_cast<uint4 *>(do_perm + r * d + c) = make_uint4(0, 0, 0, 0);
+            continue;
+        }
         const int r = pos[i];
         const int64_t t = i / k;
         float s = 0.0f;
         if (r >= 0) {
+            const float w = p[i];
+#pragma unroll 2
             for (int64_t c = lane * 8; c < d; c += 256) {
                 float a[8], b[8];
                 unpack8(__ldg(reinterpret_cast<const uint4 *>(dy + t * d + c)), a);
                 unpack8(__ldg(reinterpret_cast<const uint4 *>(o_perm + r * d + c)), b);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) s += a[q] * b[q];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[q] *= w;
+                *reinterpret_cast<uint4 *>(do_perm + r * d + c) = pack8(a);
             }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (lane == 0) dp[i] = s;
-    }
-}
-
-// One warp per row: do_perm[r] = p[t, slot] * dy[t] (bf16), zeros for padding rows.
-__global__ void gather_dout_kernel(const uint16_t *__restrict__ dy, const float *__restrict__ p,
-                                   const int *__restrict__ row_token, const int *__restrict__ row_slot,
-                                   const int *__restrict__ seg, int experts, int k, int64_t d,
-                                   uint16_t *__restrict__ do_perm) {
-    griddep_enter();
-    const int lane = threadIdx.x & 31;
-    const int64_t rows = seg[experts];
-    for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
-         r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-        const int t = row_token[r];
-        const float w = t >= 0 ? p[static_cast<int64_t>(t) * k + row_slot[r]] : 0.0f;
-        for (int64_t c = lane * 8; c < d; c += 256) {
-            float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (t >= 0) {
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(dy + t * d + c)), v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] *= w;
-            }
-            *reinterpret_cast<uint4 *>(do_perm + r * d + c) = pack8(v);
-        }
-    }
-}
-
-// One warp per token: dn_s[t] = sum_j dn_perm[pos[t,j]] (slot order, fp32).
-__global__ void scatter_dn_kernel(const float *__restrict__ dn_perm, const int *__restrict__ pos, int64_t T,
-                                  int k, int64_t d, float *__restrict__ dn_s) {
-    griddep_enter();
-    const int lane = threadIdx.x & 31;
-    for (int64_t t = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; t < T;
-         t += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-        for (int64_t c = lane * 4; c < d; c += 128) {
-            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            for (int j = 0; j < k; ++j) {
-                const int r = pos[t * k + j];
-                if (r < 0) continue;
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(dn_perm + r * d + c));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            *reinterpret_cast<float4 *>(dn_s + t * d + c) = acc;
-        }
     }
 }
 
@@ -245,23 +356,23 @@ unsigned grid_items(int64_t items, int per_block) {
 
 }  // namespace
 
-int launch_moe_route_clear(int *row_token, int64_t rows_max, cudaStream_t s) {
-    return launch_pdl(route_clear_kernel, dim3(grid_items(rows_max, 256)), dim3(256), 0, s, row_token, rows_max);
-}
+int moe_route_launches(int64_t n) { return n <= kMoeRouteSingleMax ? 1 : 3; }
 
-int launch_moe_route_rank(const int *idx, int64_t n, int experts, int *rank, int *count, cudaStream_t s) {
-    return launch_pdl(route_rank_kernel, dim3(static_cast<unsigned>(experts)), dim3(kRouteThreads), 0, s, idx, n,
-                      experts, rank, count);
-}
-
-int launch_moe_route_offsets(const int *count, int experts, int *seg, cudaStream_t s) {
-    return launch_pdl(route_offsets_kernel, dim3(1), dim3(32), 0, s, count, experts, seg);
-}
-
-int launch_moe_route_place(const int *idx, const int *rank, const int *seg, int64_t n, int k, int experts,
-                           int *pos, int *row_token, int *row_slot, cudaStream_t s) {
-    return launch_pdl(route_place_kernel, dim3(grid_items(n, 256)), dim3(256), 0, s, idx, rank, seg, n, k,
-                      experts, pos, row_token, row_slot);
+int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *chunk_base,
+                     int *count, int *seg, int *pos, int *row_token, int *row_slot, int step, cudaStream_t s) {
+    const int chunks = static_cast<int>(moe_route_chunks(n));
+    if (experts > kMaxExperts) return MLPBLK_EINVAL;
+    if (n <= kMoeRouteSingleMax)
+        return launch_pdl(route_single_kernel, dim3(1), dim3(kSingleThreads), 0, s, idx, n, k, experts, count, seg,
+                          pos, row_token, row_slot);
+    if (step == 0)
+        return launch_pdl(route_count_kernel, dim3(static_cast<unsigned>(chunks)), dim3(kRouteThreads), 0, s, idx,
+                          n, experts, chunk_count);
+    if (step == 1)
+        return launch_pdl(route_scan_kernel, dim3(1), dim3(kRouteThreads), 0, s, chunk_count, chunks, experts,
+                          chunk_base, count, seg);
+    return launch_pdl(route_place_kernel, dim3(static_cast<unsigned>(chunks)), dim3(kRouteThreads), 0, s, idx, n,
+                      k, experts, chunk_base, count, seg, pos, row_token, row_slot);
 }
 
 int launch_moe_gather(const void *x, const float *rstd, const int *row_token, const int *seg, int experts,
@@ -278,25 +389,13 @@ int launch_moe_combine(const void *x, const void *o_perm, const float *p, const 
                       static_cast<uint16_t *>(y));
 }
 
-int launch_moe_routing_grad(const void *dy, const void *o_perm, const int *pos, int64_t T, int k, int64_t d,
-                            float *dp, cudaStream_t s) {
-    return launch_pdl(routing_grad_kernel, dim3(grid_items(T * k * 32, 256)), dim3(256), 0, s,
-                      static_cast<const uint16_t *>(dy), static_cast<const uint16_t *>(o_perm), pos, T * k, k, d,
-                      dp);
-}
-
-int launch_moe_gather_dout(const void *dy, const float *p, const int *row_token, const int *row_slot,
-                           const int *seg, int experts, int k, int64_t rows_max, int64_t d, void *do_perm,
-                           cudaStream_t s) {
-    return launch_pdl(gather_dout_kernel, dim3(grid_items(rows_max * 32, 256)), dim3(256), 0, s,
-                      static_cast<const uint16_t *>(dy), p, row_token, row_slot, seg, experts, k, d,
-                      static_cast<uint16_t *>(do_perm));
-}
-
-int launch_moe_scatter_dn(const float *dn_perm, const int *pos, int64_t T, int k, int64_t d, float *dn_s,
-                          cudaStream_t s) {
-    return launch_pdl(scatter_dn_kernel, dim3(grid_items(T * 32, 256)), dim3(256), 0, s, dn_perm, pos, T, k, d,
-                      dn_s);
+int launch_moe_dout(const void *dy, const void *o_perm, const float *p, const int *pos, const int *count,
+                    const int *seg, int64_t T, int k, int experts, int64_t d, float *dp, void *do_perm,
+                    cudaStream_t s) {
+    const int64_t items = T * k + static_cast<int64_t>(experts) * kSegPad;
+    return launch_pdl(dout_kernel, dim3(grid_items(items * 32, 256)), dim3(256), 0, s,
+                      static_cast<const uint16_t *>(dy), static_cast<const uint16_t *>(o_perm), p, pos, count, seg,
+                      T * k, k, experts, d, dp, static_cast<uint16_t *>(do_perm));
 }
 
 }  // namespace mlpblk

@@ -180,6 +180,10 @@ struct Chunk<float> {
         b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
     }
     __device__ void zero() { a = b = make_float4(0.0f, 0.0f, 0.0f, 0.0f); }
+    __device__ void add(const Chunk &o) {
+        a.x += o.a.x; a.y += o.a.y; a.z += o.a.z; a.w += o.a.w;
+        b.x += o.b.x; b.y += o.b.y; b.z += o.b.z; b.w += o.b.w;
+    }
     __device__ float operator[](int i) const {
         const float4 &v = i < 4 ? a : b;
         const int k = i & 3;
@@ -203,12 +207,16 @@ struct Chunk<float> {
 // shuffle butterfly plus, for G > 32, a shared-memory sum over the group's warps
 // in warp order; the CTA's row groups then add their dgamma shares in group
 // order and the CTA writes one partial row.  Every sum has a fixed order.
-template <class T, int CPT, bool kScaleDn>
+//
+// kGather (routed experts): row t's dn_s is the sum over its k slots of the rows
+// pos[t*k + j] of dn_s (slot order, from zero; a slot with pos < 0 adds nothing).
+constexpr int kGatherRegs = 4;
+template <class T, int CPT, bool kScaleDn, bool kGather>
 __global__ void __launch_bounds__(kRowThreads, (CPT <= 3 ? 2 : 1))
 rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, const T *__restrict__ dy,
                    const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
                    float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta,
-                   int G) {
+                   int G, const int *__restrict__ pos, int k) {
     extern __shared__ float sm[];
     griddep_enter();
     const int R = kRowThreads / G;
@@ -230,11 +238,29 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
 
     const int64_t t0 = blockIdx.x * rows_per_cta;
     const int64_t t1 = min(T_rows, t0 + rows_per_cta);
+    // kGather with k <= kGatherRegs: a row's slot rows are read one row ahead,
+    // so the dn loads do not wait on the pos load
+    const bool pre = kGather && k <= kGatherRegs;
+    int rnext[kGatherRegs];
+    if (pre) {
+        const int64_t tn = t0 + grp;
+#pragma unroll
+        for (int sl = 0; sl < kGatherRegs; ++sl) rnext[sl] = (tn < t1 && sl < k) ? pos[tn * k + sl] : -1;
+    }
     int parity = 0;
     for (int64_t base = t0; base < t1; base += R, parity ^= 1) {
         const int64_t t = base + grp;
         const bool valid = t < t1;
         const float r = valid ? rstd[t] : 0.0f;
+        int rcur[kGatherRegs];
+        if (pre) {
+            const int64_t tn = t + R;
+#pragma unroll
+            for (int sl = 0; sl < kGatherRegs; ++sl) {
+                rcur[sl] = rnext[sl];
+                rnext[sl] = (tn < t1 && sl < k) ? pos[tn * k + sl] : -1;
+            }
+        }
         Chunk<T> xch[CPT], ych[CPT];
         Chunk<float> nch[CPT];
 #pragma unroll
@@ -242,7 +268,27 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
             const int q = gl + G * j;
             if (valid && q < chunks) {
                 xch[j].load(x + t * d + 8 * q);
-                nch[j].load(dn_s + t * d + 8 * q);
+                if (kGather && pre) {
+                    nch[j].zero();
+#pragma unroll
+                    for (int sl = 0; sl < kGatherRegs; ++sl) {
+                        if (rcur[sl] < 0) continue;
+                        Chunk<float> v;
+                        v.load(dn_s + static_cast<int64_t>(rcur[sl]) * d + 8 * q);
+                        nch[j].add(v);
+                    }
+                } else if (kGather) {
+                    nch[j].zero();
+                    for (int sl = 0; sl < k; ++sl) {
+                        const int r = pos[t * k + sl];
+                        if (r < 0) continue;
+                        Chunk<float> v;
+                        v.load(dn_s + static_cast<int64_t>(r) * d + 8 * q);
+                        nch[j].add(v);
+                    }
+                } else {
+                    nch[j].load(dn_s + t * d + 8 * q);
+                }
                 ych[j].load(dy + t * d + 8 * q);
             } else {
                 xch[j].zero();
@@ -410,16 +456,16 @@ void norm_shape(int64_t d, int *cpt_out, int *g_out) {
 
 // One CTA per resident slot (at most max_parts), rows split in whole multiples
 // of the rows in flight; the number of CTAs (= dgamma partial rows) is returned.
-template <class E, int CPT, bool kScaleDn>
+template <class E, int CPT, bool kScaleDn, bool kGather>
 int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
                  const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
-                 int *parts_out, int G, cudaStream_t s) {
+                 int *parts_out, int G, const int *pos, int k, cudaStream_t s) {
     const int R = kRowThreads / G;
     const int64_t floats = R > 1 ? (R * d > 2 * R * 8 ? R * d : 2 * R * 8) : 2 * 8;
     const size_t smem = floats * sizeof(float);
     int occ = 0;
     const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, rmsnorm_bwd_kernel<E, CPT, kScaleDn>, kRowThreads, smem));
+        &occ, rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather>, kRowThreads, smem));
     if (rc != MLPBLK_OK) return rc;
     int64_t parts = static_cast<int64_t>(occ > 0 ? occ : 1) * sm_count();
     if (parts > max_parts) parts = max_parts;
@@ -429,20 +475,21 @@ int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rs
     const int64_t rows_per_cta = ((T + parts - 1) / parts + R - 1) / R * R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_kernel<E, CPT, kScaleDn>, dim3(static_cast<unsigned>(parts)),
+    return launch_pdl(rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather>, dim3(static_cast<unsigned>(parts)),
                       dim3(kRowThreads), smem, s, static_cast<const E *>(x), dn,
                       static_cast<const E *>(dy), rstd, static_cast<const E *>(gamma),
-                      static_cast<E *>(dx), part, T, d, rows_per_cta, G);
+                      static_cast<E *>(dx), part, T, d, rows_per_cta, G, pos, k);
 }
 
-template <class E, bool kScaleDn>
+template <class E, bool kScaleDn, bool kGather = false>
 int dispatch_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
                       const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
-                      int *parts_out, cudaStream_t s) {
+                      int *parts_out, cudaStream_t s, const int *pos = nullptr, int k = 0) {
     int cpt = 0, G = 0;
     norm_shape(d, &cpt, &G);
 #define MLPBLK_NB(C) \
-    return run_norm_bwd<E, C, kScaleDn>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, s)
+    return run_norm_bwd<E, C, kScaleDn, kGather>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, \
+                                                 pos, k, s)
     switch (cpt) {
         case 1: MLPBLK_NB(1);
         case 2: MLPBLK_NB(2);
@@ -512,6 +559,13 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
                                                  max_parts, parts_out, s);
     return dispatch_norm_bwd<float, true>(x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
                                           parts_out, s);
+}
+
+int launch_rmsnorm_bwd_gather(const void *x, const float *dn_rows, const int *pos, int k, const void *dy,
+                              const float *rstd, const void *gamma, void *dx, float *dgamma_part, int64_t T,
+                              int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
+    return dispatch_norm_bwd<uint16_t, false, true>(x, dn_rows, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
+                                                    parts_out, s, pos, k);
 }
 
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {

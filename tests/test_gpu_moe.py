@@ -75,6 +75,7 @@ def _check(got, ref, skip_dp=None):
     (64, 64, 128, 8, 1),       # top-1, some experts get no token
     (1, 256, 512, 2, 2),       # a single token in two experts
     (520, 520, 520, 5, 3),     # top-3
+    (33000, 64, 128, 4, 2),    # over 65536 (token, slot) entries: routing in three launches
 ])
 def test_moe_against_the_oracle(shape):
     T, d, F, E, k = shape
@@ -119,3 +120,37 @@ def test_moe_one_expert_is_the_dense_block():
     assert oracle.scaled_error(got["dx"], outs[0]["dx"]) <= 1e-2
     assert oracle.scaled_error(got["dw1s"][0], grads["dw1"]) <= 1e-2
     assert oracle.scaled_error(got["dw2s"][0], grads["dw2"]) <= 1e-2
+
+
+@pytest.mark.slow
+def test_moe_full_size_sampled():
+    """The 8-expert top-2 workload at its full size (8192 tokens, d 2048, ffn 1024
+    per expert), in the calls bench.py times, on sampled outputs the oracle
+    computes alone: y, dx and d_routing_weights of 48 tokens (a token's outputs
+    depend on its own row only), and whole rows of every expert's dW1 and whole
+    columns of dW2 at 12 ffn indices (the ReLU^2 expert is separable over ffn, so
+    the oracle over all tokens with W1 cut to those rows and W2 to those columns
+    gives exactly those gradients).  dgamma needs every token's full dn and is
+    left to the smaller cases."""
+    inp = synth.moe_config_inputs("moe_e8k2")
+    got, _ = _run(inp)
+    rng = np.random.default_rng(2024)
+    toks = np.sort(rng.choice(inp.tokens, size=48, replace=False))
+    fs = np.sort(rng.choice(inp.ffn, size=12, replace=False))
+    p = inp.p.astype(np.float64)
+
+    y, h, o, r = moe_oracle.forward(inp.x[toks], inp.gamma, inp.w1s, inp.w2s, inp.idx[toks], p[toks], inp.eps)
+    g = moe_oracle.new_grads(inp.experts, inp.d, inp.ffn)
+    dx, dp = moe_oracle.backward(inp.dy[toks], inp.x[toks], inp.gamma, inp.w1s, inp.w2s, inp.idx[toks], p[toks],
+                                 h, o, r, g)
+    errs = {"y": oracle.scaled_error(got["y"][toks], y), "dx": oracle.scaled_error(got["dx"][toks], dx),
+            "dp": oracle.scaled_error(got["dp"][toks], dp)}
+
+    w1c, w2c = inp.w1s[:, fs, :], inp.w2s[:, :, fs]
+    y2, h2, o2, r2 = moe_oracle.forward(inp.x, inp.gamma, w1c, w2c, inp.idx, p, inp.eps)
+    g2 = moe_oracle.new_grads(inp.experts, inp.d, len(fs))
+    moe_oracle.backward(inp.dy, inp.x, inp.gamma, w1c, w2c, inp.idx, p, h2, o2, r2, g2)
+    errs["dw1"] = oracle.scaled_error(got["dw1s"][:, fs, :], g2["dw1"])
+    errs["dw2"] = oracle.scaled_error(got["dw2s"][:, :, fs], g2["dw2"])
+    bad = {k: v for k, v in errs.items() if not (v <= TOL)}
+    assert not bad, f"scaled error above {TOL}: {bad} (all: {errs})"
