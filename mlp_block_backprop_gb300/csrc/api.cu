@@ -950,7 +950,8 @@ int mlpblk_last_error(void) {
     const int a = take_device_error_gemm_fwd();
     const int b = take_device_error_gemm_bwd();
     const int c = take_device_error_gemm_f8();
-    return a != MLPBLK_OK ? a : (b != MLPBLK_OK ? b : c);
+    const int r = take_device_error_rowops();
+    return a != MLPBLK_OK ? a : (b != MLPBLK_OK ? b : (c != MLPBLK_OK ? c : r));
 }
 
 }  // extern "C"

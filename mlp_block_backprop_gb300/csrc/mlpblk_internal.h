@@ -154,6 +154,7 @@ bool rms_in_gemm();
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
+int take_device_error_rowops();
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
                            cudaStream_t s);
 // Same row kernel, fed the plain gradient dn of the normalised output (the rstd

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 
 #include "mlpblk_internal.h"
+#include "ptx.cuh"
 
 namespace mlpblk {
 
@@ -352,21 +353,226 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
     }
 }
 
-// dgamma[k] += sum of the partial rows.  A CTA covers 128 columns with 32
-// slices: slice s adds partial rows s, s+32, ... in increasing order (4 columns
-// per thread), then slice 0 adds the 32 slice sums in slice order.
+// Staged RMSNorm backward (bf16, d a multiple of 256 and at most 4096; dn_s
+// already scaled by rstd), used for the routed experts' gathered dn: a token's k
+// slot rows sit at scattered rows of dn_s, which the register-resident kernel
+// reads as loads that wait on the row map.  The same arithmetic as
+// rmsnorm_bwd_kernel, but the rows reach shared memory by bulk copies issued up
+// to kStagedMaxStages iterations ahead (warp 0 issues them, the slot rows' indices
+// loaded one issue ahead; an mbarrier per stage counts the bytes).  For a plain dn
+// it measured no faster than the register-resident kernel, which stays in use.
+// A CTA of kStagedThreads takes R = 4096 / d rows per iteration, d/8 threads per
+// row, 8 columns per thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16,
+// dn [R][K'][d] fp32 (K' = k slot rows with kGather, else 1).  The row sum is a
+// shuffle tree per warp then the row's warps in order; the dgamma partial of the
+// CTA is each thread's running sum, then the R row groups in order.
+constexpr int kStagedThreads = 512;
+constexpr int kStagedMaxStages = 4;
+
+template <bool kGather>
+__global__ void __launch_bounds__(kStagedThreads, 1)
+rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dn_s,
+                          const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
+                          const uint16_t *__restrict__ gamma, uint16_t *__restrict__ dx,
+                          float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta, int R,
+                          int S, int stage_bytes, const int *__restrict__ pos, int k) {
+    extern __shared__ __align__(128) uint8_t smem_st[];
+    const int kk = kGather ? k : 1;
+    uint8_t *stages = smem_st;
+    float *red = reinterpret_cast<float *>(smem_st + static_cast<size_t>(S) * stage_bytes);  // [2][R][16]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * R * 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kStagedMaxStages);
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int cpr = static_cast<int>(d / 8);  // threads per row (a multiple of 32)
+    const int grp = tid / cpr;
+    const int gl = tid - grp * cpr;
+    const int wpr = cpr / 32;                 // warps per row
+    const bool active = grp < R;
+    const float inv_d = 1.0f / static_cast<float>(d);
+    const int64_t t0 = blockIdx.x * rows_per_cta;
+    const int64_t t1 = min(T_rows, t0 + rows_per_cta);
+    const int iters = static_cast<int>((t1 - t0 + R - 1) / R);
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    float g[8], acc[8];
+    if (active) Io8<uint16_t>::load(gamma + 8 * gl, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    __syncthreads();
+    griddep_enter();
+
+    // Warp 0 issues the copies of iteration it into stage it % S: lane 0 the x
+    // and dy rows (and, without kGather, the dn_s rows); with kGather lane j < R*k
+    // the slot row (row j / k, slot j % k) whose index it loaded one issue ahead.
+    int pnext[2] = {-1, -1};
+    auto load_pos = [&](int it) {
+        if (!kGather) return;
+        const int64_t tb = t0 + static_cast<int64_t>(it) * R;
+        for (int q = 0; q < 2; ++q) {
+            const int j = lane + 32 * q;
+            const int r = j / kk;
+            pnext[q] = (it < iters && r < R && tb + r < t1) ? pos[(tb + r) * kk + j % kk] : -1;
+        }
+    };
+    auto issue = [&](int it) {
+        const int st = it % S;
+        uint8_t *sx = stages + static_cast<size_t>(st) * stage_bytes;
+        uint8_t *sy = sx + static_cast<size_t>(R) * d * 2;
+        uint8_t *sn = sy + static_cast<size_t>(R) * d * 2;
+        const int64_t tb = t0 + static_cast<int64_t>(it) * R;
+        const int nr = static_cast<int>(min(static_cast<int64_t>(R), t1 - tb));
+        uint32_t mine = 0;  // this lane's slot-row bytes
+        if (kGather)
+            for (int q = 0; q < 2; ++q)
+                if (pnext[q] >= 0) mine += static_cast<uint32_t>(d) * 4u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        if (lane == 0) {
+            uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u;  // x and dy
+            bytes += kGather ? mine : static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u;
+            mbar_arrive_expect_tx(&full[st], bytes);
+            bulk_copy_g2s(sx, x + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
+            bulk_copy_g2s(sy, dy + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
+            if (!kGather) bulk_copy_g2s(sn, dn_s + tb * d, static_cast<uint32_t>(nr * d * 4), &full[st]);
+        }
+        if (kGather)
+            for (int q = 0; q < 2; ++q)
+                if (pnext[q] >= 0)
+                    bulk_copy_g2s(sn + static_cast<size_t>(lane + 32 * q) * d * 4,
+                                  dn_s + static_cast<int64_t>(pnext[q]) * d, static_cast<uint32_t>(d * 4), &full[st]);
+        __syncwarp();
+    };
+    int issued = 0;
+    if (tid < 32) {
+        for (; issued < S && issued < iters; ++issued) {
+            load_pos(issued);
+            issue(issued);
+        }
+        load_pos(issued);
+    }
+
+    // each thread's rstd (and, kGather, its row's slot indices) two iterations ahead
+    auto row_of = [&](int it) { return t0 + static_cast<int64_t>(it) * R + grp; };
+    float r_n1 = 0.0f, r_n2 = 0.0f;
+    int p_n1[4] = {-1, -1, -1, -1}, p_n2[4] = {-1, -1, -1, -1};
+    auto fetch = [&](int it, float &rv, int (&pv)[4]) {
+        const int64_t t = row_of(it);
+        const bool v = active && it < iters && t < t1;
+        rv = v ? rstd[t] : 0.0f;
+        if (kGather)
+            for (int j = 0; j < 4; ++j) pv[j] = (v && j < kk) ? pos[t * kk + j] : -1;
+    };
+    fetch(0, r_n1, p_n1);
+    fetch(1, r_n2, p_n2);
+
+    int it = 0;
+    for (; it < iters; ++it) {
+        const int st = it % S;
+        const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+        const int64_t t = row_of(it);
+        const bool valid = active && t < t1;
+        const float r = r_n1;
+        int pv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pv[j] = p_n1[j];
+        r_n1 = r_n2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p_n1[j] = p_n2[j];
+        fetch(it + 2, r_n2, p_n2);
+        const bool ok = mbar_wait(&full[st], ph, abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        const uint8_t *sx = stages + static_cast<size_t>(st) * stage_bytes;
+        const uint8_t *sy = sx + static_cast<size_t>(R) * d * 2;
+        const uint8_t *sn = sy + static_cast<size_t>(R) * d * 2;
+        float xv[8], yv[8], nv[8];
+        float part = 0.0f;
+        if (valid) {
+            const uint4 ux = *reinterpret_cast<const uint4 *>(sx + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
+            const uint4 uy = *reinterpret_cast<const uint4 *>(sy + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
+            xv[0] = bf(ux.x & 0xFFFFu); xv[1] = bf(ux.x >> 16); xv[2] = bf(ux.y & 0xFFFFu); xv[3] = bf(ux.y >> 16);
+            xv[4] = bf(ux.z & 0xFFFFu); xv[5] = bf(ux.z >> 16); xv[6] = bf(ux.w & 0xFFFFu); xv[7] = bf(ux.w >> 16);
+            yv[0] = bf(uy.x & 0xFFFFu); yv[1] = bf(uy.x >> 16); yv[2] = bf(uy.y & 0xFFFFu); yv[3] = bf(uy.y >> 16);
+            yv[4] = bf(uy.z & 0xFFFFu); yv[5] = bf(uy.z >> 16); yv[6] = bf(uy.w & 0xFFFFu); yv[7] = bf(uy.w >> 16);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) nv[i] = 0.0f;
+            for (int j = 0; j < kk; ++j) {
+                if (kGather && pv[j] < 0) continue;
+                const float *q = reinterpret_cast<const float *>(sn) + (static_cast<size_t>(grp) * kk + j) * d + 8 * gl;
+                const float4 a0 = *reinterpret_cast<const float4 *>(q);
+                const float4 a1 = *reinterpret_cast<const float4 *>(q + 4);
+                nv[0] += a0.x; nv[1] += a0.y; nv[2] += a0.z; nv[3] += a0.w;
+                nv[4] += a1.x; nv[5] += a1.y; nv[6] += a1.z; nv[7] += a1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part += g[i] * nv[i] * xv[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        float *rr = red + (it & 1) * R * 16;
+        if (active && lane == 0) rr[grp * 16 + gl / 32] = part;
+        // every thread has read stage st and written its warp sum
+        __syncthreads();
+        if (tid < 32 && issued < iters) {
+            issue(issued++);
+            load_pos(issued);
+        }
+        if (valid) {
+            float sum = 0.0f;
+            for (int w = 0; w < wpr; ++w) sum += rr[grp * 16 + w];
+            const float cr = r * r * sum * inv_d;
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i] = yv[i] + g[i] * nv[i] - xv[i] * cr;
+                acc[i] += nv[i] * xv[i];
+            }
+            const uint4 u = make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
+            *reinterpret_cast<uint4 *>(dx + t * d + 8 * gl) = u;
+        }
+    }
+    if (it < iters) {
+        // gave up: let the copies already issued land before the CTA exits
+        if (tid == 0)
+            for (int j = it; j < issued; ++j) mbar_drain(&full[j % S], static_cast<uint32_t>(j / S) & 1u);
+        __syncthreads();
+        return;
+    }
+    // the CTA's dgamma partial row: the R row groups' sums in group order
+    __syncthreads();
+    float *gsum = reinterpret_cast<float *>(stages);  // [R][d], the stages are free now
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gsum[static_cast<size_t>(grp) * d + 8 * gl + i] = acc[i];
+    }
+    __syncthreads();
+    float *out = dg_part + blockIdx.x * d;
+    for (int64_t i = tid; i < d; i += kStagedThreads) {
+        float v = 0.0f;
+        for (int g2 = 0; g2 < R; ++g2) v += gsum[static_cast<size_t>(g2) * d + i];
+        out[i] = v;
+    }
+}
+
+// dgamma[k] += sum of the partial rows.  A CTA covers 32 columns with 128
+// slices: slice s adds partial rows s, s+128, ... in increasing order (4 columns
+// per thread), then the 128 slice sums meet in a fixed pairwise tree.
 __global__ void __launch_bounds__(1024)
 dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restrict__ dgamma,
                        int64_t d) {
-    __shared__ float4 red[32][33];
+    __shared__ float4 red[128][9];
     griddep_enter();
-    const int lane = threadIdx.x & 31;
-    const int slice = threadIdx.x >> 5;
-    const int64_t col = blockIdx.x * 128 + lane * 4;
+    const int lane = threadIdx.x & 7;
+    const int slice = threadIdx.x >> 3;
+    const int64_t col = blockIdx.x * 32 + lane * 4;
     float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (col < d) {
 #pragma unroll 4
-        for (int p = slice; p < parts; p += 32) {
+        for (int p = slice; p < parts; p += 128) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(part + p * d + col));
             s.x += v.x;
             s.y += v.y;
@@ -376,15 +582,20 @@ dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restr
     }
     red[slice][lane] = s;
     __syncthreads();
-    if (slice == 0 && col < d) {
-        float4 t = red[0][lane];
-        for (int i = 1; i < 32; ++i) {
-            const float4 v = red[i][lane];
+    for (int w = 64; w >= 1; w >>= 1) {
+        if (slice < w) {
+            const float4 v = red[slice + w][lane];
+            float4 t = red[slice][lane];
             t.x += v.x;
             t.y += v.y;
             t.z += v.z;
             t.w += v.w;
+            red[slice][lane] = t;
         }
+        __syncthreads();
+    }
+    if (slice == 0 && col < d) {
+        const float4 t = red[0][lane];
         float4 *g = reinterpret_cast<float4 *>(dgamma + col);
         float4 o = *g;
         o.x += t.x;
@@ -430,8 +641,6 @@ int grid_for(int64_t work_items, int threads) {
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
     return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
 }
-
-int status() { return launch_status(); }
 
 // Row-group shape of the norm backward for width d: chunks per thread (1..4)
 // and group size G (power of two, 8..256) with the fewest masked chunk slots.
@@ -541,6 +750,62 @@ int launch_rstd_f32(const float *x, float *rstd, int64_t T, int64_t d, float eps
     return launch_pdl(rstd_f32_kernel, dim3(grid_for(T * 32, 256)), dim3(256), 0, s, x, rstd, T, d, eps);
 }
 
+namespace {
+
+// Shape of the staged kernel for width d and k slot rows (0 when it does not
+// apply): rows per iteration R, stages S, bytes per stage.
+struct StagedShape {
+    int R, S, stage_bytes;
+    size_t smem;
+};
+
+StagedShape staged_shape(int64_t d, int k) {
+    StagedShape sh = {0, 0, 0, 0};
+    if (d % 256 != 0 || d > 4096 || k < 1 || k > 4) return sh;
+    const int R = static_cast<int>(4096 / d);
+    if (k > 1 && R * k > 64) return sh;  // warp 0 issues at most 64 slot rows
+    const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * 4 + 127) / 128 * 128;
+    const int64_t extra = 2 * R * 16 * 4 + kStagedMaxStages * 8 + 16;
+    const int64_t budget = 200 * 1024;
+    int S = static_cast<int>((budget - extra) / bytes);
+    if (S > kStagedMaxStages) S = kStagedMaxStages;
+    if (S < 2) return sh;
+    sh.R = R;
+    sh.S = S;
+    sh.stage_bytes = static_cast<int>(bytes);
+    sh.smem = static_cast<size_t>(S) * bytes + extra;
+    return sh;
+}
+
+template <bool kGather>
+int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, const void *dy, const float *rstd,
+                        const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
+                        int *parts_out, const int *pos, int k, cudaStream_t s) {
+    static bool attr[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
+    if (!attr[dev]) {
+        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 4096));
+        if (rc != MLPBLK_OK) return rc;
+        attr[dev] = true;
+    }
+    int64_t parts = sm_count();
+    if (parts > max_parts) parts = max_parts;
+    const int64_t groups = (T + sh.R - 1) / sh.R;
+    if (parts > groups) parts = groups;
+    if (parts < 1) parts = 1;
+    const int64_t rows_per_cta = ((T + parts - 1) / parts + sh.R - 1) / sh.R * sh.R;
+    parts = (T + rows_per_cta - 1) / rows_per_cta;
+    *parts_out = static_cast<int>(parts);
+    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather>, dim3(static_cast<unsigned>(parts)), dim3(kStagedThreads),
+                      sh.smem, s, static_cast<const uint16_t *>(x), dn, static_cast<const uint16_t *>(dy), rstd,
+                      static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(dx), part, T, d, rows_per_cta,
+                      sh.R, sh.S, sh.stage_bytes, pos, k);
+}
+
+}  // namespace
+
 int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
@@ -564,12 +829,25 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
 int launch_rmsnorm_bwd_gather(const void *x, const float *dn_rows, const int *pos, int k, const void *dy,
                               const float *rstd, const void *gamma, void *dx, float *dgamma_part, int64_t T,
                               int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
+    if (T > 0) {
+        const StagedShape sh = staged_shape(d, k);
+        if (sh.R > 0)
+            return run_norm_bwd_staged<true>(sh, x, dn_rows, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
+                                             parts_out, pos, k, s);
+    }
     return dispatch_norm_bwd<uint16_t, false, true>(x, dn_rows, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
                                                     parts_out, s, pos, k);
 }
 
+int take_device_error_rowops() {
+    int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MLPBLK_ECUDA;
+    if (v != 0) cudaMemcpyToSymbol(g_device_error, &z, sizeof(int));
+    return v;
+}
+
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {
-    return launch_pdl(dgamma_finalize_kernel, dim3(static_cast<unsigned>((d + 127) / 128)), dim3(1024), 0,
+    return launch_pdl(dgamma_finalize_kernel, dim3(static_cast<unsigned>((d + 31) / 32)), dim3(1024), 0,
                       s, part, parts, dgamma, d);
 }
 
