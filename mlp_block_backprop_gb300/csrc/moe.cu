@@ -168,6 +168,7 @@ route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, c
 // takes a contiguous range of entries; per-warp counts, a per-expert scan over
 // the warps, the segment offsets, then the ordered ranks as in route_place.
 constexpr int kSingleThreads = 1024;
+constexpr int kIdBatch = 8;
 constexpr int kSingleWarps = kSingleThreads / 32;
 
 __global__ void __launch_bounds__(kSingleThreads)
@@ -184,13 +185,22 @@ route_single_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, 
     const int64_t per = ((n + kSingleWarps - 1) / kSingleWarps + 31) / 32 * 32;
     const int64_t w0 = wid * per;
     const unsigned lt = (1u << lane) - 1u;
-    for (int64_t g = 0; g < per; g += 32) {
-        const int64_t i = w0 + g + lane;
-        int e = i < n ? idx[i] : -1;
-        if (e < 0 || e >= experts) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] += __popc(peers);
-        __syncwarp();
+    // a warp's ids come in batches of kIdBatch groups of 32, all loads of a batch
+    // in flight together
+    auto load_ids = [&](int64_t g0, int (&ev)[kIdBatch]) {
+#pragma unroll
+        for (int b = 0; b < kIdBatch; ++b) {
+            const int64_t i = w0 + g0 + 32 * b + lane;
+            const int e = (g0 + 32 * b < per && i < n) ? idx[i] : -1;
+            ev[b] = (e < 0 || e >= experts) ? -1 : e;
+        }
+    };
+    for (int64_t g0 = 0; g0 < per; g0 += 32 * kIdBatch) {
+        int ev[kIdBatch];
+        load_ids(g0, ev);
+#pragma unroll
+        for (int b = 0; b < kIdBatch; ++b)
+            if (ev[b] >= 0) atomicAdd(&wcnt[wid][ev[b]], 1);  // counts need no order
     }
     __syncthreads();
     for (int e = threadIdx.x; e < experts; e += kSingleThreads) {
@@ -215,23 +225,29 @@ route_single_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, 
         seg[experts] = off;
     }
     __syncthreads();
-    for (int64_t g = 0; g < per; g += 32) {
-        const int64_t i = w0 + g + lane;
-        int e = i < n ? idx[i] : -1;
-        if (e < 0 || e >= experts) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int base = e >= 0 ? wcnt[wid][e] : 0;
-        __syncwarp();
-        if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] = base + __popc(peers);
-        __syncwarp();
-        if (i < n) {
-            if (e < 0) {
-                pos[i] = -1;
-            } else {
-                const int p = segs[e] + base + __popc(peers & lt);
-                pos[i] = p;
-                row_token[p] = static_cast<int>(i / k);
-                row_slot[p] = static_cast<int>(i % k);
+    for (int64_t g0 = 0; g0 < per; g0 += 32 * kIdBatch) {
+        int ev[kIdBatch];
+        load_ids(g0, ev);
+#pragma unroll
+        for (int b = 0; b < kIdBatch; ++b) {
+            if (g0 + 32 * b >= per) break;
+            const int64_t i = w0 + g0 + 32 * b + lane;
+            const int e = ev[b];
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int base = e >= 0 ? wcnt[wid][e] : 0;
+            __syncwarp();
+            if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] = base + __popc(peers);
+            __syncwarp();
+            if (i < n) {
+                if (e < 0) {
+                    pos[i] = -1;
+                } else {
+                    const int p = segs[e] + base + __popc(peers & lt);
+                    const int ii = static_cast<int>(i);  // below kSingleMax: 32-bit division
+                    pos[i] = p;
+                    row_token[p] = ii / k;
+                    row_slot[p] = ii - (ii / k) * k;
+                }
             }
         }
     }

@@ -213,7 +213,7 @@ struct Chunk<float> {
 // pos[t*k + j] of dn_s (slot order, from zero; a slot with pos < 0 adds nothing).
 constexpr int kGatherRegs = 4;
 template <class T, int CPT, bool kScaleDn, bool kGather>
-__global__ void __launch_bounds__(kRowThreads, (CPT <= 3 ? 2 : 1))
+__global__ void __launch_bounds__(kRowThreads, (CPT <= 2 ? 3 : (CPT <= 3 ? 2 : 1)))
 rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, const T *__restrict__ dy,
                    const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
                    float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta,

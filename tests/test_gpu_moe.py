@@ -76,6 +76,11 @@ def _check(got, ref, skip_dp=None):
     (1, 256, 512, 2, 2),       # a single token in two experts
     (520, 520, 520, 5, 3),     # top-3
     (33000, 64, 128, 4, 2),    # over 65536 (token, slot) entries: routing in three launches
+    # d a multiple of 256: the RMSNorm backward gathers the slot rows by bulk copies
+    (300, 256, 256, 4, 3),
+    (257, 512, 256, 6, 4),
+    (1000, 768, 256, 3, 1),
+    (130, 2048, 256, 4, 2),
 ])
 def test_moe_against_the_oracle(shape):
     T, d, F, E, k = shape
@@ -96,6 +101,25 @@ def test_moe_expert_without_tokens_and_invalid_ids():
     _check(got, _reference(inp, valid), skip_dp=valid)
     assert got["dp"][5, 1] == 0.0 and got["dp"][17, 0] == 0.0
     assert not np.any(got["dw1s"][2]) and not np.any(got["dw2s"][2])
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_moe_invalid_ids_every_norm_path(d):
+    """Slots that select nothing (ids -1 and E) at both RMSNorm-backward paths
+    (register rows for d = 64, bulk-copied slot rows for d = 256)."""
+    inp = synth.make_moe_inputs(160, d, 256, 4, 3, seed=40 + d, eps=1e-6)
+    valid = np.ones_like(inp.idx, dtype=bool)
+    for t, j, e in ((3, 0, -1), (3, 2, 4), (50, 1, -7), (159, 2, 4)):
+        inp.idx[t, j] = e
+        valid[t, j] = False
+    inp.idx[7, :] = -1                                               # a token with no expert at all
+    valid[7, :] = False
+    got, _ = _run(inp)
+    _check(got, _reference(inp, valid), skip_dp=valid)
+    assert np.all(got["dp"][~valid] == 0.0)
+    # a token without experts: y = x and dx = dy exactly (bf16 round trip)
+    np.testing.assert_array_equal(got["y"][7], inp.x[7].astype(np.float64))
+    np.testing.assert_array_equal(got["dx"][7], inp.dy[7].astype(np.float64))
 
 
 def test_moe_outputs_are_deterministic():
