@@ -46,6 +46,8 @@ def test_small_bf16_accum4_config():
     (40, 8, 8),         # the narrowest widths (one 16-byte row)
     (77, 136, 1032),    # ffn spans five 256-wide tiles with a ragged tail
     (520, 520, 520),
+    (300, 4096, 520),   # the widest d_model the library takes
+    (97, 4088, 264),    # the widest ragged d_model (4096 - 8)
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_shapes(shape, dtype):
