@@ -242,6 +242,44 @@ int mlpblk_backward_fp8(const mlpblk_desc *desc,
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The same FP8 calls with the weights quantised once, e.g. once per optimizer
+ * step for every microbatch of a gradient-accumulation window (the weights do not
+ * change between the microbatches, so neither do their codes).
+ *
+ * mlpblk_fp8_weights_size: bytes of a pre-quantised weight buffer `wq`
+ *   (caller-owned, 16-byte aligned): E4M3 codes of W1*gamma [F,d], W2 [d,F] and
+ *   W1 [F,d], then their three scale records; 0 for an invalid descriptor.
+ * mlpblk_fp8_quantize_weights: fills `wq` from gamma, w1, w2 (bf16) with the same
+ *   per-tensor scaling as mlpblk_forward_fp8 / mlpblk_backward_fp8 (uses the FP8
+ *   workspace for its amax scratch).  Call it again whenever gamma, W1 or W2
+ *   change.
+ * mlpblk_forward_fp8_prequant / mlpblk_backward_fp8_prequant: as
+ *   mlpblk_forward_fp8 / mlpblk_backward_fp8, reading the weights' codes and
+ *   scales from `wq`; outputs are bitwise those of the quantising calls (dW1 and
+ *   dW2 up to the order of the reduce-adds of a split weight-gradient tile).
+ * Returns an MLPBLK_* code.
+ */
+size_t mlpblk_fp8_weights_size(const mlpblk_desc *desc);
+
+int mlpblk_fp8_quantize_weights(const mlpblk_desc *desc,
+                                const void *gamma, const void *w1, const void *w2,
+                                void *wq, size_t wq_bytes,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_forward_fp8_prequant(const mlpblk_desc *desc,
+                                const void *x, const void *wq,
+                                void *y, void *h_saved, void *a8_saved, void *n8_saved,
+                                float *rstd_saved, float *scales_saved,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+int mlpblk_backward_fp8_prequant(const mlpblk_desc *desc,
+                                 const void *dy, const void *x, const void *gamma, const void *wq,
+                                 const void *h_saved, const void *a8_saved, const void *n8_saved,
+                                 const float *rstd_saved, const float *scales_saved,
+                                 void *dx, float *dgamma, float *dw1, float *dw2,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Routed ReLU^2 experts ("Nemotron Kernels From Inference To Backpropagation" --
  * "Kernel 4: Routed ReLU2 MoE Inference And Backpropagation"): the pre-norm
  * shell around a mixture of ReLU^2 experts with a given top-k dispatch,

@@ -33,6 +33,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_workspace_size_recompute", "mlpblk_forward_recompute", "mlpblk_backward_recompute",
             "mlpblk_grad_norm", "mlpblk_clip_grads", "mlpblk_adamw_step", "mlpblk_set_rmsnorm_mode",
             "mlpblk_workspace_size_fp8", "mlpblk_forward_fp8", "mlpblk_backward_fp8",
+            "mlpblk_fp8_weights_size", "mlpblk_fp8_quantize_weights", "mlpblk_forward_fp8_prequant",
+            "mlpblk_backward_fp8_prequant",
             "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
@@ -110,6 +112,14 @@ def _load():
     lib.mlpblk_forward_fp8.restype = i32
     lib.mlpblk_backward_fp8.argtypes = [pd] + [vp] * 14 + [sz, vp]
     lib.mlpblk_backward_fp8.restype = i32
+    lib.mlpblk_fp8_weights_size.argtypes = [pd]
+    lib.mlpblk_fp8_weights_size.restype = sz
+    lib.mlpblk_fp8_quantize_weights.argtypes = [pd, vp, vp, vp, vp, sz, vp, sz, vp]
+    lib.mlpblk_fp8_quantize_weights.restype = i32
+    lib.mlpblk_forward_fp8_prequant.argtypes = [pd] + [vp] * 9 + [sz, vp]
+    lib.mlpblk_forward_fp8_prequant.restype = i32
+    lib.mlpblk_backward_fp8_prequant.argtypes = [pd] + [vp] * 13 + [sz, vp]
+    lib.mlpblk_backward_fp8_prequant.restype = i32
     pm = ctypes.POINTER(MoeDesc)
     lib.mlpblk_moe_saved_size.argtypes = [pm]
     lib.mlpblk_moe_saved_size.restype = sz
@@ -266,6 +276,36 @@ def mlpblk_backward_fp8(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved,
                                  _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
                                  _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "mlpblk_backward_fp8")
+
+
+def mlpblk_fp8_weights_size(desc: Desc) -> int:
+    return int(lib.mlpblk_fp8_weights_size(ctypes.byref(desc)))
+
+
+def mlpblk_fp8_quantize_weights(desc, gamma, w1, w2, wq, workspace, stream=None):
+    rc = lib.mlpblk_fp8_quantize_weights(ctypes.byref(desc), _ptr(gamma), _ptr(w1), _ptr(w2), _ptr(wq),
+                                         wq.numel() * wq.element_size(), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mlpblk_fp8_quantize_weights")
+
+
+def mlpblk_forward_fp8_prequant(desc, x, wq, y, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
+                                workspace, stream=None):
+    rc = lib.mlpblk_forward_fp8_prequant(ctypes.byref(desc), _ptr(x), _ptr(wq), _ptr(y), _ptr(h_saved),
+                                         _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved), _ptr(scales_saved),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream))
+    _check(rc, "mlpblk_forward_fp8_prequant")
+
+
+def mlpblk_backward_fp8_prequant(desc, dy, x, gamma, wq, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
+                                 dx, dgamma, dw1, dw2, workspace, stream=None):
+    rc = lib.mlpblk_backward_fp8_prequant(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(wq),
+                                          _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
+                                          _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    _check(rc, "mlpblk_backward_fp8_prequant")
 
 
 def make_moe_desc(tokens, d_model, ffn, experts, top_k, eps=1e-6) -> MoeDesc:
@@ -436,6 +476,8 @@ class BlockBuffers:
             self.a8 = torch.empty(T, F, dtype=torch.uint8, **e)
             self.n8 = torch.empty(T, d, dtype=torch.uint8, **e)
             self.scales = torch.empty(4, dtype=torch.float32, **e)
+            # the weights' E4M3 codes, for the pre-quantised calls
+            self.wq = torch.empty(mlpblk_fp8_weights_size(self.desc), dtype=torch.uint8, **e)
         self.rstd = torch.empty(T, dtype=torch.float32, **e)
         self.dx = torch.empty(T, d, dtype=self.dt, **e)
         self.dgamma = torch.zeros(d, dtype=torch.float32, **e)

@@ -540,6 +540,144 @@ size_t mlpblk_workspace_size_fp8(const mlpblk_desc *desc) {
     return static_cast<size_t>(ws_layout_f8(desc).total);
 }
 
+}  // extern "C"
+
+namespace {
+
+// E4M3 codes of the weights, each with its scale record {amax, 448/amax, amax/448, 0}.
+struct F8Weights {
+    const uint8_t *w1g, *w2, *w1;  // W1*gamma [F,d], W2 [d,F], W1 [F,d]
+    const float *s_w1g, *s_w2, *s_w1;
+};
+
+// A caller-owned pre-quantised weight buffer: the three code tensors, then the
+// three scale records.
+struct WqLayout {
+    int64_t w1g, w2, w1, scales, total;
+};
+
+WqLayout wq_layout(const mlpblk_desc *d) {
+    WqLayout l;
+    const int64_t fd = align256(d->ffn * d->d_model);
+    l.w1g = 0;
+    l.w2 = fd;
+    l.w1 = 2 * fd;
+    l.scales = 3 * fd;
+    l.total = 3 * fd + 256;
+    return l;
+}
+
+// amax pass, scale record, codes of one tensor (colmul: per-column bf16 factor)
+int quantize_tensor(const void *v, const void *colmul, int64_t cols, int64_t n, float *amax, float *rec,
+                    uint8_t *codes, cudaStream_t s) {
+    int parts = 0;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(v, colmul, cols, n, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, rec, nullptr, 0, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(v, colmul, cols, n, rec, codes, s));
+    return MLPBLK_OK;
+}
+
+int forward_fp8_impl(const mlpblk_desc *desc, const void *x, const F8Weights &w, void *y, void *h_saved,
+                     void *a8_saved, void *n8_saved, float *rstd_saved, float *scales_saved, uint8_t *ws,
+                     const WsLayoutF8 &l, int sms, cudaStream_t s) {
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    float *amax = reinterpret_cast<float *>(ws + l.amax);
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    void *a16 = ws + l.t16;
+    int parts = 0;
+    // n' = x * rstd in E4M3 (scale 1) and rstd; clears the W1 GEMM's flags
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_QUANT, s,
+                  launch_norm_quant(x, rstd_saved, static_cast<uint8_t *>(n8_saved), T, d, desc->eps,
+                                    sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    // h (saved, bf16) and a (bf16, scratch) = relu(h)^2, h = (n' . (W1*gamma)^T) * s_w1g
+    GemmArgs g1 = {};
+    g1.deq_b = w.s_w1g + 2;
+    g1.sk_partial = sk_partial;
+    g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
+                  launch_gemm_tc_f8(kEpiFwdW1Pre, (int)T, (int)F, (int)d, n8_saved, w.w1g, h_saved, a16, g1, sms, s));
+    // a in E4M3 (saved with its scale record; clears the W2 GEMM's flags)
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(a16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet, kSkFlagsPerSet,
+                                    s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s,
+                  launch_apply_e4m3(a16, nullptr, F, T * F, scales_saved, static_cast<uint8_t *>(a8_saved), s));
+    // y = x + (a . W2^T) * s_a * s_w2
+    GemmArgs g2 = {};
+    g2.aux = static_cast<const uint16_t *>(x);
+    g2.ld_aux = (int)d;
+    g2.deq_a = scales_saved + 2;
+    g2.deq_b = w.s_w2 + 2;
+    g2.sk_partial = sk_partial;
+    g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s,
+                  launch_gemm_tc_f8(kEpiFwdW2, (int)T, (int)d, (int)F, a8_saved, w.w2, y, nullptr, g2, sms, s));
+    return MLPBLK_OK;
+}
+
+int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const F8Weights &w,
+                      const void *h_saved, const void *a8_saved, const void *n8_saved, const float *rstd_saved,
+                      const float *scales_saved, void *dx, float *dgamma, float *dw1, float *dw2, uint8_t *ws,
+                      const WsLayoutF8 &l, int sms, cudaStream_t s) {
+    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    float *amax = reinterpret_cast<float *>(ws + l.amax);
+    float *sc = reinterpret_cast<float *>(ws + l.scales);  // records: 2 dy, 3 dh
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    uint8_t *dyq = ws + l.dyq, *dh8 = ws + l.dh8;
+    void *dh16 = ws + l.t16;
+    float *dn_s = reinterpret_cast<float *>(ws + l.dn);
+    float *part = reinterpret_cast<float *>(ws + l.part);
+    int parts = 0;
+    MLPBLK_TRY(quantize_tensor(dy, nullptr, d, T * d, amax, sc + 8, dyq, s));
+    // dW2 += (dy^T . a) * s_dy * s_a; clears the dgrad-h GEMM's flags
+    GemmArgs gw2 = {};
+    gw2.deq_a = sc + 8 + 2;
+    gw2.deq_b = scales_saved + 2;
+    gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
+                  launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
+    // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
+    GemmArgs gd = {};
+    gd.aux = static_cast<const uint16_t *>(h_saved);
+    gd.ld_aux = (int)F;
+    gd.deq_a = sc + 8 + 2;
+    gd.deq_b = w.s_w2 + 2;
+    gd.sk_partial = sk_partial;
+    gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
+                  launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w.w2, dh16, nullptr, gd, sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dh16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
+                  launch_scale_e4m3(amax, parts, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dh16, nullptr, F, T * F, sc + 12, dh8, s));
+    // dn_s = rstd * (dh . W1) * s_dh * s_w1   (fp32)
+    GemmArgs gn = {};
+    gn.rstd_in = rstd_saved;
+    gn.deq_a = sc + 12 + 2;
+    gn.deq_b = w.s_w1 + 2;
+    gn.sk_partial = sk_partial;
+    gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
+                  launch_gemm_tc_f8(kEpiStoreF32, (int)T, (int)d, (int)F, dh8, w.w1, dn_s, nullptr, gn, sms, s));
+    // dW1 += gamma[col] * (dh^T . n') * s_dh
+    GemmArgs gw1 = {};
+    gw1.colscale = static_cast<const uint16_t *>(gamma);
+    gw1.deq_a = sc + 12 + 2;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
+                  launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
+                                    sms, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+    return MLPBLK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int mlpblk_forward_fp8(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1, const void *w2,
                        void *y, void *h_saved, void *a8_saved, void *n8_saved, float *rstd_saved,
                        float *scales_saved, void *workspace, size_t workspace_bytes, void *stream) {
@@ -555,51 +693,16 @@ int mlpblk_forward_fp8(const mlpblk_desc *desc, const void *x, const void *gamma
     int sms = 0;
     MLPBLK_TRY(device_sms(&sms));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    const int64_t d = desc->d_model, F = desc->ffn;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *amax = reinterpret_cast<float *>(ws + l.amax);
-    float *sc = reinterpret_cast<float *>(ws + l.scales);  // [4][4]
-    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
-    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    float *sc = reinterpret_cast<float *>(ws + l.scales);  // records: 0 W1*gamma, 1 W2
     uint8_t *w1q = ws + l.w1q, *w2q = ws + l.w2q;
-    void *a16 = ws + l.t16;
-    int parts = 0;
-    // n' = x * rstd in E4M3 (scale 1) and rstd
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_QUANT, s,
-                  launch_norm_quant(x, rstd_saved, static_cast<uint8_t *>(n8_saved), T, d, desc->eps, s));
-    // W1 * gamma and W2 in E4M3 (the W2 scale record also clears the W1 GEMM's flags)
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w1, gamma, d, F * d, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 0, nullptr, 0, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w1, gamma, d, F * d, sc + 0, w1q, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w2, nullptr, F, d * F, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, sc + 4, sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w2, nullptr, F, d * F, sc + 4, w2q, s));
-    // h (saved, bf16) and a (bf16, scratch) = relu(h)^2, h = (n' . (W1*gamma)^T) * s_w1
-    GemmArgs g1 = {};
-    g1.deq_b = sc + 0 + 2;
-    g1.sk_partial = sk_partial;
-    g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
-                  launch_gemm_tc_f8(kEpiFwdW1Pre, (int)T, (int)F, (int)d, n8_saved, w1q, h_saved, a16, g1, sms, s));
-    // a in E4M3 (saved with its scale record; clears the W2 GEMM's flags)
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(a16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet, kSkFlagsPerSet,
-                                    s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s,
-                  launch_apply_e4m3(a16, nullptr, F, T * F, scales_saved, static_cast<uint8_t *>(a8_saved), s));
-    // y = x + (a . W2^T) * s_a * s_w2
-    GemmArgs g2 = {};
-    g2.aux = static_cast<const uint16_t *>(x);
-    g2.ld_aux = (int)d;
-    g2.deq_a = scales_saved + 2;
-    g2.deq_b = sc + 4 + 2;
-    g2.sk_partial = sk_partial;
-    g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s,
-                  launch_gemm_tc_f8(kEpiFwdW2, (int)T, (int)d, (int)F, a8_saved, w2q, y, nullptr, g2, sms, s));
-    return MLPBLK_OK;
+    // W1 * gamma and W2 in E4M3, into the workspace
+    MLPBLK_TRY(quantize_tensor(w1, gamma, d, F * d, amax, sc + 0, w1q, s));
+    MLPBLK_TRY(quantize_tensor(w2, nullptr, F, d * F, amax, sc + 4, w2q, s));
+    const F8Weights w = {w1q, w2q, nullptr, sc + 0, sc + 4, nullptr};
+    return forward_fp8_impl(desc, x, w, y, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, ws, l, sms, s);
 }
 
 int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const void *w1,
@@ -619,66 +722,86 @@ int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, 
     int sms = 0;
     MLPBLK_TRY(device_sms(&sms));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
+    const int64_t d = desc->d_model, F = desc->ffn;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *amax = reinterpret_cast<float *>(ws + l.amax);
-    float *sc = reinterpret_cast<float *>(ws + l.scales);  // 0 W1, 1 W2, 2 dy, 3 dh
-    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
-    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
-    uint8_t *w1q = ws + l.w1q, *w2q = ws + l.w2q, *dyq = ws + l.dyq, *dh8 = ws + l.dh8;
-    void *dh16 = ws + l.t16;
-    float *dn_s = reinterpret_cast<float *>(ws + l.dn);
-    float *part = reinterpret_cast<float *>(ws + l.part);
-    int parts = 0;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dy, nullptr, d, T * d, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 8, nullptr, 0, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dy, nullptr, d, T * d, sc + 8, dyq, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w2, nullptr, F, d * F, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s, launch_scale_e4m3(amax, parts, sc + 4, nullptr, 0, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w2, nullptr, F, d * F, sc + 4, w2q, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(w1, nullptr, d, F * d, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, sc + 0, sk_flags + kSetDgradH * kSkFlagsPerSet, kSkFlagsPerSet, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(w1, nullptr, d, F * d, sc + 0, w1q, s));
-    // dW2 += (dy^T . a) * s_dy * s_a
-    GemmArgs gw2 = {};
-    gw2.deq_a = sc + 8 + 2;
-    gw2.deq_b = scales_saved + 2;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
-                  launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
-    // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
-    GemmArgs gd = {};
-    gd.aux = static_cast<const uint16_t *>(h_saved);
-    gd.ld_aux = (int)F;
-    gd.deq_a = sc + 8 + 2;
-    gd.deq_b = sc + 4 + 2;
-    gd.sk_partial = sk_partial;
-    gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
-                  launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w2q, dh16, nullptr, gd, sms, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dh16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet, kSkFlagsPerSet, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dh16, nullptr, F, T * F, sc + 12, dh8, s));
-    // dn_s = rstd * (dh . W1) * s_dh * s_w1   (fp32)
-    GemmArgs gn = {};
-    gn.rstd_in = rstd_saved;
-    gn.deq_a = sc + 12 + 2;
-    gn.deq_b = sc + 0 + 2;
-    gn.sk_partial = sk_partial;
-    gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
-                  launch_gemm_tc_f8(kEpiStoreF32, (int)T, (int)d, (int)F, dh8, w1q, dn_s, nullptr, gn, sms, s));
-    // dW1 += gamma[col] * (dh^T . n') * s_dh
-    GemmArgs gw1 = {};
-    gw1.colscale = static_cast<const uint16_t *>(gamma);
-    gw1.deq_a = sc + 12 + 2;
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
-                  launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
-                                    sms, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+    float *sc = reinterpret_cast<float *>(ws + l.scales);  // records: 0 W1, 1 W2
+    uint8_t *w1q = ws + l.w1q, *w2q = ws + l.w2q;
+    MLPBLK_TRY(quantize_tensor(w2, nullptr, F, d * F, amax, sc + 4, w2q, s));
+    MLPBLK_TRY(quantize_tensor(w1, nullptr, d, F * d, amax, sc + 0, w1q, s));
+    const F8Weights w = {nullptr, w2q, w1q, nullptr, sc + 4, sc + 0};
+    return backward_fp8_impl(desc, dy, x, gamma, w, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
+                             dgamma, dw1, dw2, ws, l, sms, s);
+}
+
+size_t mlpblk_fp8_weights_size(const mlpblk_desc *desc) {
+    if (check_fp8_desc(desc) != MLPBLK_OK) return 0;
+    return static_cast<size_t>(wq_layout(desc).total);
+}
+
+int mlpblk_fp8_quantize_weights(const mlpblk_desc *desc, const void *gamma, const void *w1, const void *w2,
+                                void *wq, size_t wq_bytes, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (!aligned16(gamma) || !aligned16(w1) || !aligned16(w2) || !aligned16(wq) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    const WqLayout q = wq_layout(desc);
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (wq_bytes < static_cast<size_t>(q.total) || workspace_bytes < static_cast<size_t>(l.total))
+        return MLPBLK_EWORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t d = desc->d_model, F = desc->ffn;
+    uint8_t *b = static_cast<uint8_t *>(wq);
+    float *rec = reinterpret_cast<float *>(b + q.scales);  // [3][4]: W1*gamma, W2, W1
+    float *amax = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + l.amax);
+    MLPBLK_TRY(quantize_tensor(w1, gamma, d, F * d, amax, rec + 0, b + q.w1g, s));
+    MLPBLK_TRY(quantize_tensor(w2, nullptr, F, d * F, amax, rec + 4, b + q.w2, s));
+    MLPBLK_TRY(quantize_tensor(w1, nullptr, d, F * d, amax, rec + 8, b + q.w1, s));
     return MLPBLK_OK;
+}
+
+int mlpblk_forward_fp8_prequant(const mlpblk_desc *desc, const void *x, const void *wq, void *y, void *h_saved,
+                                void *a8_saved, void *n8_saved, float *rstd_saved, float *scales_saved,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(wq) || !aligned16(y) || !aligned16(h_saved) || !aligned16(a8_saved) ||
+        !aligned16(n8_saved) || !aligned16(rstd_saved) || !aligned16(scales_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    const WqLayout q = wq_layout(desc);
+    const uint8_t *b = static_cast<const uint8_t *>(wq);
+    const float *rec = reinterpret_cast<const float *>(b + q.scales);
+    const F8Weights w = {b + q.w1g, b + q.w2, b + q.w1, rec + 0, rec + 4, rec + 8};
+    return forward_fp8_impl(desc, x, w, y, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
+                            static_cast<uint8_t *>(workspace), l, sms, static_cast<cudaStream_t>(stream));
+}
+
+int mlpblk_backward_fp8_prequant(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                                 const void *wq, const void *h_saved, const void *a8_saved, const void *n8_saved,
+                                 const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma,
+                                 float *dw1, float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(wq) || !aligned16(h_saved) ||
+        !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) || !aligned16(scales_saved) ||
+        !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    const WqLayout q = wq_layout(desc);
+    const uint8_t *b = static_cast<const uint8_t *>(wq);
+    const float *rec = reinterpret_cast<const float *>(b + q.scales);
+    const F8Weights w = {b + q.w1g, b + q.w2, b + q.w1, rec + 0, rec + 4, rec + 8};
+    return backward_fp8_impl(desc, dy, x, gamma, w, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
+                             dgamma, dw1, dw2, static_cast<uint8_t *>(workspace), l, sms,
+                             static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -55,17 +55,29 @@ amax_partial_kernel(const uint16_t *__restrict__ v, const uint16_t *__restrict__
     const int64_t g0 = blockIdx.x * per;
     const int64_t g1 = min(groups, g0 + per);
     float m = 0.0f;
-    for (int64_t g = g0 + threadIdx.x; g < g1; g += kQThreads) {
-        float x[8];
-        load8(v + g * 8, x);
-        if (colmul) {
-            float c[8];
-            load8(colmul + (g * 8) % cols, c);
+    // four 16-byte loads in flight per thread
+    for (int64_t g = g0 + threadIdx.x; g < g1; g += 4 * kQThreads) {
+        float x[4][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] *= c[i];
+        for (int u = 0; u < 4; ++u) {
+            const int64_t gu = g + u * kQThreads;
+            if (gu < g1) load8(v + gu * 8, x[u]);
+            else
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[u][i] = 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+        for (int u = 0; u < 4; ++u) {
+            const int64_t gu = g + u * kQThreads;
+            if (colmul && gu < g1) {
+                float c[8];
+                load8(colmul + (gu * 8) % cols, c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[u][i] *= c[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[u][i]));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -121,8 +133,11 @@ __global__ void quantize_kernel(const uint16_t *__restrict__ v, const uint16_t *
 // One warp per row; the row's second read comes from L1/L2.
 __global__ void __launch_bounds__(256)
 norm_quant_kernel(const uint16_t *__restrict__ x, float *__restrict__ rstd, uint8_t *__restrict__ n8,
-                  int64_t T, int64_t d, float eps) {
+                  int64_t T, int64_t d, float eps, int *zero_flags, int zero_count) {
     griddep_enter();
+    // the next GEMM's stream-K flags start from zero
+    if (zero_flags && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_flags[i] = 0;
     const int lane = threadIdx.x & 31;
     const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -193,13 +208,14 @@ int launch_apply_e4m3(const void *v, const void *colmul, int64_t cols, int64_t n
                       static_cast<const uint16_t *>(v), static_cast<const uint16_t *>(colmul), cols, groups, scale, q);
 }
 
-int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_t d, float eps, cudaStream_t s) {
+int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_t d, float eps, int *zero_flags,
+                      int zero_count, cudaStream_t s) {
     int64_t blocks = (T * 32 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sm_total()) * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(norm_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                      static_cast<const uint16_t *>(x), rstd, n8, T, d, eps);
+                      static_cast<const uint16_t *>(x), rstd, n8, T, d, eps, zero_flags, zero_count);
 }
 
 }  // namespace mlpblk

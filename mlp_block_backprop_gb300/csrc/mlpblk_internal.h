@@ -200,7 +200,8 @@ int launch_scale_e4m3(const float *partial, int parts, float *scale, int *zero_f
                       cudaStream_t s);
 int launch_apply_e4m3(const void *v, const void *colmul, int64_t cols, int64_t n, const float *scale, uint8_t *q,
                       cudaStream_t s);
-int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_t d, float eps, cudaStream_t s);
+int launch_norm_quant(const void *x, float *rstd, uint8_t *n8, int64_t T, int64_t d, float eps, int *zero_flags,
+                      int zero_count, cudaStream_t s);
 int launch_gemm_tc_f8(int epi, int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
                       const GemmArgs &extra, int num_sms, cudaStream_t s);
 int take_device_error_gemm_f8();

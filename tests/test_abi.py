@@ -176,6 +176,32 @@ def test_fp8_argument_errors_need_no_device(mb):
     assert b(bwd, 16) == mb.MLPBLK_EWORKSPACE
 
 
+def test_fp8_prequant_argument_errors_need_no_device(mb):
+    d = mb.make_desc(64, 128, 256)
+    wq_size = mb.lib.mlpblk_fp8_weights_size(ctypes.byref(d))
+    assert wq_size >= 3 * 128 * 256 + 48            # three code tensors and three scale records
+    assert mb.lib.mlpblk_fp8_weights_size(ctypes.byref(mb.make_desc(64, 136, 256))) == 0
+    q = lambda wq_bytes, ws=1 << 40, g=0x10000: mb.lib.mlpblk_fp8_quantize_weights(
+        ctypes.byref(d), g, 0x20000, 0x30000, 0x40000, wq_bytes, 0x50000, ws, None)
+    assert q(wq_size - 1) == mb.MLPBLK_EWORKSPACE
+    assert q(wq_size, ws=16) == mb.MLPBLK_EWORKSPACE
+    assert q(wq_size, g=0x10004) == mb.MLPBLK_EINVAL  # gamma misaligned
+    fwd = [0x10000 * (i + 1) for i in range(9)]
+    f = lambda args, ws=1 << 40: mb.lib.mlpblk_forward_fp8_prequant(ctypes.byref(d), *args, ws, None)
+    alias = list(fwd)
+    alias[2] = alias[0]   # y == x
+    assert f(alias) == mb.MLPBLK_EINVAL
+    assert f(fwd, 16) == mb.MLPBLK_EWORKSPACE
+    bwd = [0x10000 * (i + 1) for i in range(13)]
+    b = lambda args, ws=1 << 40: mb.lib.mlpblk_backward_fp8_prequant(ctypes.byref(d), *args, ws, None)
+    bad = list(bwd)
+    bad[3] += 8   # wq misaligned
+    assert b(bad) == mb.MLPBLK_EINVAL
+    assert b(bwd, 16) == mb.MLPBLK_EWORKSPACE
+    empty = mb.make_desc(0, 128, 256)
+    assert mb.lib.mlpblk_forward_fp8_prequant(ctypes.byref(empty), *fwd, 1 << 40, None) == mb.MLPBLK_OK
+
+
 def test_moe_argument_errors_need_no_device(mb):
     d = mb.make_moe_desc(64, 128, 256, 4, 2)
     assert mb.lib.mlpblk_moe_saved_size(ctypes.byref(d)) > 0

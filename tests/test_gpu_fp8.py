@@ -113,3 +113,35 @@ def test_fp8_matches_the_bf16_block_within_fp8_error():
     assert oracle.scaled_error(outs[0]["y"] - inp.x[0], ref_outs[0]["y"] - inp.x[0]) < 0.15
     for k in ("dw1", "dw2"):
         assert oracle.scaled_error(grads[k], ref_grads[k]) < 0.15
+
+
+@pytest.mark.parametrize("shape", [(300, 128, 512), (1024, 512, 2048)])
+def test_fp8_prequantised_weights_give_the_same_bits(shape):
+    """Weights quantised once (mlpblk_fp8_quantize_weights) and used by every
+    microbatch give bitwise the outputs and dgamma of the calls that quantise them
+    each time; dW1 and dW2 agree up to the order of the fp32 reduce-adds of a
+    weight-gradient tile split between workers (the one unordered sum)."""
+    import torch
+    import mlp_block_backprop_gb300 as mb
+    T, d, F = shape
+    inp = synth.make_inputs(tokens=T, d=d, ffn=F, dtype="bf16", seed=T + F, n_mb=3, eps=1e-6)
+    outs, grads, bb = _run_fp8(inp)
+    bb.zero_grads()
+    mb.mlpblk_fp8_quantize_weights(bb.desc, bb.gamma, bb.w1, bb.w2, bb.wq, bb.ws)
+    outs2 = []
+    for x, dy in zip(inp.x, inp.dy):
+        bb.x.copy_(to_dev(x, bb.dt))
+        bb.dy.copy_(to_dev(dy, bb.dt))
+        mb.mlpblk_forward_fp8_prequant(bb.desc, bb.x, bb.wq, bb.y, bb.h, bb.a8, bb.n8, bb.rstd, bb.scales, bb.ws)
+        mb.mlpblk_backward_fp8_prequant(bb.desc, bb.dy, bb.x, bb.gamma, bb.wq, bb.h, bb.a8, bb.n8, bb.rstd,
+                                        bb.scales, bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+        outs2.append({k: to_np(getattr(bb, k)) for k in ("y", "h", "rstd", "dx")})
+    torch.cuda.synchronize()
+    for a, b in zip(outs, outs2):
+        for k in a:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    np.testing.assert_array_equal(grads["dgamma"], to_np(bb.dgamma), err_msg="dgamma")
+    for k in ("dw1", "dw2"):
+        got = to_np(getattr(bb, k))
+        np.testing.assert_allclose(got, grads[k], rtol=1e-5, atol=1e-6 * float(np.max(np.abs(grads[k]))),
+                                   err_msg=k)
