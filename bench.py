@@ -303,7 +303,7 @@ def run_ours(args, dist, peaks):
     if mb.mlpblk_last_error() != mb.MLPBLK_OK:
         raise RuntimeError("device error during warm-up")
 
-    launches_per_step = (1 + (9 if fp8 else 0) + n_mb * (18 if fp8 else 11 if recompute else 9)
+    launches_per_step = (1 + (9 if fp8 else 0) + n_mb * (16 if fp8 else 11 if recompute else 9)
                          + (1 if inp.grad_scale is not None else 0) + (3 if args.optimizer else 0))
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
     clocks = ClockSampler(dist.local_rank)

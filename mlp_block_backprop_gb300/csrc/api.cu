@@ -100,6 +100,7 @@ struct WsLayoutF8 {
 };
 
 constexpr int kAmaxParts = 2048;
+static_assert(kAmaxParts >= kMaxSkSlots * 4, "the GEMM epilogues' maxima fit the amax scratch");
 
 WsLayoutF8 ws_layout_f8(const mlpblk_desc *dsc) {
     const int64_t T = dsc->tokens, d = dsc->d_model, F = dsc->ffn;
@@ -591,17 +592,18 @@ int forward_fp8_impl(const mlpblk_desc *desc, const void *x, const F8Weights &w,
                   launch_norm_quant(x, rstd_saved, static_cast<uint8_t *>(n8_saved), T, d, desc->eps,
                                     sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
     // h (saved, bf16) and a (bf16, scratch) = relu(h)^2, h = (n' . (W1*gamma)^T) * s_w1g
+    // (the epilogue also leaves max |a| per epilogue warp in amax)
     GemmArgs g1 = {};
     g1.deq_b = w.s_w1g + 2;
     g1.sk_partial = sk_partial;
     g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+    g1.amax_out = amax;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
                   launch_gemm_tc_f8(kEpiFwdW1Pre, (int)T, (int)F, (int)d, n8_saved, w.w1g, h_saved, a16, g1, sms, s));
     // a in E4M3 (saved with its scale record; clears the W2 GEMM's flags)
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(a16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet, kSkFlagsPerSet,
-                                    s));
+                  launch_scale_e4m3(amax, kMaxSkSlots * 4, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet,
+                                    kSkFlagsPerSet, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s,
                   launch_apply_e4m3(a16, nullptr, F, T * F, scales_saved, static_cast<uint8_t *>(a8_saved), s));
     // y = x + (a . W2^T) * s_a * s_w2
@@ -640,6 +642,7 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
                   launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
     // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
+    // (the epilogue also leaves max |dh| per epilogue warp in amax)
     GemmArgs gd = {};
     gd.aux = static_cast<const uint16_t *>(h_saved);
     gd.ld_aux = (int)F;
@@ -647,11 +650,12 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     gd.deq_b = w.s_w2 + 2;
     gd.sk_partial = sk_partial;
     gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    gd.amax_out = amax;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
                   launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w.w2, dh16, nullptr, gd, sms, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_AMAX, s, launch_amax_e4m3(dh16, nullptr, F, T * F, amax, kAmaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, parts, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet, kSkFlagsPerSet, s));
+                  launch_scale_e4m3(amax, kMaxSkSlots * 4, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet,
+                                    kSkFlagsPerSet, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dh16, nullptr, F, T * F, sc + 12, dh8, s));
     // dn_s = rstd * (dh . W1) * s_dh * s_w1   (fp32)
     GemmArgs gn = {};

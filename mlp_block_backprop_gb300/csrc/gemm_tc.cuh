@@ -452,6 +452,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int sbuf = 0;
         uint32_t aux_phase = 0;
         float rsc_pre = 1.0f;
+        // max |output| of this thread's a (W1) or dh (dgrad-h) values, as stored in bf16
+        constexpr bool kAmaxEpi = C::kReluSq || C::EPI == kEpiDgradH;
+        const bool want_amax = kAmaxEpi && args.amax_out != nullptr;
+        float amax_t = 0.0f;
         const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
         SegIter si = seg_begin<C::kTileM>(args, worker);
         Seg w;
@@ -618,6 +622,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                     o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
                                 }
                             }
+                            if (want_amax)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const uint32_t av = C::kAOnly ? o[i] : o2[i];
+                                    amax_t = fmaxf(amax_t, fmaxf(bf16_lo(av), bf16_hi(av)));  // a >= 0
+                                }
                         } else if (C::EPI == kEpiStoreBf16) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
@@ -634,6 +644,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 const float d0 = g0 > 0.0f ? rsc * e[2 * i] * (2.0f * g0) : 0.0f;
                                 const float d1 = g1 > 0.0f ? rsc * e[2 * i + 1] * (2.0f * g1) : 0.0f;
                                 o[i] = pack_bf16x2(d0, d1);
+                                if (want_amax)
+                                    amax_t = fmaxf(amax_t, fmaxf(fabsf(bf16_lo(o[i])), fabsf(bf16_hi(o[i]))));
                             }
                         }
                         const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
@@ -695,6 +707,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             bulk_wait_group<0>();
             if (C::kAux && aux_pending) mbar_drain(&aux_bar[q], aux_phase);
+        }
+        if (want_amax) {
+            // one maximum per epilogue warp; CTA 0 zeroes the slots no CTA holds
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax_t = fmaxf(amax_t, __shfl_xor_sync(0xffffffffu, amax_t, o));
+            if (lane == 0) args.amax_out[slot * 4 + q] = amax_t;
+            if (blockIdx.x == 0)
+                for (int i = static_cast<int>(gridDim.x) * 4 + q * 32 + lane; i < kMaxSkSlots * 4; i += 128)
+                    args.amax_out[i] = 0.0f;
         }
         __syncwarp();
     } else if (C::kNorm) {

@@ -109,6 +109,8 @@ struct GemmArgs {
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
+    float *amax_out;           // W1 (a) and dgrad-h (dh) epilogues: max |bf16 output| per
+                               // epilogue warp, kMaxSkSlots * 4 floats (unused slots 0)
     // grouped GEMMs of the routed experts (kGroupNone otherwise)
     int grp_mode, grp_count;   // kGroupM / kGroupK; number of experts
     const int *grp_rows;       // device [grp_count + 1]: padded segment starts (rows)
