@@ -361,16 +361,17 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
 // to kStagedMaxStages iterations ahead (warp 0 issues them, the slot rows' indices
 // loaded one issue ahead; an mbarrier per stage counts the bytes).  For a plain dn
 // it measured no faster than the register-resident kernel, which stays in use.
-// A CTA of kStagedThreads takes R = 4096 / d rows per iteration, d/8 threads per
+// A CTA of 256 threads (d <= 2048: two CTAs per SM) or 512 (d = 4096) takes
+// R = 8 * threads / d rows per iteration, d/8 threads per
 // row, 8 columns per thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16,
 // dn [R][K'][d] fp32 (K' = k slot rows with kGather, else 1).  The row sum is a
 // shuffle tree per warp then the row's warps in order; the dgamma partial of the
 // CTA is each thread's running sum, then the R row groups in order.
-constexpr int kStagedThreads = 512;
+constexpr int kStagedMaxThreads = 512;
 constexpr int kStagedMaxStages = 4;
 
 template <bool kGather>
-__global__ void __launch_bounds__(kStagedThreads, 1)
+__global__ void __launch_bounds__(kStagedMaxThreads, 1)
 rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dn_s,
                           const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
                           const uint16_t *__restrict__ gamma, uint16_t *__restrict__ dx,
@@ -484,14 +485,15 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restric
 #pragma unroll
         for (int j = 0; j < 4; ++j) p_n1[j] = p_n2[j];
         fetch(it + 2, r_n2, p_n2);
+        // every thread waits on the stage's barrier; the block-wide vote below
+        // (which also publishes the warp sums) leaves the loop together if any gave up
         const bool ok = mbar_wait(&full[st], ph, abort_flag);
-        if (!__syncthreads_and(ok)) break;
         const uint8_t *sx = stages + static_cast<size_t>(st) * stage_bytes;
         const uint8_t *sy = sx + static_cast<size_t>(R) * d * 2;
         const uint8_t *sn = sy + static_cast<size_t>(R) * d * 2;
         float xv[8], yv[8], nv[8];
         float part = 0.0f;
-        if (valid) {
+        if (valid && ok) {
             const uint4 ux = *reinterpret_cast<const uint4 *>(sx + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
             const uint4 uy = *reinterpret_cast<const uint4 *>(sy + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
             xv[0] = bf(ux.x & 0xFFFFu); xv[1] = bf(ux.x >> 16); xv[2] = bf(ux.y & 0xFFFFu); xv[3] = bf(ux.y >> 16);
@@ -516,7 +518,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restric
         float *rr = red + (it & 1) * R * 16;
         if (active && lane == 0) rr[grp * 16 + gl / 32] = part;
         // every thread has read stage st and written its warp sum
-        __syncthreads();
+        if (!__syncthreads_and(ok)) break;
         if (tid < 32 && issued < iters) {
             issue(issued++);
             load_pos(issued);
@@ -551,7 +553,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restric
     }
     __syncthreads();
     float *out = dg_part + blockIdx.x * d;
-    for (int64_t i = tid; i < d; i += kStagedThreads) {
+    for (int64_t i = tid; i < d; i += blockDim.x) {
         float v = 0.0f;
         for (int g2 = 0; g2 < R; ++g2) v += gsum[static_cast<size_t>(g2) * d + i];
         out[i] = v;
@@ -755,23 +757,25 @@ namespace {
 // Shape of the staged kernel for width d and k slot rows (0 when it does not
 // apply): rows per iteration R, stages S, bytes per stage.
 struct StagedShape {
-    int R, S, stage_bytes;
+    int R, S, stage_bytes, threads;
     size_t smem;
 };
 
 StagedShape staged_shape(int64_t d, int k) {
-    StagedShape sh = {0, 0, 0, 0};
+    StagedShape sh = {0, 0, 0, 0, 0};
     if (d % 256 != 0 || d > 4096 || k < 1 || k > 4) return sh;
-    const int R = static_cast<int>(4096 / d);
+    const int threads = d <= 2048 ? 256 : 512;
+    const int R = static_cast<int>(8 * threads / d);
     if (k > 1 && R * k > 64) return sh;  // warp 0 issues at most 64 slot rows
     const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * 4 + 127) / 128 * 128;
     const int64_t extra = 2 * R * 16 * 4 + kStagedMaxStages * 8 + 16;
-    const int64_t budget = 200 * 1024;
+    const int64_t budget = threads == 256 ? 100 * 1024 : 200 * 1024;  // 256 threads: two CTAs per SM
     int S = static_cast<int>((budget - extra) / bytes);
     if (S > kStagedMaxStages) S = kStagedMaxStages;
     if (S < 2) return sh;
     sh.R = R;
     sh.S = S;
+    sh.threads = threads;
     sh.stage_bytes = static_cast<int>(bytes);
     sh.smem = static_cast<size_t>(S) * bytes + extra;
     return sh;
@@ -790,7 +794,7 @@ int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, c
         if (rc != MLPBLK_OK) return rc;
         attr[dev] = true;
     }
-    int64_t parts = sm_count();
+    int64_t parts = static_cast<int64_t>(sm_count()) * (sh.threads == 256 ? 2 : 1);
     if (parts > max_parts) parts = max_parts;
     const int64_t groups = (T + sh.R - 1) / sh.R;
     if (parts > groups) parts = groups;
@@ -798,7 +802,7 @@ int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, c
     const int64_t rows_per_cta = ((T + parts - 1) / parts + sh.R - 1) / sh.R * sh.R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather>, dim3(static_cast<unsigned>(parts)), dim3(kStagedThreads),
+    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather>, dim3(static_cast<unsigned>(parts)), dim3(sh.threads),
                       sh.smem, s, static_cast<const uint16_t *>(x), dn, static_cast<const uint16_t *>(dy), rstd,
                       static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(dx), part, T, d, rows_per_cta,
                       sh.R, sh.S, sh.stage_bytes, pos, k);
