@@ -560,7 +560,7 @@ def run_moe(args, dist, peaks):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    launches = 1 + 8 + 7   # zero_grads; forward; backward
+    launches = 1 + 7 + 7   # zero_grads; forward; backward
     trace = mb.KernelTrace(args.steps * launches + 8)
     plain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(plain):

@@ -817,8 +817,7 @@ namespace {
 struct MoeLayout {
     int64_t R;
     // saved
-    int64_t rstd, pos, row_token, row_slot, seg, count, chunk_count, chunk_base, rstd_perm, x_perm, h_perm, a_perm,
-        o_perm, saved;
+    int64_t rstd, pos, row_token, row_slot, seg, count, chunk_count, rstd_perm, x_perm, h_perm, a_perm, o_perm, saved;
     // workspace
     int64_t w1g, do_perm, dh_perm, dn_perm, part, ws;
 };
@@ -852,7 +851,6 @@ MoeLayout moe_layout(const mlpblk_moe_desc *m) {
     l.seg = take((E + 1) * 4);
     l.count = take(E * 4);
     l.chunk_count = take(moe_route_chunks(T * k) * E * 4);
-    l.chunk_base = take(moe_route_chunks(T * k) * E * 4);
     l.rstd_perm = take(l.R * 4);
     l.x_perm = take(l.R * d * 2);
     l.h_perm = take(l.R * F * 2);
@@ -911,17 +909,16 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     int *seg = reinterpret_cast<int *>(sv + l.seg);
     int *count = reinterpret_cast<int *>(sv + l.count);
     int *chunk_count = reinterpret_cast<int *>(sv + l.chunk_count);
-    int *chunk_base = reinterpret_cast<int *>(sv + l.chunk_base);
     float *rstd_perm = reinterpret_cast<float *>(sv + l.rstd_perm);
     void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
     void *w1g = ws + l.w1g;
     // rstd and every expert's W1 * gamma (the experts' W1 as one [E*F, d] matrix)
     MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
                   launch_norm_prep(MLPBLK_BF16, x, rstd, T, d, desc->base.eps, w1s, gamma, w1g, E * F, nullptr, 0, s));
-    for (int step = 0; step < moe_route_launches(T * k); ++step)
+    for (int step = 0; step < kMoeRouteLaunches; ++step)
         MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s,
-                      launch_moe_route(expert_idx, T * k, k, E, chunk_count, chunk_base, count, seg, pos, row_token,
-                                       row_slot, step, s));
+                      launch_moe_route(expert_idx, T * k, k, E, chunk_count, count, seg, pos, row_token, row_slot,
+                                       step, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_GATHER, s,
                   launch_moe_gather(x, rstd, row_token, seg, E, l.R, d, x_perm, rstd_perm, s));
     GemmArgs g1 = {};

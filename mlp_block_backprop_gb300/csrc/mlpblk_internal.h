@@ -212,13 +212,12 @@ int take_device_error_gemm_f8();
 // experts' segments of (token, slot) assignments, each padded to 256 rows.
 constexpr int kMoeRouteChunk = 1024;  // routing entries per CTA
 inline int64_t moe_route_chunks(int64_t n) { return (n + kMoeRouteChunk - 1) / kMoeRouteChunk; }
-// Up to kMoeRouteSingleMax entries, routing is one launch (one CTA); beyond, three:
-// step 0: per-chunk counts, 1: scan and segment offsets, 2: ranks, rows and the
-// row map.  chunk_count and chunk_base hold moe_route_chunks(n) * experts ints.
-constexpr int64_t kMoeRouteSingleMax = 65536;
-int moe_route_launches(int64_t n);
-int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *chunk_base,
-                     int *count, int *seg, int *pos, int *row_token, int *row_slot, int step, cudaStream_t s);
+// Routing in two launches: step 0 counts each chunk's entries per expert, step 1
+// ranks and places them (the counts' prefix and the segment offsets computed per
+// CTA).  chunk_count holds moe_route_chunks(n) * experts ints.
+constexpr int kMoeRouteLaunches = 2;
+int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *count, int *seg,
+                     int *pos, int *row_token, int *row_slot, int step, cudaStream_t s);
 int launch_moe_gather(const void *x, const float *rstd, const int *row_token, const int *seg, int experts,
                       int64_t rows_max, int64_t d, void *x_perm, float *rstd_perm, cudaStream_t s);
 int launch_moe_combine(const void *x, const void *o_perm, const float *p, const int *pos, int64_t T, int k,

@@ -39,11 +39,11 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
 
-// Routing runs in three launches over chunks of kChunk (token, slot) entries:
-// route_count (one CTA per chunk: the chunk's entries per expert), route_scan
-// (one CTA: each chunk's first rank per expert, the experts' counts and padded
-// segment offsets) and route_place (one CTA per chunk: every entry's rank in
-// (token, slot) order, its row, and the row -> (token, slot) map).
+// Routing runs in two launches over chunks of kChunk (token, slot) entries:
+// route_count (one CTA per chunk: the chunk's entries per expert) and route_place
+// (one CTA per chunk: the counts' prefix and the padded segment offsets, then
+// every entry's rank in (token, slot) order, its row, and the row -> (token,
+// slot) map).
 
 // chunk_count[b][e] = entries of chunk b with idx == e.  Entries outside
 // [0, experts) belong to no expert.
@@ -64,51 +64,53 @@ route_count_kernel(const int *__restrict__ idx, int64_t n, int experts, int *__r
         chunk_count[static_cast<int64_t>(blockIdx.x) * experts + e] = cnt[e];
 }
 
-// chunk_base[b][e] = sum over b' < b of chunk_count[b'][e]; count[e] = the
-// expert's entries; seg[e] = sum over e' < e of count[e'] rounded up to 256,
-// seg[experts] = the rows in use.
+// CTA b places chunk b.  It first adds up the chunk counts itself: the entries of
+// each expert in the chunks before b (its first rank in this chunk) and in all
+// chunks (the expert's count), then lays out the padded segments (CTA 0 publishes
+// them).  Warp w walks its kChunk/8 entries in groups of 32 in order; lanes with
+// the same expert (match_any) take consecutive ranks, so an entry's rank counts
+// the entries of its expert before it in (token, slot) order.  pos[i] = seg[e] +
+// rank (-1 for an entry that selects nothing), row_token / row_slot of that row;
+// padding rows get row_token = -1.
 __global__ void __launch_bounds__(kRouteThreads)
-route_scan_kernel(const int *__restrict__ chunk_count, int chunks, int experts, int *__restrict__ chunk_base,
-                  int *__restrict__ count, int *__restrict__ seg) {
+route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, int chunks,
+                   const int *__restrict__ chunk_count, int *__restrict__ count, int *__restrict__ seg,
+                   int *__restrict__ pos, int *__restrict__ row_token, int *__restrict__ row_slot) {
+    constexpr int kWarps = kRouteThreads / 32;
+    constexpr int kPerWarp = kChunk / kWarps;
+    __shared__ int wcnt[kWarps][kMaxExperts];
+    __shared__ int cbase[kMaxExperts];
     __shared__ int tot[kMaxExperts];
+    __shared__ int segs[kMaxExperts + 1];
     griddep_enter();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kWarps * experts; i += kRouteThreads) wcnt[i / experts][i % experts] = 0;
     for (int e = threadIdx.x; e < experts; e += kRouteThreads) {
-        int run = 0;
+        int before = 0, all = 0;
         for (int b = 0; b < chunks; ++b) {
-            const int64_t at = static_cast<int64_t>(b) * experts + e;
-            chunk_base[at] = run;
-            run += chunk_count[at];
+            const int c = chunk_count[static_cast<int64_t>(b) * experts + e];
+            if (b < static_cast<int>(blockIdx.x)) before += c;
+            all += c;
         }
-        tot[e] = run;
-        count[e] = run;
+        cbase[e] = before;
+        tot[e] = all;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         int off = 0;
         for (int e = 0; e < experts; ++e) {
-            seg[e] = off;
+            segs[e] = off;
             off += (tot[e] + kSegPad - 1) / kSegPad * kSegPad;
         }
-        seg[experts] = off;
+        segs[experts] = off;
     }
-}
-
-// CTA b places chunk b.  Warp w walks its kChunk/8 entries in groups of 32 in
-// order; lanes with the same expert (match_any) take consecutive ranks, so an
-// entry's rank counts the entries of its expert before it in (token, slot)
-// order.  pos[i] = seg[e] + rank (-1 for an entry that selects nothing),
-// row_token / row_slot of that row; padding rows get row_token = -1.
-__global__ void __launch_bounds__(kRouteThreads)
-route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, const int *__restrict__ chunk_base,
-                   const int *__restrict__ count, const int *__restrict__ seg, int *__restrict__ pos,
-                   int *__restrict__ row_token, int *__restrict__ row_slot) {
-    constexpr int kWarps = kRouteThreads / 32;
-    constexpr int kPerWarp = kChunk / kWarps;
-    __shared__ int wcnt[kWarps][kMaxExperts];
-    griddep_enter();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kWarps * experts; i += kRouteThreads) wcnt[i / experts][i % experts] = 0;
     __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e <= experts; e += kRouteThreads) {
+            seg[e] = segs[e];
+            if (e < experts) count[e] = tot[e];
+        }
+    }
     const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kChunk + wid * kPerWarp;
     const unsigned lt = (1u << lane) - 1u;
     // pass 1: this warp's entries per expert
@@ -123,7 +125,7 @@ route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, c
     __syncthreads();
     // the warp's first rank per expert: the chunk's, plus the warps before it
     for (int e = threadIdx.x; e < experts; e += kRouteThreads) {
-        int run = chunk_base[static_cast<int64_t>(blockIdx.x) * experts + e];
+        int run = cbase[e];
         for (int w = 0; w < kWarps; ++w) {
             const int c = wcnt[w][e];
             wcnt[w][e] = run;
@@ -145,7 +147,7 @@ route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, c
             if (e < 0) {
                 pos[i] = -1;
             } else {
-                const int p = seg[e] + base + __popc(peers & lt);
+                const int p = segs[e] + base + __popc(peers & lt);
                 pos[i] = p;
                 row_token[p] = static_cast<int>(i / k);
                 row_slot[p] = static_cast<int>(i % k);
@@ -156,104 +158,7 @@ route_place_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, c
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kRouteThreads + threadIdx.x;
          q < static_cast<int64_t>(experts) * kSegPad; q += static_cast<int64_t>(gridDim.x) * kRouteThreads) {
         const int e = static_cast<int>(q / kSegPad);
-        const int r = seg[e] + count[e] + static_cast<int>(q % kSegPad);
-        if (r < seg[e + 1]) {
-            row_token[r] = -1;
-            row_slot[r] = 0;
-        }
-    }
-}
-
-// All of routing in one CTA of kSingleThreads (up to kSingleMax entries): warp w
-// takes a contiguous range of entries; per-warp counts, a per-expert scan over
-// the warps, the segment offsets, then the ordered ranks as in route_place.
-constexpr int kSingleThreads = 1024;
-constexpr int kIdBatch = 8;
-constexpr int kSingleWarps = kSingleThreads / 32;
-
-__global__ void __launch_bounds__(kSingleThreads)
-route_single_kernel(const int *__restrict__ idx, int64_t n, int k, int experts, int *__restrict__ count,
-                    int *__restrict__ seg, int *__restrict__ pos, int *__restrict__ row_token,
-                    int *__restrict__ row_slot) {
-    __shared__ int wcnt[kSingleWarps][kMaxExperts];
-    __shared__ int segs[kMaxExperts + 1];
-    __shared__ int tot[kMaxExperts];
-    griddep_enter();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kSingleWarps * experts; i += kSingleThreads) wcnt[i / experts][i % experts] = 0;
-    __syncthreads();
-    const int64_t per = ((n + kSingleWarps - 1) / kSingleWarps + 31) / 32 * 32;
-    const int64_t w0 = wid * per;
-    const unsigned lt = (1u << lane) - 1u;
-    // a warp's ids come in batches of kIdBatch groups of 32, all loads of a batch
-    // in flight together
-    auto load_ids = [&](int64_t g0, int (&ev)[kIdBatch]) {
-#pragma unroll
-        for (int b = 0; b < kIdBatch; ++b) {
-            const int64_t i = w0 + g0 + 32 * b + lane;
-            const int e = (g0 + 32 * b < per && i < n) ? idx[i] : -1;
-            ev[b] = (e < 0 || e >= experts) ? -1 : e;
-        }
-    };
-    for (int64_t g0 = 0; g0 < per; g0 += 32 * kIdBatch) {
-        int ev[kIdBatch];
-        load_ids(g0, ev);
-#pragma unroll
-        for (int b = 0; b < kIdBatch; ++b)
-            if (ev[b] >= 0) atomicAdd(&wcnt[wid][ev[b]], 1);  // counts need no order
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < experts; e += kSingleThreads) {
-        int run = 0;
-        for (int w = 0; w < kSingleWarps; ++w) {
-            const int c = wcnt[w][e];
-            wcnt[w][e] = run;
-            run += c;
-        }
-        tot[e] = run;
-        count[e] = run;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int off = 0;
-        for (int e = 0; e < experts; ++e) {
-            segs[e] = off;
-            seg[e] = off;
-            off += (tot[e] + kSegPad - 1) / kSegPad * kSegPad;
-        }
-        segs[experts] = off;
-        seg[experts] = off;
-    }
-    __syncthreads();
-    for (int64_t g0 = 0; g0 < per; g0 += 32 * kIdBatch) {
-        int ev[kIdBatch];
-        load_ids(g0, ev);
-#pragma unroll
-        for (int b = 0; b < kIdBatch; ++b) {
-            if (g0 + 32 * b >= per) break;
-            const int64_t i = w0 + g0 + 32 * b + lane;
-            const int e = ev[b];
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            const int base = e >= 0 ? wcnt[wid][e] : 0;
-            __syncwarp();
-            if (e >= 0 && (peers & lt) == 0) wcnt[wid][e] = base + __popc(peers);
-            __syncwarp();
-            if (i < n) {
-                if (e < 0) {
-                    pos[i] = -1;
-                } else {
-                    const int p = segs[e] + base + __popc(peers & lt);
-                    const int ii = static_cast<int>(i);  // below kSingleMax: 32-bit division
-                    pos[i] = p;
-                    row_token[p] = ii / k;
-                    row_slot[p] = ii - (ii / k) * k;
-                }
-            }
-        }
-    }
-    for (int q = threadIdx.x; q < experts * kSegPad; q += kSingleThreads) {
-        const int e = q / kSegPad;
-        const int r = segs[e] + tot[e] + q % kSegPad;
+        const int r = segs[e] + tot[e] + static_cast<int>(q % kSegPad);
         if (r < segs[e + 1]) {
             row_token[r] = -1;
             row_slot[r] = 0;
@@ -372,23 +277,15 @@ unsigned grid_items(int64_t items, int per_block) {
 
 }  // namespace
 
-int moe_route_launches(int64_t n) { return n <= kMoeRouteSingleMax ? 1 : 3; }
-
-int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *chunk_base,
-                     int *count, int *seg, int *pos, int *row_token, int *row_slot, int step, cudaStream_t s) {
+int launch_moe_route(const int *idx, int64_t n, int k, int experts, int *chunk_count, int *count, int *seg,
+                     int *pos, int *row_token, int *row_slot, int step, cudaStream_t s) {
     const int chunks = static_cast<int>(moe_route_chunks(n));
     if (experts > kMaxExperts) return MLPBLK_EINVAL;
-    if (n <= kMoeRouteSingleMax)
-        return launch_pdl(route_single_kernel, dim3(1), dim3(kSingleThreads), 0, s, idx, n, k, experts, count, seg,
-                          pos, row_token, row_slot);
     if (step == 0)
         return launch_pdl(route_count_kernel, dim3(static_cast<unsigned>(chunks)), dim3(kRouteThreads), 0, s, idx,
                           n, experts, chunk_count);
-    if (step == 1)
-        return launch_pdl(route_scan_kernel, dim3(1), dim3(kRouteThreads), 0, s, chunk_count, chunks, experts,
-                          chunk_base, count, seg);
     return launch_pdl(route_place_kernel, dim3(static_cast<unsigned>(chunks)), dim3(kRouteThreads), 0, s, idx, n,
-                      k, experts, chunk_base, count, seg, pos, row_token, row_slot);
+                      k, experts, chunks, chunk_count, count, seg, pos, row_token, row_slot);
 }
 
 int launch_moe_gather(const void *x, const float *rstd, const int *row_token, const int *seg, int experts,

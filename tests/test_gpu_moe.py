@@ -75,7 +75,7 @@ def _check(got, ref, skip_dp=None):
     (64, 64, 128, 8, 1),       # top-1, some experts get no token
     (1, 256, 512, 2, 2),       # a single token in two experts
     (520, 520, 520, 5, 3),     # top-3
-    (33000, 64, 128, 4, 2),    # over 65536 (token, slot) entries: routing in three launches
+    (33000, 64, 128, 4, 2),    # 66000 (token, slot) entries: 65 routing chunks
     # d a multiple of 256: the RMSNorm backward gathers the slot rows by bulk copies
     (300, 256, 256, 4, 3),
     (257, 512, 256, 6, 4),
