@@ -819,7 +819,7 @@ struct MoeLayout {
     // saved
     int64_t rstd, pos, row_token, row_slot, seg, count, chunk_count, rstd_perm, x_perm, h_perm, a_perm, o_perm, saved;
     // workspace
-    int64_t w1g, do_perm, dh_perm, dn_perm, part, ws;
+    int64_t w1g, do_perm, dh_perm, dn_perm, part, sk_partial, sk_flags, ws;
 };
 
 int check_moe_desc(const mlpblk_moe_desc *m) {
@@ -865,7 +865,12 @@ MoeLayout moe_layout(const mlpblk_moe_desc *m) {
     l.dh_perm = take(l.R * F * 2);
     l.dn_perm = take(l.R * d * 4);
     l.part = take(static_cast<int64_t>(kMaxParts) * d * 4);
-    l.ws = off > w1g ? off : w1g;
+    // the M-grouped GEMMs' split schedule: partial sums and flags, apart from the
+    // forward's W1*gamma (both live in the forward)
+    off = off > w1g ? off : w1g;
+    l.sk_partial = take(static_cast<int64_t>(kMaxSkSlots) * kSkSlotFloats * 4);
+    l.sk_flags = take(static_cast<int64_t>(kSkSets) * kSkFlagsPerSet * 4);
+    l.ws = off;
     return l;
 }
 
@@ -912,9 +917,13 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     float *rstd_perm = reinterpret_cast<float *>(sv + l.rstd_perm);
     void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
     void *w1g = ws + l.w1g;
-    // rstd and every expert's W1 * gamma (the experts' W1 as one [E*F, d] matrix)
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
+    // rstd and every expert's W1 * gamma (the experts' W1 as one [E*F, d] matrix);
+    // clears the W1 GEMM's flags
     MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
-                  launch_norm_prep(MLPBLK_BF16, x, rstd, T, d, desc->base.eps, w1s, gamma, w1g, E * F, nullptr, 0, s));
+                  launch_norm_prep(MLPBLK_BF16, x, rstd, T, d, desc->base.eps, w1s, gamma, w1g, E * F,
+                                   sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
     for (int step = 0; step < kMoeRouteLaunches; ++step)
         MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_ROUTE, s,
                       launch_moe_route(expert_idx, T * k, k, E, chunk_count, count, seg, pos, row_token, row_slot,
@@ -927,6 +936,9 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     g1.grp_count = E;
     g1.grp_rows = seg;
     g1.grp_b_off = static_cast<int>(F);
+    g1.sk_partial = sk_partial;
+    g1.sk_flags = sk_flags + kSetFwdW1 * kSkFlagsPerSet;
+    g1.zero_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W1, s,
                   launch_gemm_tc_fwd(kEpiFwdW1Pre, (int)l.R, (int)F, (int)d, x_perm, w1g, h_perm, a_perm, g1, sms, s));
     GemmArgs g2 = {};
@@ -934,6 +946,8 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     g2.grp_count = E;
     g2.grp_rows = seg;
     g2.grp_b_off = static_cast<int>(d);
+    g2.sk_partial = sk_partial;
+    g2.sk_flags = sk_flags + kSetFwdW2 * kSkFlagsPerSet;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_FWD_W2, s,
                   launch_gemm_tc_fwd(kEpiStoreBf16, (int)l.R, (int)d, (int)F, a_perm, w2s, o_perm, nullptr, g2, sms, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_COMBINE, s, launch_moe_combine(x, o_perm, routing_weights, pos, T, k, d, y, s));
@@ -969,6 +983,8 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     void *do_perm = ws + l.do_perm, *dh_perm = ws + l.dh_perm;
     float *dn_perm = reinterpret_cast<float *>(ws + l.dn_perm);
     float *part = reinterpret_cast<float *>(ws + l.part);
+    float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
+    int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
     int parts = 0;
     // d_routing_weights and each slot's output gradient p * dy in segment order
     MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_DP, s,
@@ -979,6 +995,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gw2.grp_count = E;
     gw2.grp_rows = seg;
     gw2.grp_c_off = static_cast<int>(d);
+    gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
                   launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)l.R, do_perm, a_perm, dw2s, nullptr, gw2, sms, s));
     GemmArgs gd = {};
@@ -989,6 +1006,9 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gd.grp_count = E;
     gd.grp_rows = seg;
     gd.grp_b_off = static_cast<int>(d);
+    gd.sk_partial = sk_partial;
+    gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    gd.zero_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
                   launch_gemm_tc_bwd(kEpiDgradH, (int)l.R, (int)F, (int)d, do_perm, w2s, dh_perm, nullptr, gd, sms, s));
     GemmArgs gn = {};
@@ -996,6 +1016,8 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gn.grp_count = E;
     gn.grp_rows = seg;
     gn.grp_b_off = static_cast<int>(F);
+    gn.sk_partial = sk_partial;
+    gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
                   launch_gemm_tc_bwd(kEpiStoreF32, (int)l.R, (int)d, (int)F, dh_perm, w1s, dn_perm, nullptr, gn, sms, s));
     GemmArgs gw1 = {};

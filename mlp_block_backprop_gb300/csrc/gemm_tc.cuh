@@ -138,7 +138,12 @@ __device__ __forceinline__ int sk_begin(const GemmArgs &a, int w) {
 //     rows and write the expert's block of C; experts without tokens are skipped.
 struct SegIter {
     int worker, j, n_dp, pos, end, m_tiles;
+    int dp_tiles, sk_base, sk_rem, sk_total;  // the schedule (device-computed when M-grouped and split)
 };
+
+__device__ __forceinline__ int sk_begin(const SegIter &it, int w) {
+    return min(w * it.sk_base + min(w, it.sk_rem), it.sk_total);
+}
 
 template <int TILE_M>
 __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
@@ -146,6 +151,30 @@ __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
     it.worker = worker;
     it.j = 0;
     it.m_tiles = a.m_tiles;
+    it.dp_tiles = a.dp_tiles;
+    it.sk_base = a.sk_base;
+    it.sk_rem = a.sk_rem;
+    it.sk_total = a.sk_total;
+    if (a.grp_mode == kGroupM && a.grp_split) {
+        // M-grouped with the split schedule: the host's rule (whole-tile rounds
+        // while more than two remain, then the k-blocks split evenly) applied to
+        // the tile count the routing left in device memory
+        it.m_tiles = a.grp_rows[a.grp_count] / TILE_M;
+        const int tiles = it.m_tiles * a.n_tiles;
+        const int full = tiles / a.workers;
+        if (tiles % a.workers == 0) {
+            it.dp_tiles = tiles;
+        } else {
+            it.dp_tiles = full >= 2 ? (full - 1) * a.workers : 0;
+        }
+        it.sk_total = (tiles - it.dp_tiles) * a.k_blocks;
+        it.sk_base = it.sk_total / a.workers;
+        it.sk_rem = it.sk_total % a.workers;
+        it.n_dp = it.dp_tiles / a.workers;
+        it.pos = sk_begin(it, worker);
+        it.end = sk_begin(it, worker + 1);
+        return it;
+    }
     if (a.grp_mode != kGroupNone) {
         if (a.grp_mode == kGroupM) it.m_tiles = a.grp_rows[a.grp_count] / TILE_M;
         const int total = (a.grp_mode == kGroupM ? it.m_tiles : a.grp_count * a.m_tiles) * a.n_tiles;
@@ -175,7 +204,7 @@ __device__ __forceinline__ bool seg_next(const GemmArgs &a, SegIter &it, Seg &s)
             s.kb0 = it.pos - tt * a.k_blocks;
             s.kb1 = min(a.k_blocks, s.kb0 + (it.end - it.pos));
             it.pos += s.kb1 - s.kb0;
-            t = a.dp_tiles + tt;
+            t = it.dp_tiles + tt;
         } else {
             return false;
         }
@@ -484,8 +513,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // a split tile's contributors: the next workers whose ranges start in it
             int cw_end = worker + 1;
             if (fixup) {
-                const int tile_end = (w.tile - args.dp_tiles + 1) * args.k_blocks;
-                while (cw_end < args.workers && sk_begin(args, cw_end) < tile_end) ++cw_end;
+                const int tile_end = (w.tile - si.dp_tiles + 1) * args.k_blocks;
+                while (cw_end < args.workers && sk_begin(si, cw_end) < tile_end) ++cw_end;
                 for (int cw = worker + 1; cw < cw_end && ok; ++cw)
                     ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * 4 + q],
                                    abort_flag);
@@ -815,15 +844,17 @@ inline bool make_map_2d(CUtensorMap *m, const void *ptr, int type, uint64_t inne
     return r == CUDA_SUCCESS;
 }
 
-// Stream-K scheduling is used unless MLPBLK_STREAMK=0 (whole tiles only).
-inline bool streamk_enabled() {
+// Stream-K scheduling is used unless MLPBLK_STREAMK=0 (whole tiles only);
+// MLPBLK_STREAMK=2 takes it wherever the tiles do not fill whole rounds.
+inline int streamk_mode() {
     static int v = -1;
     if (v < 0) {
         const char *e = getenv("MLPBLK_STREAMK");
-        v = (e && e[0] == '0') ? 0 : 1;
+        v = (e && e[0] == '0') ? 0 : ((e && e[0] == '2') ? 2 : 1);
     }
-    return v == 1;
+    return v;
 }
+inline bool streamk_enabled() { return streamk_mode() != 0; }
 
 // M tiles per raster group: MLPBLK_GROUP_M (1..64) when set, else 16.
 inline int raster_group_m() {
@@ -879,11 +910,17 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = raster_group_m();
     int workers = slots;
-    const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode == kGroupNone && streamk_enabled() &&
+    const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode != kGroupK && streamk_enabled() &&
                     (C::kReduce || (a.sk_partial && a.sk_flags));
-    if (a.grp_mode != kGroupNone) {
+    if (a.grp_mode == kGroupM && sk && !a.whole_tiles) {
+        // M-grouped, split schedule: computed in the kernel from the device row count
+        a.grp_split = 1;
+        a.dp_tiles = 0;
+        a.sk_base = a.sk_rem = a.sk_total = 0;
+    } else if (a.grp_mode != kGroupNone) {
         // grouped: whole tiles dealt round robin over a count the kernel reads
         // from device memory (M-grouped) or over every expert's tiles (K-grouped)
+        a.grp_split = 0;
         const int64_t upper = a.grp_mode == kGroupK ? static_cast<int64_t>(tiles) * a.grp_count : tiles;
         if (upper < workers) workers = static_cast<int>(upper > 0 ? upper : 1);
         a.dp_tiles = 0;
@@ -1011,7 +1048,7 @@ inline int choose_tile(int M, int N, int K, bool sk_allowed, bool reduce, int nu
         if (operand_bytes > kL2Budget)
             fix += 0.3 * static_cast<double>(split_tiles * kb) / workers * unit;
         const double sk = static_cast<double>(per) * unit + fix;
-        if (sk < best) {
+        if (sk < best || (streamk_mode() == 2 && (mode == choice || forced >= 0))) {
             best = sk;
             choice = mode | kUseStreamK;
         }

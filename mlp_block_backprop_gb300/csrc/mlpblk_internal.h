@@ -116,6 +116,8 @@ struct GemmArgs {
     const int *grp_rows;       // device [grp_count + 1]: padded segment starts (rows)
     int grp_b_off;             // M-grouped: per-expert offset into B (rows or K)
     int grp_c_off;             // K-grouped: per-expert rows of C
+    int grp_split;             // M-grouped: split schedule computed in the kernel from
+                               // the device row count (host-side: set by the launcher)
     const uint16_t *aux;       // bf16 [M, ld_aux]: x (FwdW2) or h (DgradH)
     int ld_aux;
     const float *rstd_in;      // DgradH: per-row rstd
