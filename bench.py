@@ -473,18 +473,30 @@ def run_ours(args, dist, peaks):
                          "d2h_bytes_per_step": n_mb * T * d * elt,
                          "path": "pinned host x, dy -> device; mlpblk_forward/backward; dx -> pinned host "
                                  "(copies on a second stream, double-buffered: the next step's inputs "
-                                 "and this step's dx move while the GPU computes)"}
+                                 "and this step's dx move while the GPU computes; each buffer set's step "
+                                 "of public calls captured once as a CUDA graph and replayed)"}
     return result, inp
 
 
-def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of):
+def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_graphs=True):
     """Times k steps end to end: every step's inputs go host -> device and its
     outputs device -> host inside the timed region, on a copy stream, into two
     alternating device buffer sets, so step s+1's inputs and step s's outputs
     move while step s computes.  `compute(set, after_mb)` enqueues one step on the
     current stream (calling after_mb(i) once microbatch i's output is written);
-    `out_of(set, i)` is that output.  Returns (device ms, wall seconds)."""
+    `out_of(set, i)` is that output.  With use_graphs, each set's step (the same
+    public calls) is captured once as a CUDA graph and replayed, and the outputs
+    leave after the step.  Returns (device ms, wall seconds)."""
     import torch
+    graphs = None
+    if use_graphs:
+        graphs = []
+        for st in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                compute(sets[st], None)
+            graphs.append(g)
+        torch.cuda.synchronize()
     main = torch.cuda.current_stream()
     cs = torch.cuda.Stream()
     in_ev = [torch.cuda.Event() for _ in range(2)]
@@ -520,7 +532,16 @@ def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of):
             with torch.cuda.stream(cs):
                 host_out[i].copy_(out_of(sets[st], i), non_blocking=True)
 
-        compute(sets[st], after)
+        if graphs is not None:
+            graphs[st].replay()
+            ev = torch.cuda.Event()
+            ev.record(main)
+            cs.wait_event(ev)
+            with torch.cuda.stream(cs):
+                for i in range(len(host_out)):
+                    host_out[i].copy_(out_of(sets[st], i), non_blocking=True)
+        else:
+            compute(sets[st], after)
         free_ev[st].record(main)
         out_ev[st].record(cs)
     main.wait_stream(cs)
@@ -619,8 +640,9 @@ def run_moe(args, dist, peaks):
         bb.dy, bb.p = st[1]
         bb.dx, bb.dp = st[2]
         step()
-        after(0)
-        after(1)
+        if after is not None:
+            after(0)
+            after(1)
 
     pipelined_e2e(1, sets, [hx, hidx], [hdy, hp], [hdx, hdp], moe_compute, lambda st, i: st[2][i])
     ms_dev, wall = pipelined_e2e(k_e2e, sets, [hx, hidx], [hdy, hp], [hdx, hdp], moe_compute,
