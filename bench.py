@@ -480,7 +480,8 @@ def run_ours(args, dist, peaks):
 
 def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_graphs=True):
     """Times k steps end to end: every step's inputs go host -> device and its
-    outputs device -> host inside the timed region, on a copy stream, into two
+    outputs device -> host inside the timed region, on two copy streams (one per
+    direction), into two
     alternating device buffer sets, so step s+1's inputs and step s's outputs
     move while step s computes.  `compute(set, after_mb)` enqueues one step on the
     current stream (calling after_mb(i) once microbatch i's output is written);
@@ -498,7 +499,8 @@ def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_gra
             graphs.append(g)
         torch.cuda.synchronize()
     main = torch.cuda.current_stream()
-    cs = torch.cuda.Stream()
+    cs = torch.cuda.Stream()   # host -> device
+    co = torch.cuda.Stream()   # device -> host (the two directions overlap)
     in_ev = [torch.cuda.Event() for _ in range(2)]
     free_ev = [torch.cuda.Event() for _ in range(2)]
     out_ev = [torch.cuda.Event() for _ in range(2)]
@@ -528,23 +530,24 @@ def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_gra
         def after(i, st=st):
             ev = torch.cuda.Event()
             ev.record(main)
-            cs.wait_event(ev)
-            with torch.cuda.stream(cs):
+            co.wait_event(ev)
+            with torch.cuda.stream(co):
                 host_out[i].copy_(out_of(sets[st], i), non_blocking=True)
 
         if graphs is not None:
             graphs[st].replay()
             ev = torch.cuda.Event()
             ev.record(main)
-            cs.wait_event(ev)
-            with torch.cuda.stream(cs):
+            co.wait_event(ev)
+            with torch.cuda.stream(co):
                 for i in range(len(host_out)):
                     host_out[i].copy_(out_of(sets[st], i), non_blocking=True)
         else:
             compute(sets[st], after)
         free_ev[st].record(main)
-        out_ev[st].record(cs)
+        out_ev[st].record(co)
     main.wait_stream(cs)
+    main.wait_stream(co)
     end.record(main)
     torch.cuda.synchronize()
     return start.elapsed_time(end), time.perf_counter() - t0
