@@ -100,7 +100,7 @@ struct WsLayoutF8 {
 };
 
 constexpr int kAmaxParts = 2048;
-static_assert(kAmaxParts >= kMaxSkSlots * 4, "the GEMM epilogues' maxima fit the amax scratch");
+static_assert(kAmaxParts >= kMaxSkSlots * kMaxEpiWarps, "the GEMM epilogues' maxima fit the amax scratch");
 
 WsLayoutF8 ws_layout_f8(const mlpblk_desc *dsc) {
     const int64_t T = dsc->tokens, d = dsc->d_model, F = dsc->ffn;
@@ -602,7 +602,7 @@ int forward_fp8_impl(const mlpblk_desc *desc, const void *x, const F8Weights &w,
                   launch_gemm_tc_f8(kEpiFwdW1Pre, (int)T, (int)F, (int)d, n8_saved, w.w1g, h_saved, a16, g1, sms, s));
     // a in E4M3 (saved with its scale record; clears the W2 GEMM's flags)
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, kMaxSkSlots * 4, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet,
+                  launch_scale_e4m3(amax, kMaxSkSlots * kMaxEpiWarps, scales_saved, sk_flags + kSetFwdW2 * kSkFlagsPerSet,
                                     kSkFlagsPerSet, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s,
                   launch_apply_e4m3(a16, nullptr, F, T * F, scales_saved, static_cast<uint8_t *>(a8_saved), s));
@@ -654,7 +654,7 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
                   launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w.w2, dh16, nullptr, gd, sms, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
-                  launch_scale_e4m3(amax, kMaxSkSlots * 4, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet,
+                  launch_scale_e4m3(amax, kMaxSkSlots * kMaxEpiWarps, sc + 12, sk_flags + kSetDgradN * kSkFlagsPerSet,
                                     kSkFlagsPerSet, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_APPLY, s, launch_apply_e4m3(dh16, nullptr, F, T * F, sc + 12, dh8, s));
     // dn_s = rstd * (dh . W1) * s_dh * s_w1   (fp32)

@@ -12,6 +12,8 @@
 //   warp 0      TMA producer: A/B tiles -> shared-memory ring of kStages stages
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
+//               (warps 2..9 for the residual and gate epilogues: two warps per
+//               TMEM lane quarter, each taking half of a tile's columns)
 //   warps 6..9  (the in-GEMM RMSNorm variant of the forward W1 GEMM only) sum of
 //               x^2 per row, read from each A stage once its MMAs have completed
 //               (then the stage goes back to the producer), gives rstd for the
@@ -71,7 +73,11 @@ struct GemmCfg {
     static constexpr int kNumOut = (kReluSq && !kAOnly) ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
-    static constexpr int kThreads = kNorm ? 320 : 192;
+    // epilogue warps: one per TMEM lane quarter, or two (each draining half of a
+    // tile's columns) for the epilogues that also read an [M][N] bf16 operand, whose
+    // per-element work is the largest (the other epilogues measured no faster so)
+    static constexpr int kEpiWarps = (EPI == kEpiFwdW2 || EPI == kEpiDgradH) ? 8 : 4;
+    static constexpr int kThreads = kNorm ? 320 : 64 + 32 * kEpiWarps;
     static constexpr int kABytes = kBM * 128;
     static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -83,7 +89,7 @@ struct GemmCfg {
     // output staging per epilogue warp and output: double buffered, except for
     // the two-output W1 epilogue, whose shared memory goes to a deeper pipeline
     static constexpr int kStagingBufs = kNumOut == 2 ? 1 : 2;
-    static constexpr int kStagingBytes = kAux ? 0 : 4 * kNumOut * kStagingBufs * 4096;
+    static constexpr int kStagingBytes = kAux ? 0 : kEpiWarps * kNumOut * kStagingBufs * 4096;
     // per-row scale read from args.rstd_in (1 when that is null)
     static constexpr bool kRowScale =
         (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A || EPI == kEpiStoreF32);
@@ -264,7 +270,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t *aux_bar = acce_bar + 2;  // one per epilogue warp
     // in-GEMM RMSNorm: stage s's MMAs have completed, so its x tile may be read
     // by the norm warps (who then release the stage to the producer)
-    uint64_t *consumed_bar = aux_bar + 4;
+    uint64_t *consumed_bar = aux_bar + kMaxEpiWarps;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + 516);
     float *rs = reinterpret_cast<float *>(ctrl + 1024);  // [2][128], forward W1 only
@@ -287,9 +293,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1 + kNormArrivals);
             // the leader's MMA reuses a TMEM buffer once both CTAs' epilogues drained it
-            mbar_init(&acce_bar[b], (C::PAIR && leader) ? 8 : 4);
+            mbar_init(&acce_bar[b], (C::PAIR && leader) ? 2 * C::kEpiWarps : C::kEpiWarps);
         }
-        for (int w = 0; w < 4; ++w) mbar_init(&aux_bar[w], 1);
+        for (int w = 0; w < C::kEpiWarps; ++w) mbar_init(&aux_bar[w], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -442,9 +448,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 2 + C::kEpiWarps) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;                // TMEM lane quarter of this warp
+        const int ew = warp - 2;               // epilogue warp index
+        // this warp's chunks of a tile: all of them, or its half of them
+        const int c_lo = C::kEpiWarps == 8 ? ((ew >> 2) * C::kNumChunks) / 2 : 0;
+        const int c_hi = C::kEpiWarps == 8 ? (((ew >> 2) + 1) * C::kNumChunks) / 2 : C::kNumChunks;
         const int row_in_tile = 32 * q + lane;
         const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
         uint8_t *aux_w = aux_smem + q * C::kNumChunks * 4096;  // this warp's 32 rows
@@ -469,12 +479,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 rsc_next = args.rstd_in ? ((r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f) : 1.0f;
             if (C::kAux && wn.kb0 == 0 && lane == 0) {
                 int nch = 0;
-                for (int c = 0; c < C::kNumChunks; ++c)
+                for (int c = c_lo; c < c_hi; ++c)
                     if (wn.n0 + c * C::kChunkCols < args.N) ++nch;
-                mbar_arrive_expect_tx(&aux_bar[q], nch * 4096);
+                mbar_arrive_expect_tx(&aux_bar[ew], nch * 4096);
                 aux_pending = true;
-                for (int c = 0; c < nch; ++c)
-                    tma_load_2d(&tmAux, &aux_bar[q], aux_w + c * 4096, wn.n0 + c * C::kChunkCols, r0);
+                for (int c = c_lo; c < c_lo + nch; ++c)
+                    tma_load_2d(&tmAux, &aux_bar[ew], aux_w + c * 4096, wn.n0 + c * C::kChunkCols, r0);
             }
         };
         int it = 0;
@@ -504,7 +514,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
             bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
             if (C::kAux && head && ok) {
-                ok = mbar_wait(&aux_bar[q], aux_phase, abort_flag);
+                ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
                 if (ok) {
                     aux_pending = false;
                     aux_phase ^= 1u;
@@ -516,20 +526,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int tile_end = (w.tile - si.dp_tiles + 1) * args.k_blocks;
                 while (cw_end < args.workers && sk_begin(si, cw_end) < tile_end) ++cw_end;
                 for (int cw = worker + 1; cw < cw_end && ok; ++cw)
-                    ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * 4 + q],
+                    ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * kMaxEpiWarps + ew],
                                    abort_flag);
-                // The first contributor's partial (this warp's kUnits x 4 KB) comes
+                // The first contributor's partial (this warp's units, 4 KB each) comes
                 // into the pipeline stages with one bulk copy: this is the worker's
                 // last segment, and its MMAs, which read the stages, have completed.
+                constexpr int kCU = C::kChunkCols / 32;
+                const int u_lo = c_lo * kCU, nu = (c_hi - c_lo) * kCU;
                 if (ok && lane == 0) {
                     fence_proxy_async_global();
-                    mbar_arrive_expect_tx(&aux_bar[q], kUnits * 4096);
-                    bulk_copy_g2s(stages + q * kUnits * 4096,
-                                  part_ptr((worker + 1) * kSlotsPerWorker + static_cast<int>(rank), 0, 0) - lane * 4,
-                                  kUnits * 4096, &aux_bar[q]);
+                    mbar_arrive_expect_tx(&aux_bar[ew], nu * 4096);
+                    bulk_copy_g2s(stages + (q * kUnits + u_lo) * 4096,
+                                  part_ptr((worker + 1) * kSlotsPerWorker + static_cast<int>(rank), u_lo, 0) - lane * 4,
+                                  nu * 4096, &aux_bar[ew]);
                 }
                 if (ok) {
-                    ok = mbar_wait(&aux_bar[q], aux_phase, abort_flag);
+                    ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
                     if (ok) aux_phase ^= 1u;
                 }
             }
@@ -542,7 +554,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
 
 #pragma unroll 1
-            for (int c = 0; c < C::kNumChunks; ++c) {
+            for (int c = c_lo; c < c_hi; ++c) {
                 const int col0 = w.n0 + c * C::kChunkCols;
                 if (col0 >= args.N) break;
                 constexpr int kChunkUnits = C::kChunkCols / 32;
@@ -625,9 +637,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                 }
                 uint8_t *st0 = C::kAux ? aux_w + c * 4096
-                                       : staging + ((q * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
+                                       : staging + ((ew * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
                 uint8_t *st1 = C::kAux ? st0
-                                       : staging + ((q * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
+                                       : staging + ((ew * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
                 const uint32_t s0 = smem_u32(st0) + lane * 128;
                 const uint32_t s1 = smem_u32(st1) + lane * 128;
                 const uint32_t sw = static_cast<uint32_t>(lane & 7);
@@ -727,7 +739,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // the TMEM release, so the main loop does not wait for the stores)
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(&args.sk_flags[slot * 4 + q], 1);
+                if (lane == 0) st_release_gpu(&args.sk_flags[slot * kMaxEpiWarps + ew], 1);
             }
             // every lane is done with this segment's shared operand copy
             have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
@@ -735,16 +747,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (lane == 0) {
             bulk_wait_group<0>();
-            if (C::kAux && aux_pending) mbar_drain(&aux_bar[q], aux_phase);
+            if (C::kAux && aux_pending) mbar_drain(&aux_bar[ew], aux_phase);
         }
         if (want_amax) {
             // one maximum per epilogue warp; CTA 0 zeroes the slots no CTA holds
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax_t = fmaxf(amax_t, __shfl_xor_sync(0xffffffffu, amax_t, o));
-            if (lane == 0) args.amax_out[slot * 4 + q] = amax_t;
-            if (blockIdx.x == 0)
-                for (int i = static_cast<int>(gridDim.x) * 4 + q * 32 + lane; i < kMaxSkSlots * 4; i += 128)
-                    args.amax_out[i] = 0.0f;
+            if (lane == 0) args.amax_out[slot * kMaxEpiWarps + ew] = amax_t;
+            if (blockIdx.x == 0) {
+                // every slot no epilogue warp writes: the unused warps of each CTA and the CTAs not launched
+                for (int i = ew * 32 + lane; i < kMaxSkSlots * kMaxEpiWarps; i += C::kEpiWarps * 32)
+                    if (i >= static_cast<int>(gridDim.x) * kMaxEpiWarps || i % kMaxEpiWarps >= C::kEpiWarps)
+                        args.amax_out[i] = 0.0f;
+            }
         }
         __syncwarp();
     } else if (C::kNorm) {

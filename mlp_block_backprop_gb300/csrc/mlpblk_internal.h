@@ -90,7 +90,8 @@ enum Epilogue : int {
 // slot one flag word per epilogue warp.
 constexpr int kMaxSkSlots = 160;
 constexpr int kSkSlotFloats = 128 * 256;
-constexpr int kSkFlagsPerSet = kMaxSkSlots * 4;
+constexpr int kMaxEpiWarps = 8;                    // epilogue warps of a GEMM CTA, at most
+constexpr int kSkFlagsPerSet = kMaxSkSlots * kMaxEpiWarps;  // one flag per slot and epilogue warp
 
 enum GroupMode : int { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
 
@@ -110,7 +111,7 @@ struct GemmArgs {
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
     float *amax_out;           // W1 (a) and dgrad-h (dh) epilogues: max |bf16 output| per
-                               // epilogue warp, kMaxSkSlots * 4 floats (unused slots 0)
+                               // epilogue warp, kMaxSkSlots * kMaxEpiWarps floats (unused 0)
     // grouped GEMMs of the routed experts (kGroupNone otherwise)
     int grp_mode, grp_count;   // kGroupM / kGroupK; number of experts
     const int *grp_rows;       // device [grp_count + 1]: padded segment starts (rows)
