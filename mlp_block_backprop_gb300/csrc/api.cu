@@ -307,9 +307,14 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     int parts = 0;  // dgamma partial rows written by the norm kernel
     if (desc->dtype == MLPBLK_BF16) {
-        // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's
+        // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's.  The two
+        // independent pairs (dW2, dh) and (dn, dW1) overlap at their boundary:
+        // the second of each starts on the SMs the first frees without waiting
+        // for all of it (kPdlDeferWait), which the first allows by launching it
+        // only after its own predecessor has completed (kPdlWaitFirst)
         GemmArgs gw2 = {};
         gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+        gw2.pdl = kPdlWaitFirst;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
         GemmArgs gd = {};
         gd.aux = static_cast<const uint16_t *>(h_saved);
@@ -318,13 +323,16 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         gd.sk_partial = sk_partial;
         gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
         gd.zero_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+        gd.pdl = kPdlDeferWait;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
         GemmArgs gn = {};
         gn.sk_partial = sk_partial;
         gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+        gn.pdl = kPdlWaitFirst;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);
+        gw1.pdl = kPdlDeferWait;
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
     } else {
         const float *dyf = static_cast<const float *>(dy);
@@ -639,6 +647,7 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     gw2.deq_a = sc + 8 + 2;
     gw2.deq_b = scales_saved + 2;
     gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    gw2.pdl = kPdlWaitFirst;  // (dW2, dh) and (dn, dW1) overlap as in the bf16 backward
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
                   launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
     // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
@@ -651,6 +660,7 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     gd.sk_partial = sk_partial;
     gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
     gd.amax_out = amax;
+    gd.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
                   launch_gemm_tc_f8(kEpiDgradH, (int)T, (int)F, (int)d, dyq, w.w2, dh16, nullptr, gd, sms, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_QUANT_SCALE, s,
@@ -664,12 +674,14 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     gn.deq_b = w.s_w1 + 2;
     gn.sk_partial = sk_partial;
     gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+    gn.pdl = kPdlWaitFirst;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
                   launch_gemm_tc_f8(kEpiStoreF32, (int)T, (int)d, (int)F, dh8, w.w1, dn_s, nullptr, gn, sms, s));
     // dW1 += gamma[col] * (dh^T . n') * s_dh
     GemmArgs gw1 = {};
     gw1.colscale = static_cast<const uint16_t *>(gamma);
     gw1.deq_a = sc + 12 + 2;
+    gw1.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
                                     sms, s));
@@ -996,6 +1008,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gw2.grp_rows = seg;
     gw2.grp_c_off = static_cast<int>(d);
     gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
+    gw2.pdl = kPdlWaitFirst;  // (dW2, dh) and (dn, dW1) overlap as in the dense backward
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
                   launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)l.R, do_perm, a_perm, dw2s, nullptr, gw2, sms, s));
     GemmArgs gd = {};
@@ -1009,6 +1022,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gd.sk_partial = sk_partial;
     gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
     gd.zero_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+    gd.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s,
                   launch_gemm_tc_bwd(kEpiDgradH, (int)l.R, (int)F, (int)d, do_perm, w2s, dh_perm, nullptr, gd, sms, s));
     GemmArgs gn = {};
@@ -1018,6 +1032,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gn.grp_b_off = static_cast<int>(F);
     gn.sk_partial = sk_partial;
     gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+    gn.pdl = kPdlWaitFirst;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
                   launch_gemm_tc_bwd(kEpiStoreF32, (int)l.R, (int)d, (int)F, dh_perm, w1s, dn_perm, nullptr, gn, sms, s));
     GemmArgs gw1 = {};
@@ -1026,6 +1041,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gw1.grp_count = E;
     gw1.grp_rows = seg;
     gw1.grp_c_off = static_cast<int>(F);
+    gw1.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)l.R, dh_perm, x_perm, dw1s, nullptr, gw1,
                                      sms, s));

@@ -321,12 +321,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // set-up above overlaps the previous kernel's tail; operands and outputs
-    // are touched only after it has completed
-    griddep_launch_dependents();
-    griddep_wait();
+    // are touched only after it has completed (a deferred GEMM touches nothing
+    // the previous kernel writes, and waits for it at the end instead)
+    if (args.pdl != kPdlWaitFirst) griddep_launch_dependents();
+    if (args.pdl != kPdlDeferWait) griddep_wait();
     // the next GEMM's stream-K flags start from zero (it runs after this one)
     if (blockIdx.x == 0 && warp == 0 && args.zero_flags)
         for (int i = lane; i < kSkFlagsPerSet; i += 32) args.zero_flags[i] = 0;
+    if (args.pdl == kPdlWaitFirst) {
+        // the successor may start before this kernel ends and not wait for it:
+        // the cleared flags are visible before it can launch
+        __threadfence();
+        __syncthreads();
+        griddep_launch_dependents();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -814,6 +822,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (C::PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
         else tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    // a deferred GEMM completes only after its predecessor has
+    if (args.pdl == kPdlDeferWait) griddep_wait();
 }
 
 // ------------------------------------------------------------------ host side

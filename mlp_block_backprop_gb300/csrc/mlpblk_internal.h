@@ -95,6 +95,17 @@ constexpr int kSkFlagsPerSet = kMaxSkSlots * kMaxEpiWarps;  // one flag per slot
 
 enum GroupMode : int { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
 
+// How a GEMM orders itself against its neighbours in the stream (programmatic
+// dependent launch).  A kernel's completion must imply its predecessor's, so a
+// deferred GEMM waits before it exits, and it follows a kWaitFirst GEMM, whose
+// successor is launched only once everything before that GEMM has completed.
+enum PdlOrder : int {
+    kPdlDefault = 0,    // launch the successor, then wait for the predecessor
+    kPdlWaitFirst = 1,  // wait for the predecessor, clear zero_flags, then launch the successor
+    kPdlDeferWait = 2,  // launch the successor and start at once: reads nothing the
+                        // predecessor writes; waits for it just before exiting
+};
+
 struct GemmArgs {
     int M, N, K;
     int m_tiles, n_tiles, k_blocks;
@@ -127,6 +138,7 @@ struct GemmArgs {
     float inv_k;               // FwdW1: 1/d
     float eps;                 // FwdW1: RMSNorm epsilon
     int skip_loads;            // test fault: the producer issues no loads (waits run out)
+    int pdl;                   // PdlOrder
 };
 
 // Operand / output views handed to the GEMM launcher (row-major 2-D tensors).
