@@ -449,7 +449,7 @@ def run_ours(args, dist, peaks):
     }
 
     if not args.no_e2e:
-        k_e2e = max(3, min(args.steps, 20))
+        k_e2e = max(3, args.steps)  # the same K steps as the device number
         hx = [torch.from_numpy(x).to(dt).pin_memory() for x in inp.x]
         hdy = [torch.from_numpy(g).to(dt).pin_memory() for g in inp.dy]
         hdx = [torch.empty(T, d, dtype=dt).pin_memory() for _ in range(n_mb)]
@@ -634,7 +634,7 @@ def run_moe(args, dist, peaks):
     hp = torch.from_numpy(np.ascontiguousarray(inp.p, dtype=np.float32)).pin_memory()
     hdx = torch.empty(T, d, dtype=bf).pin_memory()
     hdp = torch.empty(T, k, dtype=torch.float32).pin_memory()
-    k_e2e = max(3, min(args.steps, 10))
+    k_e2e = max(3, args.steps)  # the same K steps as the device number
     sets = [([torch.empty_like(bb.x), torch.empty_like(bb.idx)], [torch.empty_like(bb.dy), torch.empty_like(bb.p)],
              [torch.empty_like(bb.dx), torch.empty_like(bb.dp)]) for _ in range(2)]
 

@@ -594,7 +594,6 @@ int forward_fp8_impl(const mlpblk_desc *desc, const void *x, const F8Weights &w,
     float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
     int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
     void *a16 = ws + l.t16;
-    int parts = 0;
     // n' = x * rstd in E4M3 (scale 1) and rstd; clears the W1 GEMM's flags
     MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_QUANT, s,
                   launch_norm_quant(x, rstd_saved, static_cast<uint8_t *>(n8_saved), T, d, desc->eps,
