@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import TOL, compare, gpu_buffers, run_gpu, to_dev, to_np
+from helpers import GRAD_KEYS, OUT_KEYS, TOL, compare, gpu_buffers, run_gpu, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -128,6 +128,51 @@ def test_two_backward_calls_accumulate():
     torch.cuda.synchronize()
     for o, t in zip(once, (bb.dgamma, bb.dw1, bb.dw2)):
         assert oracle.scaled_error(to_np(t), to_np(o)) <= 1e-6
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_interleaved_writers_and_readers(graph):
+    """Stream kernels that write an input just before a call, or read an output
+    just after it, see the call's reads and writes in order: three microbatches
+    with x and dy copied in between the calls and every output copied out right
+    after, eager and as one CUDA graph, match the oracle's accumulation."""
+    import torch
+    inp = synth.make_inputs(tokens=700, d=384, ffn=1032, seed=21, n_mb=3)
+    bb = gpu_buffers(inp)
+    xs = [to_dev(x, bb.dt) for x in inp.x]
+    dys = [to_dev(g, bb.dt) for g in inp.dy]
+    keep = {k: [torch.empty_like(getattr(bb, k)) for _ in inp.x] for k in OUT_KEYS}
+    for k in OUT_KEYS:
+        getattr(bb, k).fill_(3.0)
+
+    def steps():
+        bb.zero_grads()
+        for i in range(len(xs)):
+            bb.x.copy_(xs[i])
+            bb.forward()
+            for k in ("y", "h", "a", "rstd"):
+                keep[k][i].copy_(getattr(bb, k))
+            bb.dy.copy_(dys[i])
+            bb.backward()
+            keep["dx"][i].copy_(bb.dx)
+
+    if graph:
+        steps()  # warm-up outside the capture (tensor maps, attributes)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            steps()
+        for k in OUT_KEYS:
+            for t in keep[k]:
+                t.fill_(5.0)
+        g.replay()
+    else:
+        steps()
+    torch.cuda.synchronize()
+    outs = [{k: to_np(keep[k][i]) for k in OUT_KEYS} for i in range(len(xs))]
+    grads = {k: to_np(getattr(bb, k)) for k in GRAD_KEYS}
+    ref_outs, ref_grads = oracle.run_workload(inp)
+    compare(outs, grads, ref_outs, ref_grads, TOL[inp.dtype])
 
 
 def test_outputs_stay_inside_their_buffers():
