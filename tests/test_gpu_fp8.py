@@ -145,3 +145,52 @@ def test_fp8_prequantised_weights_give_the_same_bits(shape):
         got = to_np(getattr(bb, k))
         np.testing.assert_allclose(got, grads[k], rtol=1e-5, atol=1e-6 * float(np.max(np.abs(grads[k]))),
                                    err_msg=k)
+
+
+def test_fp8_interleaved_writers_and_readers_in_a_graph():
+    """Stream kernels writing x and dy right before the calls and reading the
+    outputs right after, three microbatches captured as one CUDA graph, match the
+    FP8 oracle's accumulation (the backward's GEMM pairs overlap at their launch
+    boundary)."""
+    import torch
+    import mlp_block_backprop_gb300 as mb
+    inp = synth.make_inputs(tokens=640, d=256, ffn=1040, seed=31, n_mb=3)
+    bb = mb.BlockBuffers(inp.tokens, inp.d, inp.ffn, dtype="bf16", eps=inp.eps, fp8=True)
+    bb.gamma.copy_(to_dev(inp.gamma, bb.dt))
+    bb.w1.copy_(to_dev(inp.w1, bb.dt))
+    bb.w2.copy_(to_dev(inp.w2, bb.dt))
+    xs = [to_dev(x, bb.dt) for x in inp.x]
+    dys = [to_dev(g, bb.dt) for g in inp.dy]
+    keys = ("y", "h", "rstd", "dx")
+    keep = {k: [torch.empty_like(getattr(bb, k)) for _ in inp.x] for k in keys}
+
+    def steps():
+        bb.zero_grads()
+        for i in range(len(xs)):
+            bb.x.copy_(xs[i])
+            bb.forward()
+            for k in ("y", "h", "rstd"):
+                keep[k][i].copy_(getattr(bb, k))
+            bb.dy.copy_(dys[i])
+            bb.backward()
+            keep["dx"][i].copy_(bb.dx)
+
+    steps()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        steps()
+    for k in keys:
+        for t in keep[k]:
+            t.fill_(5.0)
+    g.replay()
+    torch.cuda.synchronize()
+    ref_outs, ref_grads = fp8_oracle.run_workload(inp)
+    errs = {}
+    for i, r in enumerate(ref_outs):
+        for k, rk in (("y", "y"), ("h", "h"), ("rstd", "r"), ("dx", "dx")):
+            errs[f"{k}[{i}]"] = oracle.scaled_error(to_np(keep[k][i]), r[rk])
+    for k in ("dgamma", "dw1", "dw2"):
+        errs[k] = oracle.scaled_error(to_np(getattr(bb, k)), ref_grads[k])
+    bad = {k: v for k, v in errs.items() if not (v <= TOL)}
+    assert not bad, f"scaled error above {TOL}: {bad} (all: {errs})"
