@@ -4,6 +4,9 @@
 One step = the whole hot path over one batch of synthetic input: zero_grads,
 then forward and backward of every microbatch (fp32 += gradient accumulation),
 then scale_grads where the workload has one.  Prints one JSON line (rank 0).
+The default run times the large block (d 4096, ffn 16384, 2 x 8192 tokens) and,
+in a `secondary` object of the same line, the 120M-class block (d 768, ffn
+3072, 8192 tokens).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -51,6 +54,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the 120M-class block that the default run also times")
     p.add_argument("--optimizer", action="store_true",
                    help="end each step with the optimizer-side kernels: global gradient norm, "
                         "clip scale, fused AdamW on float32 master weights")
@@ -110,56 +115,145 @@ class Dist:
 # -------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """SM clock, power and clock-event reasons sampled DURING the timed region.
+
+    A background thread reads NVML (the driver's libnvidia-ml, through ctypes)
+    every 5 ms; `mark(True)` / `mark(False)` bracket the timed region on the
+    host clock, and only the samples between the two marks are reported.  The
+    GPU is found by its UUID as torch reports it, so the sampled device is the
+    one the run uses whatever CUDA_VISIBLE_DEVICES maps.  Where NVML cannot be
+    loaded the `nvidia-smi -lms` sampler (100 ms, all samples of the region)
+    stands in.  Only readings: no clock or other setting is changed."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits (nvml.h)
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.005
 
-    def __init__(self, index):
+    def __init__(self, index, uuid=None):
         self.index = index
-        self.proc = None
-        self.path = None
+        self.uuid = uuid
+        self.samples = []          # (host time, sm MHz, power W, reasons bitmask)
+        self.window = [None, None]
+        self.max_mhz = None
+        self.source = None
+        self._stop = None
+        self._thread = None
+        self._smi = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        rc = 1
+        if self.uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(("GPU-" + self.uuid).encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h))
+        if rc != 0:
+            raise OSError("no NVML handle")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, h, reasons_fn
 
     def start(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
+        import ctypes
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            lib, h, reasons_fn = self._nvml()
+        except (OSError, AttributeError):
+            self._start_smi()
+            return
+        self.source = "nvml (5 ms)"
+        self._stop = threading.Event()
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def run():
+            while not self._stop.is_set():
+                t = time.perf_counter()
+                if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    p = mw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else 0.0
+                    r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                    self.samples.append((t, float(clk.value), p, r))
+                time.sleep(self.PERIOD_S)
+
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+        time.sleep(0.05)
+
+    def _start_smi(self):
+        fd, path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.source = "nvidia-smi (100 ms)"
+        try:
+            self._smi = (subprocess.Popen(
+                ["nvidia-smi", f"--id={self.uuid and 'GPU-' + self.uuid or self.index}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(path, "w"), stderr=subprocess.DEVNULL), path)
         except OSError:
-            self.proc = None
+            self._smi = None
         time.sleep(0.3)
 
+    def mark(self, begin):
+        self.window[0 if begin else 1] = time.perf_counter()
+
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            t0, t1 = self.window
+            inside = [s for s in self.samples if t0 is not None and t1 is not None and t0 <= s[0] <= t1]
+            return self._summary([s[1] for s in inside], [s[2] for s in inside],
+                                 {n for s in inside for b, n in self.REASON_BITS.items() if s[3] & b},
+                                 len(inside), self.max_mhz)
+        if self._smi is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampler unavailable"]}
+        proc, path = self._smi
         time.sleep(0.25)
-        self.proc.terminate()
-        self.proc.wait()
+        proc.terminate()
+        proc.wait()
         rows = []
-        with open(self.path) as f:
+        with open(path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) == 7:
                     rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        os.unlink(path)
 
         def num(v):
             try:
                 return float(v)
             except ValueError:
                 return None
-        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
-        power = [num(r[2]) or 0.0 for r in rows]
-        pmax = max(power) if power else 0.0
-        loaded = [num(r[0]) for r, p in zip(rows, power) if p >= 0.5 * pmax and num(r[0]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": num(rows[0][1]),
-                "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+        return self._summary([num(r[0]) for r in rows if num(r[0]) is not None],
+                             [num(r[2]) or 0.0 for r in rows],
+                             {names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"},
+                             len(rows), num(rows[0][1]) if rows else None)
+
+    def _summary(self, sm, power, reasons, n, max_mhz):
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz, "reasons": sorted(reasons) or ["no samples"],
+                    "samples": 0, "source": self.source}
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": n, "power_w_max": round(max(power), 1),
+                "source": self.source, "window": "samples taken while the timed region ran"}
+
+
+def device_uuid(index):
+    import torch
+    try:
+        return str(torch.cuda.get_device_properties(index).uuid)
+    except Exception:
+        return None
 
 
 # ---------------------------------------------------------------- our arm
@@ -186,18 +280,18 @@ def csrc_hash(kernel=None):
 
 
 def recorded_traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (profiles/traffic.md: 'traffic <kernel> <workload>
-    <bytes> csrc=<hash>')."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+    """DRAM bytes per launch from the committed ncu record, if it was taken on
+    the current kernel sources (profiles/traffic.tsv: kernel, workload, bytes
+    per launch, csrc_hash(kernel) at the time of the capture)."""
+    path = os.path.join(ROOT, "profiles", "traffic.tsv")
     if not os.path.exists(path):
         return None
     cur = csrc_hash(kernel)
-    for line in open(path):
-        f = line.split()
-        if len(f) == 5 and f[0] == "traffic" and f[1] == kernel and f[2] == workload:
-            if f[4] == f"csrc={cur}":
-                return float(f[3])
+    with open(path) as f:
+        for line in f:
+            col = line.rstrip("\n").split("\t")
+            if len(col) == 4 and col[0] == kernel and col[1] == workload and col[3] == cur:
+                return float(col[2])
     return None
 
 
@@ -306,7 +400,7 @@ def run_ours(args, dist, peaks):
     launches_per_step = (1 + (9 if fp8 else 0) + n_mb * (16 if fp8 else 11 if recompute else 9)
                          + (1 if inp.grad_scale is not None else 0) + (3 if args.optimizer else 0))
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
-    clocks = ClockSampler(dist.local_rank)
+    clocks = ClockSampler(dist.local_rank, device_uuid(dist.local_rank))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launch_mode = "eager"
@@ -336,6 +430,7 @@ def run_ours(args, dist, peaks):
     dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    clocks.mark(True)
     start.record()
     if plain is not None:
         plain.replay()
@@ -344,6 +439,7 @@ def run_ours(args, dist, peaks):
             step(xs, dys)
     end.record()
     torch.cuda.synchronize()
+    clocks.mark(False)
     dist.barrier()
     clk = clocks.stop()
     # the per-kernel pass: same steps, every launch bracketed by CUDA events
@@ -386,15 +482,18 @@ def run_ours(args, dist, peaks):
         mean_s = per[kind][1] / per[kind][0] * 1e-3
         traffic = recorded_traffic(args.workload, kind)
         if unit == "flop":
-            peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-            src = f"{peaks['source']} sustained bf16"
+            # the burst figure: the timed region is a fraction of a second, not
+            # the seconds-long loop of the sustained measurement
+            peak = peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained"))
+            sus = peaks.get("bf16_tflops_sustained", peak)
+            src = f"{peaks['source']} burst bf16"
             if fp8:  # E4M3 contractions: the bf16 measurement times the nominal 4.5 / 2.25 ratio
-                peak = 2.0 * peak
+                peak, sus = 2.0 * peak, 2.0 * sus
                 src += " x 2 (nominal fp8 / bf16 dense ratio)"
             ach = amount / mean_s / 1e12
             return {"kernel": kind, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
-                    "algorithmic_per_launch": amount, "peak_source": src,
+                    "unit": "TFLOP/s", "frac": round(ach / peak, 4), "frac_of_sustained": round(ach / sus, 4),
+                    "traffic": traffic, "algorithmic_per_launch": amount, "peak_source": src,
                     "mean_launch_us": round(mean_s * 1e6, 2)}
         peak = peaks["hbm_gbs"]
         ach = amount / mean_s / 1e9
@@ -476,6 +575,29 @@ def run_ours(args, dist, peaks):
                                  "and this step's dx move while the GPU computes; each buffer set's step "
                                  "of public calls captured once as a CUDA graph and replayed)"}
     return result, inp
+
+
+SECONDARY_WORKLOAD = "block_120m"
+SECONDARY_MIN_STEPS = 100
+
+
+def secondary_block(args, dist, peaks):
+    """The 120M-class block (8192 tokens, d 768, ffn 3072), the other block the
+    targets name, timed in the same run and the same way as the main workload
+    (a CUDA graph of K steps, a traced replay for the per-kernel times).  Its
+    step is ~0.2 ms, so it runs at least SECONDARY_MIN_STEPS steps to give the
+    events and the clock sampler a timed region of some length."""
+    import copy
+    sub = copy.copy(args)
+    sub.workload = SECONDARY_WORKLOAD
+    sub.steps = max(args.steps, SECONDARY_MIN_STEPS)
+    sub.no_e2e = True
+    res, _ = run_ours(sub, dist, peaks)
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "tokens_per_s", "frac_of_peak", "roofline",
+            "roofline_hbm", "roofline_per_kernel", "clocks", "gpu_launches", "kernel_trace")
+    out = {"workload": SECONDARY_WORKLOAD, "config": res["config"]}
+    out.update({k: res[k] for k in keep if k in res})
+    return out
 
 
 def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_graphs=True):
@@ -598,15 +720,17 @@ def run_moe(args, dist, peaks):
     plain.replay()
     traced.replay()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dist.local_rank)
+    clocks = ClockSampler(dist.local_rank, device_uuid(dist.local_rank))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    clocks.mark(True)
     start.record()
     plain.replay()
     end.record()
     torch.cuda.synchronize()
+    clocks.mark(False)
     dist.barrier()
     clk = clocks.stop()
     traced.replay()
@@ -766,6 +890,8 @@ def main():
         result, inp = run_moe(args, dist, peaks)
     else:
         result, inp = run_ours(args, dist, peaks)
+        if args.workload == DEFAULT_WORKLOAD and not args.no_secondary:
+            result["secondary"] = secondary_block(args, dist, peaks)
     if dist.rank == 0:
         if dist.world == 1 and not args.no_cpu_baseline and inp is not None:
             result["cpu_baseline"] = cpu_baseline(inp)

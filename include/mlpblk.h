@@ -367,18 +367,22 @@ int mlpblk_last_error(void);
  *                                                                        (written)
  *        dgamma[d]  += sum_t dn[t,k] * xh[t,k]                float32 (accumulated)
  * Limits: d_model a multiple of 8 and at most 4096 (MLPBLK_ENOTSUP beyond: one
- * partial row must fit the array); any tokens >= 0 (at most
- * min(512, 1048576 / d_model) partial rows are used; with more tokens each
- * partial row sums more of them).
+ * partial row must fit the array); any tokens >= 0 (rows are indexed in 64
+ * bits; at most min(512, 1048576 / d_model) partial rows are used, and with
+ * more tokens each partial row sums more of them).
  * desc->ffn and desc->eps are not used.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call shares the one array and each call overwrites
- * the part it reads, so nothing needs clearing, but calls that overlap on the
- * GPU (other streams, other threads) race on it and must be serialised by the
- * caller.  Pointers are device pointers, 16-byte aligned.  Returns an MLPBLK_*
- * code.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make one call on every
+ * device before capturing any stream of that device into a CUDA graph.  Host
+ * threads may make a device's first call at the same time (each finds the same
+ * address).  Every call also queries the current device, its SM count and the
+ * row kernel's occupancy on the host; these enqueue nothing.
+ * Every call in a process shares the one array of a device, and each call
+ * overwrites the part it reads, so nothing needs clearing; but calls that
+ * overlap on the GPU (on other streams, from other threads) race on it and
+ * must be serialised by the caller.  Another process has an array of its own.  Pointers are device pointers, 16-byte
+ * aligned.  Returns an MLPBLK_* code.
  */
 int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, const float *dn,
                                     const void *dy, const void *gamma, const float *rstd,

@@ -2,6 +2,8 @@
 // kernel (with the residual gradient and dgamma) for callers that cannot hand
 // the library any device scratch.  Its only scratch, the per-block dgamma
 // partial sums, lives in a fixed array owned by the library.
+#include <atomic>
+
 #include "mlpblk_internal.h"
 
 using namespace mlpblk;
@@ -16,28 +18,28 @@ static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
 // In host code g_noalloc_scratch names a host-side stand-in, not device
 // memory; kernels get the device address looked up here, once per device.
-float *g_scratch_dev[64] = {nullptr};
-int g_sms[64] = {0};
+// Host threads may make a device's first call at the same time: each looks the
+// address up (the same value) and publishes it with a release store, so a
+// reader that sees the pointer sees a finished lookup.
+std::atomic<float *> g_scratch_dev[64];
 
-int device_setup(int *dev_out, float **scratch, int *sms) {
+int device_setup(float **scratch) {
     int dev = 0;
     if (cuda_status(cudaGetDevice(&dev)) != MLPBLK_OK || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
-    if (g_scratch_dev[dev] == nullptr) {
-        int major = 0, minor = 0, n = 0;
+    float *known = g_scratch_dev[dev].load(std::memory_order_acquire);
+    if (known == nullptr) {
+        int major = 0, minor = 0;
         if (cuda_status(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
-            cuda_status(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
-            cuda_status(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)))
+            cuda_status(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
             return MLPBLK_ECUDA;
-        if (major != 10 || minor != 3 || n <= 0) return MLPBLK_ENODEV;
+        if (major != 10 || minor != 3) return MLPBLK_ENODEV;
         void *p = nullptr;
         const int rc = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_scratch));
         if (rc != MLPBLK_OK) return rc;
-        g_sms[dev] = n;
-        g_scratch_dev[dev] = static_cast<float *>(p);
+        known = static_cast<float *>(p);
+        g_scratch_dev[dev].store(known, std::memory_order_release);
     }
-    *dev_out = dev;
-    *scratch = g_scratch_dev[dev];
-    *sms = g_sms[dev];
+    *scratch = known;
     return MLPBLK_OK;
 }
 
@@ -55,15 +57,13 @@ extern "C" int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const vo
     if (T < 0 || d <= 0) return MLPBLK_EINVAL;
     if (d % 8 != 0) return MLPBLK_ENOTSUP;
     if (d > kMaxNormD || d > kScratchFloats) return MLPBLK_ENOTSUP;  // beyond the array's row width
-    if (T >= (int64_t(1) << 31) / d) return MLPBLK_EINVAL;
     if (T == 0) return MLPBLK_OK;
     if (!aligned16(x) || !aligned16(dn) || !aligned16(dy) || !aligned16(gamma) || !aligned16(rstd) ||
         !aligned16(dx) || !aligned16(dgamma))
         return MLPBLK_EINVAL;
     if (dx == dy || dx == x) return MLPBLK_EINVAL;
-    int dev = 0, sms = 0;
     float *scratch = nullptr;
-    const int rc = device_setup(&dev, &scratch, &sms);
+    const int rc = device_setup(&scratch);
     if (rc != MLPBLK_OK) return rc;
     int max_parts = 512;
     if (max_parts > kScratchFloats / d) max_parts = static_cast<int>(kScratchFloats / d);

@@ -1,8 +1,14 @@
 """mlpblk_rmsnorm_backward_noalloc -- the RMSNorm backward for callers that
 cannot allocate device scratch (engines that plan all device memory at start-up
 and give extensions no allocator; threads that must not stall on cudaMalloc's
-implicit synchronisation) -- checked against the workspace path of
-mlpblk_backward, which runs the same row kernel on the same quantities.
+implicit synchronisation).
+
+Checked two ways: against the workspace path of mlpblk_backward, which runs the
+same row kernel on the same quantities, on two calls in a row; and against the
+float64 oracle's RMSNorm backward on the same dn, element by element, with the
+dgamma buffer starting from non-zero values so that the += contract is checked
+too, up to the widest row the fixed array holds (d_model 4096, where 256 partial
+rows each sum 32 of 8192 tokens).
 
 Kept in a file of its own that pytest collects last, so a run stopping at the
 first failure has run every other test before this one.
@@ -72,11 +78,60 @@ def test_noalloc_norm_backward_matches_workspace_path(mb, T):
         assert oracle.scaled_error(got_dg, ref_dg) <= tol, call
 
 
+def _oracle_case(mb, tokens, d, dtype, seed):
+    """One call on seeded inputs (dn drawn directly, rstd of the drawn x, dgamma
+    prefilled with seeded values) and the float64 oracle on the same inputs.
+    Returns the scaled errors of dx and of the dgamma increment."""
+    import torch
+    inp = synth.make_inputs(tokens=tokens, d=d, ffn=8, dtype=dtype, seed=seed)
+    rng = np.random.default_rng(seed + 1000)
+    x = inp.x[0].astype(np.float64)
+    dy = inp.dy[0].astype(np.float64)
+    gamma = inp.gamma.astype(np.float64)
+    dn = rng.standard_normal((tokens, d)).astype(np.float32)
+    rstd = (1.0 / np.sqrt(np.mean(x * x, axis=1) + inp.eps)).astype(np.float32)
+    prefill = rng.standard_normal(d).astype(np.float32)
+
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    on_dev = lambda a, t=dt: torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(t)
+    x_d, dy_d, g_d = on_dev(inp.x[0]), on_dev(inp.dy[0]), on_dev(inp.gamma)
+    dn_d, r_d = on_dev(dn, torch.float32), on_dev(rstd, torch.float32)
+    dx_d = torch.empty_like(x_d)
+    dg_d = on_dev(prefill, torch.float32)
+    code = mb.MLPBLK_BF16 if dtype == "bf16" else mb.MLPBLK_FP32
+    desc = mb.make_desc(tokens, d, 8, inp.eps, code)
+    mb.mlpblk_rmsnorm_backward_noalloc(desc, x_d, dn_d, dy_d, g_d, r_d, dx_d, dg_d)
+    torch.cuda.synchronize()
+    assert mb.mlpblk_last_error() == mb.MLPBLK_OK
+
+    dx_norm, dg = oracle.rmsnorm_backward(dn, x, gamma, rstd.astype(np.float64))
+    ref_dx = dy + dx_norm
+    got_dx = dx_d.float().cpu().numpy().astype(np.float64)
+    # the increment this call added on top of the prefilled values
+    got_inc = dg_d.cpu().numpy().astype(np.float64) - prefill.astype(np.float64)
+    return oracle.scaled_error(got_dx, ref_dx), oracle.scaled_error(got_inc, dg)
+
+
+@pytest.mark.parametrize("tokens,d,dtype,tol", [
+    (300, 256, "bf16", 2e-2),
+    (8192, 4096, "bf16", 2e-2),   # the widest row the array holds: 256 partial rows
+    (1000, 200, "bf16", 2e-2),    # a width that is not a multiple of 64
+    (77, 136, "f32", 1e-5),
+    (4096, 4096, "f32", 1e-5),
+])
+def test_noalloc_norm_backward_matches_oracle(mb, tokens, d, dtype, tol):
+    e_dx, e_dg = _oracle_case(mb, tokens, d, dtype, seed=tokens + d)
+    assert e_dx <= tol, e_dx
+    assert e_dg <= tol, e_dg
+
+
 def test_noalloc_rejects_what_it_cannot_hold(mb):
     import ctypes
     p = [0x10000 * (i + 1) for i in range(7)]
     too_wide = mb.make_desc(64, 8192, 8)
     assert mb.lib.mlpblk_rmsnorm_backward_noalloc(ctypes.byref(too_wide), *p, None) == mb.MLPBLK_ENOTSUP
+    ragged = mb.make_desc(64, 260, 8)
+    assert mb.lib.mlpblk_rmsnorm_backward_noalloc(ctypes.byref(ragged), *p, None) == mb.MLPBLK_ENOTSUP
     ok_shape = mb.make_desc(64, 256, 8)
     bad = list(p)
     bad[1] = None
