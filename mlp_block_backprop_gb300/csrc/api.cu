@@ -3,9 +3,10 @@
 //
 // Forward  (bf16): fold gamma into W1 -> W1 GEMM (rstd prologue, h/a epilogue)
 //                  -> W2 GEMM (residual epilogue)
-// Backward (bf16): dgrad-h GEMM (gate, dh_s = rstd*dh) -> wgrad W2 GEMM (+=)
+// Backward (bf16): wgrad W2 GEMM (+=) -> dgrad-h GEMM (gate, dh_s = rstd*dh)
 //                  -> dgrad-n GEMM (dn_s = rstd*dn) -> wgrad W1 GEMM (+= , gamma)
 //                  -> RMSNorm backward rows (dx, dgamma partials) -> dgamma (+=)
+//                  (d_model <= 768: the rows run on the wgrad-W1 GEMM's side warps)
 // The fp32 element type runs the same sequence on CUDA cores.
 #include <math.h>
 #include <stdlib.h>
@@ -185,6 +186,18 @@ bool rms_in_gemm() {
 
 namespace {
 
+// The bf16 backward runs the RMSNorm backward rows on the wgrad-W1 GEMM's side
+// warps when d_model <= kSideNormMaxD, unless MLPBLK_SIDE_NORM=0 selects the
+// separate row kernel (both paths are parity-tested).
+bool side_norm(int64_t d) {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_SIDE_NORM");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1 && d <= kSideNormMaxD;
+}
+
 // One-shot test fault (mlpblk_set_test_fault): consumed by the next bf16 forward.
 int g_test_fault = 0;
 
@@ -333,6 +346,24 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);
         gw1.pdl = kPdlDeferWait;
+        if (side_norm(d)) {
+            // the RMSNorm backward rows run on the wgrad-W1 GEMM's side warps,
+            // one dgamma partial row per CTA of that launch
+            gw1.side.x = static_cast<const uint16_t *>(x);
+            gw1.side.dy = static_cast<const uint16_t *>(dy);
+            gw1.side.gamma = static_cast<const uint16_t *>(gamma);
+            gw1.side.dn_s = dn_s;
+            gw1.side.rstd = rstd_saved;
+            gw1.side.dx = static_cast<uint16_t *>(dx);
+            gw1.side.part = part;
+            gw1.side.T = T;
+            gw1.side.d = (int)d;
+            gw1.grid_out = &parts;
+            MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScaleNorm, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
+            if (parts <= 0 || parts > kMaxParts) return MLPBLK_ECUDA;
+            MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+            return MLPBLK_OK;
+        }
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
     } else {
         const float *dyf = static_cast<const float *>(dy);

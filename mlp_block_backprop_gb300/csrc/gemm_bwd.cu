@@ -4,7 +4,8 @@
 //                                                         W2 read MN-major)
 //   wgrad W2: dW2 += dy^T . a                             (both operands MN-major)
 //   dgrad n : dn_s = dh_s . W1                            (fp32 out; W1 MN-major)
-//   wgrad W1: dW1 += (dh_s^T . x) * gamma[col]            (both operands MN-major)
+//   wgrad W1: dW1 += (dh_s^T . x) * gamma[col]            (both operands MN-major;
+//             for d_model <= 768 its side warps also run the RMSNorm backward rows)
 // dh_s = rstd*dh and dn_s = rstd*dn carry the per-row RMSNorm scale, so the
 // normalised input n never has to be stored or rebuilt: dh^T.n = (dh_s^T.x)*gamma.
 #include <stdlib.h>
@@ -17,7 +18,7 @@ int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *
                        void *C1, const GemmArgs &extra, int num_sms, cudaStream_t s) {
     // B is MN-major in every backward GEMM, so only 256-wide pairs exist
     const int pairs = pair_tiles_enabled() ? kAllowPair256 : 0;
-    const bool reduce = epi == kEpiAccF32 || epi == kEpiAccF32ColScale;
+    const bool reduce = epi == kEpiAccF32 || epi == kEpiAccF32ColScale || epi == kEpiAccF32ColScaleNorm;
     const int choice = choose_tile(M, N, K, streamk_enabled(), reduce, num_sms, pairs);
     const int mode = choice & ~kUseStreamK;
     GemmArgs args = extra;
@@ -38,6 +39,7 @@ int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *
         case kEpiStoreF32: { MLPBLK_RUN(kEpiStoreF32, false) }
         case kEpiAccF32: { MLPBLK_RUN(kEpiAccF32, true) }
         case kEpiAccF32ColScale: { MLPBLK_RUN(kEpiAccF32ColScale, true) }
+        case kEpiAccF32ColScaleNorm: { MLPBLK_RUN(kEpiAccF32ColScaleNorm, true) }
         default: return MLPBLK_EINVAL;
     }
 #undef MLPBLK_RUN

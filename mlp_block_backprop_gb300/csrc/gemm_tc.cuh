@@ -69,7 +69,9 @@ struct GemmCfg {
     static constexpr bool kReluSq = (EPI == kEpiFwdW1 || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A);
     static constexpr bool kAOnly = (EPI == kEpiFwdW1A);  // a out only (h is not kept)
     static constexpr bool kOutBf16 = (kReluSq || EPI == kEpiFwdW2 || EPI == kEpiDgradH || EPI == kEpiStoreBf16);
-    static constexpr bool kReduce = (EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
+    static constexpr bool kSide = (EPI == kEpiAccF32ColScaleNorm);  // + RMSNorm backward side warps
+    static constexpr bool kColScale = (EPI == kEpiAccF32ColScale || kSide);
+    static constexpr bool kReduce = (EPI == kEpiAccF32 || kColScale);
     static constexpr int kNumOut = (kReluSq && !kAOnly) ? 2 : 1;
     static constexpr int kChunkCols = kOutBf16 ? 64 : 32;  // 128 bytes of a row per chunk
     static constexpr int kNumChunks = BN / kChunkCols;
@@ -77,7 +79,7 @@ struct GemmCfg {
     // tile's columns) for the epilogues that also read an [M][N] bf16 operand, whose
     // per-element work is the largest (the other epilogues measured no faster so)
     static constexpr int kEpiWarps = (EPI == kEpiFwdW2 || EPI == kEpiDgradH) ? 8 : 4;
-    static constexpr int kThreads = kNorm ? 320 : 64 + 32 * kEpiWarps;
+    static constexpr int kThreads = kNorm ? 320 : 64 + 32 * kEpiWarps + (kSide ? 32 * kSideWarps : 0);
     static constexpr int kABytes = kBM * 128;
     static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -250,6 +252,111 @@ __device__ __forceinline__ float sq(float v) { return v * v; }
 __device__ __forceinline__ float sumsq_bf16x8(uint4 v) {
     return sq(bf16_lo(v.x)) + sq(bf16_hi(v.x)) + sq(bf16_lo(v.y)) + sq(bf16_hi(v.y)) +
            sq(bf16_lo(v.z)) + sq(bf16_hi(v.z)) + sq(bf16_lo(v.w)) + sq(bf16_hi(v.w));
+}
+
+// RMSNorm backward with the residual gradient for the rows of the side warps
+// (warp sw of kSideWarps in each CTA; rows sw + kSideWarps*blockIdx.x + k*stride),
+// on dn_s = rstd*dn:  dx = dy + gamma*dn_s - x*c,  c = r^2 * mean_k(gamma*dn_s*x),
+// dgamma partial += dn_s*x.  One row per warp at a time: lane l owns the 8-column
+// chunks l, l+32, l+64 (d <= kSideNormMaxD), the row sum is a shuffle butterfly.
+// The CTA's side warps then add their dgamma shares into the CTA's partial row
+// in warp order (a fixed order, as in the row kernel).
+__device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
+    constexpr int kCPT = kSideNormMaxD / 256;
+    const int lane = threadIdx.x & 31;
+    const int d = sn.d;
+    const int chunks = d / 8;
+    griddep_wait();  // dn_s: written by the previous kernel
+    uint4 g[kCPT];
+    float acc[kCPT][8];
+#pragma unroll
+    for (int j = 0; j < kCPT; ++j) {
+        const int q = lane + 32 * j;
+        g[j] = q < chunks ? ld_global_nc_v4(sn.gamma + 8 * q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+    }
+    const float inv_d = 1.0f / static_cast<float>(d);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kSideWarps;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kSideWarps + sw; t < sn.T; t += stride) {
+        const float r = sn.rstd[t];
+        uint4 xv[kCPT], yv[kCPT];
+        float nv[kCPT][8];
+#pragma unroll
+        for (int j = 0; j < kCPT; ++j) {
+            const int q = lane + 32 * j;
+            if (q < chunks) {
+                const int64_t off = t * d + 8 * q;
+                xv[j] = ld_global_nc_v4(sn.x + off);
+                yv[j] = ld_global_nc_v4(sn.dy + off);
+                const uint4 n0 = ld_global_nc_v4(sn.dn_s + off), n1 = ld_global_nc_v4(sn.dn_s + off + 4);
+                nv[j][0] = __uint_as_float(n0.x); nv[j][1] = __uint_as_float(n0.y);
+                nv[j][2] = __uint_as_float(n0.z); nv[j][3] = __uint_as_float(n0.w);
+                nv[j][4] = __uint_as_float(n1.x); nv[j][5] = __uint_as_float(n1.y);
+                nv[j][6] = __uint_as_float(n1.z); nv[j][7] = __uint_as_float(n1.w);
+            } else {
+                xv[j] = yv[j] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) nv[j][i] = 0.0f;
+            }
+        }
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kCPT; ++j) {
+            const uint32_t gw[4] = {g[j].x, g[j].y, g[j].z, g[j].w};
+            const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                s += bf16_lo(gw[i]) * nv[j][2 * i] * bf16_lo(xw[i]) + bf16_hi(gw[i]) * nv[j][2 * i + 1] * bf16_hi(xw[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float cr = r * r * s * inv_d;
+#pragma unroll
+        for (int j = 0; j < kCPT; ++j) {
+            const int q = lane + 32 * j;
+            if (q >= chunks) continue;
+            const uint32_t gw[4] = {g[j].x, g[j].y, g[j].z, g[j].w};
+            const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+            const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = bf16_lo(xw[i]), x1 = bf16_hi(xw[i]);
+                const float n0 = nv[j][2 * i], n1 = nv[j][2 * i + 1];
+                o[i] = pack_bf16x2(bf16_lo(yw[i]) + bf16_lo(gw[i]) * n0 - x0 * cr,
+                                   bf16_hi(yw[i]) + bf16_hi(gw[i]) * n1 - x1 * cr);
+                acc[j][2 * i] += n0 * x0;
+                acc[j][2 * i + 1] += n1 * x1;
+            }
+            st_global_v4(sn.dx + t * d + 8 * q, o[0], o[1], o[2], o[3]);
+        }
+    }
+    // the CTA's dgamma partial row: side warp 0 stores its share, then each
+    // next warp adds its own, in warp order
+    float *out = sn.part + static_cast<int64_t>(blockIdx.x) * d;
+    for (int w = 0; w < kSideWarps; ++w) {
+        named_barrier_sync(1, 32 * kSideWarps);
+        if (w == sw) {
+#pragma unroll
+            for (int j = 0; j < kCPT; ++j) {
+                const int q = lane + 32 * j;
+                if (q >= chunks) continue;
+                float *p = out + 8 * q;
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = acc[j][i];
+                if (w > 0) {
+                    const float4 a0 = ld_global_cg_v4(p), a1 = ld_global_cg_v4(p + 4);
+                    v[0] += a0.x; v[1] += a0.y; v[2] += a0.z; v[3] += a0.w;
+                    v[4] += a1.x; v[5] += a1.y; v[6] += a1.z; v[7] += a1.w;
+                }
+                st_global_v4(p, v[0], v[1], v[2], v[3]);
+                st_global_v4(p + 4, v[4], v[5], v[6], v[7]);
+            }
+            __threadfence_block();
+        }
+    }
 }
 
 template <class C>
@@ -625,7 +732,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         aux[j] = ld_shared_v4(arow + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4));
                 }
                 float cs[32];
-                if (C::EPI == kEpiAccF32ColScale) {
+                if (C::kColScale) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint4 g = make_uint4(0, 0, 0, 0);
@@ -708,7 +815,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             e[i] = v0[4 * j + i];
-                            if (C::EPI == kEpiAccF32ColScale) e[i] *= cs[4 * j + i];
+                            if (C::kColScale) e[i] *= cs[4 * j + i];
                             if (C::EPI == kEpiStoreF32) e[i] *= rsc;
                         }
                         const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
@@ -770,6 +877,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
         __syncwarp();
+    } else if (C::kSide) {
+        // ------------------------------- RMSNorm backward rows (side warps)
+        // dn_s is the previous kernel's output: these warps wait for it, while
+        // the GEMM's own warps (whose operands it does not write) run on
+        side_norm_rows(args.side, warp - 2 - C::kEpiWarps);
     } else if (C::kNorm) {
         // ------------------------------------------- RMSNorm prologue (fwd W1)
         const int r = 32 * (warp - 6) + lane;  // row of this CTA's 128 rows
@@ -969,6 +1081,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
         a.sk_total = iters;
     }
     a.workers = workers;
+    if (a.grid_out) *a.grid_out = cta_per_worker * workers;
 
     static int attr_set[64] = {0};
     int dev = 0;

@@ -83,6 +83,23 @@ enum Epilogue : int {
     kEpiFwdW1Pre = 6, // h = rstd*acc, a = relu(h)^2 (bf16 x2); rstd read from global
     kEpiFwdW1A = 7,   // a = relu(rstd*acc)^2 only (bf16); rstd read from global
     kEpiStoreBf16 = 8,  // out = acc (bf16): the routed experts' outputs
+    kEpiAccF32ColScaleNorm = 9,  // kEpiAccF32ColScale, and side warps run the RMSNorm
+                                 // backward rows (GemmArgs::side) meanwhile
+};
+
+// The RMSNorm backward rows that the wgrad-W1 GEMM's side warps compute while
+// its tensor-core pipeline runs (bf16 block, d_model <= kSideNormMaxD): the row
+// kernel's arithmetic on dn_s = rstd * dn, one warp per row, one dgamma partial
+// row per CTA.
+constexpr int kSideNormMaxD = 768;
+constexpr int kSideWarps = 4;
+struct SideNorm {
+    const uint16_t *x, *dy, *gamma;  // bf16 [T, d], [T, d], [d]
+    const float *dn_s, *rstd;        // fp32 [T, d], [T]
+    uint16_t *dx;                    // bf16 [T, d] (written)
+    float *part;                     // fp32 [gridDim.x, d]: this launch's dgamma partial rows
+    int64_t T;
+    int d;
 };
 
 // Arguments of one GEMM launch (the tensor maps travel separately).
@@ -139,6 +156,8 @@ struct GemmArgs {
     float eps;                 // FwdW1: RMSNorm epsilon
     int skip_loads;            // test fault: the producer issues no loads (waits run out)
     int pdl;                   // PdlOrder
+    SideNorm side;             // kEpiAccF32ColScaleNorm: the side warps' rows
+    int *grid_out;             // host-side: the launcher stores the grid size (CTAs) here
 };
 
 // Operand / output views handed to the GEMM launcher (row-major 2-D tensors).

@@ -487,6 +487,11 @@ __device__ __forceinline__ void st_global_v4(float *p, float a, float b, float c
                  : "memory");
 }
 
+__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // 16-byte load cached in L2 only (data another SM wrote during this kernel).
 __device__ __forceinline__ float4 ld_global_cg_v4(const float *p) {
     float4 v;

@@ -22,6 +22,7 @@ SETTINGS = [
     {"MLPBLK_STREAMK": "2"},          # the split schedule wherever rounds are not whole
     {"MLPBLK_GROUP_M": "3"},          # another raster
     {"MLPBLK_MAX_SMS": "38"},         # a quarter of the SMs
+    {"MLPBLK_SIDE_NORM": "0"},        # RMSNorm backward in its own kernel at every width
 ]
 
 
