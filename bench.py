@@ -295,7 +295,7 @@ def recorded_traffic(workload, kernel):
     return None
 
 
-def algorithmic_work(kind, T, d, F, parts):
+def algorithmic_work(kind, T, d, F, parts, prefold=False):
     """(amount, unit) per launch: FLOP for the GEMMs, bytes for the HBM-bound kernels."""
     if kind in GEMM_KINDS:
         return 2.0 * T * d * F, "flop"
@@ -304,8 +304,12 @@ def algorithmic_work(kind, T, d, F, parts):
         # dgamma partial rows (a few MB of scratch) are not counted
         return T * d * (2 + 2 + 4 + 2) + 4.0 * T + 2.0 * d, "byte"
     if kind == "fold_gamma":
+        if prefold:  # once per step: W1 read, W1*gamma written
+            return 2.0 * F * d * 2 + 2.0 * d, "byte"
         # statistics pass: x read, rstd written, W1 read and W1*gamma written
         return 2.0 * T * d + 4.0 * T + 2.0 * F * d * 2 + 2.0 * d, "byte"
+    if kind == "rstd":  # statistics pass alone: x read, rstd written
+        return 2.0 * T * d + 4.0 * T, "byte"
     if kind == "zero_grads":
         return 4.0 * (2 * F * d + d), "byte"
     if kind == "scale_grads":
@@ -361,11 +365,19 @@ def run_ours(args, dist, peaks):
                       (masters["w1"], bb.w1, bb.dw1, *moments["w1"], True),
                       (masters["w2"], bb.w2, bb.dw2, *moments["w2"], True)]
 
+    # with several microbatches, W1 * gamma is made once per step (the weights do
+    # not change between microbatches) and every forward reads it
+    prefold = n_mb > 1 and not fp8 and not recompute
+    if prefold:
+        bb.w1g = torch.empty_like(bb.w1)
+
     def step(x_list, dy_list, dx_list=None, after_mb=None):
         mb.mlpblk_zero_grads(desc, bb.dgamma, bb.dw1, bb.dw2)
         if fp8:
             # the weights' E4M3 codes once per step: they do not change between microbatches
             mb.mlpblk_fp8_quantize_weights(desc, bb.gamma, bb.w1, bb.w2, bb.wq, bb.ws)
+        if prefold:
+            mb.mlpblk_fold_weights(desc, bb.gamma, bb.w1, bb.w1g)
         for i in range(n_mb):
             dx = bb.dx if dx_list is None else dx_list[i]
             if fp8:
@@ -378,7 +390,10 @@ def run_ours(args, dist, peaks):
                 mb.mlpblk_backward_recompute(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.rstd,
                                              dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
             else:
-                mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
+                if prefold:
+                    mb.mlpblk_forward_prefolded(desc, x_list[i], bb.w1g, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
+                else:
+                    mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
                 mb.mlpblk_backward(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a, bb.rstd,
                                    dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
             if after_mb is not None:
@@ -397,7 +412,7 @@ def run_ours(args, dist, peaks):
     if mb.mlpblk_last_error() != mb.MLPBLK_OK:
         raise RuntimeError("device error during warm-up")
 
-    launches_per_step = (1 + (9 if fp8 else 0) + n_mb * (16 if fp8 else 11 if recompute else 9)
+    launches_per_step = (1 + (9 if fp8 else 0) + (1 if prefold else 0) + n_mb * (16 if fp8 else 11 if recompute else 9)
                          + (1 if inp.grad_scale is not None else 0) + (3 if args.optimizer else 0))
     trace = mb.KernelTrace(args.steps * launches_per_step + 8)
     clocks = ClockSampler(dist.local_rank, device_uuid(dist.local_rank))
@@ -467,6 +482,10 @@ def run_ours(args, dist, peaks):
         e = per.setdefault(kind, [0, 0.0])
         e[0] += 1
         e[1] += ms
+    # every step ran the whole path: each of the six GEMMs once per microbatch
+    missing = [k for k in GEMM_KINDS if per.get(k, [0])[0] < args.steps * n_mb]
+    if missing:
+        raise RuntimeError(f"the traced steps did not launch {missing} once per microbatch")
     total_k = sum(v[1] for v in per.values())
     kernels = {k: {"launches": v[0], "total_ms": round(v[1], 4), "mean_us": round(1e3 * v[1] / v[0], 2),
                    "share": round(v[1] / total_k, 4)} for k, v in sorted(per.items(), key=lambda kv: -kv[1][1])}
@@ -476,7 +495,7 @@ def run_ours(args, dist, peaks):
     def roofline(kind):
         if kind not in per:
             return None
-        amount, unit = algorithmic_work(kind, T, d, F, parts)
+        amount, unit = algorithmic_work(kind, T, d, F, parts, prefold)
         if amount is None:  # a launch with no bandwidth or FLOP roof of its own (a scalar finalize)
             return None
         mean_s = per[kind][1] / per[kind][0] * 1e-3
@@ -515,6 +534,8 @@ def run_ours(args, dist, peaks):
                    "precision": args.precision + (" (E4M3 GEMM operands, per-tensor scales; the weights' codes made once "
                                                   "per step for all microbatches)" if fp8 else ""),
                    "rmsnorm": args.rmsnorm,
+                   "w1_gamma_fold": "once per step (mlpblk_fold_weights + mlpblk_forward_prefolded)" if prefold
+                                    else "inside every forward",
                    "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch

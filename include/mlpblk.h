@@ -98,6 +98,29 @@ int mlpblk_forward(const mlpblk_desc *desc,
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * W1 * gamma, the forward's first GEMM operand (RMSNorm's gamma folded into W1
+ * along d: w1g[f,k] = w1[f,k] * gamma[k], rounded once to the dtype).  It depends
+ * on the weights only, so a caller that runs several microbatches with the same
+ * weights (gradient accumulation, "grow_a_language_model_backprop", accumulating
+ * across microbatches) makes it once per weight update and passes it to
+ * mlpblk_forward_prefolded; mlpblk_forward folds on every call.
+ *   in : gamma[d], w1[F,d] (desc->dtype)      out: w1g[F,d] (desc->dtype, written)
+ * desc->tokens and desc->eps are not used.  w1g must not alias w1.  Pointers
+ * are device pointers, 16-byte aligned.  Returns an MLPBLK_* code.
+ */
+int mlpblk_fold_weights(const mlpblk_desc *desc, const void *gamma, const void *w1, void *w1g,
+                        void *stream);
+
+/*
+ * mlpblk_forward with the folded weight from mlpblk_fold_weights in place of
+ * gamma and w1: the same outputs, bit for bit, without the per-call fold.
+ * Workspace as for mlpblk_forward (mlpblk_workspace_size).
+ */
+int mlpblk_forward_prefolded(const mlpblk_desc *desc, const void *x, const void *w1g, const void *w2,
+                             void *y, void *h_saved, void *a_saved, float *rstd_saved,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Backward of one microbatch (the residual branch copies forward and adds
  * backward; d relu(h)^2/dh = 2 relu(h), 0 at h = 0; RMSNorm backward from the
  * saved rstd).  Consumes the forward's saved h, a and rstd for the same x.
@@ -392,7 +415,8 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
  * Kernel timing hook for profiling harnesses (CUDA events, no profiler needed).
  * Kinds reported for each kernel launch the library makes:
  */
-#define MLPBLK_KERNEL_FOLD_GAMMA      1  /* statistics pass: rstd, W1g = W1 * gamma  */
+#define MLPBLK_KERNEL_FOLD_GAMMA      1  /* statistics pass: rstd, W1g = W1 * gamma;
+                                            mlpblk_fold_weights: W1g alone           */
 #define MLPBLK_KERNEL_GEMM_FWD_W1     2  /* h, a = RMSNorm(x) . W1^T, relu^2         */
 #define MLPBLK_KERNEL_GEMM_FWD_W2     3  /* y = x + a . W2^T                          */
 #define MLPBLK_KERNEL_GEMM_DGRAD_H    4  /* dh = (dy . W2) * 2 relu(h)                */
@@ -403,7 +427,7 @@ int mlpblk_rmsnorm_backward_noalloc(const mlpblk_desc *desc, const void *x, cons
 #define MLPBLK_KERNEL_DGAMMA_REDUCE   9  /* dgamma += sum of parts                    */
 #define MLPBLK_KERNEL_ZERO_GRADS     10
 #define MLPBLK_KERNEL_SCALE_GRADS    11
-#define MLPBLK_KERNEL_RSTD           12  /* reserved (no launch uses it)              */
+#define MLPBLK_KERNEL_RSTD           12  /* statistics pass alone: rstd (prefolded)   */
 #define MLPBLK_KERNEL_GRAD_NORM      13  /* per-CTA partial sums of g^2               */
 #define MLPBLK_KERNEL_CLIP_GRADS     14  /* g *= clip scale (device scalar)           */
 #define MLPBLK_KERNEL_ADAMW          15  /* fused AdamW update                        */

@@ -35,7 +35,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_workspace_size_fp8", "mlpblk_forward_fp8", "mlpblk_backward_fp8",
             "mlpblk_fp8_weights_size", "mlpblk_fp8_quantize_weights", "mlpblk_forward_fp8_prequant",
             "mlpblk_backward_fp8_prequant",
-            "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward")
+            "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward",
+            "mlpblk_fold_weights", "mlpblk_forward_prefolded")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
@@ -93,6 +94,10 @@ def _load():
     lib.mlpblk_forward.argtypes = [pd] + [vp] * 9 + [sz, vp]
     lib.mlpblk_forward.restype = i32
     lib.mlpblk_backward.argtypes = [pd] + [vp] * 13 + [sz, vp]
+    lib.mlpblk_fold_weights.argtypes = [pd, vp, vp, vp, vp]
+    lib.mlpblk_fold_weights.restype = i32
+    lib.mlpblk_forward_prefolded.argtypes = [pd] + [vp] * 7 + [sz, vp]
+    lib.mlpblk_forward_prefolded.restype = i32
     lib.mlpblk_backward.restype = i32
     lib.mlpblk_workspace_size_recompute.argtypes = [pd]
     lib.mlpblk_workspace_size_recompute.restype = sz
@@ -199,6 +204,20 @@ def mlpblk_forward(desc, x, gamma, w1, w2, y, h_saved, a_saved, rstd_saved, work
                             _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(workspace),
                             nbytes, _stream(stream))
     _check(rc, "mlpblk_forward")
+
+
+def mlpblk_fold_weights(desc, gamma, w1, w1g, stream=None):
+    _check(lib.mlpblk_fold_weights(ctypes.byref(desc), _ptr(gamma), _ptr(w1), _ptr(w1g), _stream(stream)),
+           "mlpblk_fold_weights")
+
+
+def mlpblk_forward_prefolded(desc, x, w1g, w2, y, h_saved, a_saved, rstd_saved, workspace,
+                             workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib.mlpblk_forward_prefolded(ctypes.byref(desc), _ptr(x), _ptr(w1g), _ptr(w2), _ptr(y),
+                                      _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(workspace),
+                                      nbytes, _stream(stream))
+    _check(rc, "mlpblk_forward_prefolded")
 
 
 def mlpblk_backward(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
@@ -500,6 +519,16 @@ class BlockBuffers:
             return
         mlpblk_forward(self.desc, self.x, self.gamma, self.w1, self.w2, self.y, self.h, self.a,
                        self.rstd, self.ws, stream=stream)
+
+    def fold_weights(self, stream=None):
+        """W1 * gamma into self.w1g (allocated on first use), for forward_prefolded."""
+        if getattr(self, "w1g", None) is None:
+            self.w1g = self.torch.empty_like(self.w1)
+        mlpblk_fold_weights(self.desc, self.gamma, self.w1, self.w1g, stream=stream)
+
+    def forward_prefolded(self, stream=None):
+        mlpblk_forward_prefolded(self.desc, self.x, self.w1g, self.w2, self.y, self.h, self.a, self.rstd,
+                                 self.ws, stream=stream)
 
     def backward(self, stream=None):
         if self.fp8:

@@ -261,18 +261,26 @@ namespace {
 
 // The forward's launches.  h_out may be null on the bf16 path (a_only: the
 // recompute variant's forward, whose W1 epilogue writes a alone).
+// prefolded: w1g already holds W1 * gamma (mlpblk_fold_weights); gamma and w1
+// are not read.
 int forward_impl(const mlpblk_desc *desc, const void *x, const void *gamma, const void *w1,
                  const void *w2, void *y, void *h_out, void *a_out, float *rstd_saved, void *w1g,
-                 float *sk_partial, int *sk_flags, int sms, cudaStream_t s, bool a_only) {
+                 float *sk_partial, int *sk_flags, int sms, cudaStream_t s, bool a_only,
+                 bool prefolded = false) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     const bool stats_in_gemm = desc->dtype == MLPBLK_BF16 && !a_only && rms_in_gemm();
-    if (stats_in_gemm)
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
-                      launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, nullptr, 0, s));
-    else
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
-                      launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, w1, gamma, w1g, F,
+    if (stats_in_gemm) {
+        // rstd inside the W1 GEMM (whole tiles: no stream-K flags to clear)
+        if (!prefolded)
+            MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                          launch_fold_gamma(desc->dtype, w1, gamma, w1g, F, d, nullptr, 0, s));
+    } else {
+        // rstd, and W1 * gamma unless it is given
+        MLPBLK_LAUNCH(prefolded ? MLPBLK_KERNEL_RSTD : MLPBLK_KERNEL_FOLD_GAMMA, s,
+                      launch_norm_prep(desc->dtype, x, rstd_saved, T, d, desc->eps, prefolded ? nullptr : w1,
+                                       gamma, prefolded ? nullptr : w1g, prefolded ? 0 : F,
                                        sk_flags + kSetFwdW1 * kSkFlagsPerSet, kSkFlagsPerSet, s));
+    }
     if (desc->dtype == MLPBLK_BF16) {
         GemmArgs g1 = {};
         if (stats_in_gemm) {
@@ -430,6 +438,38 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
                          ws + l.dh, reinterpret_cast<float *>(ws + l.dn), reinterpret_cast<float *>(ws + l.part),
                          reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
                          sms, static_cast<cudaStream_t>(stream));
+}
+
+int mlpblk_fold_weights(const mlpblk_desc *desc, const void *gamma, const void *w1, void *w1g,
+                        void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (!aligned16(gamma) || !aligned16(w1) || !aligned16(w1g)) return MLPBLK_EINVAL;
+    if (w1g == w1) return MLPBLK_EINVAL;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_FOLD_GAMMA, s,
+                  launch_fold_gamma(desc->dtype, w1, gamma, w1g, desc->ffn, desc->d_model, nullptr, 0, s));
+    return MLPBLK_OK;
+}
+
+int mlpblk_forward_prefolded(const mlpblk_desc *desc, const void *x, const void *w1g, const void *w2,
+                             void *y, void *h_saved, void *a_saved, float *rstd_saved, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    MLPBLK_TRY(check_desc(desc));
+    if (desc->tokens == 0) return MLPBLK_OK;
+    if (!aligned16(x) || !aligned16(w1g) || !aligned16(w2) || !aligned16(y) || !aligned16(h_saved) ||
+        !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (y == x) return MLPBLK_EINVAL;
+    const WsLayout l = ws_layout(desc, false);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return forward_impl(desc, x, nullptr, nullptr, w2, y, h_saved, a_saved, rstd_saved, const_cast<void *>(w1g),
+                        reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
+                        sms, static_cast<cudaStream_t>(stream), false, true);
 }
 
 size_t mlpblk_workspace_size_recompute(const mlpblk_desc *desc) {

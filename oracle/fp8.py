@@ -74,10 +74,14 @@ def round_to_bf16(a):
     return rounded.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def quantize(v):
-    """Per-tensor E4M3 quantisation of float32 values v: (dequantised values, scale)."""
+def quantize(v, amax=None):
+    """Per-tensor E4M3 quantisation of float32 values v: (dequantised values, scale).
+    `amax`, when given, is the max |v| of the whole tensor that v is a row block
+    of (the scale is the whole tensor's); by default v is the whole tensor."""
     v32 = np.asarray(v, dtype=np.float32)
-    amax = np.float32(np.max(np.abs(v32))) if v32.size else np.float32(0)
+    if amax is None:
+        amax = np.float32(np.max(np.abs(v32))) if v32.size else np.float32(0)
+    amax = np.float32(amax)
     if amax == 0:
         return np.zeros(v32.shape), np.float32(1.0)
     inv = np.float32(E4M3_MAX) / amax
@@ -92,10 +96,8 @@ def rstd32(x, eps):
     return (1.0 / np.sqrt(np.mean(x * x, axis=1) + eps)).astype(np.float32)
 
 
-def forward(x, gamma, w1, w2, eps):
-    """FP8-operand forward.  Returns (y, h, a_q, n_q, r) with h the float64
-    pre-activation (the kernels keep it in bf16), a_q and n_q the dequantised
-    GEMM operands the backward reuses."""
+def _pre_a(x, gamma, w1, eps):
+    """The forward up to a (bf16-rounded, before its quantisation): (h, a, n_q, r)."""
     x32 = np.asarray(x, dtype=np.float32)
     r = rstd32(x, eps)
     n_prime = (x32 * r[:, None]).astype(np.float32)          # n' = x * rstd, float32
@@ -104,24 +106,51 @@ def forward(x, gamma, w1, w2, eps):
     w1g_q, _ = quantize(w1g)
     h = n_q @ w1g_q.T
     a = np.where(h > 0, h, 0.0) ** 2
-    a_q, _ = quantize(round_to_bf16(a.astype(np.float32)))
-    w2_q, _ = quantize(w2)
-    y = np.asarray(x, dtype=np.float64) + a_q @ w2_q.T
-    return y, h, a_q, n_q, r.astype(np.float64)
+    return h, round_to_bf16(a.astype(np.float32)), n_q, r
 
 
-def backward(dy, x, gamma, w1, w2, h, a_q, n_q, r, grads):
-    """FP8-operand backward; adds into grads (dgamma, dw1, dw2) and returns dx."""
-    x = np.asarray(x, dtype=np.float64)
-    gamma = np.asarray(gamma, dtype=np.float64)
-    dy_q, _ = quantize(dy)
+def _pre_dh(dy, h, w2, dy_amax=None):
+    """The backward up to dh (bf16-rounded, before its quantisation): (dh, dy_q)."""
+    dy_q, _ = quantize(dy, dy_amax)
     w2_q, _ = quantize(w2)
     da = dy_q @ w2_q                                          # [T, F]
     # the gate reads h as the forward keeps it (bf16): the reverse kernel applies
     # the branch to the preserved input of ReLU^2
     hk = round_to_bf16(np.asarray(h, dtype=np.float32))
     dh = da * 2.0 * np.where(hk > 0, hk, 0.0)                 # d relu(h)^2 / dh
-    dh_q, _ = quantize(round_to_bf16(dh.astype(np.float32)))
+    return round_to_bf16(dh.astype(np.float32)), dy_q
+
+
+def forward(x, gamma, w1, w2, eps, a_amax=None):
+    """FP8-operand forward.  Returns (y, h, a_q, n_q, r) with h the float64
+    pre-activation (the kernels keep it in bf16), a_q and n_q the dequantised
+    GEMM operands the backward reuses.  a_amax: see block_amaxes."""
+    h, a, n_q, r = _pre_a(x, gamma, w1, eps)
+    a_q, _ = quantize(a, a_amax)
+    w2_q, _ = quantize(w2)
+    y = np.asarray(x, dtype=np.float64) + a_q @ w2_q.T
+    return y, h, a_q, n_q, r.astype(np.float64)
+
+
+def block_amaxes(x, dy, gamma, w1, w2, eps, dy_amax=None):
+    """max |a| and max |dh| (their bf16 values) over a row block of a microbatch,
+    dy_amax being the whole dy's max |dy| (dy is an input).  The maxima over all
+    blocks are the whole tensors' (a and dh are row-wise given the weights and
+    dy's scale), so a large microbatch can be evaluated block by block:
+    forward(..., a_amax=) and backward(..., dy_amax=, dh_amax=) then quantise
+    each block with the whole tensor's scale."""
+    h, a, _, _ = _pre_a(x, gamma, w1, eps)
+    dh, _ = _pre_dh(dy, h, w2, dy_amax)
+    return np.float32(np.max(np.abs(a))), np.float32(np.max(np.abs(dh)))
+
+
+def backward(dy, x, gamma, w1, w2, h, a_q, n_q, r, grads, dy_amax=None, dh_amax=None):
+    """FP8-operand backward; adds into grads (dgamma, dw1, dw2) and returns dx.
+    dy_amax, dh_amax: see block_amaxes."""
+    x = np.asarray(x, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    dh, dy_q = _pre_dh(dy, h, w2, dy_amax)
+    dh_q, _ = quantize(dh, dh_amax)
     grads["dw2"] += dy_q.T @ a_q
     w1_q, _ = quantize(w1)
     dn = dh_q @ w1_q                                          # [T, d]

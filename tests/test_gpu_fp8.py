@@ -81,6 +81,22 @@ def test_fp8_ragged(shape):
     _check(synth.make_inputs(tokens=T, d=d, ffn=F, dtype="bf16", seed=T + d + F, n_mb=2, eps=1e-5))
 
 
+@pytest.mark.slow
+def test_fp8_wide_workload_full_size():
+    """The wide workload (16384 tokens, d 2048, ffn 8192: K up to 16384 in
+    128-value E4M3 stages, stream-K splits and reduce-add epilogues at a benched
+    size), every element of every output against the float64 FP8 oracle, which
+    runs in row blocks with the whole tensors' scales (tests/fp8_blocks.py)."""
+    import fp8_blocks
+    inp = synth.config_inputs("wide")
+    outs, grads, _ = _run_fp8(inp)
+    ref, ref_grads = fp8_blocks.run_blocks("wide")
+    errs = {k: oracle.scaled_error(outs[0][k], ref["r" if k == "rstd" else k]) for k in ("y", "h", "rstd", "dx")}
+    errs.update({k: oracle.scaled_error(grads[k], ref_grads[k]) for k in ("dgamma", "dw1", "dw2")})
+    bad = {k: v for k, v in errs.items() if not (v <= TOL)}
+    assert not bad, f"scaled error above {TOL}: {bad} (all: {errs})"
+
+
 def test_fp8_saved_codes_and_scale():
     """The saved a codes are E4M3 bytes whose largest magnitude is 448 (the amax
     element), and a's scale record is {amax, 448/amax, amax/448, 0}."""
