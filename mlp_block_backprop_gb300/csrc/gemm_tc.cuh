@@ -12,12 +12,14 @@
 //   warp 0      TMA producer: A/B tiles -> shared-memory ring of kStages stages
 //   warp 1      owns TMEM; one lane issues tcgen05.mma (K = 16 per instruction)
 //   warps 2..5  epilogue: TMEM -> registers -> fused math -> shared -> TMA store
-//               (warps 2..9 for the residual and gate epilogues: two warps per
-//               TMEM lane quarter, each taking half of a tile's columns)
+//               (warps 2..9 for the residual, gate and fp32-output epilogues: two
+//               warps per TMEM lane quarter, each taking half of a tile's columns)
 //   warps 6..9  (the in-GEMM RMSNorm variant of the forward W1 GEMM only) sum of
 //               x^2 per row, read from each A stage once its MMAs have completed
 //               (then the stage goes back to the producer), gives rstd for the
 //               epilogue; works with pair tiles, each CTA summing its own rows
+//   warps 6..9  (the wgrad-W1 GEMM with side rows only) RMSNorm backward rows,
+//               independent of the tensor-core pipeline (side_norm_rows)
 // The accumulator is double buffered in TMEM (2 x BN columns) so the epilogue of
 // one tile overlaps the main loop of the next.
 //
@@ -77,8 +79,11 @@ struct GemmCfg {
     static constexpr int kNumChunks = BN / kChunkCols;
     // epilogue warps: one per TMEM lane quarter, or two (each draining half of a
     // tile's columns) for the epilogues that also read an [M][N] bf16 operand, whose
-    // per-element work is the largest (the other epilogues measured no faster so)
-    static constexpr int kEpiWarps = (EPI == kEpiFwdW2 || EPI == kEpiDgradH) ? 8 : 4;
+    // per-element work is the largest, and for the fp32 outputs, whose last tile's
+    // 128 KB per CTA ends the kernel (the 120M-class block's dgrad-n 38.3 -> 36.8
+    // us); the two-output W1 epilogue measured no faster so
+    static constexpr bool kF32x8 = (EPI == kEpiStoreF32 || EPI == kEpiAccF32 || EPI == kEpiAccF32ColScale);
+    static constexpr int kEpiWarps = (EPI == kEpiFwdW2 || EPI == kEpiDgradH || kF32x8) ? 8 : 4;
     static constexpr int kThreads = kNorm ? 320 : 64 + 32 * kEpiWarps + (kSide ? 32 * kSideWarps : 0);
     static constexpr int kABytes = kBM * 128;
     static constexpr int kBBytes = kBRows * 128;
@@ -89,8 +94,9 @@ struct GemmCfg {
     static constexpr bool kAux = (EPI == kEpiFwdW2 || EPI == kEpiDgradH);
     static constexpr int kAuxBytes = kAux ? 4 * kNumChunks * 4096 : 0;
     // output staging per epilogue warp and output: double buffered, except for
-    // the two-output W1 epilogue, whose shared memory goes to a deeper pipeline
-    static constexpr int kStagingBufs = kNumOut == 2 ? 1 : 2;
+    // the two-output W1 epilogue and the eight-warp fp32 epilogues, whose shared
+    // memory goes to a deeper pipeline
+    static constexpr int kStagingBufs = (kNumOut == 2 || kF32x8) ? 1 : 2;
     static constexpr int kStagingBytes = kAux ? 0 : kEpiWarps * kNumOut * kStagingBufs * 4096;
     // per-row scale read from args.rstd_in (1 when that is null)
     static constexpr bool kRowScale =
@@ -473,7 +479,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         a_pair = b_pair = true;
                         bar_a = bar_b = leader_full;
                     }
-                    if (C::A_MN) {
+                    if (C::A_MN && args.a_mn3d) {
+                        // one copy of all kBM / kMNBox boxes: the map's third
+                        // dimension walks the MN blocks (see make_map_mn3d)
+                        if (a_pair) tma_load_3d_pair(&tmA, bar_a, sa, 0, k0, a_row / C::kMNBox);
+                        else tma_load_3d(&tmA, &full_bar[stage], sa, 0, k0, a_row / C::kMNBox);
+                    } else if (C::A_MN) {
 #pragma unroll
                         for (int j = 0; j < kBM / C::kMNBox; ++j) {
                             if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
@@ -483,7 +494,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa, k0, a_row);
                         else tma_load_2d(&tmA, &full_bar[stage], sa, k0, a_row);
                     }
-                    if (C::B_MN) {
+                    if (C::B_MN && args.b_mn3d) {
+                        if (b_pair) tma_load_3d_pair(&tmB, bar_b, sb, 0, k0 + bk, b_row / C::kMNBox);
+                        else tma_load_3d(&tmB, &full_bar[stage], sb, 0, k0 + bk, b_row / C::kMNBox);
+                    } else if (C::B_MN) {
 #pragma unroll
                         for (int j = 0; j < C::kBRows / C::kMNBox; ++j) {
                             if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
@@ -981,6 +995,39 @@ inline bool make_map_2d(CUtensorMap *m, const void *ptr, int type, uint64_t inne
     return r == CUDA_SUCCESS;
 }
 
+// An MN-major operand stored [K][MN] (MN contiguous) as a 3-D map: (kMNBox
+// values of MN) x K x (MN / kMNBox blocks), box kMNBox x box_k x nblk.  One copy
+// then fills nblk consecutive 128-byte-swizzled boxes of box_k rows, the same
+// shared-memory layout as nblk 2-D copies, with one TMA instruction instead of
+// nblk (the producer's issue time per k-block halves).  The blocks' stride (the
+// box's row, 128 bytes) is below the K stride: the map walks the array in a
+// permuted order.  Needs MN a multiple of kMNBox (no partial block).
+inline bool make_map_mn3d(CUtensorMap *m, const void *ptr, int type, uint64_t mn, uint64_t k,
+                          uint32_t box_mn, uint32_t box_k, uint32_t nblk) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || mn % box_mn != 0) return false;
+    const uint64_t esz = type == kMapU8 ? 1 : 2;
+    const CUtensorMapDataType dt = type == kMapU8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {box_mn, k, mn / box_mn};
+    cuuint64_t strides[2] = {mn * esz, box_mn * esz};
+    cuuint32_t box[3] = {box_mn, box_k, nblk};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// MLPBLK_MN3D=0 loads MN-major operands box by box (2-D copies) everywhere.
+inline bool mn3d_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_MN3D");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 // Stream-K scheduling is used unless MLPBLK_STREAMK=0 (whole tiles only);
 // MLPBLK_STREAMK=2 takes it wherever the tiles do not fill whole rounds.
 inline int streamk_mode() {
@@ -1013,15 +1060,23 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     bool ok = true;
     // operands: 128-byte box rows (kBKe values of K, or kMNBox values of M / N)
     const int op = C::F8 ? kMapU8 : kMapBf16;
-    ok &= C::A_MN ? make_map_2d(&mA, A, op, M, K, C::kMNBox, C::kBKe)
-                  : make_map_2d(&mA, A, op, K, M, C::kBKe, kBM);
+    // MN-major operands whose MN is a whole number of boxes: one 3-D copy per
+    // operand and k-block
+    a.a_mn3d = C::A_MN && kBM / C::kMNBox > 1 && M % C::kMNBox == 0 && mn3d_enabled() &&
+               make_map_mn3d(&mA, A, op, M, K, C::kMNBox, C::kBKe, kBM / C::kMNBox);
+    if (!a.a_mn3d)
+        ok &= C::A_MN ? make_map_2d(&mA, A, op, M, K, C::kMNBox, C::kBKe)
+                      : make_map_2d(&mA, A, op, K, M, C::kBKe, kBM);
     // grouped GEMMs: B holds every expert's slice (M-grouped), C every expert's
     // block (K-grouped)
     const uint64_t groups = a.grp_mode != kGroupNone ? static_cast<uint64_t>(a.grp_count) : 1u;
     const uint64_t b_outer = a.grp_mode == kGroupM ? groups : 1u;
     const uint64_t c_rows = static_cast<uint64_t>(M) * (a.grp_mode == kGroupK ? groups : 1u);
-    ok &= C::B_MN ? make_map_2d(&mB, B, op, N, K * b_outer, C::kMNBox, C::kBKe)
-                  : make_map_2d(&mB, B, op, K, N * b_outer, C::kBKe, C::kBRows);
+    a.b_mn3d = C::B_MN && C::kBRows / C::kMNBox > 1 && N % C::kMNBox == 0 && mn3d_enabled() &&
+               make_map_mn3d(&mB, B, op, N, K * b_outer, C::kMNBox, C::kBKe, C::kBRows / C::kMNBox);
+    if (!a.b_mn3d)
+        ok &= C::B_MN ? make_map_2d(&mB, B, op, N, K * b_outer, C::kMNBox, C::kBKe)
+                      : make_map_2d(&mB, B, op, K, N * b_outer, C::kBKe, C::kBRows);
     if (C::kOutBf16) ok &= make_map_2d(&mC0, C0, kMapBf16, N, c_rows, 64, 32);
     else ok &= make_map_2d(&mC0, C0, kMapF32, N, c_rows, 32, 32);
     if (C::kNumOut == 2) ok &= make_map_2d(&mC1, C1, kMapBf16, N, M, 64, 32);

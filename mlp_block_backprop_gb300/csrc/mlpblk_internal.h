@@ -154,6 +154,8 @@ struct GemmArgs {
     const uint16_t *colscale;  // AccF32ColScale: bf16 per-column scale (gamma)
     float inv_k;               // FwdW1: 1/d
     float eps;                 // FwdW1: RMSNorm epsilon
+    int a_mn3d, b_mn3d;        // launcher-set: the MN-major operand's map is 3-D (one copy
+                               // of all its boxes per k-block)
     int skip_loads;            // test fault: the producer issues no loads (waits run out)
     int pdl;                   // PdlOrder
     SideNorm side;             // kEpiAccF32ColScaleNorm: the side warps' rows
