@@ -365,6 +365,494 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
     }
 }
 
+// What the roles of a CTA share: its shared-memory carve-up and identities.
+struct CtaCtx {
+    uint8_t *stages, *staging, *aux_smem;
+    uint64_t *full_bar, *empty_bar, *accf_bar, *acce_bar, *aux_bar, *consumed_bar;
+    volatile int *abort_flag;
+    float *rs;
+    uint32_t tmem_base, rank;
+    bool leader;
+    int worker, slot, warp, lane;
+};
+
+// TMA producer (one thread): the segments' A and B k-blocks into the ring of S
+// stages; `stage` and `phase` carry the ring position from call to call.
+template <class C, int S>
+__device__ __forceinline__ void producer_run(const CUtensorMap *pA, const CUtensorMap *pB, const GemmArgs &args,
+                                             const CtaCtx &x, int &stage, uint32_t &phase) {
+    uint8_t *stages = x.stages, *staging = x.staging, *aux_smem = x.aux_smem;
+    uint64_t *full_bar = x.full_bar, *empty_bar = x.empty_bar, *accf_bar = x.accf_bar, *acce_bar = x.acce_bar,
+             *aux_bar = x.aux_bar, *consumed_bar = x.consumed_bar;
+    volatile int *abort_flag = x.abort_flag;
+    float *rs = x.rs;
+    const uint32_t tmem_base = x.tmem_base, rank = x.rank;
+    const bool leader = x.leader;
+    const int worker = x.worker, slot = x.slot, warp = x.warp, lane = x.lane;
+    (void)stages; (void)staging; (void)aux_smem; (void)full_bar; (void)empty_bar; (void)accf_bar;
+    (void)acce_bar; (void)aux_bar; (void)consumed_bar; (void)abort_flag; (void)rs; (void)tmem_base;
+    (void)rank; (void)leader; (void)worker; (void)slot; (void)warp; (void)lane;
+    SegIter si = seg_begin<C::kTileM>(args, worker);
+    Seg w;
+    while (seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w)) {
+        const int a_row = w.m0 + static_cast<int>(rank) * kBM;       // this CTA's A rows
+        // this CTA's B rows (a K-major B's rows carry the expert offset)
+        const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows + (C::B_MN ? 0 : w.boff);
+        const int bk = C::B_MN ? w.boff : 0;  // an MN-major B's K carries it
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) return;
+            uint8_t *sa = stages + stage * C::kStageBytes;
+            uint8_t *sb = sa + C::kABytes;
+            const int k0 = kb * C::kBKe;
+            // where this CTA's A and B loads signal completion
+            uint32_t bar_a = smem_u32(&full_bar[stage]), bar_b = bar_a;
+            bool a_pair = false, b_pair = false;
+            if (!C::PAIR) {
+                mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+            } else if (leader) {
+                // the leader's barrier collects both CTAs' bytes
+                mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageBytes);
+            } else {
+                const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                a_pair = b_pair = true;
+                bar_a = bar_b = leader_full;
+            }
+            if (C::A_MN && args.a_mn3d) {
+                // one copy of all kBM / kMNBox boxes: the map's third
+                // dimension walks the MN blocks (see make_map_mn3d)
+                if (a_pair) tma_load_3d_pair(pA, bar_a, sa, 0, k0, a_row / C::kMNBox);
+                else tma_load_3d(pA, &full_bar[stage], sa, 0, k0, a_row / C::kMNBox);
+            } else if (C::A_MN) {
+#pragma unroll
+                for (int j = 0; j < kBM / C::kMNBox; ++j) {
+                    if (a_pair) tma_load_2d_pair(pA, bar_a, sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
+                    else tma_load_2d(pA, &full_bar[stage], sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
+                }
+            } else {
+                if (a_pair) tma_load_2d_pair(pA, bar_a, sa, k0, a_row);
+                else tma_load_2d(pA, &full_bar[stage], sa, k0, a_row);
+            }
+            if (C::B_MN && args.b_mn3d) {
+                if (b_pair) tma_load_3d_pair(pB, bar_b, sb, 0, k0 + bk, b_row / C::kMNBox);
+                else tma_load_3d(pB, &full_bar[stage], sb, 0, k0 + bk, b_row / C::kMNBox);
+            } else if (C::B_MN) {
+#pragma unroll
+                for (int j = 0; j < C::kBRows / C::kMNBox; ++j) {
+                    if (b_pair) tma_load_2d_pair(pB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
+                    else tma_load_2d(pB, &full_bar[stage], sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
+                }
+            } else {
+                if (b_pair) tma_load_2d_pair(pB, bar_b, sb, k0, b_row);
+                else tma_load_2d(pB, &full_bar[stage], sb, k0, b_row);
+            }
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// MMA issuer (one thread of the leader CTA): every segment's k-blocks into a
+// TMEM accumulator; `it` counts segments (the accumulator buffer's parity).
+template <class C, int S>
+__device__ __forceinline__ void mma_run(const GemmArgs &args, const CtaCtx &x, int &stage, uint32_t &phase,
+                                        int &it) {
+    uint8_t *stages = x.stages, *staging = x.staging, *aux_smem = x.aux_smem;
+    uint64_t *full_bar = x.full_bar, *empty_bar = x.empty_bar, *accf_bar = x.accf_bar, *acce_bar = x.acce_bar,
+             *aux_bar = x.aux_bar, *consumed_bar = x.consumed_bar;
+    volatile int *abort_flag = x.abort_flag;
+    float *rs = x.rs;
+    const uint32_t tmem_base = x.tmem_base, rank = x.rank;
+    const bool leader = x.leader;
+    const int worker = x.worker, slot = x.slot, warp = x.warp, lane = x.lane;
+    (void)stages; (void)staging; (void)aux_smem; (void)full_bar; (void)empty_bar; (void)accf_bar;
+    (void)acce_bar; (void)aux_bar; (void)consumed_bar; (void)abort_flag; (void)rs; (void)tmem_base;
+    (void)rank; (void)leader; (void)worker; (void)slot; (void)warp; (void)lane;
+    SegIter si = seg_begin<C::kTileM>(args, worker);
+    Seg w;
+    for (; seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w); ++it) {
+        const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+        const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+        if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + buf * C::BN;
+        bool failed = false;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+                failed = true;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_u32(stages + stage * C::kStageBytes);
+            const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < C::kBKe / C::kUmmaKe; ++kk) {
+                // K-major: the next 32 bytes of each row; MN-major: the next
+                // kUmmaKe rows of 128 bytes
+                const uint32_t mn_step = static_cast<uint32_t>(C::kUmmaKe * 128);
+                const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * mn_step, C::kMNBoxBytes, 1024)
+                                            : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * mn_step, C::kMNBoxBytes, 1024)
+                                            : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
+                const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                if (C::F8) {
+                    if (C::PAIR) umma_e4m3_pair(d_tmem, ad, bd, C::kIdesc, acc);
+                    else umma_e4m3(d_tmem, ad, bd, C::kIdesc, acc);
+                } else {
+                    if (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, acc);
+                    else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
+                }
+            }
+            // the stage is reusable (in both CTAs) once these MMAs finish
+            // (and, in-GEMM RMSNorm, once the norm warps have read its x)
+            if (C::PAIR) umma_commit_pair(&empty_bar[stage], 3);
+            else umma_commit(&empty_bar[stage]);
+            if (C::kNorm) {
+                if (C::PAIR) umma_commit_pair(&consumed_bar[stage], 3);
+                else umma_commit(&consumed_bar[stage]);
+            }
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (failed) break;
+        // accumulator ready for the epilogue(s)
+        if (C::PAIR) umma_commit_pair(&accf_bar[buf], 3);
+        else umma_commit(&accf_bar[buf]);
+    }
+}
+
+// Epilogue warp: every segment's accumulator out of TMEM, through the fused
+// epilogue, to global memory; `it` and `aux_phase` carry over between calls.
+template <class C, int S>
+__device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUtensorMap *pC1,
+                                             const CUtensorMap *pAux, const GemmArgs &args, const CtaCtx &x,
+                                             int &it, uint32_t &aux_phase) {
+    uint8_t *stages = x.stages, *staging = x.staging, *aux_smem = x.aux_smem;
+    uint64_t *full_bar = x.full_bar, *empty_bar = x.empty_bar, *accf_bar = x.accf_bar, *acce_bar = x.acce_bar,
+             *aux_bar = x.aux_bar, *consumed_bar = x.consumed_bar;
+    volatile int *abort_flag = x.abort_flag;
+    float *rs = x.rs;
+    const uint32_t tmem_base = x.tmem_base, rank = x.rank;
+    const bool leader = x.leader;
+    const int worker = x.worker, slot = x.slot, warp = x.warp, lane = x.lane;
+    (void)stages; (void)staging; (void)aux_smem; (void)full_bar; (void)empty_bar; (void)accf_bar;
+    (void)acce_bar; (void)aux_bar; (void)consumed_bar; (void)abort_flag; (void)rs; (void)tmem_base;
+    (void)rank; (void)leader; (void)worker; (void)slot; (void)warp; (void)lane;
+    const int q = warp & 3;                // TMEM lane quarter of this warp
+    const int ew = warp - 2;               // epilogue warp index
+    // this warp's chunks of a tile: all of them, or its half of them
+    const int c_lo = C::kEpiWarps == 8 ? ((ew >> 2) * C::kNumChunks) / 2 : 0;
+    const int c_hi = C::kEpiWarps == 8 ? (((ew >> 2) + 1) * C::kNumChunks) / 2 : C::kNumChunks;
+    const int row_in_tile = 32 * q + lane;
+    const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
+    uint8_t *aux_w = aux_smem + q * C::kNumChunks * 4096;  // this warp's 32 rows
+    constexpr int kUnits = C::BN / 32;  // 32-column units of a partial-slot row
+    constexpr int kSlotsPerWorker = C::PAIR ? 2 : 1;
+    // This warp's part of stream-K partial slot `sl`: 32-column unit u, vector
+    // j, lane -> float4 ((q * kUnits + u) * 8 + j) * 32 + lane, so that every
+    // warp-wide access is 512 contiguous bytes.
+    auto part_ptr = [&](int sl, int u, int j) {
+        return args.sk_partial + static_cast<size_t>(sl) * kSkSlotFloats +
+               ((static_cast<size_t>(q * kUnits + u) * 8 + j) * 32 + lane) * 4;
+    };
+    // The next segment's operands of this warp (its 32 rows of x or h into
+    // shared memory by TMA, its rows' rstd into a register) are fetched as
+    // soon as the current segment no longer needs them, so their latency
+    // overlaps the main loop instead of the epilogue.  A segment that only
+    // writes a partial sum needs neither.
+    bool aux_pending = false;  // a prefetch copy issued and not yet waited for
+    auto prefetch = [&](const Seg &wn, float &rsc_next) {
+        const int r0 = wn.m0 + static_cast<int>(rank) * kBM + 32 * q;
+        if (C::kRowScale)
+            rsc_next = args.rstd_in ? ((r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f) : 1.0f;
+        if (C::kAux && wn.kb0 == 0 && lane == 0) {
+            int nch = 0;
+            for (int c = c_lo; c < c_hi; ++c)
+                if (wn.n0 + c * C::kChunkCols < args.N) ++nch;
+            mbar_arrive_expect_tx(&aux_bar[ew], nch * 4096);
+            aux_pending = true;
+            for (int c = c_lo; c < c_lo + nch; ++c)
+                tma_load_2d(pAux, &aux_bar[ew], aux_w + c * 4096, wn.n0 + c * C::kChunkCols, r0);
+        }
+    };
+    int sbuf = 0;
+    float rsc_pre = 1.0f;
+    // max |output| of this thread's a (W1) or dh (dgrad-h) values, as stored in bf16
+    constexpr bool kAmaxEpi = C::kReluSq || C::EPI == kEpiDgradH;
+    const bool want_amax = kAmaxEpi && args.amax_out != nullptr;
+    float amax_t = 0.0f;
+    const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
+    SegIter si = seg_begin<C::kTileM>(args, worker);
+    Seg w;
+    bool have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
+    if (have) prefetch(w, rsc_pre);
+    for (; have; ++it) {
+        // The fused epilogues are nonlinear in the sum over k, so a tile split
+        // between workers is finished by the worker holding its first k-blocks
+        // (in its last segment); the others (in their first segment) leave
+        // fp32 partial sums, which it adds before the fused math.  Reduce
+        // epilogues are linear: every segment adds into the output as it is.
+        const bool head = w.kb0 == 0;
+        const bool to_partial = !C::kReduce && !head;
+        const bool fixup = !C::kReduce && head && w.kb1 < args.k_blocks;
+        const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
+        const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+        const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+        bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
+        if (C::kAux && head && ok) {
+            ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
+            if (ok) {
+                aux_pending = false;
+                aux_phase ^= 1u;
+            }
+        }
+        // a split tile's contributors: the next workers whose ranges start in it
+        int cw_end = worker + 1;
+        if (fixup) {
+            const int tile_end = (w.tile - si.dp_tiles + 1) * args.k_blocks;
+            while (cw_end < args.workers && sk_begin(si, cw_end) < tile_end) ++cw_end;
+            for (int cw = worker + 1; cw < cw_end && ok; ++cw)
+                ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * kMaxEpiWarps + ew],
+                               abort_flag);
+            // The first contributor's partial (this warp's units, 4 KB each) comes
+            // into the pipeline stages with one bulk copy: this is the worker's
+            // last segment, and its MMAs, which read the stages, have completed.
+            constexpr int kCU = C::kChunkCols / 32;
+            const int u_lo = c_lo * kCU, nu = (c_hi - c_lo) * kCU;
+            if (ok && lane == 0) {
+                fence_proxy_async_global();
+                mbar_arrive_expect_tx(&aux_bar[ew], nu * 4096);
+                bulk_copy_g2s(stages + (q * kUnits + u_lo) * 4096,
+                              part_ptr((worker + 1) * kSlotsPerWorker + static_cast<int>(rank), u_lo, 0) - lane * 4,
+                              nu * 4096, &aux_bar[ew]);
+            }
+            if (ok) {
+                ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
+                if (ok) aux_phase ^= 1u;
+            }
+        }
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after_sync();
+        const bool warp_rows = (m0 + 32 * q) < args.M;
+        float rsc = 1.0f;
+        if (C::EPI == kEpiFwdW1) rsc = rs[buf * 128 + row_in_tile];
+        if (C::kRowScale) rsc = rsc_pre;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
+
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; ++c) {
+            const int col0 = w.n0 + c * C::kChunkCols;
+            if (col0 >= args.N) break;
+            constexpr int kChunkUnits = C::kChunkCols / 32;
+            float v0[32], v1[32];
+            if (C::kOutBf16) tmem_load_64cols(t_row + c * C::kChunkCols, v0, v1);
+            else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
+            if (to_partial) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    st_global_v4(part_ptr(slot, c * kChunkUnits, j), v0[4 * j], v0[4 * j + 1],
+                                 v0[4 * j + 2], v0[4 * j + 3]);
+                    if (kChunkUnits == 2)
+                        st_global_v4(part_ptr(slot, c * kChunkUnits + 1, j), v1[4 * j], v1[4 * j + 1],
+                                     v1[4 * j + 2], v1[4 * j + 3]);
+                }
+                continue;
+            }
+            if (fixup) {
+                const uint32_t ps = smem_u32(stages + q * kUnits * 4096) + lane * 16;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 p = ld_shared_v4(ps + ((c * kChunkUnits) * 8 + j) * 512);
+                    v0[4 * j] += __uint_as_float(p.x); v0[4 * j + 1] += __uint_as_float(p.y);
+                    v0[4 * j + 2] += __uint_as_float(p.z); v0[4 * j + 3] += __uint_as_float(p.w);
+                    if (kChunkUnits == 2) {
+                        const uint4 p1 = ld_shared_v4(ps + ((c * kChunkUnits + 1) * 8 + j) * 512);
+                        v1[4 * j] += __uint_as_float(p1.x); v1[4 * j + 1] += __uint_as_float(p1.y);
+                        v1[4 * j + 2] += __uint_as_float(p1.z); v1[4 * j + 3] += __uint_as_float(p1.w);
+                    }
+                }
+                // further contributors (ranges shorter than a tile): from L2
+                for (int cw = worker + 2; cw < cw_end; ++cw) {
+                    const int sl = cw * kSlotsPerWorker + static_cast<int>(rank);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 p = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits, j));
+                        v0[4 * j] += p.x; v0[4 * j + 1] += p.y; v0[4 * j + 2] += p.z; v0[4 * j + 3] += p.w;
+                        if (kChunkUnits == 2) {
+                            const float4 p1 = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits + 1, j));
+                            v1[4 * j] += p1.x; v1[4 * j + 1] += p1.y; v1[4 * j + 2] += p1.z; v1[4 * j + 3] += p1.w;
+                        }
+                    }
+                }
+            }
+            if (C::F8) {
+                // E4M3 operands: the dequantisation scales of A and B
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v0[i] *= deq;
+                    if (kChunkUnits == 2) v1[i] *= deq;
+                }
+            }
+            // the fused epilogues' [M][N] operand: this row's 64 values of the
+            // chunk, from the swizzled shared copy (zero beyond M and N)
+            uint4 aux[8];
+            if (C::kAux) {
+                const uint32_t arow = smem_u32(aux_w + c * 4096) + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    aux[j] = ld_shared_v4(arow + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4));
+            }
+            float cs[32];
+            if (C::kColScale) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 g = make_uint4(0, 0, 0, 0);
+                    if (col0 + 8 * j < args.N) g = ld_global_nc_v4(args.colscale + col0 + 8 * j);
+                    cs[8 * j + 0] = bf16_lo(g.x); cs[8 * j + 1] = bf16_hi(g.x);
+                    cs[8 * j + 2] = bf16_lo(g.y); cs[8 * j + 3] = bf16_hi(g.y);
+                    cs[8 * j + 4] = bf16_lo(g.z); cs[8 * j + 5] = bf16_hi(g.z);
+                    cs[8 * j + 6] = bf16_lo(g.w); cs[8 * j + 7] = bf16_hi(g.w);
+                }
+            }
+
+            // the staging buffer written kStagingBufs chunks ago must have been
+            // read by its TMA store (in-place staging: this chunk's operand copy,
+            // already in registers, is not stored from before this tile ends)
+            if (!C::kAux) {
+                if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+                __syncwarp();
+            }
+            uint8_t *st0 = C::kAux ? aux_w + c * 4096
+                                   : staging + ((ew * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
+            uint8_t *st1 = C::kAux ? st0
+                                   : staging + ((ew * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
+            const uint32_t s0 = smem_u32(st0) + lane * 128;
+            const uint32_t s1 = smem_u32(st1) + lane * 128;
+            const uint32_t sw = static_cast<uint32_t>(lane & 7);
+
+            if (C::kOutBf16) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float e[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) e[i] = (j < 4) ? v0[8 * j + i] : v1[8 * (j - 4) + i];
+                    uint32_t o[4], o2[4];
+                    if (C::kReluSq) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float h0 = rsc * e[2 * i], h1 = rsc * e[2 * i + 1];
+                            const float r0 = h0 > 0.0f ? h0 : 0.0f, r1 = h1 > 0.0f ? h1 : 0.0f;
+                            if (C::kAOnly) {
+                                o[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                            } else {
+                                o[i] = pack_bf16x2(h0, h1);
+                                o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
+                            }
+                        }
+                        if (want_amax)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t av = C::kAOnly ? o[i] : o2[i];
+                                amax_t = fmaxf(amax_t, fmaxf(bf16_lo(av), bf16_hi(av)));  // a >= 0
+                            }
+                    } else if (C::EPI == kEpiStoreBf16) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
+                    } else if (C::EPI == kEpiFwdW2) {
+                        const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            o[i] = pack_bf16x2(bf16_lo(xs[i]) + e[2 * i], bf16_hi(xs[i]) + e[2 * i + 1]);
+                    } else {  // kEpiDgradH
+                        const uint32_t hs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float g0 = bf16_lo(hs[i]), g1 = bf16_hi(hs[i]);
+                            const float d0 = g0 > 0.0f ? rsc * e[2 * i] * (2.0f * g0) : 0.0f;
+                            const float d1 = g1 > 0.0f ? rsc * e[2 * i + 1] * (2.0f * g1) : 0.0f;
+                            o[i] = pack_bf16x2(d0, d1);
+                            if (want_amax)
+                                amax_t = fmaxf(amax_t, fmaxf(fabsf(bf16_lo(o[i])), fabsf(bf16_hi(o[i]))));
+                        }
+                    }
+                    const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
+                    st_shared_v4(s0 + off, o[0], o[1], o[2], o[3]);
+                    if (C::kNumOut == 2) st_shared_v4(s1 + off, o2[0], o2[1], o2[2], o2[3]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float e[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        e[i] = v0[4 * j + i];
+                        if (C::kColScale) e[i] *= cs[4 * j + i];
+                        if (C::EPI == kEpiStoreF32) e[i] *= rsc;
+                    }
+                    const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
+                    st_shared_v4(s0 + off, __float_as_uint(e[0]), __float_as_uint(e[1]),
+                                 __float_as_uint(e[2]), __float_as_uint(e[3]));
+                }
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                if (warp_rows) {
+                    const int r0 = m0 + 32 * q + w.crow;
+                    if (C::kReduce) {
+                        tma_reduce_add_2d(pC0, st0, col0, r0);
+                    } else {
+                        tma_store_2d(pC0, st0, col0, r0);
+                        if (C::kNumOut == 2) tma_store_2d(pC1, st1, col0, r0);
+                    }
+                }
+                bulk_commit_group();
+            }
+            sbuf = C::kStagingBufs == 2 ? sbuf ^ 1 : 0;
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+            // TMEM buffer free again (every tcgen05.ld of it has completed)
+            mbar_arrive_relaxed(&acce_bar[buf]);
+            if (C::PAIR && !leader) mbar_arrive_cluster_relaxed(leader_acce0 + buf * 8);
+            // in-place staging: the stores must have read the operand buffers
+            // before the next segment's operands are loaded into them
+            if (C::kAux) bulk_wait_group_read<0>();
+        }
+        if (to_partial) {
+            // every lane's partial stores are visible before the flag is (after
+            // the TMEM release, so the main loop does not wait for the stores)
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(&args.sk_flags[slot * kMaxEpiWarps + ew], 1);
+        }
+        // every lane is done with this segment's shared operand copy
+        have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
+        if (have) prefetch(w, rsc_pre);
+    }
+    if (lane == 0) {
+        bulk_wait_group<0>();
+        if (C::kAux && aux_pending) mbar_drain(&aux_bar[ew], aux_phase);
+    }
+    if (want_amax) {
+        // one maximum per epilogue warp; CTA 0 zeroes the slots no CTA holds
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax_t = fmaxf(amax_t, __shfl_xor_sync(0xffffffffu, amax_t, o));
+        if (lane == 0) args.amax_out[slot * kMaxEpiWarps + ew] = amax_t;
+        if (blockIdx.x == 0) {
+            // every slot no epilogue warp writes: the unused warps of each CTA and the CTAs not launched
+            for (int i = ew * 32 + lane; i < kMaxSkSlots * kMaxEpiWarps; i += C::kEpiWarps * 32)
+                if (i >= static_cast<int>(gridDim.x) * kMaxEpiWarps || i % kMaxEpiWarps >= C::kEpiWarps)
+                    args.amax_out[i] = 0.0f;
+        }
+    }
+    __syncwarp();
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -449,71 +937,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         griddep_launch_dependents();
     }
 
+    const CtaCtx x = {stages, staging, aux_smem, full_bar, empty_bar, accf_bar, acce_bar, aux_bar, consumed_bar,
+                      abort_flag, rs, tmem_base, rank, leader, worker, slot, warp, lane};
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !args.skip_loads) {
             int stage = 0;
             uint32_t phase = 0;
-            SegIter si = seg_begin<C::kTileM>(args, worker);
-            Seg w;
-            while (seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w)) {
-                const int a_row = w.m0 + static_cast<int>(rank) * kBM;       // this CTA's A rows
-                // this CTA's B rows (a K-major B's rows carry the expert offset)
-                const int b_row = w.n0 + static_cast<int>(rank) * C::kBRows + (C::B_MN ? 0 : w.boff);
-                const int bk = C::B_MN ? w.boff : 0;  // an MN-major B's K carries it
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) goto producer_done;
-                    uint8_t *sa = stages + stage * C::kStageBytes;
-                    uint8_t *sb = sa + C::kABytes;
-                    const int k0 = kb * C::kBKe;
-                    // where this CTA's A and B loads signal completion
-                    uint32_t bar_a = smem_u32(&full_bar[stage]), bar_b = bar_a;
-                    bool a_pair = false, b_pair = false;
-                    if (!C::PAIR) {
-                        mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
-                    } else if (leader) {
-                        // the leader's barrier collects both CTAs' bytes
-                        mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageBytes);
-                    } else {
-                        const uint32_t leader_full = mapa_shared(smem_u32(&full_bar[stage]), 0);
-                        a_pair = b_pair = true;
-                        bar_a = bar_b = leader_full;
-                    }
-                    if (C::A_MN && args.a_mn3d) {
-                        // one copy of all kBM / kMNBox boxes: the map's third
-                        // dimension walks the MN blocks (see make_map_mn3d)
-                        if (a_pair) tma_load_3d_pair(&tmA, bar_a, sa, 0, k0, a_row / C::kMNBox);
-                        else tma_load_3d(&tmA, &full_bar[stage], sa, 0, k0, a_row / C::kMNBox);
-                    } else if (C::A_MN) {
-#pragma unroll
-                        for (int j = 0; j < kBM / C::kMNBox; ++j) {
-                            if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
-                            else tma_load_2d(&tmA, &full_bar[stage], sa + j * C::kMNBoxBytes, a_row + C::kMNBox * j, k0);
-                        }
-                    } else {
-                        if (a_pair) tma_load_2d_pair(&tmA, bar_a, sa, k0, a_row);
-                        else tma_load_2d(&tmA, &full_bar[stage], sa, k0, a_row);
-                    }
-                    if (C::B_MN && args.b_mn3d) {
-                        if (b_pair) tma_load_3d_pair(&tmB, bar_b, sb, 0, k0 + bk, b_row / C::kMNBox);
-                        else tma_load_3d(&tmB, &full_bar[stage], sb, 0, k0 + bk, b_row / C::kMNBox);
-                    } else if (C::B_MN) {
-#pragma unroll
-                        for (int j = 0; j < C::kBRows / C::kMNBox; ++j) {
-                            if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
-                            else tma_load_2d(&tmB, &full_bar[stage], sb + j * C::kMNBoxBytes, b_row + C::kMNBox * j, k0 + bk);
-                        }
-                    } else {
-                        if (b_pair) tma_load_2d_pair(&tmB, bar_b, sb, k0, b_row);
-                        else tma_load_2d(&tmB, &full_bar[stage], sb, k0, b_row);
-                    }
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        producer_done:;
+            producer_run<C, C::kStages>(&tmA, &tmB, args, x, stage, phase);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -522,375 +953,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            SegIter si = seg_begin<C::kTileM>(args, worker);
-            Seg w;
-            for (; seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w); ++it) {
-                const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
-                const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
-                if (!mbar_wait(&acce_bar[buf], aph ^ 1u, abort_flag)) break;
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * C::BN;
-                bool failed = false;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(stages + stage * C::kStageBytes);
-                    const uint32_t b_addr = a_addr + C::kABytes;
-#pragma unroll
-                    for (int kk = 0; kk < C::kBKe / C::kUmmaKe; ++kk) {
-                        // K-major: the next 32 bytes of each row; MN-major: the next
-                        // kUmmaKe rows of 128 bytes
-                        const uint32_t mn_step = static_cast<uint32_t>(C::kUmmaKe * 128);
-                        const uint64_t ad = C::A_MN ? smem_desc_sw128(a_addr + kk * mn_step, C::kMNBoxBytes, 1024)
-                                                    : smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = C::B_MN ? smem_desc_sw128(b_addr + kk * mn_step, C::kMNBoxBytes, 1024)
-                                                    : smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        if (C::F8) {
-                            if (C::PAIR) umma_e4m3_pair(d_tmem, ad, bd, C::kIdesc, acc);
-                            else umma_e4m3(d_tmem, ad, bd, C::kIdesc, acc);
-                        } else {
-                            if (C::PAIR) umma_bf16_pair(d_tmem, ad, bd, C::kIdesc, acc);
-                            else umma_bf16(d_tmem, ad, bd, C::kIdesc, acc);
-                        }
-                    }
-                    // the stage is reusable (in both CTAs) once these MMAs finish
-                    // (and, in-GEMM RMSNorm, once the norm warps have read its x)
-                    if (C::PAIR) umma_commit_pair(&empty_bar[stage], 3);
-                    else umma_commit(&empty_bar[stage]);
-                    if (C::kNorm) {
-                        if (C::PAIR) umma_commit_pair(&consumed_bar[stage], 3);
-                        else umma_commit(&consumed_bar[stage]);
-                    }
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (failed) break;
-                // accumulator ready for the epilogue(s)
-                if (C::PAIR) umma_commit_pair(&accf_bar[buf], 3);
-                else umma_commit(&accf_bar[buf]);
-            }
+            mma_run<C, C::kStages>(args, x, stage, phase, it);
         }
         __syncwarp();
     } else if (warp < 2 + C::kEpiWarps) {
         // --------------------------------------------------------- epilogue
-        const int q = warp & 3;                // TMEM lane quarter of this warp
-        const int ew = warp - 2;               // epilogue warp index
-        // this warp's chunks of a tile: all of them, or its half of them
-        const int c_lo = C::kEpiWarps == 8 ? ((ew >> 2) * C::kNumChunks) / 2 : 0;
-        const int c_hi = C::kEpiWarps == 8 ? (((ew >> 2) + 1) * C::kNumChunks) / 2 : C::kNumChunks;
-        const int row_in_tile = 32 * q + lane;
-        const uint32_t leader_acce0 = C::PAIR ? mapa_shared(smem_u32(&acce_bar[0]), 0) : 0u;
-        uint8_t *aux_w = aux_smem + q * C::kNumChunks * 4096;  // this warp's 32 rows
-        constexpr int kUnits = C::BN / 32;  // 32-column units of a partial-slot row
-        constexpr int kSlotsPerWorker = C::PAIR ? 2 : 1;
-        // This warp's part of stream-K partial slot `sl`: 32-column unit u, vector
-        // j, lane -> float4 ((q * kUnits + u) * 8 + j) * 32 + lane, so that every
-        // warp-wide access is 512 contiguous bytes.
-        auto part_ptr = [&](int sl, int u, int j) {
-            return args.sk_partial + static_cast<size_t>(sl) * kSkSlotFloats +
-                   ((static_cast<size_t>(q * kUnits + u) * 8 + j) * 32 + lane) * 4;
-        };
-        // The next segment's operands of this warp (its 32 rows of x or h into
-        // shared memory by TMA, its rows' rstd into a register) are fetched as
-        // soon as the current segment no longer needs them, so their latency
-        // overlaps the main loop instead of the epilogue.  A segment that only
-        // writes a partial sum needs neither.
-        bool aux_pending = false;  // a prefetch copy issued and not yet waited for
-        auto prefetch = [&](const Seg &wn, float &rsc_next) {
-            const int r0 = wn.m0 + static_cast<int>(rank) * kBM + 32 * q;
-            if (C::kRowScale)
-                rsc_next = args.rstd_in ? ((r0 + lane < args.M) ? args.rstd_in[r0 + lane] : 0.0f) : 1.0f;
-            if (C::kAux && wn.kb0 == 0 && lane == 0) {
-                int nch = 0;
-                for (int c = c_lo; c < c_hi; ++c)
-                    if (wn.n0 + c * C::kChunkCols < args.N) ++nch;
-                mbar_arrive_expect_tx(&aux_bar[ew], nch * 4096);
-                aux_pending = true;
-                for (int c = c_lo; c < c_lo + nch; ++c)
-                    tma_load_2d(&tmAux, &aux_bar[ew], aux_w + c * 4096, wn.n0 + c * C::kChunkCols, r0);
-            }
-        };
         int it = 0;
-        int sbuf = 0;
         uint32_t aux_phase = 0;
-        float rsc_pre = 1.0f;
-        // max |output| of this thread's a (W1) or dh (dgrad-h) values, as stored in bf16
-        constexpr bool kAmaxEpi = C::kReluSq || C::EPI == kEpiDgradH;
-        const bool want_amax = kAmaxEpi && args.amax_out != nullptr;
-        float amax_t = 0.0f;
-        const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
-        SegIter si = seg_begin<C::kTileM>(args, worker);
-        Seg w;
-        bool have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
-        if (have) prefetch(w, rsc_pre);
-        for (; have; ++it) {
-            // The fused epilogues are nonlinear in the sum over k, so a tile split
-            // between workers is finished by the worker holding its first k-blocks
-            // (in its last segment); the others (in their first segment) leave
-            // fp32 partial sums, which it adds before the fused math.  Reduce
-            // epilogues are linear: every segment adds into the output as it is.
-            const bool head = w.kb0 == 0;
-            const bool to_partial = !C::kReduce && !head;
-            const bool fixup = !C::kReduce && head && w.kb1 < args.k_blocks;
-            const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
-            const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
-            const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
-            bool ok = mbar_wait(&accf_bar[buf], aph, abort_flag);
-            if (C::kAux && head && ok) {
-                ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
-                if (ok) {
-                    aux_pending = false;
-                    aux_phase ^= 1u;
-                }
-            }
-            // a split tile's contributors: the next workers whose ranges start in it
-            int cw_end = worker + 1;
-            if (fixup) {
-                const int tile_end = (w.tile - si.dp_tiles + 1) * args.k_blocks;
-                while (cw_end < args.workers && sk_begin(si, cw_end) < tile_end) ++cw_end;
-                for (int cw = worker + 1; cw < cw_end && ok; ++cw)
-                    ok = flag_wait(&args.sk_flags[(cw * kSlotsPerWorker + static_cast<int>(rank)) * kMaxEpiWarps + ew],
-                                   abort_flag);
-                // The first contributor's partial (this warp's units, 4 KB each) comes
-                // into the pipeline stages with one bulk copy: this is the worker's
-                // last segment, and its MMAs, which read the stages, have completed.
-                constexpr int kCU = C::kChunkCols / 32;
-                const int u_lo = c_lo * kCU, nu = (c_hi - c_lo) * kCU;
-                if (ok && lane == 0) {
-                    fence_proxy_async_global();
-                    mbar_arrive_expect_tx(&aux_bar[ew], nu * 4096);
-                    bulk_copy_g2s(stages + (q * kUnits + u_lo) * 4096,
-                                  part_ptr((worker + 1) * kSlotsPerWorker + static_cast<int>(rank), u_lo, 0) - lane * 4,
-                                  nu * 4096, &aux_bar[ew]);
-                }
-                if (ok) {
-                    ok = mbar_wait(&aux_bar[ew], aux_phase, abort_flag);
-                    if (ok) aux_phase ^= 1u;
-                }
-            }
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after_sync();
-            const bool warp_rows = (m0 + 32 * q) < args.M;
-            float rsc = 1.0f;
-            if (C::EPI == kEpiFwdW1) rsc = rs[buf * 128 + row_in_tile];
-            if (C::kRowScale) rsc = rsc_pre;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * C::BN;
-
-#pragma unroll 1
-            for (int c = c_lo; c < c_hi; ++c) {
-                const int col0 = w.n0 + c * C::kChunkCols;
-                if (col0 >= args.N) break;
-                constexpr int kChunkUnits = C::kChunkCols / 32;
-                float v0[32], v1[32];
-                if (C::kOutBf16) tmem_load_64cols(t_row + c * C::kChunkCols, v0, v1);
-                else tmem_load_32cols(t_row + c * C::kChunkCols, v0);
-                if (to_partial) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        st_global_v4(part_ptr(slot, c * kChunkUnits, j), v0[4 * j], v0[4 * j + 1],
-                                     v0[4 * j + 2], v0[4 * j + 3]);
-                        if (kChunkUnits == 2)
-                            st_global_v4(part_ptr(slot, c * kChunkUnits + 1, j), v1[4 * j], v1[4 * j + 1],
-                                         v1[4 * j + 2], v1[4 * j + 3]);
-                    }
-                    continue;
-                }
-                if (fixup) {
-                    const uint32_t ps = smem_u32(stages + q * kUnits * 4096) + lane * 16;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 p = ld_shared_v4(ps + ((c * kChunkUnits) * 8 + j) * 512);
-                        v0[4 * j] += __uint_as_float(p.x); v0[4 * j + 1] += __uint_as_float(p.y);
-                        v0[4 * j + 2] += __uint_as_float(p.z); v0[4 * j + 3] += __uint_as_float(p.w);
-                        if (kChunkUnits == 2) {
-                            const uint4 p1 = ld_shared_v4(ps + ((c * kChunkUnits + 1) * 8 + j) * 512);
-                            v1[4 * j] += __uint_as_float(p1.x); v1[4 * j + 1] += __uint_as_float(p1.y);
-                            v1[4 * j + 2] += __uint_as_float(p1.z); v1[4 * j + 3] += __uint_as_float(p1.w);
-                        }
-                    }
-                    // further contributors (ranges shorter than a tile): from L2
-                    for (int cw = worker + 2; cw < cw_end; ++cw) {
-                        const int sl = cw * kSlotsPerWorker + static_cast<int>(rank);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 p = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits, j));
-                            v0[4 * j] += p.x; v0[4 * j + 1] += p.y; v0[4 * j + 2] += p.z; v0[4 * j + 3] += p.w;
-                            if (kChunkUnits == 2) {
-                                const float4 p1 = ld_global_cg_v4(part_ptr(sl, c * kChunkUnits + 1, j));
-                                v1[4 * j] += p1.x; v1[4 * j + 1] += p1.y; v1[4 * j + 2] += p1.z; v1[4 * j + 3] += p1.w;
-                            }
-                        }
-                    }
-                }
-                if (C::F8) {
-                    // E4M3 operands: the dequantisation scales of A and B
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v0[i] *= deq;
-                        if (kChunkUnits == 2) v1[i] *= deq;
-                    }
-                }
-                // the fused epilogues' [M][N] operand: this row's 64 values of the
-                // chunk, from the swizzled shared copy (zero beyond M and N)
-                uint4 aux[8];
-                if (C::kAux) {
-                    const uint32_t arow = smem_u32(aux_w + c * 4096) + lane * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        aux[j] = ld_shared_v4(arow + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4));
-                }
-                float cs[32];
-                if (C::kColScale) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 g = make_uint4(0, 0, 0, 0);
-                        if (col0 + 8 * j < args.N) g = ld_global_nc_v4(args.colscale + col0 + 8 * j);
-                        cs[8 * j + 0] = bf16_lo(g.x); cs[8 * j + 1] = bf16_hi(g.x);
-                        cs[8 * j + 2] = bf16_lo(g.y); cs[8 * j + 3] = bf16_hi(g.y);
-                        cs[8 * j + 4] = bf16_lo(g.z); cs[8 * j + 5] = bf16_hi(g.z);
-                        cs[8 * j + 6] = bf16_lo(g.w); cs[8 * j + 7] = bf16_hi(g.w);
-                    }
-                }
-
-                // the staging buffer written kStagingBufs chunks ago must have been
-                // read by its TMA store (in-place staging: this chunk's operand copy,
-                // already in registers, is not stored from before this tile ends)
-                if (!C::kAux) {
-                    if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
-                    __syncwarp();
-                }
-                uint8_t *st0 = C::kAux ? aux_w + c * 4096
-                                       : staging + ((ew * C::kNumOut + 0) * C::kStagingBufs + sbuf) * 4096;
-                uint8_t *st1 = C::kAux ? st0
-                                       : staging + ((ew * C::kNumOut + (C::kNumOut - 1)) * C::kStagingBufs + sbuf) * 4096;
-                const uint32_t s0 = smem_u32(st0) + lane * 128;
-                const uint32_t s1 = smem_u32(st1) + lane * 128;
-                const uint32_t sw = static_cast<uint32_t>(lane & 7);
-
-                if (C::kOutBf16) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float e[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) e[i] = (j < 4) ? v0[8 * j + i] : v1[8 * (j - 4) + i];
-                        uint32_t o[4], o2[4];
-                        if (C::kReluSq) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float h0 = rsc * e[2 * i], h1 = rsc * e[2 * i + 1];
-                                const float r0 = h0 > 0.0f ? h0 : 0.0f, r1 = h1 > 0.0f ? h1 : 0.0f;
-                                if (C::kAOnly) {
-                                    o[i] = pack_bf16x2(r0 * r0, r1 * r1);
-                                } else {
-                                    o[i] = pack_bf16x2(h0, h1);
-                                    o2[i] = pack_bf16x2(r0 * r0, r1 * r1);
-                                }
-                            }
-                            if (want_amax)
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const uint32_t av = C::kAOnly ? o[i] : o2[i];
-                                    amax_t = fmaxf(amax_t, fmaxf(bf16_lo(av), bf16_hi(av)));  // a >= 0
-                                }
-                        } else if (C::EPI == kEpiStoreBf16) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
-                        } else if (C::EPI == kEpiFwdW2) {
-                            const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = pack_bf16x2(bf16_lo(xs[i]) + e[2 * i], bf16_hi(xs[i]) + e[2 * i + 1]);
-                        } else {  // kEpiDgradH
-                            const uint32_t hs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float g0 = bf16_lo(hs[i]), g1 = bf16_hi(hs[i]);
-                                const float d0 = g0 > 0.0f ? rsc * e[2 * i] * (2.0f * g0) : 0.0f;
-                                const float d1 = g1 > 0.0f ? rsc * e[2 * i + 1] * (2.0f * g1) : 0.0f;
-                                o[i] = pack_bf16x2(d0, d1);
-                                if (want_amax)
-                                    amax_t = fmaxf(amax_t, fmaxf(fabsf(bf16_lo(o[i])), fabsf(bf16_hi(o[i]))));
-                            }
-                        }
-                        const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
-                        st_shared_v4(s0 + off, o[0], o[1], o[2], o[3]);
-                        if (C::kNumOut == 2) st_shared_v4(s1 + off, o2[0], o2[1], o2[2], o2[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float e[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            e[i] = v0[4 * j + i];
-                            if (C::kColScale) e[i] *= cs[4 * j + i];
-                            if (C::EPI == kEpiStoreF32) e[i] *= rsc;
-                        }
-                        const uint32_t off = ((static_cast<uint32_t>(j) ^ sw) << 4);
-                        st_shared_v4(s0 + off, __float_as_uint(e[0]), __float_as_uint(e[1]),
-                                     __float_as_uint(e[2]), __float_as_uint(e[3]));
-                    }
-                }
-                fence_proxy_async_shared();
-                __syncwarp();
-                if (lane == 0) {
-                    if (warp_rows) {
-                        const int r0 = m0 + 32 * q + w.crow;
-                        if (C::kReduce) {
-                            tma_reduce_add_2d(&tmC0, st0, col0, r0);
-                        } else {
-                            tma_store_2d(&tmC0, st0, col0, r0);
-                            if (C::kNumOut == 2) tma_store_2d(&tmC1, st1, col0, r0);
-                        }
-                    }
-                    bulk_commit_group();
-                }
-                sbuf = C::kStagingBufs == 2 ? sbuf ^ 1 : 0;
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                // TMEM buffer free again (every tcgen05.ld of it has completed)
-                mbar_arrive_relaxed(&acce_bar[buf]);
-                if (C::PAIR && !leader) mbar_arrive_cluster_relaxed(leader_acce0 + buf * 8);
-                // in-place staging: the stores must have read the operand buffers
-                // before the next segment's operands are loaded into them
-                if (C::kAux) bulk_wait_group_read<0>();
-            }
-            if (to_partial) {
-                // every lane's partial stores are visible before the flag is (after
-                // the TMEM release, so the main loop does not wait for the stores)
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_gpu(&args.sk_flags[slot * kMaxEpiWarps + ew], 1);
-            }
-            // every lane is done with this segment's shared operand copy
-            have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
-            if (have) prefetch(w, rsc_pre);
-        }
-        if (lane == 0) {
-            bulk_wait_group<0>();
-            if (C::kAux && aux_pending) mbar_drain(&aux_bar[ew], aux_phase);
-        }
-        if (want_amax) {
-            // one maximum per epilogue warp; CTA 0 zeroes the slots no CTA holds
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax_t = fmaxf(amax_t, __shfl_xor_sync(0xffffffffu, amax_t, o));
-            if (lane == 0) args.amax_out[slot * kMaxEpiWarps + ew] = amax_t;
-            if (blockIdx.x == 0) {
-                // every slot no epilogue warp writes: the unused warps of each CTA and the CTAs not launched
-                for (int i = ew * 32 + lane; i < kMaxSkSlots * kMaxEpiWarps; i += C::kEpiWarps * 32)
-                    if (i >= static_cast<int>(gridDim.x) * kMaxEpiWarps || i % kMaxEpiWarps >= C::kEpiWarps)
-                        args.amax_out[i] = 0.0f;
-            }
-        }
-        __syncwarp();
+        epilogue_run<C, C::kStages>(&tmC0, &tmC1, &tmAux, args, x, it, aux_phase);
     } else if (C::kSide) {
         // ------------------------------- RMSNorm backward rows (side warps)
         // dn_s is the previous kernel's output: these warps wait for it, while
@@ -1053,10 +1123,10 @@ inline int raster_group_m() {
 
 // Builds the tensor maps and launches one GEMM of configuration C.  Pair mode
 // launches clusters of two CTAs, one pair per two SMs.
+// The tensor maps of one GEMM of configuration C (sets a.a_mn3d, a.b_mn3d).
 template <class C>
-int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
-                GemmArgs a, int num_sms, cudaStream_t stream) {
-    CUtensorMap mA, mB, mC0, mC1, mAux;
+bool build_maps(int M, int N, int K, const void *A, const void *B, void *C0, void *C1, GemmArgs &a,
+                CUtensorMap &mA, CUtensorMap &mB, CUtensorMap &mC0, CUtensorMap &mC1, CUtensorMap &mAux) {
     bool ok = true;
     // operands: 128-byte box rows (kBKe values of K, or kMNBox values of M / N)
     const int op = C::F8 ? kMapU8 : kMapBf16;
@@ -1084,7 +1154,14 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     // the epilogue's [M][N] operand (row stride N), in the output chunks' boxes
     if (C::kAux) ok &= a.aux != nullptr && a.ld_aux == N && make_map_2d(&mAux, a.aux, kMapBf16, N, M, 64, 32);
     else mAux = mC0;
-    if (!ok) return MLPBLK_ECUDA;
+    return ok;
+}
+
+template <class C>
+int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, void *C1,
+                GemmArgs a, int num_sms, cudaStream_t stream) {
+    CUtensorMap mA, mB, mC0, mC1, mAux;
+    if (!build_maps<C>(M, N, K, A, B, C0, C1, a, mA, mB, mC0, mC1, mAux)) return MLPBLK_ECUDA;
 
     // concurrent tile workers: one CTA (pair) per SM (pair of SMs), at most one
     // stream-K partial slot per CTA

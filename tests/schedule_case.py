@@ -52,6 +52,7 @@ if __name__ == "__main__":
     import mlp_block_backprop_gb300 as mb
     dense(520, 520, 520, 2)
     dense(1024, 512, 2048, 2)
+    dense(2048, 256, 2560, 1)   # a 256 x 256 dgrad-h tile for every CTA pair
     routed(600, 512, 512, 4, 2)
     routed(300, 256, 256, 4, 3)
     rc = mb.mlpblk_last_error()

@@ -23,6 +23,7 @@ SETTINGS = [
     {"MLPBLK_GROUP_M": "3"},          # another raster
     {"MLPBLK_MAX_SMS": "38"},         # a quarter of the SMs
     {"MLPBLK_SIDE_NORM": "0"},        # RMSNorm backward in its own kernel at every width
+    {"MLPBLK_MN3D": "0"},             # MN-major operands box by box
 ]
 
 
