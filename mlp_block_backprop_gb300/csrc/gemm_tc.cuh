@@ -153,6 +153,7 @@ __device__ __forceinline__ int sk_begin(const GemmArgs &a, int w) {
 struct SegIter {
     int worker, j, n_dp, pos, end, m_tiles;
     int dp_tiles, sk_base, sk_rem, sk_total;  // the schedule (device-computed when M-grouped and split)
+    int sub_j, sub_n;                         // k-parts of the last tiles (GemmArgs::sub_parts)
 };
 
 __device__ __forceinline__ int sk_begin(const SegIter &it, int w) {
@@ -169,6 +170,7 @@ __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
     it.sk_base = a.sk_base;
     it.sk_rem = a.sk_rem;
     it.sk_total = a.sk_total;
+    it.sub_j = it.sub_n = 0;
     if (a.grp_mode == kGroupM && a.grp_split) {
         // M-grouped with the split schedule: the host's rule (whole-tile rounds
         // while more than two remain, then the k-blocks split evenly) applied to
@@ -197,6 +199,12 @@ __device__ __forceinline__ SegIter seg_begin(const GemmArgs &a, int worker) {
         return it;
     }
     it.n_dp = a.dp_tiles / a.workers;
+    if (a.sub_parts > 0) {
+        const int items = (a.tiles - a.dp_tiles) * a.sub_parts;
+        it.sub_n = items > worker ? (items - worker + a.workers - 1) / a.workers : 0;
+        it.pos = it.end = 0;
+        return it;
+    }
     it.pos = sk_begin(a, worker);
     it.end = sk_begin(a, worker + 1);
     return it;
@@ -213,6 +221,15 @@ __device__ __forceinline__ bool seg_next(const GemmArgs &a, SegIter &it, Seg &s)
             s.kb0 = 0;
             s.kb1 = a.k_blocks;
             ++it.j;
+        } else if (it.sub_j < it.sub_n) {
+            // k-part `part` of tile dp_tiles + i: the parts go round robin, part by part
+            const int item = it.worker + it.sub_j * a.workers;
+            const int rem = a.tiles - it.dp_tiles;
+            const int part = item / rem;
+            t = it.dp_tiles + (item - part * rem);
+            s.kb0 = part * a.sub_kb;
+            s.kb1 = min(a.k_blocks, s.kb0 + a.sub_kb);
+            ++it.sub_j;
         } else if (it.pos < it.end) {
             const int tt = it.pos / a.k_blocks;
             s.kb0 = it.pos - tt * a.k_blocks;
@@ -1088,6 +1105,16 @@ inline bool make_map_mn3d(CUtensorMap *m, const void *ptr, int type, uint64_t mn
     return r == CUDA_SUCCESS;
 }
 
+// MLPBLK_SUBSPLIT=0 keeps stream-K ranges for the reduce GEMMs' last round.
+inline bool sub_split_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_SUBSPLIT");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 // MLPBLK_MN3D=0 loads MN-major operands box by box (2-D copies) everywhere.
 inline bool mn3d_enabled() {
     static int v = -1;
@@ -1211,6 +1238,29 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
         a.sk_base = iters / workers;
         a.sk_rem = iters % workers;
         a.sk_total = iters;
+    }
+    a.sub_parts = 0;
+    a.sub_kb = 0;
+    const int64_t operand_bytes = (static_cast<int64_t>(M) + N) * K * (C::F8 ? 1 : 2);
+    if (C::kReduce && sk && a.grp_mode == kGroupNone && tiles % workers != 0 && operand_bytes > (64ll << 20) &&
+        sub_split_enabled()) {
+        // the last partial round of tiles in k-parts rather than stream-K ranges:
+        // S parts of ceil(kb / S) k-blocks (at least 8), S minimising the parts'
+        // rounds ceil(R S / workers) / S
+        const int full = tiles / workers, rem = tiles - full * workers;
+        int best_s = 1;
+        double best = 1e30;
+        for (int sp = 1; sp <= 8 && (kb + sp - 1) / sp >= 8; ++sp) {
+            const double cost = static_cast<double>((rem * sp + workers - 1) / workers) * ((kb + sp - 1) / sp);
+            if (cost < best - 1e-9) {
+                best = cost;
+                best_s = sp;
+            }
+        }
+        a.dp_tiles = full * workers;
+        a.sub_parts = best_s;
+        a.sub_kb = (kb + best_s - 1) / best_s;
+        a.sk_base = a.sk_rem = a.sk_total = 0;
     }
     a.workers = workers;
     if (a.grid_out) *a.grid_out = cta_per_worker * workers;

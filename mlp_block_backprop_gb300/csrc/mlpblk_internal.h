@@ -133,6 +133,11 @@ struct GemmArgs {
     // iterations of tiles [dp_tiles, tiles) are cut into contiguous ranges of
     // sk_base (+1 for the first sk_rem workers) each ("stream-K").
     int workers, dp_tiles, sk_base, sk_rem, sk_total;
+    // reduce (+=) GEMMs whose operands exceed L2: the tiles after dp_tiles are
+    // cut into sub_parts ranges of sub_kb k-blocks, dealt round robin part by
+    // part, so that the workers of a round stream the same k-range of tiles
+    // that share operand panels (0: the stream-K ranges above)
+    int sub_parts, sub_kb;
     float *sk_partial;         // kMaxSkSlots slots of kSkSlotFloats: split-tile partial sums
     int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
