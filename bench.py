@@ -295,14 +295,15 @@ def recorded_traffic(workload, kernel):
     return None
 
 
-def algorithmic_work(kind, T, d, F, parts, prefold=False):
-    """(amount, unit) per launch: FLOP for the GEMMs, bytes for the HBM-bound kernels."""
+def algorithmic_work(kind, T, d, F, parts, prefold=False, dn_bytes=2):
+    """(amount, unit) per launch: FLOP for the GEMMs, bytes for the HBM-bound kernels.
+    dn_bytes: the element size of dn_s (bf16 on the bf16 path, fp32 on the FP8 path)."""
     if kind in GEMM_KINDS:
         return 2.0 * T * d * F, "flop"
     if kind == "norm_bwd":
-        # x, dy (bf16) and dn (fp32) read, dx (bf16) written, rstd and gamma read; the
+        # x, dy (bf16) and dn_s read, dx (bf16) written, rstd and gamma read; the
         # dgamma partial rows (a few MB of scratch) are not counted
-        return T * d * (2 + 2 + 4 + 2) + 4.0 * T + 2.0 * d, "byte"
+        return T * d * (2 + 2 + dn_bytes + 2) + 4.0 * T + 2.0 * d, "byte"
     if kind == "fold_gamma":
         if prefold:  # once per step: W1 read, W1*gamma written
             return 2.0 * F * d * 2 + 2.0 * d, "byte"
@@ -495,7 +496,7 @@ def run_ours(args, dist, peaks):
     def roofline(kind):
         if kind not in per:
             return None
-        amount, unit = algorithmic_work(kind, T, d, F, parts, prefold)
+        amount, unit = algorithmic_work(kind, T, d, F, parts, prefold, dn_bytes=4 if fp8 else 2)
         if amount is None:  # a launch with no bandwidth or FLOP roof of its own (a scalar finalize)
             return None
         mean_s = per[kind][1] / per[kind][0] * 1e-3

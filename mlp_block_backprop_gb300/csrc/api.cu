@@ -4,7 +4,7 @@
 // Forward  (bf16): fold gamma into W1 -> W1 GEMM (rstd prologue, h/a epilogue)
 //                  -> W2 GEMM (residual epilogue)
 // Backward (bf16): wgrad W2 GEMM (+=) -> dgrad-h GEMM (gate, dh_s = rstd*dh)
-//                  -> dgrad-n GEMM (dn_s = rstd*dn) -> wgrad W1 GEMM (+= , gamma)
+//                  -> dgrad-n GEMM (dn_s = rstd*dn, bf16) -> wgrad W1 GEMM (+= , gamma)
 //                  -> RMSNorm backward rows (dx, dgamma partials) -> dgamma (+=)
 //                  (d_model <= 768: the rows run on the wgrad-W1 GEMM's side warps)
 // The fp32 element type runs the same sequence on CUDA cores.
@@ -76,7 +76,7 @@ WsLayout ws_layout(const mlpblk_desc *d, bool recompute) {
     l.a = recompute ? off : -1;
     if (recompute) off += tf;
     l.dn = off;
-    l.part = l.dn + align256(d->tokens * d->d_model * 4);
+    l.part = l.dn + align256(d->tokens * d->d_model * elt);  // dn_s in the block dtype
     const int64_t bwd = l.part + align256(static_cast<int64_t>(kMaxParts) * d->d_model * 4);
     // the GEMMs' stream-K partial sums and flags, apart from everything above
     l.sk_partial = fd > bwd ? fd : bwd;
@@ -323,7 +323,7 @@ int forward_impl(const mlpblk_desc *desc, const void *x, const void *gamma, cons
 int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
                   const void *w1, const void *w2, const void *h_saved, const void *a_saved,
                   const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
-                  void *dh_s, float *dn_s, float *part, float *sk_partial, int *sk_flags, int sms,
+                  void *dh_s, void *dn_s, float *part, float *sk_partial, int *sk_flags, int sms,
                   cudaStream_t s) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     int parts = 0;  // dgamma partial rows written by the norm kernel
@@ -350,7 +350,8 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         gn.sk_partial = sk_partial;
         gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
         gn.pdl = kPdlWaitFirst;
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreF32, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
+        // dn_s = rstd * dn stored in bf16 like dh_s (rstd rides in dh_s already)
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreBf16, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);
         gw1.pdl = kPdlDeferWait;
@@ -360,7 +361,7 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
             gw1.side.x = static_cast<const uint16_t *>(x);
             gw1.side.dy = static_cast<const uint16_t *>(dy);
             gw1.side.gamma = static_cast<const uint16_t *>(gamma);
-            gw1.side.dn_s = dn_s;
+            gw1.side.dn_s = static_cast<const uint16_t *>(dn_s);
             gw1.side.rstd = rstd_saved;
             gw1.side.dx = static_cast<uint16_t *>(dx);
             gw1.side.part = part;
@@ -385,12 +386,12 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_simt(kEpiAccF32, (int)d, (int)F, (int)T, dyf, 1, d,
                                     static_cast<const float *>(a_saved), 1, F, dw2, nullptr, e0, s));
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_simt(kEpiStoreF32, (int)T, (int)d, (int)F, dhf, F, 1,
-                                    static_cast<const float *>(w1), 1, d, dn_s, nullptr, e0, s));
+                                    static_cast<const float *>(w1), 1, d, static_cast<float *>(dn_s), nullptr, e0, s));
         SimtEpi ec = {nullptr, nullptr, static_cast<const float *>(gamma)};
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_simt(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dhf, 1, F, xf, 1, d,
                                     dw1, nullptr, ec, s));
     }
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, desc->dtype == MLPBLK_BF16, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
 }
@@ -435,7 +436,7 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
     MLPBLK_TRY(device_sms(&sms));
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     return backward_impl(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
-                         ws + l.dh, reinterpret_cast<float *>(ws + l.dn), reinterpret_cast<float *>(ws + l.part),
+                         ws + l.dh, ws + l.dn, reinterpret_cast<float *>(ws + l.part),
                          reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
                          sms, static_cast<cudaStream_t>(stream));
 }
@@ -542,7 +543,7 @@ int mlpblk_backward_recompute(const mlpblk_desc *desc, const void *dy, const voi
     }
     // dh_s takes the W1*gamma region, which the GEMM above was the last to read
     return backward_impl(desc, dy, x, gamma, w1, w2, h, a, rstd_saved, dx, dgamma, dw1, dw2, ws + l.dh,
-                         reinterpret_cast<float *>(ws + l.dn), reinterpret_cast<float *>(ws + l.part),
+                         ws + l.dn, reinterpret_cast<float *>(ws + l.part),
                          sk_partial, sk_flags, sms, s);
 }
 
@@ -755,7 +756,7 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
                                     sms, s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s, launch_rmsnorm_bwd(desc->dtype, x, dn_s, 0, dy, rstd_saved, gamma, dx, part, T, d, kMaxParts, &parts, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;
 }
@@ -945,7 +946,7 @@ MoeLayout moe_layout(const mlpblk_moe_desc *m) {
     l.w1g = 0;
     l.do_perm = take(l.R * d * 2);
     l.dh_perm = take(l.R * F * 2);
-    l.dn_perm = take(l.R * d * 4);
+    l.dn_perm = take(l.R * d * 2);
     l.part = take(static_cast<int64_t>(kMaxParts) * d * 4);
     // the M-grouped GEMMs' split schedule: partial sums and flags, apart from the
     // forward's W1*gamma (both live in the forward)
@@ -1063,7 +1064,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     const float *rstd_perm = reinterpret_cast<const float *>(sv + l.rstd_perm);
     const void *x_perm = sv + l.x_perm, *h_perm = sv + l.h_perm, *a_perm = sv + l.a_perm, *o_perm = sv + l.o_perm;
     void *do_perm = ws + l.do_perm, *dh_perm = ws + l.dh_perm;
-    float *dn_perm = reinterpret_cast<float *>(ws + l.dn_perm);
+    uint16_t *dn_perm = reinterpret_cast<uint16_t *>(ws + l.dn_perm);  // bf16
     float *part = reinterpret_cast<float *>(ws + l.part);
     float *sk_partial = reinterpret_cast<float *>(ws + l.sk_partial);
     int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
@@ -1104,7 +1105,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
     gn.pdl = kPdlWaitFirst;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
-                  launch_gemm_tc_bwd(kEpiStoreF32, (int)l.R, (int)d, (int)F, dh_perm, w1s, dn_perm, nullptr, gn, sms, s));
+                  launch_gemm_tc_bwd(kEpiStoreBf16, (int)l.R, (int)d, (int)F, dh_perm, w1s, dn_perm, nullptr, gn, sms, s));
     GemmArgs gw1 = {};
     gw1.colscale = static_cast<const uint16_t *>(gamma);
     gw1.grp_mode = kGroupK;
@@ -1117,7 +1118,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
                                      sms, s));
     // the slots' dn meet at n (sum rule) inside the RMSNorm backward
     MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s,
-                  launch_rmsnorm_bwd_gather(x, dn_perm, pos, k, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts,
+                  launch_rmsnorm_bwd_gather(x, dn_perm, 1, pos, k, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts,
                                             s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
     return MLPBLK_OK;

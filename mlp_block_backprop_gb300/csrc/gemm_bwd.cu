@@ -3,7 +3,8 @@
 //   dgrad h : dh_s = rstd * (dy . W2) * 2 relu(h)       (ReLU^2 gate in the epilogue;
 //                                                         W2 read MN-major)
 //   wgrad W2: dW2 += dy^T . a                             (both operands MN-major)
-//   dgrad n : dn_s = dh_s . W1                            (fp32 out; W1 MN-major)
+//   dgrad n : dn_s = dh_s . W1                            (bf16 out, or fp32 on the FP8
+//                                                         path; W1 MN-major)
 //   wgrad W1: dW1 += (dh_s^T . x) * gamma[col]            (both operands MN-major;
 //             for d_model <= 768 its side warps also run the RMSNorm backward rows)
 // dh_s = rstd*dh and dn_s = rstd*dn carry the per-row RMSNorm scale, so the
@@ -37,6 +38,7 @@ int launch_gemm_tc_bwd(int epi, int M, int N, int K, const void *A, const void *
     switch (epi) {
         case kEpiDgradH: { MLPBLK_RUN(kEpiDgradH, false) }
         case kEpiStoreF32: { MLPBLK_RUN(kEpiStoreF32, false) }
+        case kEpiStoreBf16: { MLPBLK_RUN(kEpiStoreBf16, false) }
         case kEpiAccF32: { MLPBLK_RUN(kEpiAccF32, true) }
         case kEpiAccF32ColScale: { MLPBLK_RUN(kEpiAccF32ColScale, true) }
         case kEpiAccF32ColScaleNorm: { MLPBLK_RUN(kEpiAccF32ColScaleNorm, true) }

@@ -99,8 +99,8 @@ struct GemmCfg {
     static constexpr int kStagingBufs = (kNumOut == 2 || kF32x8) ? 1 : 2;
     static constexpr int kStagingBytes = kAux ? 0 : kEpiWarps * kNumOut * kStagingBufs * 4096;
     // per-row scale read from args.rstd_in (1 when that is null)
-    static constexpr bool kRowScale =
-        (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A || EPI == kEpiStoreF32);
+    static constexpr bool kRowScale = (EPI == kEpiDgradH || EPI == kEpiFwdW1Pre || EPI == kEpiFwdW1A ||
+                                       EPI == kEpiStoreF32 || EPI == kEpiStoreBf16);
     static constexpr int kCtrlBytes = 1024 + (kNorm ? 1024 : 0);  // barriers (+ rstd[2][128])
     static constexpr int kAlignSlack = 1024;
     static constexpr int kStagesRaw =
@@ -312,11 +312,11 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
                 const int64_t off = t * d + 8 * q;
                 xv[j] = ld_global_nc_v4(sn.x + off);
                 yv[j] = ld_global_nc_v4(sn.dy + off);
-                const uint4 n0 = ld_global_nc_v4(sn.dn_s + off), n1 = ld_global_nc_v4(sn.dn_s + off + 4);
-                nv[j][0] = __uint_as_float(n0.x); nv[j][1] = __uint_as_float(n0.y);
-                nv[j][2] = __uint_as_float(n0.z); nv[j][3] = __uint_as_float(n0.w);
-                nv[j][4] = __uint_as_float(n1.x); nv[j][5] = __uint_as_float(n1.y);
-                nv[j][6] = __uint_as_float(n1.z); nv[j][7] = __uint_as_float(n1.w);
+                const uint4 n0 = ld_global_nc_v4(sn.dn_s + off);  // 8 bf16 values
+                nv[j][0] = bf16_lo(n0.x); nv[j][1] = bf16_hi(n0.x);
+                nv[j][2] = bf16_lo(n0.y); nv[j][3] = bf16_hi(n0.y);
+                nv[j][4] = bf16_lo(n0.z); nv[j][5] = bf16_hi(n0.z);
+                nv[j][6] = bf16_lo(n0.w); nv[j][7] = bf16_hi(n0.w);
             } else {
                 xv[j] = yv[j] = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -777,7 +777,7 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
                             }
                     } else if (C::EPI == kEpiStoreBf16) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
+                        for (int i = 0; i < 4; ++i) o[i] = pack_bf16x2(rsc * e[2 * i], rsc * e[2 * i + 1]);
                     } else if (C::EPI == kEpiFwdW2) {
                         const uint32_t xs[4] = {aux[j].x, aux[j].y, aux[j].z, aux[j].w};
 #pragma unroll

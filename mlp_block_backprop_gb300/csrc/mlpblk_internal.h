@@ -95,7 +95,8 @@ constexpr int kSideNormMaxD = 768;
 constexpr int kSideWarps = 4;
 struct SideNorm {
     const uint16_t *x, *dy, *gamma;  // bf16 [T, d], [T, d], [d]
-    const float *dn_s, *rstd;        // fp32 [T, d], [T]
+    const uint16_t *dn_s;            // bf16 [T, d]: rstd * dn
+    const float *rstd;               // fp32 [T]
     uint16_t *dx;                    // bf16 [T, d] (written)
     float *part;                     // fp32 [gridDim.x, d]: this launch's dgamma partial rows
     int64_t T;
@@ -193,8 +194,9 @@ int launch_norm_prep(int dtype, const void *x, float *rstd, int64_t T, int64_t d
 // MLPBLK_RMS_IN_GEMM=1; by default the statistics pass computes rstd.
 bool rms_in_gemm();
 // RMSNorm backward rows; writes at most max_parts dgamma partial rows of d
-// floats to dgamma_part and returns their count in *parts_out.
-int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
+// floats to dgamma_part and returns their count in *parts_out.  dn_s is float32,
+// or bf16 when dn_bf16 is set (the bf16 block's dgrad-n GEMM stores it so).
+int launch_rmsnorm_bwd(int dtype, const void *x, const void *dn_s, int dn_bf16, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int take_device_error_rowops();
@@ -204,9 +206,9 @@ int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t 
 // scale is applied inside the kernel).
 // Routed experts, bf16: row t's dn_s is the sum of the rows pos[t*k + j] of
 // dn_rows (slot order; pos < 0 adds nothing).
-int launch_rmsnorm_bwd_gather(const void *x, const float *dn_rows, const int *pos, int k, const void *dy,
-                              const float *rstd, const void *gamma, void *dx, float *dgamma_part, int64_t T,
-                              int64_t d, int max_parts, int *parts_out, cudaStream_t s);
+int launch_rmsnorm_bwd_gather(const void *x, const void *dn_rows, int dn_bf16, const int *pos, int k,
+                              const void *dy, const float *rstd, const void *gamma, void *dx, float *dgamma_part,
+                              int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
                                 const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                                 int64_t T, int64_t d, int max_parts, int *parts_out,

@@ -192,6 +192,16 @@ struct Chunk<float> {
     }
 };
 
+// Eight consecutive elements of dn as floats: dn is float32, or bf16 where the
+// dgrad-n GEMM stores it so (the bf16 block: half the bytes to write and read).
+__device__ __forceinline__ void load_dn(Chunk<float> &c, const float *p) { c.load(p); }
+__device__ __forceinline__ void load_dn(Chunk<float> &c, const uint16_t *p) {
+    Chunk<uint16_t> u;
+    u.load(p);
+    c.a = make_float4(u[0], u[1], u[2], u[3]);
+    c.b = make_float4(u[4], u[5], u[6], u[7]);
+}
+
 // RMSNorm backward with the residual gradient.  The gradient input carries the
 // per-row scale already, dn_s = rstd * dn (the dgrad GEMM writes it that way);
 // kScaleDn = true instead takes the plain dn and applies rstd here.  With
@@ -212,9 +222,9 @@ struct Chunk<float> {
 // kGather (routed experts): row t's dn_s is the sum over its k slots of the rows
 // pos[t*k + j] of dn_s (slot order, from zero; a slot with pos < 0 adds nothing).
 constexpr int kGatherRegs = 4;
-template <class T, int CPT, bool kScaleDn, bool kGather>
+template <class T, int CPT, bool kScaleDn, bool kGather, class DN>
 __global__ void __launch_bounds__(kRowThreads, (CPT <= 2 ? 3 : (CPT <= 3 ? 2 : 1)))
-rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, const T *__restrict__ dy,
+rmsnorm_bwd_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, const T *__restrict__ dy,
                    const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
                    float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta,
                    int G, const int *__restrict__ pos, int k) {
@@ -275,7 +285,7 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
                     for (int sl = 0; sl < kGatherRegs; ++sl) {
                         if (rcur[sl] < 0) continue;
                         Chunk<float> v;
-                        v.load(dn_s + static_cast<int64_t>(rcur[sl]) * d + 8 * q);
+                        load_dn(v, dn_s + static_cast<int64_t>(rcur[sl]) * d + 8 * q);
                         nch[j].add(v);
                     }
                 } else if (kGather) {
@@ -284,11 +294,11 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
                         const int r = pos[t * k + sl];
                         if (r < 0) continue;
                         Chunk<float> v;
-                        v.load(dn_s + static_cast<int64_t>(r) * d + 8 * q);
+                        load_dn(v, dn_s + static_cast<int64_t>(r) * d + 8 * q);
                         nch[j].add(v);
                     }
                 } else {
-                    nch[j].load(dn_s + t * d + 8 * q);
+                    load_dn(nch[j], dn_s + t * d + 8 * q);
                 }
                 ych[j].load(dy + t * d + 8 * q);
             } else {
@@ -364,15 +374,15 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const float *__restrict__ dn_s, cons
 // A CTA of 256 threads (d <= 2048: two CTAs per SM) or 512 (d = 4096) takes
 // R = 8 * threads / d rows per iteration, d/8 threads per
 // row, 8 columns per thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16,
-// dn [R][K'][d] fp32 (K' = k slot rows with kGather, else 1).  The row sum is a
+// dn [R][K'][d] fp32 or bf16 (K' = k slot rows with kGather, else 1).  The row sum is a
 // shuffle tree per warp then the row's warps in order; the dgamma partial of the
 // CTA is each thread's running sum, then the R row groups in order.
 constexpr int kStagedMaxThreads = 512;
 constexpr int kStagedMaxStages = 4;
 
-template <bool kGather>
+template <bool kGather, class DN>
 __global__ void __launch_bounds__(kStagedMaxThreads, 1)
-rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dn_s,
+rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__ dn_s,
                           const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
                           const uint16_t *__restrict__ gamma, uint16_t *__restrict__ dx,
                           float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta, int R,
@@ -430,22 +440,23 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restric
         uint32_t mine = 0;  // this lane's slot-row bytes
         if (kGather)
             for (int q = 0; q < 2; ++q)
-                if (pnext[q] >= 0) mine += static_cast<uint32_t>(d) * 4u;
+                if (pnext[q] >= 0) mine += static_cast<uint32_t>(d) * sizeof(DN);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
         if (lane == 0) {
             uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u;  // x and dy
-            bytes += kGather ? mine : static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u;
+            bytes += kGather ? mine : static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * sizeof(DN);
             mbar_arrive_expect_tx(&full[st], bytes);
             bulk_copy_g2s(sx, x + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
             bulk_copy_g2s(sy, dy + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
-            if (!kGather) bulk_copy_g2s(sn, dn_s + tb * d, static_cast<uint32_t>(nr * d * 4), &full[st]);
+            if (!kGather) bulk_copy_g2s(sn, dn_s + tb * d, static_cast<uint32_t>(nr * d * sizeof(DN)), &full[st]);
         }
         if (kGather)
             for (int q = 0; q < 2; ++q)
                 if (pnext[q] >= 0)
-                    bulk_copy_g2s(sn + static_cast<size_t>(lane + 32 * q) * d * 4,
-                                  dn_s + static_cast<int64_t>(pnext[q]) * d, static_cast<uint32_t>(d * 4), &full[st]);
+                    bulk_copy_g2s(sn + static_cast<size_t>(lane + 32 * q) * d * sizeof(DN),
+                                  dn_s + static_cast<int64_t>(pnext[q]) * d, static_cast<uint32_t>(d * sizeof(DN)),
+                                  &full[st]);
         __syncwarp();
     };
     int issued = 0;
@@ -504,11 +515,18 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const float *__restric
             for (int i = 0; i < 8; ++i) nv[i] = 0.0f;
             for (int j = 0; j < kk; ++j) {
                 if (kGather && pv[j] < 0) continue;
-                const float *q = reinterpret_cast<const float *>(sn) + (static_cast<size_t>(grp) * kk + j) * d + 8 * gl;
-                const float4 a0 = *reinterpret_cast<const float4 *>(q);
-                const float4 a1 = *reinterpret_cast<const float4 *>(q + 4);
-                nv[0] += a0.x; nv[1] += a0.y; nv[2] += a0.z; nv[3] += a0.w;
-                nv[4] += a1.x; nv[5] += a1.y; nv[6] += a1.z; nv[7] += a1.w;
+                const DN *q = reinterpret_cast<const DN *>(sn) + (static_cast<size_t>(grp) * kk + j) * d + 8 * gl;
+                if (sizeof(DN) == 4) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(q);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(q) + 4);
+                    nv[0] += a0.x; nv[1] += a0.y; nv[2] += a0.z; nv[3] += a0.w;
+                    nv[4] += a1.x; nv[5] += a1.y; nv[6] += a1.z; nv[7] += a1.w;
+                } else {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(q);
+                    nv[0] += bf(u.x & 0xFFFFu); nv[1] += bf(u.x >> 16); nv[2] += bf(u.y & 0xFFFFu);
+                    nv[3] += bf(u.y >> 16); nv[4] += bf(u.z & 0xFFFFu); nv[5] += bf(u.z >> 16);
+                    nv[6] += bf(u.w & 0xFFFFu); nv[7] += bf(u.w >> 16);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) part += g[i] * nv[i] * xv[i];
@@ -667,8 +685,8 @@ void norm_shape(int64_t d, int *cpt_out, int *g_out) {
 
 // One CTA per resident slot (at most max_parts), rows split in whole multiples
 // of the rows in flight; the number of CTAs (= dgamma partial rows) is returned.
-template <class E, int CPT, bool kScaleDn, bool kGather>
-int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
+template <class E, int CPT, bool kScaleDn, bool kGather, class DN>
+int run_norm_bwd(const void *x, const DN *dn, const void *dy, const float *rstd,
                  const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                  int *parts_out, int G, const int *pos, int k, cudaStream_t s) {
     const int R = kRowThreads / G;
@@ -676,7 +694,7 @@ int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rs
     const size_t smem = floats * sizeof(float);
     int occ = 0;
     const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather>, kRowThreads, smem));
+        &occ, rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather, DN>, kRowThreads, smem));
     if (rc != MLPBLK_OK) return rc;
     int64_t parts = static_cast<int64_t>(occ > 0 ? occ : 1) * sm_count();
     if (parts > max_parts) parts = max_parts;
@@ -686,20 +704,20 @@ int run_norm_bwd(const void *x, const float *dn, const void *dy, const float *rs
     const int64_t rows_per_cta = ((T + parts - 1) / parts + R - 1) / R * R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather>, dim3(static_cast<unsigned>(parts)),
+    return launch_pdl(rmsnorm_bwd_kernel<E, CPT, kScaleDn, kGather, DN>, dim3(static_cast<unsigned>(parts)),
                       dim3(kRowThreads), smem, s, static_cast<const E *>(x), dn,
                       static_cast<const E *>(dy), rstd, static_cast<const E *>(gamma),
                       static_cast<E *>(dx), part, T, d, rows_per_cta, G, pos, k);
 }
 
-template <class E, bool kScaleDn, bool kGather = false>
-int dispatch_norm_bwd(const void *x, const float *dn, const void *dy, const float *rstd,
+template <class E, bool kScaleDn, bool kGather = false, class DN = float>
+int dispatch_norm_bwd(const void *x, const DN *dn, const void *dy, const float *rstd,
                       const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                       int *parts_out, cudaStream_t s, const int *pos = nullptr, int k = 0) {
     int cpt = 0, G = 0;
     norm_shape(d, &cpt, &G);
 #define MLPBLK_NB(C) \
-    return run_norm_bwd<E, C, kScaleDn, kGather>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, \
+    return run_norm_bwd<E, C, kScaleDn, kGather, DN>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, \
                                                  pos, k, s)
     switch (cpt) {
         case 1: MLPBLK_NB(1);
@@ -761,13 +779,13 @@ struct StagedShape {
     size_t smem;
 };
 
-StagedShape staged_shape(int64_t d, int k) {
+StagedShape staged_shape(int64_t d, int k, int dn_bytes) {
     StagedShape sh = {0, 0, 0, 0, 0};
     if (d % 256 != 0 || d > 4096 || k < 1 || k > 4) return sh;
     const int threads = d <= 2048 ? 256 : 512;
     const int R = static_cast<int>(8 * threads / d);
     if (k > 1 && R * k > 64) return sh;  // warp 0 issues at most 64 slot rows
-    const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * 4 + 127) / 128 * 128;
+    const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * dn_bytes + 127) / 128 * 128;
     const int64_t extra = 2 * R * 16 * 4 + kStagedMaxStages * 8 + 16;
     const int64_t budget = threads == 256 ? 100 * 1024 : 200 * 1024;  // 256 threads: two CTAs per SM
     int S = static_cast<int>((budget - extra) / bytes);
@@ -781,15 +799,15 @@ StagedShape staged_shape(int64_t d, int k) {
     return sh;
 }
 
-template <bool kGather>
-int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, const void *dy, const float *rstd,
+template <bool kGather, class DN>
+int run_norm_bwd_staged(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
                         const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                         int *parts_out, const int *pos, int k, cudaStream_t s) {
     static bool attr[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
     if (!attr[dev]) {
-        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather>,
+        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather, DN>,
                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 4096));
         if (rc != MLPBLK_OK) return rc;
         attr[dev] = true;
@@ -802,7 +820,7 @@ int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, c
     const int64_t rows_per_cta = ((T + parts - 1) / parts + sh.R - 1) / sh.R * sh.R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather>, dim3(static_cast<unsigned>(parts)), dim3(sh.threads),
+    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather, DN>, dim3(static_cast<unsigned>(parts)), dim3(sh.threads),
                       sh.smem, s, static_cast<const uint16_t *>(x), dn, static_cast<const uint16_t *>(dy), rstd,
                       static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(dx), part, T, d, rows_per_cta,
                       sh.R, sh.S, sh.stage_bytes, pos, k);
@@ -810,14 +828,17 @@ int run_norm_bwd_staged(const StagedShape &sh, const void *x, const float *dn, c
 
 }  // namespace
 
-int launch_rmsnorm_bwd(int dtype, const void *x, const float *dn_s, const void *dy,
+int launch_rmsnorm_bwd(int dtype, const void *x, const void *dn_s, int dn_bf16, const void *dy,
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
+    if (dtype == MLPBLK_BF16 && dn_bf16)
+        return dispatch_norm_bwd<uint16_t, false, false, uint16_t>(x, static_cast<const uint16_t *>(dn_s), dy, rstd,
+                                                                   gamma, dx, dgamma_part, T, d, max_parts, parts_out, s);
     if (dtype == MLPBLK_BF16)
-        return dispatch_norm_bwd<uint16_t, false>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d,
-                                                  max_parts, parts_out, s);
-    return dispatch_norm_bwd<float, false>(x, dn_s, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
-                                           parts_out, s);
+        return dispatch_norm_bwd<uint16_t, false>(x, static_cast<const float *>(dn_s), dy, rstd, gamma, dx,
+                                                  dgamma_part, T, d, max_parts, parts_out, s);
+    return dispatch_norm_bwd<float, false>(x, static_cast<const float *>(dn_s), dy, rstd, gamma, dx, dgamma_part,
+                                           T, d, max_parts, parts_out, s);
 }
 
 int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const void *dy,
@@ -830,17 +851,25 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
                                           parts_out, s);
 }
 
-int launch_rmsnorm_bwd_gather(const void *x, const float *dn_rows, const int *pos, int k, const void *dy,
-                              const float *rstd, const void *gamma, void *dx, float *dgamma_part, int64_t T,
-                              int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
+int launch_rmsnorm_bwd_gather(const void *x, const void *dn_rows, int dn_bf16, const int *pos, int k,
+                              const void *dy, const float *rstd, const void *gamma, void *dx, float *dgamma_part,
+                              int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
     if (T > 0) {
-        const StagedShape sh = staged_shape(d, k);
-        if (sh.R > 0)
-            return run_norm_bwd_staged<true>(sh, x, dn_rows, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
-                                             parts_out, pos, k, s);
+        const StagedShape sh = staged_shape(d, k, dn_bf16 ? 2 : 4);
+        if (sh.R > 0) {
+            if (dn_bf16)
+                return run_norm_bwd_staged<true>(sh, x, static_cast<const uint16_t *>(dn_rows), dy, rstd, gamma, dx,
+                                                 dgamma_part, T, d, max_parts, parts_out, pos, k, s);
+            return run_norm_bwd_staged<true>(sh, x, static_cast<const float *>(dn_rows), dy, rstd, gamma, dx,
+                                             dgamma_part, T, d, max_parts, parts_out, pos, k, s);
+        }
     }
-    return dispatch_norm_bwd<uint16_t, false, true>(x, dn_rows, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts,
-                                                    parts_out, s, pos, k);
+    if (dn_bf16)
+        return dispatch_norm_bwd<uint16_t, false, true, uint16_t>(x, static_cast<const uint16_t *>(dn_rows), dy, rstd,
+                                                                  gamma, dx, dgamma_part, T, d, max_parts, parts_out,
+                                                                  s, pos, k);
+    return dispatch_norm_bwd<uint16_t, false, true>(x, static_cast<const float *>(dn_rows), dy, rstd, gamma, dx,
+                                                    dgamma_part, T, d, max_parts, parts_out, s, pos, k);
 }
 
 int take_device_error_rowops() {
