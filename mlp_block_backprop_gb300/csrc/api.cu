@@ -58,7 +58,8 @@ struct WsLayout {
 
 // Stream-K flag sets, one per tensor-core GEMM that can split a tile; each set
 // is zeroed by the kernel launched just before that GEMM.
-enum SkFlagSet : int { kSetFwdW1 = 0, kSetFwdW2 = 1, kSetDgradH = 2, kSetDgradN = 3, kSkSets = 4 };
+// kSetSide: the wgrad-W1 side warps' arrival count (its first word).
+enum SkFlagSet : int { kSetFwdW1 = 0, kSetFwdW2 = 1, kSetDgradH = 2, kSetDgradN = 3, kSetSide = 4, kSkSets = 5 };
 
 // Workspace regions.  W1*gamma (forward, and the recompute backward's first
 // GEMM) shares its region with dh_s (backward).  `recompute` adds the T x F
@@ -349,6 +350,7 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         GemmArgs gn = {};
         gn.sk_partial = sk_partial;
         gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
+        gn.zero_flags = side_norm(d) ? sk_flags + kSetSide * kSkFlagsPerSet : nullptr;
         gn.pdl = kPdlWaitFirst;
         // dn_s = rstd * dn stored in bf16 like dh_s (rstd rides in dh_s already)
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreBf16, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
@@ -357,7 +359,8 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         gw1.pdl = kPdlDeferWait;
         if (side_norm(d)) {
             // the RMSNorm backward rows run on the wgrad-W1 GEMM's side warps,
-            // one dgamma partial row per CTA of that launch
+            // one dgamma partial row per CTA of that launch, summed into dgamma
+            // by the same warps once every CTA's row is complete
             gw1.side.x = static_cast<const uint16_t *>(x);
             gw1.side.dy = static_cast<const uint16_t *>(dy);
             gw1.side.gamma = static_cast<const uint16_t *>(gamma);
@@ -365,12 +368,13 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
             gw1.side.rstd = rstd_saved;
             gw1.side.dx = static_cast<uint16_t *>(dx);
             gw1.side.part = part;
+            gw1.side.dgamma = dgamma;
+            gw1.side.arrive = sk_flags + kSetSide * kSkFlagsPerSet;
             gw1.side.T = T;
             gw1.side.d = (int)d;
             gw1.grid_out = &parts;
             MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScaleNorm, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
             if (parts <= 0 || parts > kMaxParts) return MLPBLK_ECUDA;
-            MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
             return MLPBLK_OK;
         }
         MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));

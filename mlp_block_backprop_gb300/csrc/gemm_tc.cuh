@@ -283,8 +283,12 @@ __device__ __forceinline__ float sumsq_bf16x8(uint4 v) {
 // dgamma partial += dn_s*x.  One row per warp at a time: lane l owns the 8-column
 // chunks l, l+32, l+64 (d <= kSideNormMaxD), the row sum is a shuffle butterfly.
 // The CTA's side warps then add their dgamma shares into the CTA's partial row
-// in warp order (a fixed order, as in the row kernel).
-__device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
+// in warp order (a fixed order, as in the row kernel).  Once every CTA's row is
+// complete (an arrival count), warp 0 of CTA b adds the partial rows of the
+// 8-column chunks b, b + grid, ... into dgamma: lane l sums rows l, l + 32, ...
+// and a butterfly over the lanes finishes, so the order is fixed by the grid.
+// The GEMM's warps do not wait for any of this.
+__device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw, volatile int *abort) {
     constexpr int kCPT = kSideNormMaxD / 256;
     const int lane = threadIdx.x & 31;
     const int d = sn.d;
@@ -301,7 +305,27 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
     }
     const float inv_d = 1.0f / static_cast<float>(d);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kSideWarps;
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kSideWarps + sw; t < sn.T; t += stride) {
+    // the loop is bound by load latency (one row in flight per warp): lane 0
+    // asks L2 for the rows kAhead strides ahead, so the row loads hit L2
+    constexpr int kAhead = 2;
+    const uint32_t row_bytes = static_cast<uint32_t>(d) * 2;
+    const int64_t t_first = static_cast<int64_t>(blockIdx.x) * kSideWarps + sw;
+    if (lane == 0)
+        for (int a = 0; a < kAhead; ++a) {
+            const int64_t tp = t_first + a * stride;
+            if (tp < sn.T) {
+                bulk_prefetch_l2(sn.x + tp * d, row_bytes);
+                bulk_prefetch_l2(sn.dy + tp * d, row_bytes);
+                bulk_prefetch_l2(sn.dn_s + tp * d, row_bytes);
+            }
+        }
+    for (int64_t t = t_first; t < sn.T; t += stride) {
+        if (lane == 0 && t + kAhead * stride < sn.T) {
+            const int64_t tp = t + kAhead * stride;
+            bulk_prefetch_l2(sn.x + tp * d, row_bytes);
+            bulk_prefetch_l2(sn.dy + tp * d, row_bytes);
+            bulk_prefetch_l2(sn.dn_s + tp * d, row_bytes);
+        }
         const float r = sn.rstd[t];
         uint4 xv[kCPT], yv[kCPT];
         float nv[kCPT][8];
@@ -378,6 +402,65 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw) {
                 st_global_v4(p + 4, v[4], v[5], v[6], v[7]);
             }
             __threadfence_block();
+        }
+    }
+    // the row is complete (the barrier orders every side warp's stores before
+    // the release of the one arrival; a reader's acquire of the count sees them)
+    named_barrier_sync(1, 32 * kSideWarps);
+    if (sw != 0) return;
+    if (lane == 0) red_release_gpu_add(sn.arrive, 1);
+    const int P = static_cast<int>(gridDim.x);
+    if (static_cast<int>(blockIdx.x) >= chunks) return;
+    // this CTA's first chunk of dgamma, read before the wait (nothing else writes it)
+    float g0[8];
+    if (lane == 0) {
+        const float *dg = sn.dgamma + 8 * blockIdx.x;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g0[i] = dg[i];
+    }
+    // one lane polls (with a pause between polls), then every lane acquires
+    int ok = 1;
+    if (lane == 0) ok = count_wait_sleep(sn.arrive, P, abort);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    (void)ld_acquire_gpu(sn.arrive);
+    for (int q = blockIdx.x; q < chunks; q += P) {
+        // every lane's rows in flight at once (one pass while P <= kMaxSkSlots)
+        constexpr int kRowsPerLane = (kMaxSkSlots + 31) / 32;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        for (int p0 = 0; p0 < P; p0 += 32 * kRowsPerLane) {
+        float4 a[kRowsPerLane][2];
+#pragma unroll
+        for (int k = 0; k < kRowsPerLane; ++k) {
+            const int p = p0 + lane + 32 * k;
+            if (p < P) {
+                const float *src = sn.part + static_cast<int64_t>(p) * d + 8 * q;
+                a[k][0] = ld_global_cg_v4(src);
+                a[k][1] = ld_global_cg_v4(src + 4);
+            } else {
+                a[k][0] = a[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRowsPerLane; ++k) {
+            v[0] += a[k][0].x; v[1] += a[k][0].y; v[2] += a[k][0].z; v[3] += a[k][0].w;
+            v[4] += a[k][1].x; v[5] += a[k][1].y; v[6] += a[k][1].z; v[7] += a[k][1].w;
+        }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+        if (lane == 0) {
+            float *dg = sn.dgamma + 8 * q;
+            if (q == static_cast<int>(blockIdx.x)) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dg[i] = g0[i] + v[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dg[i] += v[i];
+            }
         }
     }
 }
@@ -982,7 +1065,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------- RMSNorm backward rows (side warps)
         // dn_s is the previous kernel's output: these warps wait for it, while
         // the GEMM's own warps (whose operands it does not write) run on
-        side_norm_rows(args.side, warp - 2 - C::kEpiWarps);
+        side_norm_rows(args.side, warp - 2 - C::kEpiWarps, abort_flag);
     } else if (C::kNorm) {
         // ------------------------------------------- RMSNorm prologue (fwd W1)
         const int r = 32 * (warp - 6) + lane;  // row of this CTA's 128 rows

@@ -92,13 +92,15 @@ enum Epilogue : int {
 // kernel's arithmetic on dn_s = rstd * dn, one warp per row, one dgamma partial
 // row per CTA.
 constexpr int kSideNormMaxD = 768;
-constexpr int kSideWarps = 4;
+constexpr int kSideWarps = 6;
 struct SideNorm {
     const uint16_t *x, *dy, *gamma;  // bf16 [T, d], [T, d], [d]
     const uint16_t *dn_s;            // bf16 [T, d]: rstd * dn
     const float *rstd;               // fp32 [T]
     uint16_t *dx;                    // bf16 [T, d] (written)
     float *part;                     // fp32 [gridDim.x, d]: this launch's dgamma partial rows
+    float *dgamma;                   // fp32 [d]: += the sum of the partial rows
+    int *arrive;                     // CTAs whose partial row is complete (zero at launch)
     int64_t T;
     int d;
 };

@@ -466,6 +466,12 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -488,10 +494,55 @@ __device__ __forceinline__ bool flag_wait(const int *flag, volatile int *abort) 
     }
 }
 
+// Adds v to *p with release semantics at GPU scope (no value returned).
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *ctr >= target (acquire), with the same bound and abort protocol
+// as flag_wait.  Returns false when the wait gave up.
+__device__ __forceinline__ bool count_wait(const int *ctr, int target, volatile int *abort) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (ld_acquire_gpu(ctr) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            record_device_error(MLPBLK_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+// count_wait with a pause of about 128 ns between polls, for a wait that may
+// last microseconds while other warps of the SM issue.
+__device__ __forceinline__ bool count_wait_sleep(const int *ctr, int target, volatile int *abort) {
+    // relaxed polls; the caller acquires once the count is reached
+    if (ld_relaxed_gpu(ctr) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(128);
+        if (ld_relaxed_gpu(ctr) >= target) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            record_device_error(MLPBLK_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Orders this thread's earlier generic-proxy accesses (e.g. an acquire of a
 // flag) before its later async-proxy accesses of global memory (bulk copies).
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Asks L2 to fetch [p, p + bytes) (no data returned).  p 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Untiled bulk copy global -> this CTA's shared memory; completion is signalled
