@@ -3,7 +3,12 @@
 
 One step = the whole hot path over one batch of synthetic input: zero_grads,
 then forward and backward of every microbatch (fp32 += gradient accumulation),
-then scale_grads where the workload has one.  Prints one JSON line (rank 0).
+then scale_grads where the workload has one.  The routed-expert block's step is
+forward and mlpblk_moe_backward_overwrite, which sets the gradients (its expert
+GEMMs store whole tiles where they would add them); --grads overwrite|zero picks
+either form for either block (the dense block's overwrite clears the gradients
+in the backward's first launch: the same work as zero_grads, measured 0.5 %
+slower there).  Prints one JSON line (rank 0).
 The default run times the large block (d 4096, ffn 16384, 2 x 8192 tokens) and,
 in a `secondary` object of the same line, the 120M-class block (d 768, ffn
 3072, 8192 tokens).
@@ -54,6 +59,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    p.add_argument("--grads", default="auto", choices=["auto", "zero", "overwrite"],
+                   help="zero: zero_grads at the start of each step, every backward adds; overwrite: the first "
+                        "microbatch's backward sets the gradients; auto: zero for the dense block, overwrite for "
+                        "the routed experts")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the 120M-class block that the default run also times")
     p.add_argument("--optimizer", action="store_true",
@@ -372,8 +381,12 @@ def run_ours(args, dist, peaks):
     if prefold:
         bb.w1g = torch.empty_like(bb.w1)
 
+    # --grads overwrite: the first microbatch's backward sets the gradients
+    overwrite = args.grads == "overwrite" and not (fp8 or recompute)
+
     def step(x_list, dy_list, dx_list=None, after_mb=None):
-        mb.mlpblk_zero_grads(desc, bb.dgamma, bb.dw1, bb.dw2)
+        if not overwrite:
+            mb.mlpblk_zero_grads(desc, bb.dgamma, bb.dw1, bb.dw2)
         if fp8:
             # the weights' E4M3 codes once per step: they do not change between microbatches
             mb.mlpblk_fp8_quantize_weights(desc, bb.gamma, bb.w1, bb.w2, bb.wq, bb.ws)
@@ -396,7 +409,7 @@ def run_ours(args, dist, peaks):
                 else:
                     mb.mlpblk_forward(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.h, bb.a, bb.rstd, bb.ws)
                 mb.mlpblk_backward(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.h, bb.a, bb.rstd,
-                                   dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+                                   dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws, overwrite=overwrite and i == 0)
             if after_mb is not None:
                 after_mb(i)
         if inp.grad_scale is not None:
@@ -537,6 +550,8 @@ def run_ours(args, dist, peaks):
                    "rmsnorm": args.rmsnorm,
                    "w1_gamma_fold": "once per step (mlpblk_fold_weights + mlpblk_forward_prefolded)" if prefold
                                     else "inside every forward",
+                   "gradients": ("written by the first microbatch's backward (mlpblk_backward_overwrite), "
+                                 "added by the others" if overwrite else "zero_grads, then every backward adds"),
                    "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch
@@ -700,7 +715,7 @@ def pipelined_e2e(k, sets, host_in, host_in2, host_out, compute, out_of, use_gra
 # --------------------------------------------------------- oracle on the host
 
 def run_moe(args, dist, peaks):
-    """The routed ReLU^2 expert block: zero_grads + forward + backward per step,
+    """The routed ReLU^2 expert block: forward + backward (writing the gradients) per step,
     timed like run_ours (CUDA graph of the K steps, then a traced replay)."""
     import torch
 
@@ -720,10 +735,13 @@ def run_moe(args, dist, peaks):
     bb.idx.copy_(to(inp.idx, torch.int32))
     bb.p.copy_(to(inp.p, torch.float32))
 
+    overwrite = args.grads != "zero"
+
     def step():
-        bb.zero_grads()
+        if not overwrite:
+            bb.zero_grads()
         bb.forward()
-        bb.backward()
+        bb.backward(overwrite=overwrite)
 
     for _ in range(args.warmup):
         step()
@@ -804,6 +822,8 @@ def run_moe(args, dist, peaks):
         "data": "synthetic (seeded numpy normals, bf16-rounded; uniform random top-k routing; no dataset)",
         "config": {"workload": args.workload, "tokens": T, "d_model": d, "ffn_per_expert": F, "experts": E,
                    "top_k": k, "flop_per_step": flop_step, "launch": "cuda_graph",
+                   "gradients": ("written by the backward (mlpblk_moe_backward_overwrite)" if overwrite
+                                 else "zero_grads, then the backward adds"),
                    "parallelism": "replicas" if dist.world > 1 else "single"},
         "tokens_per_s": round(dist.world * T / (ms_step * 1e-3), 1),
         "frac_of_peak": {"sustained": round(value / dist.world / peak, 4)},

@@ -141,6 +141,26 @@ int mlpblk_backward(const mlpblk_desc *desc,
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The first microbatch of an accumulation window: the same backward with the
+ * gradients set rather than added into ("grow_a_language_model_backprop" --
+ * accumulation across microbatches: zero_grads() then += is = for the first
+ * microbatch):
+ *        dgamma[d]  = sum_t dn[t,k] * x[t,k] * r[t]
+ *        dw1[F,d]   = dh^T . n,   dw2[d,F] = dy^T . a        (float32, written)
+ * The buffers' prior contents do not matter (NaN included), so the window needs
+ * no mlpblk_zero_grads; with T = 0 they are set to zero.  This dense block
+ * clears them in its first launch and then adds, so the results are bitwise
+ * those of mlpblk_zero_grads + mlpblk_backward.  dx, the other arguments, the
+ * workspace and the return codes are as for mlpblk_backward.
+ */
+int mlpblk_backward_overwrite(const mlpblk_desc *desc,
+                              const void *dy, const void *x, const void *gamma,
+                              const void *w1, const void *w2,
+                              const void *h_saved, const void *a_saved, const float *rstd_saved,
+                              void *dx, float *dgamma, float *dw1, float *dw2,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Recompute variant: save x and rstd only, and rebuild h and a at the start of
  * the backward ("Nemotron Kernels From Inference To Backpropagation" -- Part II:
  * training must preserve or later recompute what reverse mode needs, and an
@@ -344,6 +364,19 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc,
                         const void *saved, void *dx, float *d_routing_weights,
                         float *dgamma, float *dw1s, float *dw2s,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* As mlpblk_moe_backward, with dgamma, dw1s and dw2s set instead of added
+ * into (the first microbatch of an accumulation window; see
+ * mlpblk_backward_overwrite).  Here each expert's weight-gradient tile is one
+ * worker's whole sum, so the GEMMs store it where they would add it (bitwise
+ * the same values), and the blocks of experts that no token chose are set to
+ * zero by the first launch of the backward. */
+int mlpblk_moe_backward_overwrite(const mlpblk_moe_desc *desc,
+                                  const void *dy, const void *x, const void *gamma,
+                                  const void *w1s, const void *w2s, const float *routing_weights,
+                                  const void *saved, void *dx, float *d_routing_weights,
+                                  float *dgamma, float *dw1s, float *dw2s,
+                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * zero_grads() of the accumulation loop ("grow_a_language_model_backprop" --

@@ -36,7 +36,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_fp8_weights_size", "mlpblk_fp8_quantize_weights", "mlpblk_forward_fp8_prequant",
             "mlpblk_backward_fp8_prequant",
             "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward",
-            "mlpblk_fold_weights", "mlpblk_forward_prefolded")
+            "mlpblk_fold_weights", "mlpblk_forward_prefolded", "mlpblk_backward_overwrite",
+            "mlpblk_moe_backward_overwrite")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
@@ -99,6 +100,8 @@ def _load():
     lib.mlpblk_forward_prefolded.argtypes = [pd] + [vp] * 7 + [sz, vp]
     lib.mlpblk_forward_prefolded.restype = i32
     lib.mlpblk_backward.restype = i32
+    lib.mlpblk_backward_overwrite.argtypes = lib.mlpblk_backward.argtypes
+    lib.mlpblk_backward_overwrite.restype = i32
     lib.mlpblk_workspace_size_recompute.argtypes = [pd]
     lib.mlpblk_workspace_size_recompute.restype = sz
     lib.mlpblk_forward_recompute.argtypes = [pd] + [vp] * 7 + [sz, vp]
@@ -134,6 +137,8 @@ def _load():
     lib.mlpblk_moe_forward.restype = i32
     lib.mlpblk_moe_backward.argtypes = [pm] + [vp] * 13 + [sz, vp]
     lib.mlpblk_moe_backward.restype = i32
+    lib.mlpblk_moe_backward_overwrite.argtypes = lib.mlpblk_moe_backward.argtypes
+    lib.mlpblk_moe_backward_overwrite.restype = i32
     lib.mlpblk_zero_grads.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_zero_grads.restype = i32
     lib.mlpblk_scale_grads.argtypes = [pd, vp, vp, vp, f32, vp]
@@ -221,12 +226,14 @@ def mlpblk_forward_prefolded(desc, x, w1g, w2, y, h_saved, a_saved, rstd_saved, 
 
 
 def mlpblk_backward(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
-                    workspace, workspace_bytes=None, stream=None):
+                    workspace, workspace_bytes=None, stream=None, overwrite=False):
+    """overwrite=True calls mlpblk_backward_overwrite (gradients written, not added into)."""
     nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
-    rc = lib.mlpblk_backward(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
-                             _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(dx), _ptr(dgamma),
-                             _ptr(dw1), _ptr(dw2), _ptr(workspace), nbytes, _stream(stream))
-    _check(rc, "mlpblk_backward")
+    fn = lib.mlpblk_backward_overwrite if overwrite else lib.mlpblk_backward
+    rc = fn(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
+            _ptr(h_saved), _ptr(a_saved), _ptr(rstd_saved), _ptr(dx), _ptr(dgamma),
+            _ptr(dw1), _ptr(dw2), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_backward_overwrite" if overwrite else "mlpblk_backward")
 
 
 def mlpblk_workspace_size_recompute(desc: Desc) -> int:
@@ -347,12 +354,14 @@ def mlpblk_moe_forward(desc, x, gamma, w1s, w2s, expert_idx, routing_weights, y,
 
 
 def mlpblk_moe_backward(desc, dy, x, gamma, w1s, w2s, routing_weights, saved, dx, d_routing_weights, dgamma,
-                        dw1s, dw2s, workspace, stream=None):
-    rc = lib.mlpblk_moe_backward(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1s), _ptr(w2s),
-                                 _ptr(routing_weights), _ptr(saved), _ptr(dx), _ptr(d_routing_weights),
-                                 _ptr(dgamma), _ptr(dw1s), _ptr(dw2s), _ptr(workspace), workspace.numel(),
-                                 _stream(stream))
-    _check(rc, "mlpblk_moe_backward")
+                        dw1s, dw2s, workspace, stream=None, overwrite=False):
+    """overwrite=True calls mlpblk_moe_backward_overwrite (gradients written, not added into)."""
+    fn = lib.mlpblk_moe_backward_overwrite if overwrite else lib.mlpblk_moe_backward
+    rc = fn(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1s), _ptr(w2s),
+            _ptr(routing_weights), _ptr(saved), _ptr(dx), _ptr(d_routing_weights),
+            _ptr(dgamma), _ptr(dw1s), _ptr(dw2s), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    _check(rc, "mlpblk_moe_backward_overwrite" if overwrite else "mlpblk_moe_backward")
 
 
 class MoeBuffers:
@@ -388,9 +397,10 @@ class MoeBuffers:
         mlpblk_moe_forward(self.desc, self.x, self.gamma, self.w1s, self.w2s, self.idx, self.p, self.y, self.saved,
                            self.ws, stream=stream)
 
-    def backward(self, stream=None):
+    def backward(self, stream=None, overwrite=False):
         mlpblk_moe_backward(self.desc, self.dy, self.x, self.gamma, self.w1s, self.w2s, self.p, self.saved,
-                            self.dx, self.dp, self.dgamma, self.dw1s, self.dw2s, self.ws, stream=stream)
+                            self.dx, self.dp, self.dgamma, self.dw1s, self.dw2s, self.ws, stream=stream,
+                            overwrite=overwrite)
 
     def zero_grads(self, stream=None):
         # the experts' gradients as one block's of ffn E*F (same element counts)
@@ -530,7 +540,11 @@ class BlockBuffers:
         mlpblk_forward_prefolded(self.desc, self.x, self.w1g, self.w2, self.y, self.h, self.a, self.rstd,
                                  self.ws, stream=stream)
 
-    def backward(self, stream=None):
+    def backward(self, stream=None, overwrite=False):
+        """overwrite: write the gradients instead of adding into them (saving
+        variant, bf16 or fp32; the FP8 and recompute variants only add)."""
+        if overwrite and (self.fp8 or self.recompute):
+            raise MlpBlkError(MLPBLK_EINVAL, "overwrite is offered by the saving variant only")
         if self.fp8:
             mlpblk_backward_fp8(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a8,
                                 self.n8, self.rstd, self.scales, self.dx, self.dgamma, self.dw1, self.dw2, self.ws,
@@ -541,7 +555,8 @@ class BlockBuffers:
                                       self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)
             return
         mlpblk_backward(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a,
-                        self.rstd, self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream)
+                        self.rstd, self.dx, self.dgamma, self.dw1, self.dw2, self.ws, stream=stream,
+                        overwrite=overwrite)
 
     def zero_grads(self, stream=None):
         mlpblk_zero_grads(self.desc, self.dgamma, self.dw1, self.dw2, stream=stream)

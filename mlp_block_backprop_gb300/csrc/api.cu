@@ -325,9 +325,15 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
                   const void *w1, const void *w2, const void *h_saved, const void *a_saved,
                   const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
                   void *dh_s, void *dn_s, float *part, float *sk_partial, int *sk_flags, int sms,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool overwrite) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     int parts = 0;  // dgamma partial rows written by the norm kernel
+    // = instead of +=: the gradients are cleared, then added into.  (Writing them
+    // from the weight-gradient GEMMs directly would need their split tiles fixed
+    // up from partial sums, which measured slower than the stream-K adds plus
+    // the clearing launch: 120M-class block 1104 vs 1150 TFLOP/s.)
+    if (overwrite)
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, d * F, s));
     if (desc->dtype == MLPBLK_BF16) {
         // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's.  The two
         // independent pairs (dW2, dh) and (dn, dW1) overlap at their boundary:
@@ -423,12 +429,24 @@ int mlpblk_forward(const mlpblk_desc *desc, const void *x, const void *gamma, co
                         sms, static_cast<cudaStream_t>(stream), false);
 }
 
-int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
-                    const void *w1, const void *w2, const void *h_saved, const void *a_saved,
-                    const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
-                    void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int backward_entry(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                   const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                   const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                   void *workspace, size_t workspace_bytes, void *stream, bool overwrite) {
     MLPBLK_TRY(check_desc(desc));
-    if (desc->tokens == 0) return MLPBLK_OK;
+    if (desc->tokens == 0) {
+        // no rows: += adds nothing; = leaves zero gradients
+        if (!overwrite) return MLPBLK_OK;
+        if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const int64_t d = desc->d_model, F = desc->ffn;
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, d * F, s));
+        return MLPBLK_OK;
+    }
     if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
         !aligned16(h_saved) || !aligned16(a_saved) || !aligned16(rstd_saved) || !aligned16(dx) ||
         !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
@@ -442,7 +460,27 @@ int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, cons
     return backward_impl(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
                          ws + l.dh, ws + l.dn, reinterpret_cast<float *>(ws + l.part),
                          reinterpret_cast<float *>(ws + l.sk_partial), reinterpret_cast<int *>(ws + l.sk_flags),
-                         sms, static_cast<cudaStream_t>(stream));
+                         sms, static_cast<cudaStream_t>(stream), overwrite);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlpblk_backward(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                    const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                    const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_entry(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
+                          workspace, workspace_bytes, stream, false);
+}
+
+int mlpblk_backward_overwrite(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                              const void *w1, const void *w2, const void *h_saved, const void *a_saved,
+                              const float *rstd_saved, void *dx, float *dgamma, float *dw1, float *dw2,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_entry(desc, dy, x, gamma, w1, w2, h_saved, a_saved, rstd_saved, dx, dgamma, dw1, dw2,
+                          workspace, workspace_bytes, stream, true);
 }
 
 int mlpblk_fold_weights(const mlpblk_desc *desc, const void *gamma, const void *w1, void *w1g,
@@ -548,7 +586,7 @@ int mlpblk_backward_recompute(const mlpblk_desc *desc, const void *dy, const voi
     // dh_s takes the W1*gamma region, which the GEMM above was the last to read
     return backward_impl(desc, dy, x, gamma, w1, w2, h, a, rstd_saved, dx, dgamma, dw1, dw2, ws + l.dh,
                          ws + l.dn, reinterpret_cast<float *>(ws + l.part),
-                         sk_partial, sk_flags, sms, s);
+                         sk_partial, sk_flags, sms, s, false);
 }
 
 int mlpblk_grad_norm(const mlpblk_desc *desc, const float *dgamma, const float *dw1, const float *dw2,
@@ -1041,12 +1079,25 @@ int mlpblk_moe_forward(const mlpblk_moe_desc *desc, const void *x, const void *g
     return MLPBLK_OK;
 }
 
-int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void *x, const void *gamma,
-                        const void *w1s, const void *w2s, const float *routing_weights, const void *saved, void *dx,
-                        float *d_routing_weights, float *dgamma, float *dw1s, float *dw2s, void *workspace,
-                        size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int moe_backward_entry(const mlpblk_moe_desc *desc, const void *dy, const void *x, const void *gamma,
+                       const void *w1s, const void *w2s, const float *routing_weights, const void *saved,
+                       void *dx, float *d_routing_weights, float *dgamma, float *dw1s, float *dw2s,
+                       void *workspace, size_t workspace_bytes, void *stream, bool overwrite) {
     MLPBLK_TRY(check_moe_desc(desc));
-    if (desc->base.tokens == 0) return MLPBLK_OK;
+    if (desc->base.tokens == 0) {
+        // no rows: += adds nothing; = leaves zero gradients
+        if (!overwrite) return MLPBLK_OK;
+        if (!aligned16(dgamma) || !aligned16(dw1s) || !aligned16(dw2s)) return MLPBLK_EINVAL;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const int64_t d = desc->base.d_model, EF = static_cast<int64_t>(desc->experts) * desc->base.ffn;
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s,
+                      launch_grads(true, 0.0f, dgamma, d, dw1s, EF * d, dw2s, d * EF, s));
+        return MLPBLK_OK;
+    }
     if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1s) || !aligned16(w2s) ||
         !aligned16(routing_weights) || !aligned16(saved) || !aligned16(dx) || !aligned16(d_routing_weights) ||
         !aligned16(dgamma) || !aligned16(dw1s) || !aligned16(dw2s) || !aligned16(workspace))
@@ -1074,14 +1125,17 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     int *sk_flags = reinterpret_cast<int *>(ws + l.sk_flags);
     int parts = 0;
     // d_routing_weights and each slot's output gradient p * dy in segment order
+    // (overwrite: it also clears the gradient blocks of experts no token chose,
+    // which the K-grouped wgrads skip)
     MLPBLK_LAUNCH(MLPBLK_KERNEL_MOE_DP, s,
                   launch_moe_dout(dy, o_perm, routing_weights, pos, count, seg, T, k, E, d, d_routing_weights, do_perm,
-                                  s));
+                                  overwrite ? dw1s : nullptr, overwrite ? dw2s : nullptr, F, s));
     GemmArgs gw2 = {};
     gw2.grp_mode = kGroupK;
     gw2.grp_count = E;
     gw2.grp_rows = seg;
     gw2.grp_c_off = static_cast<int>(d);
+    gw2.overwrite = overwrite ? 1 : 0;  // whole tiles: a store instead of an add
     gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
     gw2.pdl = kPdlWaitFirst;  // (dW2, dh) and (dn, dW1) overlap as in the dense backward
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
@@ -1116,6 +1170,7 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     gw1.grp_count = E;
     gw1.grp_rows = seg;
     gw1.grp_c_off = static_cast<int>(F);
+    gw1.overwrite = overwrite ? 1 : 0;
     gw1.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)l.R, dh_perm, x_perm, dw1s, nullptr, gw1,
@@ -1124,8 +1179,29 @@ int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void 
     MLPBLK_LAUNCH(MLPBLK_KERNEL_NORM_BWD, s,
                   launch_rmsnorm_bwd_gather(x, dn_perm, 1, pos, k, dy, rstd, gamma, dx, part, T, d, kMaxParts, &parts,
                                             s));
-    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s, launch_dgamma_finalize(part, parts, dgamma, d, s));
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_DGAMMA_REDUCE, s,
+                  launch_dgamma_finalize(part, parts, dgamma, d, s, overwrite ? 1 : 0));
     return MLPBLK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlpblk_moe_backward(const mlpblk_moe_desc *desc, const void *dy, const void *x, const void *gamma,
+                        const void *w1s, const void *w2s, const float *routing_weights, const void *saved, void *dx,
+                        float *d_routing_weights, float *dgamma, float *dw1s, float *dw2s, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+    return moe_backward_entry(desc, dy, x, gamma, w1s, w2s, routing_weights, saved, dx, d_routing_weights, dgamma,
+                              dw1s, dw2s, workspace, workspace_bytes, stream, false);
+}
+
+int mlpblk_moe_backward_overwrite(const mlpblk_moe_desc *desc, const void *dy, const void *x, const void *gamma,
+                                  const void *w1s, const void *w2s, const float *routing_weights, const void *saved,
+                                  void *dx, float *d_routing_weights, float *dgamma, float *dw1s, float *dw2s,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    return moe_backward_entry(desc, dy, x, gamma, w1s, w2s, routing_weights, saved, dx, d_routing_weights, dgamma,
+                              dw1s, dw2s, workspace, workspace_bytes, stream, true);
 }
 
 int mlpblk_zero_grads(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream) {

@@ -423,30 +423,30 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw, volat
     if (lane == 0) ok = count_wait_sleep(sn.arrive, P, abort);
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     (void)ld_acquire_gpu(sn.arrive);
+    constexpr int kRowsPerLane = (kMaxSkSlots + 31) / 32;
     for (int q = blockIdx.x; q < chunks; q += P) {
-        // every lane's rows in flight at once (one pass while P <= kMaxSkSlots)
-        constexpr int kRowsPerLane = (kMaxSkSlots + 31) / 32;
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        // every lane's rows in flight at once (one pass while P <= kMaxSkSlots)
         for (int p0 = 0; p0 < P; p0 += 32 * kRowsPerLane) {
-        float4 a[kRowsPerLane][2];
+            float4 a[kRowsPerLane][2];
 #pragma unroll
-        for (int k = 0; k < kRowsPerLane; ++k) {
-            const int p = p0 + lane + 32 * k;
-            if (p < P) {
-                const float *src = sn.part + static_cast<int64_t>(p) * d + 8 * q;
-                a[k][0] = ld_global_cg_v4(src);
-                a[k][1] = ld_global_cg_v4(src + 4);
-            } else {
-                a[k][0] = a[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int k = 0; k < kRowsPerLane; ++k) {
+                const int p = p0 + lane + 32 * k;
+                if (p < P) {
+                    const float *src = sn.part + static_cast<int64_t>(p) * d + 8 * q;
+                    a[k][0] = ld_global_cg_v4(src);
+                    a[k][1] = ld_global_cg_v4(src + 4);
+                } else {
+                    a[k][0] = a[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
             }
-        }
 #pragma unroll
-        for (int k = 0; k < kRowsPerLane; ++k) {
-            v[0] += a[k][0].x; v[1] += a[k][0].y; v[2] += a[k][0].z; v[3] += a[k][0].w;
-            v[4] += a[k][1].x; v[5] += a[k][1].y; v[6] += a[k][1].z; v[7] += a[k][1].w;
-        }
+            for (int k = 0; k < kRowsPerLane; ++k) {
+                v[0] += a[k][0].x; v[1] += a[k][0].y; v[2] += a[k][0].z; v[3] += a[k][0].w;
+                v[4] += a[k][1].x; v[5] += a[k][1].y; v[6] += a[k][1].z; v[7] += a[k][1].w;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
@@ -685,6 +685,7 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
     const bool want_amax = kAmaxEpi && args.amax_out != nullptr;
     float amax_t = 0.0f;
     const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
+    const bool lin = C::kReduce && !args.overwrite;  // segments add into C (else: store)
     SegIter si = seg_begin<C::kTileM>(args, worker);
     Seg w;
     bool have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
@@ -694,7 +695,8 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
         // between workers is finished by the worker holding its first k-blocks
         // (in its last segment); the others (in their first segment) leave
         // fp32 partial sums, which it adds before the fused math.  Reduce
-        // epilogues are linear: every segment adds into the output as it is.
+        // epilogues are linear: every segment adds into the output as it is
+        // (or, K-grouped and overwriting, stores its whole tile).
         const bool head = w.kb0 == 0;
         const bool to_partial = !C::kReduce && !head;
         const bool fixup = !C::kReduce && head && w.kb1 < args.k_blocks;
@@ -902,7 +904,7 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
             if (lane == 0) {
                 if (warp_rows) {
                     const int r0 = m0 + 32 * q + w.crow;
-                    if (C::kReduce) {
+                    if (lin) {
                         tma_reduce_add_2d(pC0, st0, col0, r0);
                     } else {
                         tma_store_2d(pC0, st0, col0, r0);
@@ -1289,6 +1291,8 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = raster_group_m();
     int workers = slots;
+    // C = (not +=) only where every tile is one worker's whole sum: K-grouped
+    if (a.overwrite && (!C::kReduce || a.grp_mode != kGroupK)) return MLPBLK_EINVAL;
     const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode != kGroupK && streamk_enabled() &&
                     (C::kReduce || (a.sk_partial && a.sk_flags));
     if (a.grp_mode == kGroupM && sk && !a.whole_tiles) {

@@ -144,6 +144,7 @@ struct GemmArgs {
     float *sk_partial;         // kMaxSkSlots slots of kSkSlotFloats: split-tile partial sums
     int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
+    int overwrite;             // K-grouped reduce epilogues: C = (not +=) each whole tile
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
     float *amax_out;           // W1 (a) and dgrad-h (dh) epilogues: max |bf16 output| per
@@ -202,8 +203,9 @@ int launch_rmsnorm_bwd(int dtype, const void *x, const void *dn_s, int dn_bf16, 
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int take_device_error_rowops();
+// dgamma += (or =, overwrite != 0) the sum of the partial rows, in a fixed order.
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
-                           cudaStream_t s);
+                           cudaStream_t s, int overwrite = 0);
 // Same row kernel, fed the plain gradient dn of the normalised output (the rstd
 // scale is applied inside the kernel).
 // Routed experts, bf16: row t's dn_s is the sum of the rows pos[t*k + j] of
@@ -267,10 +269,12 @@ int launch_moe_gather(const void *x, const float *rstd, const int *row_token, co
                       int64_t rows_max, int64_t d, void *x_perm, float *rstd_perm, cudaStream_t s);
 int launch_moe_combine(const void *x, const void *o_perm, const float *p, const int *pos, int64_t T, int k,
                        int64_t d, void *y, cudaStream_t s);
-// d_routing_weights and the slots' output gradients p * dy in segment order
+// d_routing_weights and the slots' output gradients p * dy in segment order;
+// with dw1s / dw2s non-null, also zero the [ffn, d] / [d, ffn] gradient blocks of
+// every expert without tokens
 int launch_moe_dout(const void *dy, const void *o_perm, const float *p, const int *pos, const int *count,
                     const int *seg, int64_t T, int k, int experts, int64_t d, float *dp, void *do_perm,
-                    cudaStream_t s);
+                    float *dw1s, float *dw2s, int64_t ffn, cudaStream_t s);
 
 // Host: fp32 CUDA-core GEMM path (simt_f32.cu).  Strides are in elements:
 // A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk], outputs row-major [M][N].

@@ -17,6 +17,7 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 constexpr int kSegPad = 256;
+constexpr int kZeroChunkFloats = 2048;  // one warp item of the dout kernel's gradient clearing
 constexpr int kChunk = kMoeRouteChunk;  // routing entries per CTA (8 warps x 128)
 constexpr int kMaxExperts = 256;
 
@@ -223,12 +224,28 @@ __global__ void combine_kernel(const uint16_t *__restrict__ x, const uint16_t *_
 __global__ void dout_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ o_perm,
                             const float *__restrict__ p, const int *__restrict__ pos,
                             const int *__restrict__ count, const int *__restrict__ seg, int64_t n, int k,
-                            int experts, int64_t d, float *__restrict__ dp, uint16_t *__restrict__ do_perm) {
+                            int experts, int64_t d, float *__restrict__ dp, uint16_t *__restrict__ do_perm,
+                            float *__restrict__ dw1s, float *__restrict__ dw2s, int64_t ffn) {
     griddep_enter();
     const int lane = threadIdx.x & 31;
-    const int64_t items = n + static_cast<int64_t>(experts) * kSegPad;
+    const int64_t pad_end = n + static_cast<int64_t>(experts) * kSegPad;
+    // overwrite: the experts without tokens get zero gradient blocks, in chunks
+    // of 8 KB over the concatenation of the expert's dW1 and dW2 blocks
+    const int64_t fd = ffn * d;
+    const int64_t chunks = dw1s ? (2 * fd + kZeroChunkFloats - 1) / kZeroChunkFloats : 0;
+    const int64_t items = pad_end + static_cast<int64_t>(experts) * chunks;
     for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; i < items;
          i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        if (i >= pad_end) {
+            const int e = static_cast<int>((i - pad_end) / chunks);
+            if (count[e] != 0) continue;
+            const int64_t c0 = ((i - pad_end) % chunks) * kZeroChunkFloats;
+            for (int64_t f = c0 + 4 * lane; f < c0 + kZeroChunkFloats && f < 2 * fd; f += 128) {
+                float *dst = f < fd ? dw1s + e * fd + f : dw2s + e * fd + (f - fd);
+                *reinterpret_cast<float4 *>(dst) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+            continue;
+        }
         if (i >= n) {
             const int e = static_cast<int>((i - n) / kSegPad);
             const int r = seg[e] + count[e] + static_cast<int>((i - n) % kSegPad);
@@ -304,11 +321,11 @@ int launch_moe_combine(const void *x, const void *o_perm, const float *p, const 
 
 int launch_moe_dout(const void *dy, const void *o_perm, const float *p, const int *pos, const int *count,
                     const int *seg, int64_t T, int k, int experts, int64_t d, float *dp, void *do_perm,
-                    cudaStream_t s) {
+                    float *dw1s, float *dw2s, int64_t ffn, cudaStream_t s) {
     const int64_t items = T * k + static_cast<int64_t>(experts) * kSegPad;
     return launch_pdl(dout_kernel, dim3(grid_items(items * 32, 256)), dim3(256), 0, s,
                       static_cast<const uint16_t *>(dy), static_cast<const uint16_t *>(o_perm), p, pos, count, seg,
-                      T * k, k, experts, d, dp, static_cast<uint16_t *>(do_perm));
+                      T * k, k, experts, d, dp, static_cast<uint16_t *>(do_perm), dw1s, dw2s, ffn);
 }
 
 }  // namespace mlpblk

@@ -578,12 +578,12 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     }
 }
 
-// dgamma[k] += sum of the partial rows.  A CTA covers 32 columns with 128
+// dgamma[k] += (or =, overwrite) sum of the partial rows.  A CTA covers 32 columns with 128
 // slices: slice s adds partial rows s, s+128, ... in increasing order (4 columns
 // per thread), then the 128 slice sums meet in a fixed pairwise tree.
 __global__ void __launch_bounds__(1024)
 dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restrict__ dgamma,
-                       int64_t d) {
+                       int64_t d, int overwrite) {
     __shared__ float4 red[128][9];
     griddep_enter();
     const int lane = threadIdx.x & 7;
@@ -617,7 +617,7 @@ dgamma_finalize_kernel(const float *__restrict__ part, int parts, float *__restr
     if (slice == 0 && col < d) {
         const float4 t = red[0][lane];
         float4 *g = reinterpret_cast<float4 *>(dgamma + col);
-        float4 o = *g;
+        float4 o = overwrite ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : *g;
         o.x += t.x;
         o.y += t.y;
         o.z += t.z;
@@ -879,9 +879,10 @@ int take_device_error_rowops() {
     return v;
 }
 
-int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s) {
+int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d, cudaStream_t s,
+                           int overwrite) {
     return launch_pdl(dgamma_finalize_kernel, dim3(static_cast<unsigned>((d + 31) / 32)), dim3(1024), 0,
-                      s, part, parts, dgamma, d);
+                      s, part, parts, dgamma, d, overwrite);
 }
 
 int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,

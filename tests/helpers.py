@@ -30,17 +30,23 @@ def gpu_buffers(inp):
     return bb
 
 
-def run_gpu(inp, keep_outputs=True):
-    """Forward + backward of every microbatch through the C ABI; grad_scale at the end."""
+def run_gpu(inp, keep_outputs=True, overwrite_first=False):
+    """Forward + backward of every microbatch through the C ABI; grad_scale at the end.
+    overwrite_first: no zero_grads; the gradient buffers start as NaN and the first
+    microbatch's backward writes them (mlpblk_backward_overwrite)."""
     import torch
     bb = gpu_buffers(inp)
-    bb.zero_grads()
+    if overwrite_first:
+        for k in GRAD_KEYS:
+            getattr(bb, k).fill_(float("nan"))
+    else:
+        bb.zero_grads()
     outs = []
-    for x, dy in zip(inp.x, inp.dy):
+    for i, (x, dy) in enumerate(zip(inp.x, inp.dy)):
         bb.x.copy_(to_dev(x, bb.dt))
         bb.dy.copy_(to_dev(dy, bb.dt))
         bb.forward()
-        bb.backward()
+        bb.backward(overwrite=overwrite_first and i == 0)
         if keep_outputs:
             outs.append({k: to_np(getattr(bb, k)) for k in OUT_KEYS})
     if inp.grad_scale is not None:
