@@ -371,7 +371,7 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, const T
 // to kStagedMaxStages iterations ahead (warp 0 issues them, the slot rows' indices
 // loaded one issue ahead; an mbarrier per stage counts the bytes).  For a plain dn
 // it measured no faster than the register-resident kernel, which stays in use.
-// A CTA of 256 threads (d <= 2048: two CTAs per SM) or 512 (d = 4096) takes
+// A CTA of 256 threads (d <= 2048: three CTAs per SM) or 512 (d = 4096) takes
 // R = 8 * threads / d rows per iteration, d/8 threads per
 // row, 8 columns per thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16,
 // dn [R][K'][d] fp32 or bf16 (K' = k slot rows with kGather, else 1).  The row sum is a
@@ -380,8 +380,10 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, const T
 constexpr int kStagedMaxThreads = 512;
 constexpr int kStagedMaxStages = 4;
 
-template <bool kGather, class DN>
-__global__ void __launch_bounds__(kStagedMaxThreads, 1)
+// kThreads: 256 (three CTAs per SM, 80 registers; two CTAs measured 53.5 vs 51 us
+// on the 8-expert block, four spill) or kStagedMaxThreads (one CTA per SM).
+template <bool kGather, class DN, int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
 rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__ dn_s,
                           const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
                           const uint16_t *__restrict__ gamma, uint16_t *__restrict__ dx,
@@ -787,7 +789,7 @@ StagedShape staged_shape(int64_t d, int k, int dn_bytes) {
     if (k > 1 && R * k > 64) return sh;  // warp 0 issues at most 64 slot rows
     const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * dn_bytes + 127) / 128 * 128;
     const int64_t extra = 2 * R * 16 * 4 + kStagedMaxStages * 8 + 16;
-    const int64_t budget = threads == 256 ? 100 * 1024 : 200 * 1024;  // 256 threads: two CTAs per SM
+    const int64_t budget = threads == 256 ? 66 * 1024 : 200 * 1024;  // 256 threads: three CTAs per SM
     int S = static_cast<int>((budget - extra) / bytes);
     if (S > kStagedMaxStages) S = kStagedMaxStages;
     if (S < 2) return sh;
@@ -799,20 +801,20 @@ StagedShape staged_shape(int64_t d, int k, int dn_bytes) {
     return sh;
 }
 
-template <bool kGather, class DN>
-int run_norm_bwd_staged(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
-                        const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
-                        int *parts_out, const int *pos, int k, cudaStream_t s) {
+template <bool kGather, class DN, int kThreads>
+int run_norm_bwd_staged_t(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
+                          const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
+                          int *parts_out, const int *pos, int k, cudaStream_t s) {
     static bool attr[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
     if (!attr[dev]) {
-        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather, DN>,
+        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather, DN, kThreads>,
                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 4096));
         if (rc != MLPBLK_OK) return rc;
         attr[dev] = true;
     }
-    int64_t parts = static_cast<int64_t>(sm_count()) * (sh.threads == 256 ? 2 : 1);
+    int64_t parts = static_cast<int64_t>(sm_count()) * (kThreads == 256 ? 3 : 1);
     if (parts > max_parts) parts = max_parts;
     const int64_t groups = (T + sh.R - 1) / sh.R;
     if (parts > groups) parts = groups;
@@ -820,10 +822,21 @@ int run_norm_bwd_staged(const StagedShape &sh, const void *x, const DN *dn, cons
     const int64_t rows_per_cta = ((T + parts - 1) / parts + sh.R - 1) / sh.R * sh.R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather, DN>, dim3(static_cast<unsigned>(parts)), dim3(sh.threads),
-                      sh.smem, s, static_cast<const uint16_t *>(x), dn, static_cast<const uint16_t *>(dy), rstd,
-                      static_cast<const uint16_t *>(gamma), static_cast<uint16_t *>(dx), part, T, d, rows_per_cta,
-                      sh.R, sh.S, sh.stage_bytes, pos, k);
+    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather, DN, kThreads>, dim3(static_cast<unsigned>(parts)),
+                      dim3(kThreads), sh.smem, s, static_cast<const uint16_t *>(x), dn,
+                      static_cast<const uint16_t *>(dy), rstd, static_cast<const uint16_t *>(gamma),
+                      static_cast<uint16_t *>(dx), part, T, d, rows_per_cta, sh.R, sh.S, sh.stage_bytes, pos, k);
+}
+
+template <bool kGather, class DN>
+int run_norm_bwd_staged(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
+                        const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
+                        int *parts_out, const int *pos, int k, cudaStream_t s) {
+    if (sh.threads == 256)
+        return run_norm_bwd_staged_t<kGather, DN, 256>(sh, x, dn, dy, rstd, gamma, dx, part, T, d, max_parts,
+                                                       parts_out, pos, k, s);
+    return run_norm_bwd_staged_t<kGather, DN, kStagedMaxThreads>(sh, x, dn, dy, rstd, gamma, dx, part, T, d,
+                                                                 max_parts, parts_out, pos, k, s);
 }
 
 }  // namespace
