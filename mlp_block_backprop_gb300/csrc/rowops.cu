@@ -363,6 +363,112 @@ rmsnorm_bwd_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, const T
     }
 }
 
+// The same arithmetic when a row takes all kRowThreads threads (G = 256: d = 2048
+// with one chunk per thread, d = 4096 with two): each CTA takes two consecutive
+// rows per iteration and issues both rows' loads before either row's reduction.
+// With one row per iteration a CTA had one row's loads in flight, and the launch
+// took the same time whether dn_s was 4 or 2 bytes per element: it is bound by the
+// rows in flight per SM (two CTAs of two rows here, three of one before).  Sums
+// keep the single-row kernel's order (shuffle tree, then the warps in order).
+template <class T, int CPT, bool kScaleDn, class DN>
+__global__ void __launch_bounds__(kRowThreads, 2)
+rmsnorm_bwd_rows2_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, const T *__restrict__ dy,
+                         const float *__restrict__ rstd, const T *__restrict__ gamma, T *__restrict__ dx,
+                         float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta) {
+    constexpr int kWarps = kRowThreads / 32;
+    __shared__ float rsum[2][2][kWarps];  // [parity][row][warp]
+    griddep_enter();
+    const int tid = threadIdx.x;
+    const int wid = tid >> 5, lane = tid & 31;
+    const int chunks = static_cast<int>(d / 8);
+    const float inv_d = 1.0f / static_cast<float>(d);
+    Chunk<T> gch[CPT];
+    float acc[CPT][8];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const int q = tid + kRowThreads * j;
+        if (q < chunks) gch[j].load(gamma + 8 * q);
+        else gch[j].zero();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+    }
+    const int64_t t0 = blockIdx.x * rows_per_cta;
+    const int64_t t1 = min(T_rows, t0 + rows_per_cta);
+    int parity = 0;
+    for (int64_t base = t0; base < t1; base += 2, parity ^= 1) {
+        Chunk<T> xch[2][CPT], ych[2][CPT];
+        Chunk<float> nch[2][CPT];
+        float r[2];
+        bool valid[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int64_t t = base + rr;
+            valid[rr] = t < t1;
+            r[rr] = valid[rr] ? rstd[t] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                const int q = tid + kRowThreads * j;
+                if (valid[rr] && q < chunks) {
+                    xch[rr][j].load(x + t * d + 8 * q);
+                    load_dn(nch[rr][j], dn_s + t * d + 8 * q);
+                    ych[rr][j].load(dy + t * d + 8 * q);
+                } else {
+                    xch[rr][j].zero();
+                    nch[rr][j].zero();
+                    ych[rr][j].zero();
+                }
+            }
+        }
+        float s[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const float nscale = kScaleDn ? r[rr] : 1.0f;
+            float v = 0.0f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v += gch[j][i] * (nch[rr][j][i] * nscale) * xch[rr][j][i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            s[rr] = v;
+        }
+        if (lane == 0) {
+            rsum[parity][0][wid] = s[0];
+            rsum[parity][1][wid] = s[1];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            if (!valid[rr]) continue;
+            float v = 0.0f;
+            for (int w = 0; w < kWarps; ++w) v += rsum[parity][rr][w];
+            const float cr = r[rr] * r[rr] * v * inv_d;
+            const float nscale = kScaleDn ? r[rr] : 1.0f;
+            const int64_t t = base + rr;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                const int q = tid + kRowThreads * j;
+                if (q >= chunks) continue;
+                float o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float nv = nch[rr][j][i] * nscale;
+                    const float xv = xch[rr][j][i];
+                    o[i] = ych[rr][j][i] + gch[j][i] * nv - xv * cr;
+                    acc[j][i] += nv * xv;
+                }
+                Io8<T>::store(dx + t * d + 8 * q, o);
+            }
+        }
+    }
+    float *out = dg_part + blockIdx.x * d;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const int q = tid + kRowThreads * j;
+        if (q < chunks) Io8<float>::store(out + 8 * q, acc[j]);
+    }
+}
+
 // Staged RMSNorm backward (bf16, d a multiple of 256 and at most 4096; dn_s
 // already scaled by rstd), used for the routed experts' gathered dn: a token's k
 // slot rows sit at scattered rows of dn_s, which the register-resident kernel
@@ -712,12 +818,50 @@ int run_norm_bwd(const void *x, const DN *dn, const void *dy, const float *rstd,
                       static_cast<E *>(dx), part, T, d, rows_per_cta, G, pos, k);
 }
 
+template <class E, int CPT, bool kScaleDn, class DN>
+int run_norm_bwd_rows2(const void *x, const DN *dn, const void *dy, const float *rstd, const void *gamma,
+                       void *dx, float *part, int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
+    int occ = 0;
+    const int rc = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, rmsnorm_bwd_rows2_kernel<E, CPT, kScaleDn, DN>, kRowThreads, 0));
+    if (rc != MLPBLK_OK) return rc;
+    int64_t parts = static_cast<int64_t>(occ > 0 ? occ : 1) * sm_count();
+    if (parts > max_parts) parts = max_parts;
+    const int64_t pairs = (T + 1) / 2;
+    if (parts > pairs) parts = pairs;
+    if (parts < 1) parts = 1;
+    const int64_t rows_per_cta = ((T + parts - 1) / parts + 1) / 2 * 2;
+    parts = (T + rows_per_cta - 1) / rows_per_cta;
+    *parts_out = static_cast<int>(parts);
+    return launch_pdl(rmsnorm_bwd_rows2_kernel<E, CPT, kScaleDn, DN>, dim3(static_cast<unsigned>(parts)),
+                      dim3(kRowThreads), 0, s, static_cast<const E *>(x), dn, static_cast<const E *>(dy), rstd,
+                      static_cast<const E *>(gamma), static_cast<E *>(dx), part, T, d, rows_per_cta);
+}
+
+// Two rows per CTA iteration where a bf16 row takes the whole CTA
+// (MLPBLK_NORM_ROWS2=0: one row per iteration, the general kernel).
+bool rows2_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("MLPBLK_NORM_ROWS2");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 template <class E, bool kScaleDn, bool kGather = false, class DN = float>
 int dispatch_norm_bwd(const void *x, const DN *dn, const void *dy, const float *rstd,
                       const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                       int *parts_out, cudaStream_t s, const int *pos = nullptr, int k = 0) {
     int cpt = 0, G = 0;
     norm_shape(d, &cpt, &G);
+    if (!kGather && sizeof(E) == 2 && G == kRowThreads && cpt <= 2 && T > 0 && rows2_enabled()) {
+        if (cpt == 1)
+            return run_norm_bwd_rows2<E, 1, kScaleDn, DN>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts,
+                                                          parts_out, s);
+        return run_norm_bwd_rows2<E, 2, kScaleDn, DN>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts,
+                                                      parts_out, s);
+    }
 #define MLPBLK_NB(C) \
     return run_norm_bwd<E, C, kScaleDn, kGather, DN>(x, dn, dy, rstd, gamma, dx, part, T, d, max_parts, parts_out, G, \
                                                  pos, k, s)

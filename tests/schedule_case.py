@@ -59,6 +59,8 @@ if __name__ == "__main__":
     dense(2048, 256, 2560, 1)   # a 256 x 256 dgrad-h tile for every CTA pair
     dense(1024, 512, 2048, 2, overwrite=True)   # first microbatch writes the gradients
     dense(600, 1024, 1536, 1, overwrite=True)   # (row-kernel RMSNorm backward)
+    dense(131, 2048, 512, 1)    # RMSNorm backward rows that take a whole CTA (odd row count)
+    dense(67, 4096, 256, 2)
     routed(600, 512, 512, 4, 2)
     routed(300, 256, 256, 4, 3)
     routed(600, 512, 512, 4, 2, overwrite=True)

@@ -24,6 +24,7 @@ SETTINGS = [
     {"MLPBLK_MAX_SMS": "38"},         # a quarter of the SMs
     {"MLPBLK_SIDE_NORM": "0"},        # RMSNorm backward in its own kernel at every width
     {"MLPBLK_MN3D": "0"},             # MN-major operands box by box
+    {"MLPBLK_NORM_ROWS2": "0"},       # RMSNorm backward one row per CTA iteration at every width
 ]
 
 
