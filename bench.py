@@ -513,7 +513,8 @@ def run_ours(args, dist, peaks):
         if amount is None:  # a launch with no bandwidth or FLOP roof of its own (a scalar finalize)
             return None
         mean_s = per[kind][1] / per[kind][0] * 1e-3
-        traffic = recorded_traffic(args.workload, kind)
+        # the record holds captures of the bf16 kernels; the E4M3 GEMMs are other kernels
+        traffic = None if fp8 else recorded_traffic(args.workload, kind)
         if unit == "flop":
             # the burst figure: the timed region is a fraction of a second, not
             # the seconds-long loop of the sustained measurement
