@@ -1222,13 +1222,16 @@ inline int streamk_mode() {
 }
 inline bool streamk_enabled() { return streamk_mode() != 0; }
 
-// M tiles per raster group: MLPBLK_GROUP_M (1..64) when set, else 16.
+// M tiles per raster group: MLPBLK_GROUP_M (1..64) when set, else 8.  A round of
+// 76 pair tiles then spans ~8 M-tiles x ~10 N-tiles, about the fewest operand panels
+// per round (16 spans 16 x ~5); on the large block the K = 16384 GEMMs re-read less
+// and the power-capped step measured 1.5 % faster.
 inline int raster_group_m() {
     static int v = -1;
     if (v < 0) {
         const char *e = getenv("MLPBLK_GROUP_M");
         const int g = e ? atoi(e) : 0;
-        v = (g >= 1 && g <= 64) ? g : 16;
+        v = (g >= 1 && g <= 64) ? g : 8;
     }
     return v;
 }
