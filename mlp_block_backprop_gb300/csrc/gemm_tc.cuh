@@ -1222,18 +1222,22 @@ inline int streamk_mode() {
 }
 inline bool streamk_enabled() { return streamk_mode() != 0; }
 
-// M tiles per raster group: MLPBLK_GROUP_M (1..64) when set, else 8.  A round of
-// 76 pair tiles then spans ~8 M-tiles x ~10 N-tiles, about the fewest operand panels
-// per round (16 spans 16 x ~5); on the large block the K = 16384 GEMMs re-read less
-// and the power-capped step measured 1.5 % faster.
-inline int raster_group_m() {
+// M tiles per raster group: MLPBLK_GROUP_M (1..64) when set.  Otherwise 8 when an
+// A panel (a tile's rows over all of K) is over 2 MB: a round of 76 pair tiles then
+// spans ~8 M-tiles x ~10 N-tiles, about the fewest panels per round, which matters
+// once a round's panels no longer fit L2 (the large block's K = 8192 and 16384
+// GEMMs re-read 9-12 % less and the power-capped step ran 1.1-1.5 % faster than
+// with 16).  With smaller panels 16: a group's A panels stay in L2 across its
+// rounds, so B is streamed half as often (the K = 4096 GEMMs read ~10 % less).
+inline int raster_group_m(int64_t a_panel_bytes) {
     static int v = -1;
     if (v < 0) {
         const char *e = getenv("MLPBLK_GROUP_M");
         const int g = e ? atoi(e) : 0;
-        v = (g >= 1 && g <= 64) ? g : 8;
+        v = (g >= 1 && g <= 64) ? g : 0;
     }
-    return v;
+    if (v > 0) return v;
+    return a_panel_bytes > (2ll << 20) ? 8 : 16;
 }
 
 // Builds the tensor maps and launches one GEMM of configuration C.  Pair mode
@@ -1292,7 +1296,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     const int tiles = a.m_tiles * a.n_tiles;
     const int kb = a.k_blocks;
     a.tiles = tiles;
-    if (a.group_m <= 0) a.group_m = raster_group_m();
+    if (a.group_m <= 0) a.group_m = raster_group_m(static_cast<int64_t>(C::kTileM) * K * (C::F8 ? 1 : 2));
     int workers = slots;
     // C = (not +=) only where every tile is one worker's whole sum: K-grouped
     if (a.overwrite && (!C::kReduce || a.grp_mode != kGroupK)) return MLPBLK_EINVAL;
