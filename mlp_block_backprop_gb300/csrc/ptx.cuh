@@ -499,24 +499,10 @@ __device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Waits until *ctr >= target (acquire), with the same bound and abort protocol
-// as flag_wait.  Returns false when the wait gave up.
-__device__ __forceinline__ bool count_wait(const int *ctr, int target, volatile int *abort) {
-    if (ld_acquire_gpu(ctr) >= target) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (ld_acquire_gpu(ctr) >= target) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            record_device_error(MLPBLK_ETIMEOUT);
-            return false;
-        }
-    }
-}
-
-// count_wait with a pause of about 128 ns between polls, for a wait that may
-// last microseconds while other warps of the SM issue.
+// Waits until *ctr >= target, with the same bound and abort protocol as
+// flag_wait, pausing ~128 ns between relaxed polls (a wait that may last
+// microseconds while other warps of the SM issue); the caller acquires once the
+// count is reached.  Returns false when the wait gave up.
 __device__ __forceinline__ bool count_wait_sleep(const int *ctr, int target, volatile int *abort) {
     // relaxed polls; the caller acquires once the count is reached
     if (ld_relaxed_gpu(ctr) >= target) return true;
