@@ -311,8 +311,8 @@ __device__ __forceinline__ void side_norm_rows(const SideNorm &sn, int sw, volat
     const uint32_t row_bytes = static_cast<uint32_t>(d) * 2;
     const int64_t t_first = static_cast<int64_t>(blockIdx.x) * kSideWarps + sw;
     if (lane == 0)
-        for (int a = 0; a < kAhead; ++a) {
-            const int64_t tp = t_first + a * stride;
+        for (int ahead = 0; ahead < kAhead; ++ahead) {
+            const int64_t tp = t_first + ahead * stride;
             if (tp < sn.T) {
                 bulk_prefetch_l2(sn.x + tp * d, row_bytes);
                 bulk_prefetch_l2(sn.dy + tp * d, row_bytes);
