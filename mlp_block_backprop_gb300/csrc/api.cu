@@ -6,7 +6,8 @@
 // Backward (bf16): wgrad W2 GEMM (+=) -> dgrad-h GEMM (gate, dh_s = rstd*dh)
 //                  -> dgrad-n GEMM (dn_s = rstd*dn, bf16) -> wgrad W1 GEMM (+= , gamma)
 //                  -> RMSNorm backward rows (dx, dgamma partials) -> dgamma (+=)
-//                  (d_model <= 768: the rows run on the wgrad-W1 GEMM's side warps)
+//                  (d_model <= 768: the rows and the dgamma sum run on the
+//                  wgrad-W1 GEMM's side warps)
 // The fp32 element type runs the same sequence on CUDA cores.
 #include <math.h>
 #include <stdlib.h>
