@@ -1,14 +1,15 @@
 #!/usr/bin/env python
 """Forward + backward of the pre-norm residual ReLU² MLP block on GB300.
 
-One step = the whole hot path over one batch of synthetic input: zero_grads,
-then forward and backward of every microbatch (fp32 += gradient accumulation),
-then scale_grads where the workload has one.  The routed-expert block's step is
-forward and mlpblk_moe_backward_overwrite, which sets the gradients (its expert
-GEMMs store whole tiles where they would add them); --grads overwrite|zero picks
-either form for either block (the dense block's overwrite clears the gradients
-in the backward's first launch: the same work as zero_grads, measured 0.5 %
-slower there).  Prints one JSON line (rank 0).
+One step = the whole hot path over one batch of synthetic input: forward and
+backward of every microbatch with fp32 gradient accumulation, then scale_grads
+where the workload has one.  The gradients start either from a zero_grads launch
+at the step's start or from the first microbatch's backward setting them
+(mlpblk_backward_overwrite / mlpblk_moe_backward_overwrite: the weight-gradient
+GEMMs store the tiles they sum whole and only their split tiles are cleared
+first).  --grads auto (default) sets them in the backward for the routed experts
+and for dense blocks with over 64 MB of gradients, and zeroes them otherwise;
+--grads overwrite|zero forces either form.  Prints one JSON line (rank 0).
 The default run times the large block (d 4096, ffn 16384, 2 x 8192 tokens) and,
 in a `secondary` object of the same line, the 120M-class block (d 768, ffn
 3072, 8192 tokens).
@@ -61,8 +62,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
     p.add_argument("--grads", default="auto", choices=["auto", "zero", "overwrite"],
                    help="zero: zero_grads at the start of each step, every backward adds; overwrite: the first "
-                        "microbatch's backward sets the gradients; auto: zero for the dense block, overwrite for "
-                        "the routed experts")
+                        "microbatch's backward sets the gradients; auto: overwrite for the routed experts and for "
+                        "dense blocks with over 64 MB of gradients, zero otherwise")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the 120M-class block that the default run also times")
     p.add_argument("--optimizer", action="store_true",
@@ -381,8 +382,14 @@ def run_ours(args, dist, peaks):
     if prefold:
         bb.w1g = torch.empty_like(bb.w1)
 
-    # --grads overwrite: the first microbatch's backward sets the gradients
-    overwrite = args.grads == "overwrite" and not (fp8 or recompute)
+    # the first microbatch's backward sets the gradients (--grads overwrite, or auto
+    # where zero_grads would clear more than 64 MB: there the weight-gradient GEMMs
+    # store the tiles they sum whole and only their split tiles are cleared; a small
+    # block's zero_grads at the step's start costs less than a clearing launch
+    # between the forward and the backward)
+    grad_bytes = 4 * (2 * F * d + d)
+    overwrite = (args.grads == "overwrite" or (args.grads == "auto" and grad_bytes > (64 << 20))) \
+        and not (fp8 or recompute)
 
     def step(x_list, dy_list, dx_list=None, after_mb=None):
         if not overwrite:

@@ -148,9 +148,12 @@ int mlpblk_backward(const mlpblk_desc *desc,
  *        dgamma[d]  = sum_t dn[t,k] * x[t,k] * r[t]
  *        dw1[F,d]   = dh^T . n,   dw2[d,F] = dy^T . a        (float32, written)
  * The buffers' prior contents do not matter (NaN included), so the window needs
- * no mlpblk_zero_grads; with T = 0 they are set to zero.  This dense block
- * clears them in its first launch and then adds, so the results are bitwise
- * those of mlpblk_zero_grads + mlpblk_backward.  dx, the other arguments, the
+ * no mlpblk_zero_grads; with T = 0 they are set to zero.  The weight-gradient
+ * GEMMs store every output tile that one worker sums whole and add the parts of
+ * the tiles they split between workers into regions that the call's first
+ * launch clears (with dgamma), so the values are those of mlpblk_zero_grads +
+ * mlpblk_backward up to the order in which a split tile's parts are added (the
+ * fp32 path clears all three buffers and adds).  dx, the other arguments, the
  * workspace and the return codes are as for mlpblk_backward.
  */
 int mlpblk_backward_overwrite(const mlpblk_desc *desc,

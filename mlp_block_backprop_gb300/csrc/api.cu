@@ -329,12 +329,6 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
                   cudaStream_t s, bool overwrite) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     int parts = 0;  // dgamma partial rows written by the norm kernel
-    // = instead of +=: the gradients are cleared, then added into.  (Writing them
-    // from the weight-gradient GEMMs directly would need their split tiles fixed
-    // up from partial sums, which measured slower than the stream-K adds plus
-    // the clearing launch: 120M-class block 1104 vs 1150 TFLOP/s.)
-    if (overwrite)
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, d * F, s));
     if (desc->dtype == MLPBLK_BF16) {
         // dW2 first: it needs no flags and zeroes the dgrad-h GEMM's.  The two
         // independent pairs (dW2, dh) and (dn, dW1) overlap at their boundary:
@@ -344,7 +338,6 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         GemmArgs gw2 = {};
         gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
         gw2.pdl = kPdlWaitFirst;
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
         GemmArgs gd = {};
         gd.aux = static_cast<const uint16_t *>(h_saved);
         gd.ld_aux = (int)F;
@@ -353,18 +346,16 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
         gd.sk_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
         gd.zero_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
         gd.pdl = kPdlDeferWait;
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
         GemmArgs gn = {};
         gn.sk_partial = sk_partial;
         gn.sk_flags = sk_flags + kSetDgradN * kSkFlagsPerSet;
         gn.zero_flags = side_norm(d) ? sk_flags + kSetSide * kSkFlagsPerSet : nullptr;
         gn.pdl = kPdlWaitFirst;
-        // dn_s = rstd * dn stored in bf16 like dh_s (rstd rides in dh_s already)
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreBf16, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
         GemmArgs gw1 = {};
         gw1.colscale = static_cast<const uint16_t *>(gamma);
         gw1.pdl = kPdlDeferWait;
-        if (side_norm(d)) {
+        const bool side = side_norm(d);
+        if (side) {
             // the RMSNorm backward rows run on the wgrad-W1 GEMM's side warps,
             // one dgamma partial row per CTA of that launch, summed into dgamma
             // by the same warps once every CTA's row is complete
@@ -380,12 +371,40 @@ int backward_impl(const mlpblk_desc *desc, const void *dy, const void *x, const 
             gw1.side.T = T;
             gw1.side.d = (int)d;
             gw1.grid_out = &parts;
-            MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScaleNorm, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
+        }
+        const int epi_w1 = side ? kEpiAccF32ColScaleNorm : kEpiAccF32ColScale;
+        if (overwrite) {
+            // = instead of +=: the weight-gradient GEMMs store every tile one
+            // worker sums whole, and add the split tiles' parts into regions
+            // that one small launch clears first (with dgamma, which the norm
+            // backward then adds into).  It runs before dW2's GEMM, whose
+            // completion dW1's GEMM follows through the chain of waits above.
+            gw2.overwrite = 1;
+            gw1.overwrite = 1;
+            GemmArgs plan2 = {}, plan1 = {};
+            GemmArgs q2 = gw2, q1 = gw1;
+            q2.plan_out = &plan2;
+            q1.plan_out = &plan1;
+            MLPBLK_TRY(launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, q2, sms, s));
+            MLPBLK_TRY(launch_gemm_tc_bwd(epi_w1, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, q1, sms, s));
+            MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s,
+                          launch_zero_split_tiles(split_tiles_of(plan2, dw2, F), split_tiles_of(plan1, dw1, d),
+                                                  dgamma, d, s));
+        }
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s, launch_gemm_tc_bwd(kEpiAccF32, (int)d, (int)F, (int)T, dy, a_saved, dw2, nullptr, gw2, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_H, s, launch_gemm_tc_bwd(kEpiDgradH, (int)T, (int)F, (int)d, dy, w2, dh_s, nullptr, gd, sms, s));
+        // dn_s = rstd * dn stored in bf16 like dh_s (rstd rides in dh_s already)
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s, launch_gemm_tc_bwd(kEpiStoreBf16, (int)T, (int)d, (int)F, dh_s, w1, dn_s, nullptr, gn, sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(epi_w1, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
+        if (side) {
             if (parts <= 0 || parts > kMaxParts) return MLPBLK_ECUDA;
             return MLPBLK_OK;
         }
-        MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s, launch_gemm_tc_bwd(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh_s, x, dw1, nullptr, gw1, sms, s));
     } else {
+        // CUDA-core path, = instead of +=: the gradients are cleared, then added into
+        if (overwrite)
+            MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s,
+                          launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, d * F, s));
         const float *dyf = static_cast<const float *>(dy);
         const float *xf = static_cast<const float *>(x);
         const float *dhf = static_cast<const float *>(dh_s);

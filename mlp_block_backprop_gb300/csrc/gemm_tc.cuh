@@ -251,15 +251,11 @@ __device__ __forceinline__ bool seg_next(const GemmArgs &a, SegIter &it, Seg &s)
             if (s.kb0 == s.kb1) continue;  // an expert without tokens: no tile
             s.crow = e * a.grp_c_off;
         }
-        const int mt = it.m_tiles;
-        const int group = a.group_m * a.n_tiles;
-        const int g = t / group;
-        const int first_m = g * a.group_m;
-        const int gm = min(mt - first_m, a.group_m);
-        const int r = t - g * group;
-        s.n_blk = r / gm;
-        s.m0 = (first_m + r % gm) * TILE_M;
-        s.n0 = s.n_blk * BN;
+        int mi = 0, ni = 0;
+        raster_tile(t, it.m_tiles, a.n_tiles, a.group_m, mi, ni);
+        s.n_blk = ni;
+        s.m0 = mi * TILE_M;
+        s.n0 = ni * BN;
         if (a.grp_mode == kGroupM) {
             int e = 0;
             while (e + 1 < a.grp_count && a.grp_rows[e + 1] <= s.m0) ++e;
@@ -685,7 +681,6 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
     const bool want_amax = kAmaxEpi && args.amax_out != nullptr;
     float amax_t = 0.0f;
     const float deq = C::F8 ? (args.deq_a ? *args.deq_a : 1.0f) * (args.deq_b ? *args.deq_b : 1.0f) : 1.0f;
-    const bool lin = C::kReduce && !args.overwrite;  // segments add into C (else: store)
     SegIter si = seg_begin<C::kTileM>(args, worker);
     Seg w;
     bool have = seg_next<C::BN, C::kTileM, C::kBKe>(args, si, w);
@@ -696,10 +691,14 @@ __device__ __forceinline__ void epilogue_run(const CUtensorMap *pC0, const CUten
         // (in its last segment); the others (in their first segment) leave
         // fp32 partial sums, which it adds before the fused math.  Reduce
         // epilogues are linear: every segment adds into the output as it is
-        // (or, K-grouped and overwriting, stores its whole tile).
+        // (or, overwriting, a tile that one worker sums whole is stored).
         const bool head = w.kb0 == 0;
         const bool to_partial = !C::kReduce && !head;
         const bool fixup = !C::kReduce && head && w.kb1 < args.k_blocks;
+        // a reduce segment adds into C, unless the GEMM overwrites C and this is
+        // a tile one worker sums whole (its region was not cleared)
+        const bool lin =
+            C::kReduce && (!args.overwrite || (args.grp_mode != kGroupK && w.tile >= args.dp_tiles));
         const int m0 = w.m0 + static_cast<int>(rank) * kBM;  // this CTA's rows
         const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
         const uint32_t aph = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -1298,8 +1297,7 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
     a.tiles = tiles;
     if (a.group_m <= 0) a.group_m = raster_group_m(static_cast<int64_t>(C::kTileM) * K * (C::F8 ? 1 : 2));
     int workers = slots;
-    // C = (not +=) only where every tile is one worker's whole sum: K-grouped
-    if (a.overwrite && (!C::kReduce || a.grp_mode != kGroupK)) return MLPBLK_EINVAL;
+    if (a.overwrite && !C::kReduce) return MLPBLK_EINVAL;
     const bool sk = !C::kNorm && !a.whole_tiles && a.grp_mode != kGroupK && streamk_enabled() &&
                     (C::kReduce || (a.sk_partial && a.sk_flags));
     if (a.grp_mode == kGroupM && sk && !a.whole_tiles) {
@@ -1357,7 +1355,13 @@ int run_gemm_tc(int M, int N, int K, const void *A, const void *B, void *C0, voi
         a.sk_base = a.sk_rem = a.sk_total = 0;
     }
     a.workers = workers;
+    a.tile_m = C::kTileM;
+    a.tile_n = C::BN;
     if (a.grid_out) *a.grid_out = cta_per_worker * workers;
+    if (a.plan_out) {
+        *a.plan_out = a;
+        return MLPBLK_OK;
+    }
 
     static int attr_set[64] = {0};
     int dev = 0;

@@ -105,6 +105,18 @@ struct SideNorm {
     int d;
 };
 
+// Tile t of a GEMM rastered in groups of group_m M-tiles that sweep all N-tiles
+// together: its M-tile and N-tile indices.
+__host__ __device__ inline void raster_tile(int t, int m_tiles, int n_tiles, int group_m, int &mi, int &ni) {
+    const int group = group_m * n_tiles;
+    const int g = t / group;
+    const int first_m = g * group_m;
+    const int gm = (m_tiles - first_m) < group_m ? (m_tiles - first_m) : group_m;
+    const int r = t - g * group;
+    ni = r / gm;
+    mi = first_m + r % gm;
+}
+
 // Arguments of one GEMM launch (the tensor maps travel separately).
 // Stream-K partial accumulators: one slot of 128 x 256 fp32 per CTA, and per
 // slot one flag word per epilogue warp.
@@ -144,7 +156,10 @@ struct GemmArgs {
     float *sk_partial;         // kMaxSkSlots slots of kSkSlotFloats: split-tile partial sums
     int *sk_flags;             // kSkFlagsPerSet words, zero at launch: partial slot ready
     int *zero_flags;           // the next GEMM's flag set, zeroed by this launch (or null)
-    int overwrite;             // K-grouped reduce epilogues: C = (not +=) each whole tile
+    int overwrite;             // reduce epilogues: C = (not +=) each tile one worker sums whole
+                               // (K-grouped: every tile; otherwise tiles below dp_tiles);
+                               // the split tiles at or beyond dp_tiles still add into C,
+                               // which the caller has cleared there (zero_split_tiles)
     int whole_tiles;           // host-side: schedule whole tiles only (no stream-K)
     const float *deq_a, *deq_b;  // E4M3 operands: dequantisation scales (device scalars)
     float *amax_out;           // W1 (a) and dgrad-h (dh) epilogues: max |bf16 output| per
@@ -169,6 +184,9 @@ struct GemmArgs {
     int pdl;                   // PdlOrder
     SideNorm side;             // kEpiAccF32ColScaleNorm: the side warps' rows
     int *grid_out;             // host-side: the launcher stores the grid size (CTAs) here
+    GemmArgs *plan_out;        // host-side: when set, the launcher resolves the schedule,
+                               // stores these arguments here and launches nothing
+    int tile_m, tile_n;        // launcher-set: rows and columns of an output tile
 };
 
 // Operand / output views handed to the GEMM launcher (row-major 2-D tensors).
@@ -203,6 +221,18 @@ int launch_rmsnorm_bwd(int dtype, const void *x, const void *dn_s, int dn_bf16, 
                        const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                        int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s);
 int take_device_error_rowops();
+// Clears the output regions of the tiles that a dense reduce GEMM planned with
+// `plan` splits between workers (tiles plan.dp_tiles .. plan.tiles - 1, which add
+// into C when the GEMM overwrites), for up to two GEMMs (b may have tiles == 0),
+// and dgamma[0, d).  C is fp32 [M][ldc].
+struct SplitTiles {
+    float *c;
+    int64_t ldc;
+    int M, N, tiles, dp_tiles, m_tiles, n_tiles, group_m, tile_m, tile_n;
+};
+SplitTiles split_tiles_of(const GemmArgs &plan, float *c, int64_t ldc);
+int launch_zero_split_tiles(const SplitTiles &a, const SplitTiles &b, float *dgamma, int64_t d, cudaStream_t s);
+
 // dgamma += (or =, overwrite != 0) the sum of the partial rows, in a fixed order.
 int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t d,
                            cudaStream_t s, int overwrite = 0);

@@ -1042,6 +1042,63 @@ int launch_dgamma_finalize(const float *part, int parts, float *dgamma, int64_t 
                       s, part, parts, dgamma, d, overwrite);
 }
 
+namespace {
+
+// kZeroSlices blocks per split tile of `a` (then of `b`), each clearing a slice of
+// the tile's rows of C with 16-byte stores; the last block clears dgamma.
+constexpr int kZeroSlices = 8;
+__global__ void __launch_bounds__(256)
+zero_split_tiles_kernel(SplitTiles a, SplitTiles b, float *__restrict__ dgamma, int64_t d) {
+    griddep_enter();
+    const int na = a.tiles - a.dp_tiles, nb = b.tiles - b.dp_tiles;
+    int idx = static_cast<int>(blockIdx.x) / kZeroSlices;
+    const int slice = static_cast<int>(blockIdx.x) % kZeroSlices;
+    if (idx >= na + nb) {
+        for (int64_t i = threadIdx.x; i < d; i += blockDim.x) dgamma[i] = 0.0f;
+        return;
+    }
+    const SplitTiles &g = idx < na ? a : b;
+    if (idx >= na) idx -= na;
+    int mi = 0, ni = 0;
+    raster_tile(g.dp_tiles + idx, g.m_tiles, g.n_tiles, g.group_m, mi, ni);
+    const int rows = (g.tile_m + kZeroSlices - 1) / kZeroSlices;
+    const int r0 = mi * g.tile_m + slice * rows;
+    const int r1 = min(min(g.M, mi * g.tile_m + g.tile_m), r0 + rows);
+    if (r0 >= r1) return;
+    const int c0 = ni * g.tile_n, c1 = min(g.N, c0 + g.tile_n);
+    const int cols4 = (c1 - c0) / 4;  // N and the tile widths are multiples of 8
+    const int64_t n4 = static_cast<int64_t>(r1 - r0) * cols4;
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        const int r = r0 + static_cast<int>(i / cols4);
+        const int c = c0 + 4 * static_cast<int>(i % cols4);
+        *reinterpret_cast<float4 *>(g.c + r * g.ldc + c) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+}
+
+}  // namespace
+
+SplitTiles split_tiles_of(const GemmArgs &plan, float *c, int64_t ldc) {
+    SplitTiles t;
+    t.c = c;
+    t.ldc = ldc;
+    t.M = plan.M;
+    t.N = plan.N;
+    t.tiles = plan.tiles;
+    t.dp_tiles = plan.dp_tiles < plan.tiles ? plan.dp_tiles : plan.tiles;
+    t.m_tiles = plan.m_tiles;
+    t.n_tiles = plan.n_tiles;
+    t.group_m = plan.group_m;
+    t.tile_m = plan.tile_m;
+    t.tile_n = plan.tile_n;
+    return t;
+}
+
+int launch_zero_split_tiles(const SplitTiles &a, const SplitTiles &b, float *dgamma, int64_t d, cudaStream_t s) {
+    const int blocks = ((a.tiles - a.dp_tiles) + (b.tiles - b.dp_tiles)) * kZeroSlices + 1;
+    return launch_pdl(zero_split_tiles_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a, b, dgamma,
+                      d);
+}
+
 int launch_grads(bool zero, float sc, float *p0, int64_t n0, float *p1, int64_t n1, float *p2,
                  int64_t n2, cudaStream_t s) {
     const int64_t a = n0 / 4, b = n1 / 4, c = n2 / 4;
