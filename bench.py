@@ -19,7 +19,7 @@ in a `secondary` object of the same line, the 120M-class block (d 768, ffn
 --impl reference times the float64 oracle on the host cores on a bounded token
 sample of the same workload (the only other place this script runs the oracle
 is the cpu_baseline leg).  Under torchrun each rank runs an independent replica
-(the block has no cross-rank step in this build); the time is the max over ranks.
+(the block has no cross-rank step); the time is the max over ranks.
 """
 
 from __future__ import annotations
