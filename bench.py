@@ -5,10 +5,11 @@ One step = the whole hot path over one batch of synthetic input: forward and
 backward of every microbatch with fp32 gradient accumulation, then scale_grads
 where the workload has one.  The gradients start either from a zero_grads launch
 at the step's start or from the first microbatch's backward setting them
-(mlpblk_backward_overwrite / mlpblk_moe_backward_overwrite: the weight-gradient
-GEMMs store the tiles they sum whole and only their split tiles are cleared
-first).  --grads auto (default) sets them in the backward for the routed experts
-and for dense blocks with over 64 MB of gradients, and zeroes them otherwise;
+(mlpblk_backward_overwrite, its FP8 form, mlpblk_moe_backward_overwrite: the
+weight-gradient GEMMs store the tiles they sum whole and only their split tiles
+are cleared first).  --grads auto (default) sets them in the backward for the
+routed experts and for dense blocks with over 64 MB of gradients (not the
+recompute variant), and zeroes them otherwise;
 --grads overwrite|zero forces either form.  Prints one JSON line (rank 0).
 The default run times the large block (d 4096, ffn 16384, 2 x 8192 tokens) and,
 in a `secondary` object of the same line, the 120M-class block (d 768, ffn
@@ -389,7 +390,7 @@ def run_ours(args, dist, peaks):
     # between the forward and the backward)
     grad_bytes = 4 * (2 * F * d + d)
     overwrite = (args.grads == "overwrite" or (args.grads == "auto" and grad_bytes > (64 << 20))) \
-        and not (fp8 or recompute)
+        and not recompute
 
     def step(x_list, dy_list, dx_list=None, after_mb=None):
         if not overwrite:
@@ -405,7 +406,8 @@ def run_ours(args, dist, peaks):
                 mb.mlpblk_forward_fp8_prequant(desc, x_list[i], bb.wq, bb.y, bb.h, bb.a8, bb.n8, bb.rstd, bb.scales,
                                                bb.ws)
                 mb.mlpblk_backward_fp8_prequant(desc, dy_list[i], x_list[i], bb.gamma, bb.wq, bb.h, bb.a8, bb.n8,
-                                                bb.rstd, bb.scales, dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws)
+                                                bb.rstd, bb.scales, dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws,
+                                                overwrite=overwrite and i == 0)
             elif recompute:
                 mb.mlpblk_forward_recompute(desc, x_list[i], bb.gamma, bb.w1, bb.w2, bb.y, bb.rstd, bb.ws)
                 mb.mlpblk_backward_recompute(desc, dy_list[i], x_list[i], bb.gamma, bb.w1, bb.w2, bb.rstd,
@@ -558,8 +560,9 @@ def run_ours(args, dist, peaks):
                    "rmsnorm": args.rmsnorm,
                    "w1_gamma_fold": "once per step (mlpblk_fold_weights + mlpblk_forward_prefolded)" if prefold
                                     else "inside every forward",
-                   "gradients": ("written by the first microbatch's backward (mlpblk_backward_overwrite), "
-                                 "added by the others" if overwrite else "zero_grads, then every backward adds"),
+                   "gradients": ("written by the first microbatch's backward (mlpblk_backward"
+                                 + ("_fp8_prequant" if fp8 else "") + "_overwrite), added by the others"
+                                 if overwrite else "zero_grads, then every backward adds"),
                    "optimizer": "grad norm + clip + AdamW (fp32 masters)" if args.optimizer else None,
                    # the recompute variant runs one more W1 GEMM per microbatch; the
                    # metric stays the algorithmic 12*T*d*F per microbatch

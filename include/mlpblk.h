@@ -325,6 +325,24 @@ int mlpblk_backward_fp8_prequant(const mlpblk_desc *desc,
                                  void *dx, float *dgamma, float *dw1, float *dw2,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* The two FP8 backwards with dgamma, dw1 and dw2 set instead of added into (the
+ * first microbatch of an accumulation window), as mlpblk_backward_overwrite is
+ * to mlpblk_backward: the weight-gradient GEMMs store the tiles one worker sums
+ * whole and add split tiles' parts into regions the call's first launch clears. */
+int mlpblk_backward_fp8_overwrite(const mlpblk_desc *desc,
+                                  const void *dy, const void *x, const void *gamma,
+                                  const void *w1, const void *w2,
+                                  const void *h_saved, const void *a8_saved, const void *n8_saved,
+                                  const float *rstd_saved, const float *scales_saved,
+                                  void *dx, float *dgamma, float *dw1, float *dw2,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+int mlpblk_backward_fp8_prequant_overwrite(const mlpblk_desc *desc,
+                                           const void *dy, const void *x, const void *gamma, const void *wq,
+                                           const void *h_saved, const void *a8_saved, const void *n8_saved,
+                                           const float *rstd_saved, const float *scales_saved,
+                                           void *dx, float *dgamma, float *dw1, float *dw2,
+                                           void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Routed ReLU^2 experts ("Nemotron Kernels From Inference To Backpropagation" --
  * "Kernel 4: Routed ReLU2 MoE Inference And Backpropagation"): the pre-norm

@@ -37,7 +37,8 @@ EXPORTED = ("mlpblk_workspace_size", "mlpblk_forward", "mlpblk_backward", "mlpbl
             "mlpblk_backward_fp8_prequant",
             "mlpblk_moe_saved_size", "mlpblk_moe_workspace_size", "mlpblk_moe_forward", "mlpblk_moe_backward",
             "mlpblk_fold_weights", "mlpblk_forward_prefolded", "mlpblk_backward_overwrite",
-            "mlpblk_moe_backward_overwrite")
+            "mlpblk_moe_backward_overwrite", "mlpblk_backward_fp8_overwrite",
+            "mlpblk_backward_fp8_prequant_overwrite")
 MLPBLK_RMSNORM_STATS_PASS = 0
 MLPBLK_RMSNORM_IN_W1_PROLOGUE = 1
 MLPBLK_TEST_FAULT_NONE = 0
@@ -128,6 +129,10 @@ def _load():
     lib.mlpblk_forward_fp8_prequant.restype = i32
     lib.mlpblk_backward_fp8_prequant.argtypes = [pd] + [vp] * 13 + [sz, vp]
     lib.mlpblk_backward_fp8_prequant.restype = i32
+    lib.mlpblk_backward_fp8_overwrite.argtypes = lib.mlpblk_backward_fp8.argtypes
+    lib.mlpblk_backward_fp8_overwrite.restype = i32
+    lib.mlpblk_backward_fp8_prequant_overwrite.argtypes = lib.mlpblk_backward_fp8_prequant.argtypes
+    lib.mlpblk_backward_fp8_prequant_overwrite.restype = i32
     pm = ctypes.POINTER(MoeDesc)
     lib.mlpblk_moe_saved_size.argtypes = [pm]
     lib.mlpblk_moe_saved_size.restype = sz
@@ -295,13 +300,15 @@ def mlpblk_forward_fp8(desc, x, gamma, w1, w2, y, h_saved, a8_saved, n8_saved, r
 
 
 def mlpblk_backward_fp8(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
-                        dx, dgamma, dw1, dw2, workspace, workspace_bytes=None, stream=None):
+                        dx, dgamma, dw1, dw2, workspace, workspace_bytes=None, stream=None, overwrite=False):
+    """overwrite=True calls mlpblk_backward_fp8_overwrite (gradients set, not added into)."""
     nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
-    rc = lib.mlpblk_backward_fp8(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
-                                 _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
-                                 _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
-                                 _ptr(workspace), nbytes, _stream(stream))
-    _check(rc, "mlpblk_backward_fp8")
+    fn = lib.mlpblk_backward_fp8_overwrite if overwrite else lib.mlpblk_backward_fp8
+    rc = fn(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(w1), _ptr(w2),
+            _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
+            _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
+            _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "mlpblk_backward_fp8_overwrite" if overwrite else "mlpblk_backward_fp8")
 
 
 def mlpblk_fp8_weights_size(desc: Desc) -> int:
@@ -325,13 +332,15 @@ def mlpblk_forward_fp8_prequant(desc, x, wq, y, h_saved, a8_saved, n8_saved, rst
 
 
 def mlpblk_backward_fp8_prequant(desc, dy, x, gamma, wq, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved,
-                                 dx, dgamma, dw1, dw2, workspace, stream=None):
-    rc = lib.mlpblk_backward_fp8_prequant(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(wq),
-                                          _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
-                                          _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
-                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                          _stream(stream))
-    _check(rc, "mlpblk_backward_fp8_prequant")
+                                 dx, dgamma, dw1, dw2, workspace, stream=None, overwrite=False):
+    """overwrite=True calls mlpblk_backward_fp8_prequant_overwrite (gradients set, not added into)."""
+    fn = lib.mlpblk_backward_fp8_prequant_overwrite if overwrite else lib.mlpblk_backward_fp8_prequant
+    rc = fn(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(wq),
+            _ptr(h_saved), _ptr(a8_saved), _ptr(n8_saved), _ptr(rstd_saved),
+            _ptr(scales_saved), _ptr(dx), _ptr(dgamma), _ptr(dw1), _ptr(dw2),
+            _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    _check(rc, "mlpblk_backward_fp8_prequant_overwrite" if overwrite else "mlpblk_backward_fp8_prequant")
 
 
 def make_moe_desc(tokens, d_model, ffn, experts, top_k, eps=1e-6) -> MoeDesc:
@@ -541,14 +550,14 @@ class BlockBuffers:
                                  self.ws, stream=stream)
 
     def backward(self, stream=None, overwrite=False):
-        """overwrite: write the gradients instead of adding into them (saving
-        variant, bf16 or fp32; the FP8 and recompute variants only add)."""
-        if overwrite and (self.fp8 or self.recompute):
-            raise MlpBlkError(MLPBLK_EINVAL, "overwrite is offered by the saving variant only")
+        """overwrite: set the gradients instead of adding into them (the saving
+        and FP8 variants; the recompute variant only adds)."""
+        if overwrite and self.recompute:
+            raise MlpBlkError(MLPBLK_EINVAL, "overwrite is not offered by the recompute variant")
         if self.fp8:
             mlpblk_backward_fp8(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.h, self.a8,
                                 self.n8, self.rstd, self.scales, self.dx, self.dgamma, self.dw1, self.dw2, self.ws,
-                                stream=stream)
+                                stream=stream, overwrite=overwrite)
             return
         if self.recompute:
             mlpblk_backward_recompute(self.desc, self.dy, self.x, self.gamma, self.w1, self.w2, self.rstd,

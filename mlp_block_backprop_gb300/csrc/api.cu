@@ -763,7 +763,7 @@ int forward_fp8_impl(const mlpblk_desc *desc, const void *x, const F8Weights &w,
 int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const F8Weights &w,
                       const void *h_saved, const void *a8_saved, const void *n8_saved, const float *rstd_saved,
                       const float *scales_saved, void *dx, float *dgamma, float *dw1, float *dw2, uint8_t *ws,
-                      const WsLayoutF8 &l, int sms, cudaStream_t s) {
+                      const WsLayoutF8 &l, int sms, cudaStream_t s, bool overwrite) {
     const int64_t T = desc->tokens, d = desc->d_model, F = desc->ffn;
     float *amax = reinterpret_cast<float *>(ws + l.amax);
     float *sc = reinterpret_cast<float *>(ws + l.scales);  // records: 2 dy, 3 dh
@@ -774,13 +774,34 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     float *dn_s = reinterpret_cast<float *>(ws + l.dn);
     float *part = reinterpret_cast<float *>(ws + l.part);
     int parts = 0;
-    MLPBLK_TRY(quantize_tensor(dy, nullptr, d, T * d, amax, sc + 8, dyq, s));
     // dW2 += (dy^T . a) * s_dy * s_a; clears the dgrad-h GEMM's flags
     GemmArgs gw2 = {};
     gw2.deq_a = sc + 8 + 2;
     gw2.deq_b = scales_saved + 2;
     gw2.zero_flags = sk_flags + kSetDgradH * kSkFlagsPerSet;
     gw2.pdl = kPdlWaitFirst;  // (dW2, dh) and (dn, dW1) overlap as in the bf16 backward
+    // dW1 += gamma[col] * (dh^T . n') * s_dh
+    GemmArgs gw1 = {};
+    gw1.colscale = static_cast<const uint16_t *>(gamma);
+    gw1.deq_a = sc + 12 + 2;
+    gw1.pdl = kPdlDeferWait;
+    if (overwrite) {
+        // = instead of +=, as in the bf16 backward: whole tiles stored, the split
+        // tiles' regions (and dgamma) cleared by the call's first launch
+        gw2.overwrite = 1;
+        gw1.overwrite = 1;
+        GemmArgs plan2 = {}, plan1 = {};
+        GemmArgs q2 = gw2, q1 = gw1;
+        q2.plan_out = &plan2;
+        q1.plan_out = &plan1;
+        MLPBLK_TRY(launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, q2, sms, s));
+        MLPBLK_TRY(launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, q1,
+                                     sms, s));
+        MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s,
+                      launch_zero_split_tiles(split_tiles_of(plan2, dw2, F), split_tiles_of(plan1, dw1, d), dgamma,
+                                              d, s));
+    }
+    MLPBLK_TRY(quantize_tensor(dy, nullptr, d, T * d, amax, sc + 8, dyq, s));
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W2, s,
                   launch_gemm_tc_f8(kEpiAccF32, (int)d, (int)F, (int)T, dyq, a8_saved, dw2, nullptr, gw2, sms, s));
     // dh = (dy . W2) * s_dy * s_w2 * 2 relu(h)   (bf16; the row scale goes to dgrad-n)
@@ -810,11 +831,6 @@ int backward_fp8_impl(const mlpblk_desc *desc, const void *dy, const void *x, co
     gn.pdl = kPdlWaitFirst;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_DGRAD_N, s,
                   launch_gemm_tc_f8(kEpiStoreF32, (int)T, (int)d, (int)F, dh8, w.w1, dn_s, nullptr, gn, sms, s));
-    // dW1 += gamma[col] * (dh^T . n') * s_dh
-    GemmArgs gw1 = {};
-    gw1.colscale = static_cast<const uint16_t *>(gamma);
-    gw1.deq_a = sc + 12 + 2;
-    gw1.pdl = kPdlDeferWait;
     MLPBLK_LAUNCH(MLPBLK_KERNEL_GEMM_WGRAD_W1, s,
                   launch_gemm_tc_f8(kEpiAccF32ColScale, (int)F, (int)d, (int)T, dh8, n8_saved, dw1, nullptr, gw1,
                                     sms, s));
@@ -854,12 +870,26 @@ int mlpblk_forward_fp8(const mlpblk_desc *desc, const void *x, const void *gamma
     return forward_fp8_impl(desc, x, w, y, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, ws, l, sms, s);
 }
 
-int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const void *w1,
-                        const void *w2, const void *h_saved, const void *a8_saved, const void *n8_saved,
-                        const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma, float *dw1,
-                        float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// T = 0: += adds nothing; = leaves zero gradients.
+int empty_backward(const mlpblk_desc *desc, float *dgamma, float *dw1, float *dw2, void *stream, bool overwrite) {
+    if (!overwrite) return MLPBLK_OK;
+    if (!aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2)) return MLPBLK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t d = desc->d_model, F = desc->ffn;
+    MLPBLK_LAUNCH(MLPBLK_KERNEL_ZERO_GRADS, s, launch_grads(true, 0.0f, dgamma, d, dw1, F * d, dw2, d * F, s));
+    return MLPBLK_OK;
+}
+
+int backward_fp8_entry(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const void *w1,
+                       const void *w2, const void *h_saved, const void *a8_saved, const void *n8_saved,
+                       const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma, float *dw1,
+                       float *dw2, void *workspace, size_t workspace_bytes, void *stream, bool overwrite) {
     MLPBLK_TRY(check_fp8_desc(desc));
-    if (desc->tokens == 0) return MLPBLK_OK;
+    if (desc->tokens == 0) return empty_backward(desc, dgamma, dw1, dw2, stream, overwrite);
     if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(w1) || !aligned16(w2) ||
         !aligned16(h_saved) || !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) ||
         !aligned16(scales_saved) || !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) ||
@@ -880,7 +910,53 @@ int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, 
     MLPBLK_TRY(quantize_tensor(w1, nullptr, d, F * d, amax, sc + 0, w1q, s));
     const F8Weights w = {nullptr, w2q, w1q, nullptr, sc + 4, sc + 0};
     return backward_fp8_impl(desc, dy, x, gamma, w, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
-                             dgamma, dw1, dw2, ws, l, sms, s);
+                             dgamma, dw1, dw2, ws, l, sms, s, overwrite);
+}
+
+int backward_fp8_prequant_entry(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                                const void *wq, const void *h_saved, const void *a8_saved, const void *n8_saved,
+                                const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma,
+                                float *dw1, float *dw2, void *workspace, size_t workspace_bytes, void *stream,
+                                bool overwrite) {
+    MLPBLK_TRY(check_fp8_desc(desc));
+    if (desc->tokens == 0) return empty_backward(desc, dgamma, dw1, dw2, stream, overwrite);
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(wq) || !aligned16(h_saved) ||
+        !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) || !aligned16(scales_saved) ||
+        !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
+        return MLPBLK_EINVAL;
+    if (dx == dy || dx == x) return MLPBLK_EINVAL;
+    const WsLayoutF8 l = ws_layout_f8(desc);
+    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
+    int sms = 0;
+    MLPBLK_TRY(device_sms(&sms));
+    const WqLayout q = wq_layout(desc);
+    const uint8_t *b = static_cast<const uint8_t *>(wq);
+    const float *rec = reinterpret_cast<const float *>(b + q.scales);
+    const F8Weights w = {b + q.w1g, b + q.w2, b + q.w1, rec + 0, rec + 4, rec + 8};
+    return backward_fp8_impl(desc, dy, x, gamma, w, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
+                             dgamma, dw1, dw2, static_cast<uint8_t *>(workspace), l, sms,
+                             static_cast<cudaStream_t>(stream), overwrite);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlpblk_backward_fp8(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma, const void *w1,
+                        const void *w2, const void *h_saved, const void *a8_saved, const void *n8_saved,
+                        const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma, float *dw1,
+                        float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_fp8_entry(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
+                              dgamma, dw1, dw2, workspace, workspace_bytes, stream, false);
+}
+
+int mlpblk_backward_fp8_overwrite(const mlpblk_desc *desc, const void *dy, const void *x, const void *gamma,
+                                  const void *w1, const void *w2, const void *h_saved, const void *a8_saved,
+                                  const void *n8_saved, const float *rstd_saved, const float *scales_saved,
+                                  void *dx, float *dgamma, float *dw1, float *dw2, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    return backward_fp8_entry(desc, dy, x, gamma, w1, w2, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
+                              dgamma, dw1, dw2, workspace, workspace_bytes, stream, true);
 }
 
 size_t mlpblk_fp8_weights_size(const mlpblk_desc *desc) {
@@ -933,24 +1009,17 @@ int mlpblk_backward_fp8_prequant(const mlpblk_desc *desc, const void *dy, const 
                                  const void *wq, const void *h_saved, const void *a8_saved, const void *n8_saved,
                                  const float *rstd_saved, const float *scales_saved, void *dx, float *dgamma,
                                  float *dw1, float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
-    MLPBLK_TRY(check_fp8_desc(desc));
-    if (desc->tokens == 0) return MLPBLK_OK;
-    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(wq) || !aligned16(h_saved) ||
-        !aligned16(a8_saved) || !aligned16(n8_saved) || !aligned16(rstd_saved) || !aligned16(scales_saved) ||
-        !aligned16(dx) || !aligned16(dgamma) || !aligned16(dw1) || !aligned16(dw2) || !aligned16(workspace))
-        return MLPBLK_EINVAL;
-    if (dx == dy || dx == x) return MLPBLK_EINVAL;
-    const WsLayoutF8 l = ws_layout_f8(desc);
-    if (workspace_bytes < static_cast<size_t>(l.total)) return MLPBLK_EWORKSPACE;
-    int sms = 0;
-    MLPBLK_TRY(device_sms(&sms));
-    const WqLayout q = wq_layout(desc);
-    const uint8_t *b = static_cast<const uint8_t *>(wq);
-    const float *rec = reinterpret_cast<const float *>(b + q.scales);
-    const F8Weights w = {b + q.w1g, b + q.w2, b + q.w1, rec + 0, rec + 4, rec + 8};
-    return backward_fp8_impl(desc, dy, x, gamma, w, h_saved, a8_saved, n8_saved, rstd_saved, scales_saved, dx,
-                             dgamma, dw1, dw2, static_cast<uint8_t *>(workspace), l, sms,
-                             static_cast<cudaStream_t>(stream));
+    return backward_fp8_prequant_entry(desc, dy, x, gamma, wq, h_saved, a8_saved, n8_saved, rstd_saved,
+                                       scales_saved, dx, dgamma, dw1, dw2, workspace, workspace_bytes, stream, false);
+}
+
+int mlpblk_backward_fp8_prequant_overwrite(const mlpblk_desc *desc, const void *dy, const void *x,
+                                           const void *gamma, const void *wq, const void *h_saved,
+                                           const void *a8_saved, const void *n8_saved, const float *rstd_saved,
+                                           const float *scales_saved, void *dx, float *dgamma, float *dw1,
+                                           float *dw2, void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_fp8_prequant_entry(desc, dy, x, gamma, wq, h_saved, a8_saved, n8_saved, rstd_saved,
+                                       scales_saved, dx, dgamma, dw1, dw2, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"

@@ -210,3 +210,65 @@ def test_fp8_interleaved_writers_and_readers_in_a_graph():
         errs[k] = oracle.scaled_error(to_np(getattr(bb, k)), ref_grads[k])
     bad = {k: v for k, v in errs.items() if not (v <= TOL)}
     assert not bad, f"scaled error above {TOL}: {bad} (all: {errs})"
+
+
+@pytest.mark.parametrize("shape", [(2304, 768, 3072), (8192, 1024, 4096)], ids=["d768", "d1024_operands_beyond_l2"])
+@pytest.mark.parametrize("prequant", [False, True], ids=["quantise_each_call", "prequantised"])
+def test_fp8_overwrite_is_zero_then_add(shape, prequant):
+    """mlpblk_backward_fp8_overwrite / _prequant_overwrite on the first of two
+    microbatches: the gradient buffers start as NaN and come out as zero_grads
+    followed by adding backwards would leave them, the outputs bit for bit and
+    dW1, dW2, dgamma up to the order in which a split tile's parts reach it."""
+    import torch
+    import mlp_block_backprop_gb300 as mb
+    T, d, F = shape
+    inp = synth.make_inputs(tokens=T, d=d, ffn=F, dtype="bf16", seed=T + 7, n_mb=2, eps=1e-5)
+    bb = mb.BlockBuffers(inp.tokens, inp.d, inp.ffn, dtype="bf16", eps=inp.eps, fp8=True)
+    bb.gamma.copy_(to_dev(inp.gamma, bb.dt))
+    bb.w1.copy_(to_dev(inp.w1, bb.dt))
+    bb.w2.copy_(to_dev(inp.w2, bb.dt))
+    if prequant:
+        mb.mlpblk_fp8_quantize_weights(bb.desc, bb.gamma, bb.w1, bb.w2, bb.wq, bb.ws)
+    runs = []
+    for overwrite in (False, True):
+        if overwrite:
+            for k in ("dgamma", "dw1", "dw2"):
+                getattr(bb, k).fill_(float("nan"))
+        else:
+            bb.zero_grads()
+        outs = []
+        for i, (x, dy) in enumerate(zip(inp.x, inp.dy)):
+            bb.x.copy_(to_dev(x, bb.dt))
+            bb.dy.copy_(to_dev(dy, bb.dt))
+            first = overwrite and i == 0
+            if prequant:
+                mb.mlpblk_forward_fp8_prequant(bb.desc, bb.x, bb.wq, bb.y, bb.h, bb.a8, bb.n8, bb.rstd, bb.scales,
+                                               bb.ws)
+                mb.mlpblk_backward_fp8_prequant(bb.desc, bb.dy, bb.x, bb.gamma, bb.wq, bb.h, bb.a8, bb.n8, bb.rstd,
+                                                bb.scales, bb.dx, bb.dgamma, bb.dw1, bb.dw2, bb.ws, overwrite=first)
+            else:
+                bb.forward()
+                bb.backward(overwrite=first)
+            outs.append({k: to_np(getattr(bb, k)) for k in ("y", "h", "rstd", "dx")})
+        torch.cuda.synchronize()
+        runs.append((outs, {k: to_np(getattr(bb, k)) for k in ("dgamma", "dw1", "dw2")}))
+    (outs_a, grads_a), (outs_b, grads_b) = runs
+    for a, b in zip(outs_a, outs_b):
+        for k in a:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    for k in grads_a:
+        assert np.isfinite(grads_b[k]).all(), f"{k}: an element was not written"
+        err = oracle.scaled_error(grads_b[k], grads_a[k])
+        assert err <= 1e-6, f"{k}: {err}"
+
+
+def test_fp8_overwrite_with_no_tokens_leaves_zero_gradients():
+    import torch
+    import mlp_block_backprop_gb300 as mb
+    bb = mb.BlockBuffers(0, 256, 512, dtype="bf16", fp8=True)
+    for k in ("dgamma", "dw1", "dw2"):
+        getattr(bb, k).fill_(float("nan"))
+    bb.backward(overwrite=True)
+    torch.cuda.synchronize()
+    for k in ("dgamma", "dw1", "dw2"):
+        assert torch.count_nonzero(getattr(bb, k)).item() == 0, k
