@@ -469,26 +469,30 @@ rmsnorm_bwd_rows2_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, c
     }
 }
 
-// Staged RMSNorm backward (bf16, d a multiple of 256 and at most 4096; dn_s
-// already scaled by rstd), used for the routed experts' gathered dn: a token's k
-// slot rows sit at scattered rows of dn_s, which the register-resident kernel
-// reads as loads that wait on the row map.  The same arithmetic as
-// rmsnorm_bwd_kernel, but the rows reach shared memory by bulk copies issued up
-// to kStagedMaxStages iterations ahead (warp 0 issues them, the slot rows' indices
-// loaded one issue ahead; an mbarrier per stage counts the bytes).  For a plain dn
-// it measured no faster than the register-resident kernel, which stays in use.
+// Staged RMSNorm backward for the routed experts' gathered dn (bf16 x and dy, d a
+// multiple of 256 up to 4096, k <= 4 slot rows per token; dn_s already scaled by
+// rstd): a token's k slot rows sit at scattered rows of dn_s.  The same
+// arithmetic as rmsnorm_bwd_kernel, but the rows reach shared memory by bulk
+// copies issued up to kStagedMaxStages iterations ahead by warp 0, counted by an
+// mbarrier per stage.  Warp 0 holds the row map and rstd of kMetaRows rows at a
+// time in registers (the next kMetaRows already loading) and writes each stage's
+// rstd and valid-slot mask into the stage before its arrival, so the loop itself
+// loads nothing from global memory but the bulk copies: with per-iteration loads
+// of rstd and the row map, the load latency on warp 0's path, not the bytes, set
+// the kernel's time.
 // A CTA of 256 threads (d <= 2048: three CTAs per SM) or 512 (d = 4096) takes
-// R = 8 * threads / d rows per iteration, d/8 threads per
-// row, 8 columns per thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16,
-// dn [R][K'][d] fp32 or bf16 (K' = k slot rows with kGather, else 1).  The row sum is a
-// shuffle tree per warp then the row's warps in order; the dgamma partial of the
-// CTA is each thread's running sum, then the R row groups in order.
+// R = 8 * threads / d rows per iteration, d/8 threads per row, 8 columns per
+// thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16, dn [R][k][d] fp32 or bf16,
+// rstd [R] fp32, slot mask [R] int.  The row sum is a shuffle tree per warp then
+// the row's warps in order; the dgamma partial of the CTA is each thread's
+// running sum, then the R row groups in order.
 constexpr int kStagedMaxThreads = 512;
 constexpr int kStagedMaxStages = 4;
+constexpr int kMetaRows = 32;
 
-// kThreads: 256 (three CTAs per SM, 80 registers; two CTAs measured 53.5 vs 51 us
-// on the 8-expert block, four spill) or kStagedMaxThreads (one CTA per SM).
-template <bool kGather, class DN, int kThreads>
+// kMaxK: 2 (k <= 2) or 4.  kThreads: 256 (three CTAs per SM, 80 registers) or
+// kStagedMaxThreads (one CTA per SM).
+template <int kMaxK, class DN, int kThreads>
 __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
 rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__ dn_s,
                           const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
@@ -496,7 +500,6 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
                           float *__restrict__ dg_part, int64_t T_rows, int64_t d, int64_t rows_per_cta, int R,
                           int S, int stage_bytes, const int *__restrict__ pos, int k) {
     extern __shared__ __align__(128) uint8_t smem_st[];
-    const int kk = kGather ? k : 1;
     uint8_t *stages = smem_st;
     float *red = reinterpret_cast<float *>(smem_st + static_cast<size_t>(S) * stage_bytes);  // [2][R][16]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * R * 16);
@@ -512,6 +515,8 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     const int64_t t0 = blockIdx.x * rows_per_cta;
     const int64_t t1 = min(T_rows, t0 + rows_per_cta);
     const int iters = static_cast<int>((t1 - t0 + R - 1) / R);
+    const size_t x_bytes = static_cast<size_t>(R) * d * 2;
+    const size_t meta_off = 2 * x_bytes + static_cast<size_t>(R) * k * d * sizeof(DN);
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
@@ -525,94 +530,97 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     __syncthreads();
     griddep_enter();
 
-    // Warp 0 issues the copies of iteration it into stage it % S: lane 0 the x
-    // and dy rows (and, without kGather, the dn_s rows); with kGather lane j < R*k
-    // the slot row (row j / k, slot j % k) whose index it loaded one issue ahead.
-    int pnext[2] = {-1, -1};
-    auto load_pos = [&](int it) {
-        if (!kGather) return;
-        const int64_t tb = t0 + static_cast<int64_t>(it) * R;
-        for (int q = 0; q < 2; ++q) {
-            const int j = lane + 32 * q;
-            const int r = j / kk;
-            pnext[q] = (it < iters && r < R && tb + r < t1) ? pos[(tb + r) * kk + j % kk] : -1;
-        }
+    // Warp 0: lane l holds rstd and the k slot indices of row (chunk base + l) of
+    // the current and the next chunk of kMetaRows rows.
+    float cur_r = 0.0f, nxt_r = 0.0f;
+    int cur_p[kMaxK], nxt_p[kMaxK];
+    int cur_chunk = 0;
+    auto load_chunk = [&](int c, float &rv, int (&pv)[kMaxK]) {
+        const int64_t t = t0 + static_cast<int64_t>(c) * kMetaRows + lane;
+        const bool v = t < t1;
+        rv = v ? rstd[t] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) pv[j] = (v && j < k) ? pos[t * k + j] : -1;
     };
+    // Issues iteration it into stage it % S: lane r < R writes row r's rstd and
+    // slot mask; lane j < R * kMaxK copies slot j % kMaxK of row j / kMaxK; lane 0
+    // arrives with the stage's byte count and copies the x and dy rows.
     auto issue = [&](int it) {
+        const int c = it * R / kMetaRows;  // R divides kMetaRows
+        if (c != cur_chunk) {
+            cur_r = nxt_r;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) cur_p[j] = nxt_p[j];
+            cur_chunk = c;
+            load_chunk(c + 1, nxt_r, nxt_p);
+        }
         const int st = it % S;
         uint8_t *sx = stages + static_cast<size_t>(st) * stage_bytes;
-        uint8_t *sy = sx + static_cast<size_t>(R) * d * 2;
-        uint8_t *sn = sy + static_cast<size_t>(R) * d * 2;
+        uint8_t *sy = sx + x_bytes;
+        uint8_t *sn = sy + x_bytes;
+        float *m_r = reinterpret_cast<float *>(sx + meta_off);
+        int *m_mask = reinterpret_cast<int *>(m_r + R);
+        const int base = it * R - c * kMetaRows;
         const int64_t tb = t0 + static_cast<int64_t>(it) * R;
         const int nr = static_cast<int>(min(static_cast<int64_t>(R), t1 - tb));
-        uint32_t mine = 0;  // this lane's slot-row bytes
-        if (kGather)
-            for (int q = 0; q < 2; ++q)
-                if (pnext[q] >= 0) mine += static_cast<uint32_t>(d) * sizeof(DN);
+        // the lane's own row as a meta writer, and its (row, slot) as a copier
+        const int mrow = min(lane, R - 1);
+        const int crow = min(lane / kMaxK, R - 1);
+        const int cslot = lane % kMaxK;
+        const float rv = __shfl_sync(0xffffffffu, cur_r, base + mrow);
+        int mask = 0, prow = -1;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            const int vm = __shfl_sync(0xffffffffu, cur_p[j], base + mrow);
+            const int vc = __shfl_sync(0xffffffffu, cur_p[j], base + crow);
+            if (vm >= 0) mask |= 1 << j;
+            if (j == cslot) prow = vc;
+        }
+        const bool copies = lane < R * kMaxK && lane / kMaxK < nr && cslot < k && prow >= 0;
+        uint32_t mine = copies ? static_cast<uint32_t>(d) * sizeof(DN) : 0u;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        if (lane < R) {
+            m_r[lane] = lane < nr ? rv : 0.0f;
+            m_mask[lane] = lane < nr ? mask : 0;
+        }
+        __syncwarp();  // the meta stores before lane 0's (release) arrival
         if (lane == 0) {
-            uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u;  // x and dy
-            bytes += kGather ? mine : static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * sizeof(DN);
-            mbar_arrive_expect_tx(&full[st], bytes);
+            mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nr) * static_cast<uint32_t>(d) * 4u + mine);
             bulk_copy_g2s(sx, x + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
             bulk_copy_g2s(sy, dy + tb * d, static_cast<uint32_t>(nr * d * 2), &full[st]);
-            if (!kGather) bulk_copy_g2s(sn, dn_s + tb * d, static_cast<uint32_t>(nr * d * sizeof(DN)), &full[st]);
         }
-        if (kGather)
-            for (int q = 0; q < 2; ++q)
-                if (pnext[q] >= 0)
-                    bulk_copy_g2s(sn + static_cast<size_t>(lane + 32 * q) * d * sizeof(DN),
-                                  dn_s + static_cast<int64_t>(pnext[q]) * d, static_cast<uint32_t>(d * sizeof(DN)),
-                                  &full[st]);
+        if (copies)
+            bulk_copy_g2s(sn + (static_cast<size_t>(lane / kMaxK) * k + cslot) * d * sizeof(DN),
+                          dn_s + static_cast<int64_t>(prow) * d, static_cast<uint32_t>(d * sizeof(DN)), &full[st]);
         __syncwarp();
     };
     int issued = 0;
     if (tid < 32) {
-        for (; issued < S && issued < iters; ++issued) {
-            load_pos(issued);
-            issue(issued);
-        }
-        load_pos(issued);
+        load_chunk(0, cur_r, cur_p);
+        load_chunk(1, nxt_r, nxt_p);
+        for (; issued < S && issued < iters; ++issued) issue(issued);
     }
-
-    // each thread's rstd (and, kGather, its row's slot indices) two iterations ahead
-    auto row_of = [&](int it) { return t0 + static_cast<int64_t>(it) * R + grp; };
-    float r_n1 = 0.0f, r_n2 = 0.0f;
-    int p_n1[4] = {-1, -1, -1, -1}, p_n2[4] = {-1, -1, -1, -1};
-    auto fetch = [&](int it, float &rv, int (&pv)[4]) {
-        const int64_t t = row_of(it);
-        const bool v = active && it < iters && t < t1;
-        rv = v ? rstd[t] : 0.0f;
-        if (kGather)
-            for (int j = 0; j < 4; ++j) pv[j] = (v && j < kk) ? pos[t * kk + j] : -1;
-    };
-    fetch(0, r_n1, p_n1);
-    fetch(1, r_n2, p_n2);
 
     int it = 0;
     for (; it < iters; ++it) {
         const int st = it % S;
         const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-        const int64_t t = row_of(it);
+        const int64_t t = t0 + static_cast<int64_t>(it) * R + grp;
         const bool valid = active && t < t1;
-        const float r = r_n1;
-        int pv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) pv[j] = p_n1[j];
-        r_n1 = r_n2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) p_n1[j] = p_n2[j];
-        fetch(it + 2, r_n2, p_n2);
         // every thread waits on the stage's barrier; the block-wide vote below
         // (which also publishes the warp sums) leaves the loop together if any gave up
         const bool ok = mbar_wait(&full[st], ph, abort_flag);
         const uint8_t *sx = stages + static_cast<size_t>(st) * stage_bytes;
-        const uint8_t *sy = sx + static_cast<size_t>(R) * d * 2;
-        const uint8_t *sn = sy + static_cast<size_t>(R) * d * 2;
+        const uint8_t *sy = sx + x_bytes;
+        const uint8_t *sn = sy + x_bytes;
+        const float *m_r = reinterpret_cast<const float *>(sx + meta_off);
+        const int *m_mask = reinterpret_cast<const int *>(m_r + R);
         float xv[8], yv[8], nv[8];
-        float part = 0.0f;
+        float part = 0.0f, r = 0.0f;
         if (valid && ok) {
+            r = m_r[grp];
+            const int mask = m_mask[grp];
             const uint4 ux = *reinterpret_cast<const uint4 *>(sx + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
             const uint4 uy = *reinterpret_cast<const uint4 *>(sy + (static_cast<size_t>(grp) * d + 8 * gl) * 2);
             xv[0] = bf(ux.x & 0xFFFFu); xv[1] = bf(ux.x >> 16); xv[2] = bf(ux.y & 0xFFFFu); xv[3] = bf(ux.y >> 16);
@@ -621,9 +629,10 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
             yv[4] = bf(uy.z & 0xFFFFu); yv[5] = bf(uy.z >> 16); yv[6] = bf(uy.w & 0xFFFFu); yv[7] = bf(uy.w >> 16);
 #pragma unroll
             for (int i = 0; i < 8; ++i) nv[i] = 0.0f;
-            for (int j = 0; j < kk; ++j) {
-                if (kGather && pv[j] < 0) continue;
-                const DN *q = reinterpret_cast<const DN *>(sn) + (static_cast<size_t>(grp) * kk + j) * d + 8 * gl;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (!((mask >> j) & 1)) continue;
+                const DN *q = reinterpret_cast<const DN *>(sn) + (static_cast<size_t>(grp) * k + j) * d + 8 * gl;
                 if (sizeof(DN) == 4) {
                     const float4 a0 = *reinterpret_cast<const float4 *>(q);
                     const float4 a1 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(q) + 4);
@@ -645,10 +654,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
         if (active && lane == 0) rr[grp * 16 + gl / 32] = part;
         // every thread has read stage st and written its warp sum
         if (!__syncthreads_and(ok)) break;
-        if (tid < 32 && issued < iters) {
-            issue(issued++);
-            load_pos(issued);
-        }
+        if (tid < 32 && issued < iters) issue(issued++);
         if (valid) {
             float sum = 0.0f;
             for (int w = 0; w < wpr; ++w) sum += rr[grp * 16 + w];
@@ -930,8 +936,10 @@ StagedShape staged_shape(int64_t d, int k, int dn_bytes) {
     if (d % 256 != 0 || d > 4096 || k < 1 || k > 4) return sh;
     const int threads = d <= 2048 ? 256 : 512;
     const int R = static_cast<int>(8 * threads / d);
-    if (k > 1 && R * k > 64) return sh;  // warp 0 issues at most 64 slot rows
-    const int64_t bytes = (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * dn_bytes + 127) / 128 * 128;
+    if (R * (k <= 2 ? 2 : 4) > 32 || kMetaRows % R != 0) return sh;  // one copy lane per (row, slot)
+    // x, dy, the slot rows, then each row's rstd and slot mask
+    const int64_t bytes =
+        (static_cast<int64_t>(R) * d * 4 + static_cast<int64_t>(R) * k * d * dn_bytes + 8 * R + 127) / 128 * 128;
     const int64_t extra = 2 * R * 16 * 4 + kStagedMaxStages * 8 + 16;
     const int64_t budget = threads == 256 ? 66 * 1024 : 200 * 1024;  // 256 threads: three CTAs per SM
     int S = static_cast<int>((budget - extra) / bytes);
@@ -945,7 +953,7 @@ StagedShape staged_shape(int64_t d, int k, int dn_bytes) {
     return sh;
 }
 
-template <bool kGather, class DN, int kThreads>
+template <int kMaxK, class DN, int kThreads>
 int run_norm_bwd_staged_t(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
                           const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                           int *parts_out, const int *pos, int k, cudaStream_t s) {
@@ -953,7 +961,7 @@ int run_norm_bwd_staged_t(const StagedShape &sh, const void *x, const DN *dn, co
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLPBLK_ECUDA;
     if (!attr[dev]) {
-        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kGather, DN, kThreads>,
+        const int rc = cuda_status(cudaFuncSetAttribute(rmsnorm_bwd_staged_kernel<kMaxK, DN, kThreads>,
                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 4096));
         if (rc != MLPBLK_OK) return rc;
         attr[dev] = true;
@@ -966,21 +974,21 @@ int run_norm_bwd_staged_t(const StagedShape &sh, const void *x, const DN *dn, co
     const int64_t rows_per_cta = ((T + parts - 1) / parts + sh.R - 1) / sh.R * sh.R;
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
-    return launch_pdl(rmsnorm_bwd_staged_kernel<kGather, DN, kThreads>, dim3(static_cast<unsigned>(parts)),
+    return launch_pdl(rmsnorm_bwd_staged_kernel<kMaxK, DN, kThreads>, dim3(static_cast<unsigned>(parts)),
                       dim3(kThreads), sh.smem, s, static_cast<const uint16_t *>(x), dn,
                       static_cast<const uint16_t *>(dy), rstd, static_cast<const uint16_t *>(gamma),
                       static_cast<uint16_t *>(dx), part, T, d, rows_per_cta, sh.R, sh.S, sh.stage_bytes, pos, k);
 }
 
-template <bool kGather, class DN>
-int run_norm_bwd_staged(const StagedShape &sh, const void *x, const DN *dn, const void *dy, const float *rstd,
+template <int kMaxK>
+int run_norm_bwd_staged(const StagedShape &sh, const void *x, const uint16_t *dn, const void *dy, const float *rstd,
                         const void *gamma, void *dx, float *part, int64_t T, int64_t d, int max_parts,
                         int *parts_out, const int *pos, int k, cudaStream_t s) {
     if (sh.threads == 256)
-        return run_norm_bwd_staged_t<kGather, DN, 256>(sh, x, dn, dy, rstd, gamma, dx, part, T, d, max_parts,
-                                                       parts_out, pos, k, s);
-    return run_norm_bwd_staged_t<kGather, DN, kStagedMaxThreads>(sh, x, dn, dy, rstd, gamma, dx, part, T, d,
-                                                                 max_parts, parts_out, pos, k, s);
+        return run_norm_bwd_staged_t<kMaxK, uint16_t, 256>(sh, x, dn, dy, rstd, gamma, dx, part, T, d, max_parts,
+                                                           parts_out, pos, k, s);
+    return run_norm_bwd_staged_t<kMaxK, uint16_t, kStagedMaxThreads>(sh, x, dn, dy, rstd, gamma, dx, part, T, d,
+                                                                     max_parts, parts_out, pos, k, s);
 }
 
 }  // namespace
@@ -1011,15 +1019,15 @@ int launch_rmsnorm_bwd_unscaled(int dtype, const void *x, const float *dn, const
 int launch_rmsnorm_bwd_gather(const void *x, const void *dn_rows, int dn_bf16, const int *pos, int k,
                               const void *dy, const float *rstd, const void *gamma, void *dx, float *dgamma_part,
                               int64_t T, int64_t d, int max_parts, int *parts_out, cudaStream_t s) {
-    if (T > 0) {
-        const StagedShape sh = staged_shape(d, k, dn_bf16 ? 2 : 4);
-        if (sh.R > 0) {
-            if (dn_bf16)
-                return run_norm_bwd_staged<true>(sh, x, static_cast<const uint16_t *>(dn_rows), dy, rstd, gamma, dx,
-                                                 dgamma_part, T, d, max_parts, parts_out, pos, k, s);
-            return run_norm_bwd_staged<true>(sh, x, static_cast<const float *>(dn_rows), dy, rstd, gamma, dx,
-                                             dgamma_part, T, d, max_parts, parts_out, pos, k, s);
-        }
+    if (T > 0 && dn_bf16) {
+        const StagedShape sh = staged_shape(d, k, 2);
+        const uint16_t *dn = static_cast<const uint16_t *>(dn_rows);
+        if (sh.R > 0 && k <= 2)
+            return run_norm_bwd_staged<2>(sh, x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts, parts_out,
+                                          pos, k, s);
+        if (sh.R > 0)
+            return run_norm_bwd_staged<4>(sh, x, dn, dy, rstd, gamma, dx, dgamma_part, T, d, max_parts, parts_out,
+                                          pos, k, s);
     }
     if (dn_bf16)
         return dispatch_norm_bwd<uint16_t, false, true, uint16_t>(x, static_cast<const uint16_t *>(dn_rows), dy, rstd,

@@ -81,6 +81,8 @@ def _check(got, ref, skip_dp=None):
     (257, 512, 256, 6, 4),
     (1000, 768, 256, 3, 1),
     (130, 2048, 256, 4, 2),
+    (70, 4096, 256, 3, 2),     # 512-thread CTAs
+    (45, 4096, 256, 4, 3),
 ])
 def test_moe_against_the_oracle(shape):
     T, d, F, E, k = shape
