@@ -474,26 +474,44 @@ rmsnorm_bwd_rows2_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, c
 // rstd): a token's k slot rows sit at scattered rows of dn_s.  The same
 // arithmetic as rmsnorm_bwd_kernel, but the rows reach shared memory by bulk
 // copies issued up to kStagedMaxStages iterations ahead by warp 0, counted by an
-// mbarrier per stage.  Warp 0 holds the row map and rstd of kMetaRows rows at a
-// time in registers (the next kMetaRows already loading) and writes each stage's
-// rstd and valid-slot mask into the stage before its arrival, so the loop itself
-// loads nothing from global memory but the bulk copies: with per-iteration loads
-// of rstd and the row map, the load latency on warp 0's path, not the bytes, set
-// the kernel's time.
-// A CTA of 256 threads (d <= 2048: three CTAs per SM) or 512 (d = 4096) takes
-// R = 8 * threads / d rows per iteration, d/8 threads per row, 8 columns per
+// mbarrier per stage.  A producer warp beside the row threads issues them: it
+// holds the row map and rstd of kMetaRows rows at a time in registers (the next
+// kMetaRows already loading) and writes each stage's rstd and valid-slot mask
+// into the stage before its arrival, so the loop loads nothing from global memory
+// but the bulk copies, and the copies' issue (~0.7 us a stage) runs while the row
+// threads compute instead of between their iterations.  Both take part in the one
+// CTA barrier per iteration, after which the producer refills the stage just read.
+// The row threads of a CTA, 256 (d <= 2048: three CTAs per SM) or 512 (d = 4096),
+// take R = 8 * threads / d rows per iteration, d/8 threads per row, 8 columns per
 // thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16, dn [R][k][d] fp32 or bf16,
 // rstd [R] fp32, slot mask [R] int.  The row sum is a shuffle tree per warp then
 // the row's warps in order; the dgamma partial of the CTA is each thread's
 // running sum, then the R row groups in order.
 constexpr int kStagedMaxThreads = 512;
+
+// AND of pred over the nthreads threads that reach named barrier id (which may
+// arrive from different code: the producer warp and the row threads).
+__device__ __forceinline__ bool barrier_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p, q;\n"
+        "  setp.ne.u32 p, %1, 0;\n"
+        "  bar.red.and.pred q, %2, %3, p;\n"
+        "  selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 constexpr int kStagedMaxStages = 4;
 constexpr int kMetaRows = 32;
 
-// kMaxK: 2 (k <= 2) or 4.  kThreads: 256 (three CTAs per SM, 80 registers) or
-// kStagedMaxThreads (one CTA per SM).
+// kMaxK: 2 (k <= 2) or 4.  kThreads: the row threads, 256 (three CTAs per SM) or
+// kStagedMaxThreads (one CTA per SM); the block has kThreads + 32 threads.
 template <int kMaxK, class DN, int kThreads>
-__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 3 : 1)
+__global__ void __launch_bounds__(kThreads + 32, kThreads == 256 ? 3 : 1)
 rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__ dn_s,
                           const uint16_t *__restrict__ dy, const float *__restrict__ rstd,
                           const uint16_t *__restrict__ gamma, uint16_t *__restrict__ dx,
@@ -506,11 +524,12 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kStagedMaxStages);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
+    const bool producer = tid >= kThreads;
     const int cpr = static_cast<int>(d / 8);  // threads per row (a multiple of 32)
     const int grp = tid / cpr;
     const int gl = tid - grp * cpr;
     const int wpr = cpr / 32;                 // warps per row
-    const bool active = grp < R;
+    const bool active = !producer && grp < R;
     const float inv_d = 1.0f / static_cast<float>(d);
     const int64_t t0 = blockIdx.x * rows_per_cta;
     const int64_t t1 = min(T_rows, t0 + rows_per_cta);
@@ -530,7 +549,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     __syncthreads();
     griddep_enter();
 
-    // Warp 0: lane l holds rstd and the k slot indices of row (chunk base + l) of
+    // The producer: lane l holds rstd and the k slot indices of row (chunk base + l) of
     // the current and the next chunk of kMetaRows rows.
     float cur_r = 0.0f, nxt_r = 0.0f;
     int cur_p[kMaxK], nxt_p[kMaxK];
@@ -596,14 +615,19 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
         __syncwarp();
     };
     int issued = 0;
-    if (tid < 32) {
+    int it = 0;
+    if (producer) {
         load_chunk(0, cur_r, cur_p);
         load_chunk(1, nxt_r, nxt_p);
         for (; issued < S && issued < iters; ++issued) issue(issued);
+        // one barrier per iteration with the row threads; after it the stage they
+        // just read is free
+        for (; it < iters; ++it) {
+            if (!barrier_and(1, kThreads + 32, true)) break;
+            if (issued < iters) issue(issued++);
+        }
     }
-
-    int it = 0;
-    for (; it < iters; ++it) {
+    for (; !producer && it < iters; ++it) {
         const int st = it % S;
         const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
         const int64_t t = t0 + static_cast<int64_t>(it) * R + grp;
@@ -653,8 +677,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
         float *rr = red + (it & 1) * R * 16;
         if (active && lane == 0) rr[grp * 16 + gl / 32] = part;
         // every thread has read stage st and written its warp sum
-        if (!__syncthreads_and(ok)) break;
-        if (tid < 32 && issued < iters) issue(issued++);
+        if (!barrier_and(1, kThreads + 32, ok)) break;
         if (valid) {
             float sum = 0.0f;
             for (int w = 0; w < wpr; ++w) sum += rr[grp * 16 + w];
@@ -671,7 +694,7 @@ rmsnorm_bwd_staged_kernel(const uint16_t *__restrict__ x, const DN *__restrict__
     }
     if (it < iters) {
         // gave up: let the copies already issued land before the CTA exits
-        if (tid == 0)
+        if (producer && lane == 0)
             for (int j = it; j < issued; ++j) mbar_drain(&full[j % S], static_cast<uint32_t>(j / S) & 1u);
         __syncthreads();
         return;
@@ -975,7 +998,7 @@ int run_norm_bwd_staged_t(const StagedShape &sh, const void *x, const DN *dn, co
     parts = (T + rows_per_cta - 1) / rows_per_cta;
     *parts_out = static_cast<int>(parts);
     return launch_pdl(rmsnorm_bwd_staged_kernel<kMaxK, DN, kThreads>, dim3(static_cast<unsigned>(parts)),
-                      dim3(kThreads), sh.smem, s, static_cast<const uint16_t *>(x), dn,
+                      dim3(kThreads + 32), sh.smem, s, static_cast<const uint16_t *>(x), dn,
                       static_cast<const uint16_t *>(dy), rstd, static_cast<const uint16_t *>(gamma),
                       static_cast<uint16_t *>(dx), part, T, d, rows_per_cta, sh.R, sh.S, sh.stage_bytes, pos, k);
 }
