@@ -98,7 +98,7 @@ def _load():
     lib.mlpblk_backward.argtypes = [pd] + [vp] * 13 + [sz, vp]
     lib.mlpblk_fold_weights.argtypes = [pd, vp, vp, vp, vp]
     lib.mlpblk_fold_weights.restype = i32
-    lib.mlpblk_forward_prefolded.argtypes = [pd] + [vp] * 7 + [sz, vp]
+    lib.mlpblk_forward_prefolded.argtypes = [pd] + [vp] * 8 + [sz, vp]
     lib.mlpblk_forward_prefolded.restype = i32
     lib.mlpblk_backward.restype = i32
     lib.mlpblk_backward_overwrite.argtypes = lib.mlpblk_backward.argtypes
@@ -117,9 +117,9 @@ def _load():
     lib.mlpblk_adamw_step.restype = i32
     lib.mlpblk_workspace_size_fp8.argtypes = [pd]
     lib.mlpblk_workspace_size_fp8.restype = sz
-    lib.mlpblk_forward_fp8.argtypes = [pd] + [vp] * 10 + [sz, vp]
+    lib.mlpblk_forward_fp8.argtypes = [pd] + [vp] * 11 + [sz, vp]
     lib.mlpblk_forward_fp8.restype = i32
-    lib.mlpblk_backward_fp8.argtypes = [pd] + [vp] * 14 + [sz, vp]
+    lib.mlpblk_backward_fp8.argtypes = [pd] + [vp] * 15 + [sz, vp]
     lib.mlpblk_backward_fp8.restype = i32
     lib.mlpblk_fp8_weights_size.argtypes = [pd]
     lib.mlpblk_fp8_weights_size.restype = sz
@@ -127,7 +127,7 @@ def _load():
     lib.mlpblk_fp8_quantize_weights.restype = i32
     lib.mlpblk_forward_fp8_prequant.argtypes = [pd] + [vp] * 9 + [sz, vp]
     lib.mlpblk_forward_fp8_prequant.restype = i32
-    lib.mlpblk_backward_fp8_prequant.argtypes = [pd] + [vp] * 13 + [sz, vp]
+    lib.mlpblk_backward_fp8_prequant.argtypes = [pd] + [vp] * 14 + [sz, vp]
     lib.mlpblk_backward_fp8_prequant.restype = i32
     lib.mlpblk_backward_fp8_overwrite.argtypes = lib.mlpblk_backward_fp8.argtypes
     lib.mlpblk_backward_fp8_overwrite.restype = i32

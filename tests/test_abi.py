@@ -38,6 +38,30 @@ def test_every_declared_symbol_is_exported(mb):
     assert set(mb.EXPORTED) <= declared
 
 
+def _declared_parameters():
+    """{function: number of parameters} of every declaration in include/*.h."""
+    import glob
+    out = {}
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for name, params in re.findall(r"\b(mlpblk_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+            ps = [q.strip() for q in params.split(",") if q.strip()]
+            out[name] = 0 if ps == ["void"] else len(ps)
+    return out
+
+
+def test_binding_declares_every_parameter(mb):
+    """The binding's ctypes argtypes list every parameter the header declares, so
+    no argument (the stream last of all) falls to ctypes' default int conversion."""
+    decl = _declared_parameters()
+    assert len(decl) >= 30
+    wrong = {n: (k, len(getattr(mb.lib, n).argtypes or []))
+             for n, k in decl.items() if len(getattr(mb.lib, n).argtypes or []) != k}
+    assert not wrong, f"header parameters vs argtypes: {wrong}"
+
+
 def test_version_and_strerror(mb):
     assert mb.mlpblk_version() >= 100
     for code in range(0, 7):
@@ -161,14 +185,14 @@ def test_fp8_argument_errors_need_no_device(mb):
     assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(d)) > 0
     assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(mb.make_desc(64, 136, 256))) == 0   # d % 16
     assert mb.lib.mlpblk_workspace_size_fp8(ctypes.byref(mb.make_desc(64, 128, 256, dtype=mb.MLPBLK_FP32))) == 0
-    fwd = [0x10000 * (i + 1) for i in range(10)]
+    fwd = [0x10000 * (i + 1) for i in range(11)]   # x ... scales, workspace
     f = lambda args, ws=1 << 40, dd=d: mb.lib.mlpblk_forward_fp8(ctypes.byref(dd), *args, ws, None)
     assert f(fwd, dd=mb.make_desc(64, 136, 256)) == mb.MLPBLK_ENOTSUP
     bad = list(fwd)
     bad[9] += 4   # scales misaligned
     assert f(bad) == mb.MLPBLK_EINVAL
     assert f(fwd, 16) == mb.MLPBLK_EWORKSPACE
-    bwd = [0x10000 * (i + 1) for i in range(14)]
+    bwd = [0x10000 * (i + 1) for i in range(15)]   # dy ... dw2, workspace
     b = lambda args, ws=1 << 40: mb.lib.mlpblk_backward_fp8(ctypes.byref(d), *args, ws, None)
     alias = list(bwd)
     alias[10] = alias[0]   # dx == dy
@@ -192,7 +216,7 @@ def test_fp8_prequant_argument_errors_need_no_device(mb):
     alias[2] = alias[0]   # y == x
     assert f(alias) == mb.MLPBLK_EINVAL
     assert f(fwd, 16) == mb.MLPBLK_EWORKSPACE
-    bwd = [0x10000 * (i + 1) for i in range(13)]
+    bwd = [0x10000 * (i + 1) for i in range(14)]   # dy ... dw2, workspace
     b = lambda args, ws=1 << 40: mb.lib.mlpblk_backward_fp8_prequant(ctypes.byref(d), *args, ws, None)
     bad = list(bwd)
     bad[3] += 8   # wq misaligned
@@ -224,6 +248,50 @@ def test_moe_argument_errors_need_no_device(mb):
     alias = list(bargs)
     alias[7] = alias[0]   # dx == dy
     assert b(alias) == mb.MLPBLK_EINVAL
+
+
+def test_overwrite_argument_errors_need_no_device(mb):
+    """The forms that set the gradients check their arguments as the adding forms
+    do, before any device call; with no tokens they only check the gradient
+    buffers (they still zero them, which needs a device)."""
+    d = mb.make_desc(64, 128, 256)
+    empty = mb.make_desc(0, 128, 256)
+    good = [0x10000 * (i + 1) for i in range(13)]
+    b = lambda a, ws=1 << 40, dd=d: mb.lib.mlpblk_backward_overwrite(ctypes.byref(dd), *a, ws, None)
+    bad = list(good)
+    bad[11] += 4   # dw2 misaligned
+    assert b(bad) == mb.MLPBLK_EINVAL
+    assert b(bad, dd=empty) == mb.MLPBLK_EINVAL
+    alias = list(good)
+    alias[8] = alias[1]   # dx == x
+    assert b(alias) == mb.MLPBLK_EINVAL
+    assert b(good, 0) == mb.MLPBLK_EWORKSPACE
+    f8 = [0x10000 * (i + 1) for i in range(15)]
+    b8 = lambda a, ws=1 << 40, dd=d: mb.lib.mlpblk_backward_fp8_overwrite(ctypes.byref(dd), *a, ws, None)
+    bad = list(f8)
+    bad[13] += 8   # dw2 misaligned
+    assert b8(bad) == mb.MLPBLK_EINVAL
+    assert b8(bad, dd=empty) == mb.MLPBLK_EINVAL
+    assert b8(f8, 16) == mb.MLPBLK_EWORKSPACE
+    assert b8(f8, dd=mb.make_desc(64, 136, 256)) == mb.MLPBLK_ENOTSUP
+    q8 = [0x10000 * (i + 1) for i in range(14)]
+    bq = lambda a, ws=1 << 40, dd=d: mb.lib.mlpblk_backward_fp8_prequant_overwrite(ctypes.byref(dd), *a, ws, None)
+    bad = list(q8)
+    bad[10] += 4   # dgamma misaligned
+    assert bq(bad) == mb.MLPBLK_EINVAL
+    assert bq(bad, dd=empty) == mb.MLPBLK_EINVAL
+    alias = list(q8)
+    alias[9] = alias[0]   # dx == dy
+    assert bq(alias) == mb.MLPBLK_EINVAL
+    assert bq(q8, 16) == mb.MLPBLK_EWORKSPACE
+    md = mb.make_moe_desc(64, 128, 256, 4, 2)
+    margs = [0x10000 * (i + 1) for i in range(13)]
+    bm = lambda a, ws=1 << 40, dd=md: mb.lib.mlpblk_moe_backward_overwrite(ctypes.byref(dd), *a, ws, None)
+    assert bm(margs, 16) == mb.MLPBLK_EWORKSPACE
+    bad = list(margs)
+    bad[10] += 4   # dw1s misaligned
+    assert bm(bad) == mb.MLPBLK_EINVAL
+    assert bm(bad, dd=mb.make_moe_desc(0, 128, 256, 4, 2)) == mb.MLPBLK_EINVAL
 
 
 def test_grad_buffers_are_float32_by_contract():
