@@ -328,7 +328,11 @@ int mlpblk_backward_fp8_prequant(const mlpblk_desc *desc,
 /* The two FP8 backwards with dgamma, dw1 and dw2 set instead of added into (the
  * first microbatch of an accumulation window), as mlpblk_backward_overwrite is
  * to mlpblk_backward: the weight-gradient GEMMs store the tiles one worker sums
- * whole and add split tiles' parts into regions the call's first launch clears. */
+ * whole and add split tiles' parts into regions the call's first launch clears.
+ * Arguments, layouts, ownership and error codes are those of the adding forms;
+ * the old contents of the three gradient buffers are never read (NaN is fine).
+ * With tokens == 0 the call zeroes dgamma, dw1 and dw2 (MLPBLK_EINVAL if one of
+ * them is not 16-byte aligned). */
 int mlpblk_backward_fp8_overwrite(const mlpblk_desc *desc,
                                   const void *dy, const void *x, const void *gamma,
                                   const void *w1, const void *w2,
