@@ -30,6 +30,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -278,15 +279,24 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_text(src):
+    """The code of a C/CUDA source without its comments and with every run of
+    white space as one space: an edit to comments or layout leaves it unchanged."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def csrc_hash(kernel=None):
-    """Hash of the kernel's sources (KERNEL_SOURCES), else of every CUDA source."""
+    """Hash of the code (comments and layout aside) of the kernel's sources
+    (KERNEL_SOURCES), else of every CUDA source."""
     csrc = os.path.join(ROOT, "mlp_block_backprop_gb300", "csrc")
     names = KERNEL_SOURCES.get(kernel)
     paths = [os.path.join(csrc, n) for n in names] if names else sorted(glob.glob(os.path.join(csrc, "*")))
     h = hashlib.sha256()
     for p in paths:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_text(f.read()).encode("utf-8"))
     return h.hexdigest()[:12]
 
 

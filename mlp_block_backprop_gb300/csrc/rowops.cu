@@ -473,8 +473,8 @@ rmsnorm_bwd_rows2_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, c
 // multiple of 256 up to 4096, k <= 4 slot rows per token; dn_s already scaled by
 // rstd): a token's k slot rows sit at scattered rows of dn_s.  The same
 // arithmetic as rmsnorm_bwd_kernel, but the rows reach shared memory by bulk
-// copies issued up to kStagedMaxStages iterations ahead by warp 0, counted by an
-// mbarrier per stage.  A producer warp beside the row threads issues them: it
+// copies issued up to kStagedMaxStages iterations ahead, counted by an mbarrier
+// per stage.  A producer warp beside the row threads issues them: it
 // holds the row map and rstd of kMetaRows rows at a time in registers (the next
 // kMetaRows already loading) and writes each stage's rstd and valid-slot mask
 // into the stage before its arrival, so the loop loads nothing from global memory
@@ -483,8 +483,8 @@ rmsnorm_bwd_rows2_kernel(const T *__restrict__ x, const DN *__restrict__ dn_s, c
 // CTA barrier per iteration, after which the producer refills the stage just read.
 // The row threads of a CTA, 256 (d <= 2048: three CTAs per SM) or 512 (d = 4096),
 // take R = 8 * threads / d rows per iteration, d/8 threads per row, 8 columns per
-// thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16, dn [R][k][d] fp32 or bf16,
-// rstd [R] fp32, slot mask [R] int.  The row sum is a shuffle tree per warp then
+// thread.  Stage layout: x [R][d] bf16, dy [R][d] bf16, dn [R][k][d] (bf16 as
+// launched), rstd [R] fp32, slot mask [R] int.  The row sum is a shuffle tree per warp then
 // the row's warps in order; the dgamma partial of the CTA is each thread's
 // running sum, then the R row groups in order.
 constexpr int kStagedMaxThreads = 512;
